@@ -1,0 +1,380 @@
+"""Benchmark of the attention core: one step = forward + backward of one packed batch.
+
+Default workload: the packed batch of 12 + 925 + 4253 + 8349 tokens (13539),
+48 heads, head_dim 128, bf16 q/k/v ~ N(0, 1), dO ~ N(0, 1) (synthetic, seeded).
+The metric is attention forward+backward TFLOP/s on that batch, counting
+4 H d sum_s L_s^2 forward and 2.5x that backward (algorithmic flops of the
+per-sample attention; the masked cross-sample blocks are not counted).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same batch on its own GPU (replicas;
+the path has no data-path collective) and the value is the sum over ranks.
+``--impl reference`` times the FP64 CPU oracle on the host cores instead,
+on a bounded sample of the same workload (one 925-token sample per step).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from invariant_dit_attention_gb300 import workloads as W  # noqa: E402
+
+METRIC = "attention fwd/bwd TFLOP/s at 8349 packed tokens, % of GB300 BF16 peak"
+WORKLOAD = "packed_13539"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            flat = {}
+
+            def walk(x, pre=""):
+                if isinstance(x, dict):
+                    for k, v in x.items():
+                        walk(v, f"{pre}{k}.")
+                elif isinstance(x, (int, float)):
+                    flat[pre[:-1]] = float(x)
+            walk(d)
+            out = {}
+            for key in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+                cands = [v for k, v in flat.items() if k.split(".")[-1] == key]
+                if cands:
+                    out[key] = cands[0]
+            if "hbm_gbs" in out and "bf16_tflops" in out:
+                out.setdefault("bf16_tflops_sustained", out["bf16_tflops"])
+                out["source"] = "measured"
+                return out
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def barrier_max(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def bwd_flops(fwd):
+    return 2.5 * fwd
+
+
+def run_ours(args):
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    from invariant_dit_attention_gb300 import build
+    build.build()
+    from invariant_dit_attention_gb300.h3attn import H3Attn, to_device
+
+    w, inp = W.make_workload(WORKLOAD)
+    inp = W.make_inputs(w.samples, w.num_heads, w.seed, w.std, w.outlier_frac, w.outlier_scale, with_grad=True)
+    S, H = inp.total_tokens, inp.num_heads
+    fwd_flops = w.fwd_flops()
+    step_flops = fwd_flops + bwd_flops(fwd_flops)
+    h = H3Attn(H, S, 8)
+    d = to_device(inp)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        out, lse = h.forward(d["q"], d["k"], d["v"], d["q_norm_w"], d["k_norm_w"], d["pos"], d["seg_offsets"])
+        g = h.backward(d["q"], d["k"], d["v"], d["q_norm_w"], d["k_norm_w"], d["pos"], d["seg_offsets"],
+                       out, lse, d["dout"], grads=grads)
+        return out, g
+
+    grads = {"dq": torch.empty_like(d["q"]), "dk": torch.empty_like(d["k"]), "dv": torch.empty_like(d["v"]),
+             "dq_norm_w": torch.empty(128, device="cuda"), "dk_norm_w": torch.empty(128, device="cuda"),
+             "dq_norm_w_per_sample": torch.empty(inp.num_samples, 128, device="cuda"),
+             "dk_norm_w_per_sample": torch.empty(inp.num_samples, 128, device="cuda")}
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    h.check()
+
+    # ---- device-resident timed region
+    h.set_stage_timing(True)
+    h.stage_times()  # reset
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(ws)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+    ms = e0.elapsed_time(e1)
+    stages = h.stage_times()
+    h.set_stage_timing(False)
+    h.check()
+    ms_max = barrier_max(ms, ws)
+    value = step_flops * args.steps * ws / (ms_max * 1e-3) / 1e12
+
+    # ---- forward-only rates: whole batch and every sample alone (same kernels)
+    fwd_ms = stages["fwd"][0] + 0.5 * (stages["prologue"][0] + stages["plan"][0])
+    per_sample = {}
+    for s in range(inp.num_samples):
+        alone = to_device(W.slice_sample(inp, s))
+        L = inp.meta["lengths"][s]
+        for _ in range(3):
+            h.forward(alone["q"], alone["k"], alone["v"], alone["q_norm_w"], alone["k_norm_w"], alone["pos"],
+                      alone["seg_offsets"])
+        reps = 10 if L > 1000 else 50
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(reps):
+            h.forward(alone["q"], alone["k"], alone["v"], alone["q_norm_w"], alone["k_norm_w"], alone["pos"],
+                      alone["seg_offsets"])
+        a1.record(stream)
+        torch.cuda.synchronize()
+        t = a0.elapsed_time(a1) / reps
+        per_sample[str(L)] = {"fwd_ms": round(t, 4),
+                              "fwd_tflops": round(4.0 * H * 128 * L * L / (t * 1e-3) / 1e12, 2)}
+        del alone
+
+    # ---- end to end: host (pinned) inputs -> device -> fwd + bwd -> host results
+    host_in = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in
+               {"q": inp.q, "k": inp.k, "v": inp.v, "q_norm_w": inp.q_norm_w, "k_norm_w": inp.k_norm_w,
+                "dout": inp.dout, "seg_offsets": inp.seg_offsets}.items()}
+    host_pos = [inp.pos[a].contiguous().pin_memory() for a in range(3)]
+    host_out = {"out": torch.empty_like(inp.q).pin_memory(), "dq": torch.empty_like(inp.q).pin_memory(),
+                "dk": torch.empty_like(inp.k).pin_memory(), "dv": torch.empty_like(inp.v).pin_memory(),
+                "dq_norm_w": torch.empty(128).pin_memory(), "dk_norm_w": torch.empty(128).pin_memory()}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + sum(
+        t.numel() * t.element_size() for t in host_pos)
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def e2e_step():
+        for k in host_in:
+            d[k].copy_(host_in[k], non_blocking=True)
+        for a in range(3):
+            d["pos"][a].copy_(host_pos[a], non_blocking=True)
+        out, g = step()
+        host_out["out"].copy_(out, non_blocking=True)
+        for k in ("dq", "dk", "dv", "dq_norm_w", "dk_norm_w"):
+            host_out[k].copy_(g[k], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(ws)
+    t0 = time.perf_counter()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = barrier_max(e0.elapsed_time(e1), ws)
+    e2e_value = step_flops * args.steps * ws / (e2e_ms * 1e-3) / 1e12
+    h.check()
+
+    # ---- roofline of the dominant kernel (stage timing over the timed region)
+    pk = peaks()
+    L2 = [L * L for L in inp.meta["lengths"]]
+    unit = 2.0 * H * 128 * float(sum(L2))  # one S-shaped GEMM over the batch
+    algo = {"fwd": 2 * unit, "bwd_dkdv": 4 * unit, "bwd_dq": 1 * unit}
+    kern = max(("fwd", "bwd_dkdv", "bwd_dq"), key=lambda k: stages[k][0])
+    kms = stages[kern][0] / max(stages[kern][1], 1)
+    ach = algo[kern] / (kms * 1e-3) / 1e12
+    roof = {"kernel": kern, "bound": "tensor", "achieved": round(ach, 2), "peak": pk["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops"], 4), "traffic": None,
+            "peak_source": f"{pk['source']} bf16 burst",
+            "frac_of_sustained": round(ach / pk["bf16_tflops_sustained"], 4)}
+    pro_ms = stages["prologue"][0] / max(stages["prologue"][1], 1)
+    pro_bytes = 8.0 * S * H * 128  # q, k read (bf16) + q^, k^ written (bf16)
+    prologue = {"achieved_gbs": round(pro_bytes / (pro_ms * 1e-3) / 1e9, 1), "peak_gbs": pk["hbm_gbs"],
+                "frac": round(pro_bytes / (pro_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4), "ms": round(pro_ms, 4)}
+    launches_per_step = 3 + 7
+
+    # ---- CPU baseline: the oracle as it stands, bounded sample, rank 0 only
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(H)
+
+    result = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "samples": inp.meta["lengths"], "heads": H, "head_dim": 128,
+                   "total_tokens": S, "step": "forward + backward (attention core, norm/RoPE prologue, "
+                   "norm-weight gradients)", "flops_per_step": step_flops,
+                   "l2": "inputs larger than L2 (q, k, v, dO 166 MB each)", "parallelism": f"replicas x{ws}"},
+        "fwd_tflops_batch": round(fwd_flops / (fwd_ms / args.steps * 1e-3) / 1e12, 2) if fwd_ms else None,
+        "fwd_per_sample": per_sample,
+        "stages_ms_per_step": {k: round(v[0] / args.steps, 4) for k, v in stages.items()},
+        "roofline": roof, "prologue_roofline": prologue,
+        "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / args.steps, 4)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(result))
+    h.close()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def cpu_baseline(H):
+    """The FP64 oracle on the host cores: forward + backward of one 925-token sample."""
+    import oracle
+    w = W.WORKLOADS[WORKLOAD]
+    inp = W.make_inputs([W.S925], H, seed=w.seed + 1, with_grad=True)
+    L = inp.total_tokens
+    flops = 3.5 * 4.0 * H * 128 * L * L
+    t0 = time.perf_counter()
+    oracle.forward(inp.q, inp.k, inp.v, inp.q_norm_w, inp.k_norm_w, inp.pos, inp.seg_offsets)
+    oracle.backward(inp.q, inp.k, inp.v, inp.q_norm_w, inp.k_norm_w, inp.pos, inp.seg_offsets, inp.dout)
+    t = time.perf_counter() - t0
+    return {"value": round(flops / t / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": round(t, 2),
+            "sample": f"oracle forward + backward of one {L}-token sample of the workload layout, H={H}, FP64"}
+
+
+def run_reference(args):
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    w = W.WORKLOADS[WORKLOAD]
+    H = w.num_heads
+    inp = W.make_inputs([W.S925], H, seed=w.seed + 1, with_grad=True)
+    L = inp.total_tokens
+    flops = 3.5 * 4.0 * H * 128 * L * L
+
+    def step():
+        oracle.forward(inp.q, inp.k, inp.v, inp.q_norm_w, inp.k_norm_w, inp.pos, inp.seg_offsets)
+        oracle.backward(inp.q, inp.k, inp.v, inp.q_norm_w, inp.k_norm_w, inp.pos, inp.seg_offsets, inp.dout)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    t = time.perf_counter() - t0
+    value = flops * args.steps / t / 1e12
+    cores = oracle.num_threads()
+    sample = f"one {L}-token sample of the {WORKLOAD} workload per step (forward + backward, H={H}, FP64)"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "samples": [L], "heads": H, "head_dim": 128},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

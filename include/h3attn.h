@@ -1,0 +1,164 @@
+/*
+ * h3attn.h -- C ABI of the batch-invariant MiniMax-H3 attention core (sm_103a).
+ *
+ * The library computes, for a packed sequence of independent samples,
+ *
+ *   q^ = RoPE(RMSNorm(q) * q_norm_w),  k^ = RoPE(RMSNorm(k) * k_norm_w)
+ *   out_i = sum_j softmax_j(scale * q^_i . k^_j) v_j     (j in i's sample only)
+ *
+ * and its gradients.  The operations are the q_norm/k_norm, rope_q/rope_k and
+ * attention nodes of one MiniMax-H3 transformer block as bound on the
+ * "ws1_one_h3_block" page of RL-Kernel (PR #539), Bindings table: RMSNorm on
+ * the 128-wide heads with a 128-element weight, partial 3-axis multimodal RoPE
+ * from packed (t, h, w) position ids, non-causal attention per packed sample.
+ * The numerical contract follows the strict mode of the "ws1_full_h3_transformer"
+ * page (PR #571), Scope / Known limitations: no TF32, no fast-math, no split-K,
+ * FP32 accumulation, and unsupported shapes, dtypes and devices are rejected
+ * with an error instead of falling back.  Each sample's results are bitwise
+ * identical whether it runs alone or packed with other samples, and from run
+ * to run (same page, rollout-vs-train control).
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ * - Tensors are caller-owned DEVICE memory on the current CUDA device, except
+ *   where a comment says otherwise.  The library never frees them.
+ * - bf16 tensors q, k, v, out, dout, dq, dk, dv are token-major and contiguous:
+ *   element (token i, head h, channel c) sits at index (i * H + h) * 128 + c.
+ *   Every tensor pointer must be 16-byte aligned.
+ * - pos_ids[0..2] are int32 [total_tokens] arrays of the t, h and w position of
+ *   each token.  seg_offsets is int32 [num_samples + 1]: 0, then strictly
+ *   increasing sample ends, the last equal to total_tokens.  Sample s owns
+ *   tokens [seg_offsets[s], seg_offsets[s + 1]).  Both are read on the device.
+ * - lse is float32 [H, total_tokens]: lse[h * S + i] = log sum_j exp(scale q^_i.k^_j).
+ * - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *   stream) and is asynchronous.  A handle must not be used by two streams at
+ *   the same time (it owns one workspace).
+ * - Errors found on the host (bad arguments, capacity, unsupported config)
+ *   return immediately and enqueue nothing.  Errors found on the device (an
+ *   invalid seg_offsets array, a bounded wait that timed out) are recorded in
+ *   the handle and returned by h3attn_device_status().
+ */
+#ifndef H3ATTN_H
+#define H3ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct h3attn_ctx *h3attn_t;
+
+/* IEEE bfloat16 bit pattern. */
+typedef uint16_t h3attn_bf16;
+
+typedef enum {
+    H3ATTN_OK = 0,
+    H3ATTN_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad sizes, bad offsets */
+    H3ATTN_ERR_UNSUPPORTED = 2,  /* head_dim != 128, unsupported RoPE layout, device not sm_103 */
+    H3ATTN_ERR_CAPACITY = 3,     /* total_tokens > max_tokens or num_samples > max_samples */
+    H3ATTN_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed */
+    H3ATTN_ERR_TIMEOUT = 5       /* a bounded on-device wait expired (kernel returned early) */
+} h3attn_status;
+
+typedef struct {
+    int num_heads;         /* H, heads of q, k and v (no grouped heads), >= 1           */
+    int head_dim;          /* must be 128                                               */
+    float eps;             /* RMSNorm epsilon, added to the mean square inside the sqrt */
+    float rope_theta;      /* RoPE base, e.g. 10000                                     */
+    int rope_sections[3];  /* rotary channels of the t, h, w axes, in that order from
+                              channel 0; each a multiple of 8, sum <= 128; channels
+                              past the sum are not rotated.  e.g. {16, 24, 24}         */
+    int rope_pairing;      /* 0 = rotate-half inside each section (the only one)        */
+    float softmax_scale;   /* 0 -> 1/sqrt(128)                                          */
+    int max_tokens;        /* capacity: largest total_tokens of any call                */
+    int max_samples;       /* capacity: largest num_samples of any call                 */
+} h3attn_config;
+
+/*
+ * Creates a handle on the current CUDA device and allocates its workspace
+ * (rotated q^/k^ buffers of max_tokens * H * 128 bf16 each, softmax row terms,
+ * weight-gradient partials, a small per-call plan).  The workspace is bounded
+ * by the config, never by the inputs.  *out receives the handle.
+ * Errors: INVALID_ARG (null pointer, sizes < 1), UNSUPPORTED (head_dim,
+ * pairing, sections, device not sm_103), CUDA (allocation failed).
+ */
+h3attn_status h3attn_create(const h3attn_config *cfg, h3attn_t *out);
+
+/* Frees the workspace and the handle (synchronises the device first). NULL is OK. */
+h3attn_status h3attn_destroy(h3attn_t h);
+
+/*
+ * Forward: out = attention(RoPE(RMSNorm(q) w_q), RoPE(RMSNorm(k) w_k), v) per sample.
+ * q, k, v: bf16 [S, H, 128]; q_norm_w, k_norm_w: float32 [128]; out: bf16 [S, H, 128]
+ * (written for every token); lse: float32 [H, S] or NULL (not needed for
+ * inference, required by h3attn_backward).
+ * total_tokens == 0 is a no-op.  Errors: INVALID_ARG, CAPACITY, CUDA.
+ */
+h3attn_status h3attn_forward(h3attn_t h,
+                             const h3attn_bf16 *q, const h3attn_bf16 *k, const h3attn_bf16 *v,
+                             const float *q_norm_w, const float *k_norm_w,
+                             const int32_t *const pos_ids[3], const int32_t *seg_offsets,
+                             int num_samples, int total_tokens,
+                             h3attn_bf16 *out, float *lse, void *stream);
+
+/*
+ * Backward of sum(out * dout) through attention, RoPE and RMSNorm.
+ * Inputs as in h3attn_forward plus out (bf16 [S, H, 128]) and lse (float32
+ * [H, S]) from the forward of the same inputs, and dout (bf16 [S, H, 128]).
+ * Outputs: dq, dk, dv bf16 [S, H, 128]; dq_norm_w, dk_norm_w float32 [128]
+ * (overwritten with the sum over all tokens and heads, samples added in index
+ * order); dq_norm_w_per_sample, dk_norm_w_per_sample float32 [num_samples, 128]
+ * or NULL (per-sample sums; these, like dq/dk/dv, are identical whether a sample
+ * runs alone or packed).  All reductions run in a fixed order, no atomics.
+ * Errors: INVALID_ARG, CAPACITY, CUDA.
+ */
+h3attn_status h3attn_backward(h3attn_t h,
+                              const h3attn_bf16 *q, const h3attn_bf16 *k, const h3attn_bf16 *v,
+                              const float *q_norm_w, const float *k_norm_w,
+                              const int32_t *const pos_ids[3], const int32_t *seg_offsets,
+                              int num_samples, int total_tokens,
+                              const h3attn_bf16 *out, const float *lse, const h3attn_bf16 *dout,
+                              h3attn_bf16 *dq, h3attn_bf16 *dk, h3attn_bf16 *dv,
+                              float *dq_norm_w, float *dk_norm_w,
+                              float *dq_norm_w_per_sample, float *dk_norm_w_per_sample,
+                              void *stream);
+
+/*
+ * Waits for `stream`, then returns and clears the errors the device recorded
+ * since the last call: INVALID_ARG (seg_offsets not 0 / increasing / ending at
+ * total_tokens; outputs of that call are unspecified), TIMEOUT (a bounded wait
+ * expired; outputs unspecified), CUDA (an asynchronous CUDA error), else OK.
+ */
+h3attn_status h3attn_device_status(h3attn_t h, void *stream);
+
+/*
+ * Per-stage GPU time, for profiling (instrumentation; not part of the method).
+ * When enabled, every launch of a stage is bracketed by CUDA events on the call's
+ * stream (about 2 x 7 events per forward + backward; up to 4096 per handle,
+ * later launches are not timed).  h3attn_stage_times() waits for those events,
+ * writes the summed milliseconds and launch counts of each stage (arrays of
+ * n_stages, stage order below) and resets the record.  Events are created on
+ * first use.  Errors: INVALID_ARG, CUDA.
+ */
+enum {
+    H3ATTN_STAGE_PLAN = 0,      /* seg_offsets check + sample order            */
+    H3ATTN_STAGE_PROLOGUE = 1,  /* q/k RMSNorm + RoPE -> q^, k^                */
+    H3ATTN_STAGE_FWD = 2,       /* QK^T, online softmax, PV, lse               */
+    H3ATTN_STAGE_BWD_DELTA = 3, /* rowsum(dO * O)                              */
+    H3ATTN_STAGE_BWD_DKDV = 4,  /* dK (through RoPE/RMSNorm), dV               */
+    H3ATTN_STAGE_BWD_DQ = 5,    /* dQ (through RoPE/RMSNorm)                   */
+    H3ATTN_STAGE_BWD_DW = 6,    /* fixed-order norm-weight gradient reduction  */
+    H3ATTN_NUM_STAGES = 7
+};
+h3attn_status h3attn_set_stage_timing(h3attn_t h, int enable);
+h3attn_status h3attn_stage_times(h3attn_t h, float *total_ms, int *launches, int n_stages);
+
+/* Static, human-readable name of a status code. */
+const char *h3attn_status_string(h3attn_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* H3ATTN_H */

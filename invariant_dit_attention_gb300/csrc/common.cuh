@@ -1,0 +1,142 @@
+// common.cuh -- shared device helpers and launch parameters of libh3attn.
+//
+// Layout conventions (all kernels): bf16 tensors are token-major [S, H, 128];
+// element (i, h, c) sits at (i * H + h) * 128 + c.  Samples are addressed by
+// the segment offsets; every tile of queries or keys is anchored at its sample's
+// first token, never at a global tile boundary, so that a sample's arithmetic
+// is the same whether it runs alone or packed with others.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace h3 {
+
+constexpr int kD = 128;  // head dim
+
+// Bits of the device error word.
+constexpr unsigned kErrBadOffsets = 1u;
+constexpr unsigned kErrTimeout = 2u;
+
+// Rotary layout, per channel group of 4 (lane l of a warp owns channels 4l..4l+3).
+// A section of n channels pairs channel o+j with o+j+n/2, so with n a multiple
+// of 8 the partner of a group is another whole group.
+struct RopeTable {
+    float inv_freq[kD];       // frequency of the pair channel c belongs to (0 if not rotated)
+    int8_t axis[32];          // 0/1/2 = t/h/w, -1 = not rotated
+    int8_t partner[32];       // lane holding the paired channels
+    int8_t second[32];        // 1 if this group is the second half of its section
+};
+
+// Per-call plan written on the device from seg_offsets: samples ordered by
+// decreasing length (ties by index) and cumulative tile counts in that order.
+struct Plan {
+    int* order;      // [max_samples] sample index of rank r
+    int* cum64;      // [max_samples + 1] tiles of 64 tokens before rank r
+    int* cum128;     // [max_samples + 1] tiles of 128 tokens before rank r
+    int* rank_of;    // [max_samples] rank of sample s
+    unsigned* err;   // device error word
+};
+
+struct Seq {
+    const int32_t* seg;   // [n + 1] offsets
+    const int32_t* pos_t;
+    const int32_t* pos_h;
+    const int32_t* pos_w;
+    int n;                // samples
+    int S;                // tokens
+};
+
+// ---------------------------------------------------------------- helpers
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);  // round to nearest even
+    return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// 2^x on the SFU (MUFU.EX2); results below 2^-126 flush to zero.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+    // fixed butterfly: every lane ends with the same, order-fixed sum
+    v += __shfl_xor_sync(0xffffffffu, v, 16);
+    v += __shfl_xor_sync(0xffffffffu, v, 8);
+    v += __shfl_xor_sync(0xffffffffu, v, 4);
+    v += __shfl_xor_sync(0xffffffffu, v, 2);
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    return v;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Maps a tile index of the plan (tiles of `tile` tokens, samples in rank order)
+// to its sample and the tile's first token.  Returns false past the last tile.
+__device__ __forceinline__ bool plan_tile(const int* __restrict__ cum, const int* __restrict__ order,
+                                          const int32_t* __restrict__ seg, int n, int tile, int t,
+                                          int& sample, int& row0, int& row_end, int& local) {
+    if (t >= cum[n]) return false;
+    int lo = 0, hi = n;  // find rank r with cum[r] <= t < cum[r+1]
+    while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if (cum[mid] <= t) lo = mid; else hi = mid;
+    }
+    sample = order[lo];
+    local = t - cum[lo];
+    row0 = seg[sample] + local * tile;
+    row_end = seg[sample + 1];
+    return true;
+}
+
+// ------------------------------------------------------- launch interface
+
+struct Workspace {
+    __nv_bfloat16* qhat;     // [max_tokens, H, 128]
+    __nv_bfloat16* khat;     // [max_tokens, H, 128]
+    float* delta;            // [H, max_tokens]
+    float* dwq_part;         // [max_tiles64, H, 128]
+    float* dwk_part;         // [max_tiles64, H, 128]
+    float* dwq_sample;       // [max_samples, 128]
+    float* dwk_sample;       // [max_samples, 128]
+    Plan plan;
+};
+
+struct Problem {
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* v;
+    const float* wq;
+    const float* wk;
+    Seq seq;
+    int H;
+    float eps;
+    float scale;
+};
+
+// Stages of one call, in launch order (timed separately when stage timing is on).
+enum Stage { kStagePlan = 0, kStagePrologue, kStageFwd, kStageDelta, kStageDkdv, kStageDq, kStageDw, kStages };
+
+cudaError_t init_fwd_attributes();
+cudaError_t init_bwd_attributes();
+cudaError_t launch_plan(const Problem& p, const Workspace& ws, cudaStream_t st);
+cudaError_t launch_prologue(const Problem& p, const Workspace& ws, const RopeTable* rope, cudaStream_t st);
+cudaError_t launch_fwd(const Problem& p, const Workspace& ws, __nv_bfloat16* out, float* lse, cudaStream_t st);
+cudaError_t launch_bwd_delta(const Problem& p, const Workspace& ws, const __nv_bfloat16* out,
+                             const __nv_bfloat16* dout, cudaStream_t st);
+cudaError_t launch_bwd_dkdv(const Problem& p, const Workspace& ws, const RopeTable* rope, const float* lse,
+                            const __nv_bfloat16* dout, __nv_bfloat16* dk, __nv_bfloat16* dv, cudaStream_t st);
+cudaError_t launch_bwd_dq(const Problem& p, const Workspace& ws, const RopeTable* rope, const float* lse,
+                          const __nv_bfloat16* dout, __nv_bfloat16* dq, cudaStream_t st);
+cudaError_t launch_bwd_dw(const Problem& p, const Workspace& ws, float* dwq, float* dwk, float* dwq_s,
+                          float* dwk_s, cudaStream_t st);
+
+}  // namespace h3

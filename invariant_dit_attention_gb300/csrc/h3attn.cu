@@ -1,0 +1,303 @@
+// h3attn.cu -- the C ABI (include/h3attn.h): argument checks, workspace, launches.
+//
+// Strict contract of the "ws1_full_h3_transformer" page (RL-Kernel PR #571),
+// Scope / Known limitations: unsupported shapes, dtypes and devices are
+// rejected with an error code, never run through another path.
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "../../include/h3attn.h"
+#include "common.cuh"
+
+using namespace h3;
+
+static constexpr int kMaxEvents = 4096;
+
+struct h3attn_ctx {
+    h3attn_config cfg;
+    int device;
+    RopeTable rope;
+    Workspace ws;
+    int max_tiles64;
+    unsigned* host_err;  // pinned
+    void* allocs[16];
+    int nalloc;
+    // stage timing (instrumentation)
+    int timing;
+    cudaEvent_t* events;  // kMaxEvents, created on first use
+    int ev_used;
+    int ev_stage[kMaxEvents / 2];
+};
+
+namespace {
+
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+h3attn_status build_rope(const h3attn_config& c, RopeTable& rt) {
+    memset(&rt, 0, sizeof rt);
+    for (int g = 0; g < 32; ++g) { rt.axis[g] = -1; rt.partner[g] = (int8_t)g; rt.second[g] = 0; }
+    int off = 0;
+    for (int a = 0; a < 3; ++a) {
+        const int n = c.rope_sections[a];
+        if (n < 0 || n % 8 != 0 || off + n > kD) return H3ATTN_ERR_UNSUPPORTED;
+        const int half = n / 2;
+        for (int j = 0; j < half; ++j) {
+            // frequency of pair j of an n-channel axis: theta^(-2j/n)
+            const float f = (float)pow((double)c.rope_theta, -2.0 * j / (double)n);
+            rt.inv_freq[off + j] = f;
+            rt.inv_freq[off + j + half] = f;
+        }
+        for (int grp = off / 4; grp < (off + n) / 4; ++grp) {
+            const bool second = grp * 4 - off >= half;
+            rt.axis[grp] = (int8_t)a;
+            rt.second[grp] = second ? 1 : 0;
+            rt.partner[grp] = (int8_t)(second ? grp - half / 4 : grp + half / 4);
+        }
+        off += n;
+    }
+    return H3ATTN_OK;
+}
+
+template <class T>
+bool ws_alloc(h3attn_ctx* h, T** p, size_t bytes) {
+    void* d = nullptr;
+    if (cudaMalloc(&d, bytes < 256 ? 256 : bytes) != cudaSuccess) return false;
+    h->allocs[h->nalloc++] = d;
+    *p = reinterpret_cast<T*>(d);
+    return true;
+}
+
+void free_ctx(h3attn_ctx* h) {
+    if (h->events) {
+        for (int i = 0; i < kMaxEvents; ++i) cudaEventDestroy(h->events[i]);
+        free(h->events);
+    }
+    for (int i = 0; i < h->nalloc; ++i) cudaFree(h->allocs[i]);
+    if (h->host_err) cudaFreeHost(h->host_err);
+    free(h);
+}
+
+// Checks shared by forward and backward.
+h3attn_status check_common(h3attn_t h, const void* q, const void* k, const void* v, const float* wq,
+                           const float* wk, const int32_t* const pos_ids[3], const int32_t* seg,
+                           int num_samples, int total_tokens) {
+    if (!h) return H3ATTN_ERR_INVALID_ARG;
+    if (total_tokens < 0 || num_samples < 0) return H3ATTN_ERR_INVALID_ARG;
+    if (total_tokens == 0) return H3ATTN_OK;
+    if (num_samples < 1 || num_samples > total_tokens) return H3ATTN_ERR_INVALID_ARG;
+    if (total_tokens > h->cfg.max_tokens || num_samples > h->cfg.max_samples) return H3ATTN_ERR_CAPACITY;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(wq) || !aligned16(wk))
+        return H3ATTN_ERR_INVALID_ARG;
+    if (!pos_ids || !aligned4(pos_ids[0]) || !aligned4(pos_ids[1]) || !aligned4(pos_ids[2]) || !aligned4(seg))
+        return H3ATTN_ERR_INVALID_ARG;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return H3ATTN_ERR_CUDA;
+    if (dev != h->device) return H3ATTN_ERR_INVALID_ARG;
+    return H3ATTN_OK;
+}
+
+Problem make_problem(h3attn_t h, const void* q, const void* k, const void* v, const float* wq, const float* wk,
+                     const int32_t* const pos_ids[3], const int32_t* seg, int n, int S) {
+    Problem p;
+    p.q = reinterpret_cast<const __nv_bfloat16*>(q);
+    p.k = reinterpret_cast<const __nv_bfloat16*>(k);
+    p.v = reinterpret_cast<const __nv_bfloat16*>(v);
+    p.wq = wq;
+    p.wk = wk;
+    p.seq.seg = seg;
+    p.seq.pos_t = pos_ids[0];
+    p.seq.pos_h = pos_ids[1];
+    p.seq.pos_w = pos_ids[2];
+    p.seq.n = n;
+    p.seq.S = S;
+    p.H = h->cfg.num_heads;
+    p.eps = h->cfg.eps;
+    p.scale = h->cfg.softmax_scale;
+    return p;
+}
+
+// Runs one stage's launches, bracketed by events when stage timing is on.
+template <class F>
+cudaError_t stage(h3attn_ctx* h, int which, cudaStream_t s, F&& launch) {
+    const bool rec = h->timing && h->events && h->ev_used + 2 <= kMaxEvents;
+    if (rec && cudaEventRecord(h->events[h->ev_used], s) != cudaSuccess) return cudaErrorUnknown;
+    cudaError_t e = launch();
+    if (e != cudaSuccess) return e;
+    if (rec) {
+        if (cudaEventRecord(h->events[h->ev_used + 1], s) != cudaSuccess) return cudaErrorUnknown;
+        h->ev_stage[h->ev_used / 2] = which;
+        h->ev_used += 2;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* h3attn_status_string(h3attn_status s) {
+    switch (s) {
+        case H3ATTN_OK: return "ok";
+        case H3ATTN_ERR_INVALID_ARG: return "invalid argument";
+        case H3ATTN_ERR_UNSUPPORTED: return "unsupported configuration or device";
+        case H3ATTN_ERR_CAPACITY: return "exceeds the handle's capacity";
+        case H3ATTN_ERR_CUDA: return "CUDA error";
+        case H3ATTN_ERR_TIMEOUT: return "on-device wait timed out";
+    }
+    return "unknown status";
+}
+
+h3attn_status h3attn_create(const h3attn_config* cfg, h3attn_t* out) {
+    if (!cfg || !out) return H3ATTN_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (cfg->num_heads < 1 || cfg->max_tokens < 1 || cfg->max_samples < 1) return H3ATTN_ERR_INVALID_ARG;
+    if (!(cfg->eps >= 0.f) || !(cfg->rope_theta > 0.f) || !(cfg->softmax_scale >= 0.f)) return H3ATTN_ERR_INVALID_ARG;
+    if (cfg->head_dim != kD || cfg->rope_pairing != 0) return H3ATTN_ERR_UNSUPPORTED;
+    if ((long)cfg->max_tokens * cfg->num_heads * kD >= (1L << 40)) return H3ATTN_ERR_CAPACITY;
+    RopeTable rt;
+    if (build_rope(*cfg, rt) != H3ATTN_OK) return H3ATTN_ERR_UNSUPPORTED;
+    int dev = 0;
+    cudaDeviceProp prop;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaGetDeviceProperties(&prop, dev) != cudaSuccess)
+        return H3ATTN_ERR_CUDA;
+    if (!(prop.major == 10 && prop.minor == 3)) return H3ATTN_ERR_UNSUPPORTED;
+
+    h3attn_ctx* h = static_cast<h3attn_ctx*>(calloc(1, sizeof(h3attn_ctx)));
+    if (!h) return H3ATTN_ERR_CUDA;
+    h->cfg = *cfg;
+    if (h->cfg.softmax_scale == 0.f) h->cfg.softmax_scale = 1.0f / sqrtf((float)kD);
+    h->device = dev;
+    h->rope = rt;
+    const size_t H = cfg->num_heads, T = cfg->max_tokens, N = cfg->max_samples;
+    h->max_tiles64 = (int)((T + 63) / 64 + N);
+    Workspace& ws = h->ws;
+    bool ok = ws_alloc(h, &ws.qhat, T * H * kD * 2) && ws_alloc(h, &ws.khat, T * H * kD * 2) &&
+              ws_alloc(h, &ws.delta, T * H * 4) &&
+              ws_alloc(h, &ws.dwq_part, (size_t)h->max_tiles64 * H * kD * 4) &&
+              ws_alloc(h, &ws.dwk_part, (size_t)h->max_tiles64 * H * kD * 4) &&
+              ws_alloc(h, &ws.dwq_sample, N * kD * 4) && ws_alloc(h, &ws.dwk_sample, N * kD * 4) &&
+              ws_alloc(h, &ws.plan.order, N * 4) && ws_alloc(h, &ws.plan.rank_of, N * 4) &&
+              ws_alloc(h, &ws.plan.cum64, (N + 1) * 4) && ws_alloc(h, &ws.plan.cum128, (N + 1) * 4) &&
+              ws_alloc(h, &ws.plan.err, 4);
+    if (ok) ok = cudaMemset(ws.plan.err, 0, 4) == cudaSuccess;
+    if (ok) ok = cudaMallocHost(&h->host_err, 4) == cudaSuccess;
+    if (ok) ok = init_fwd_attributes() == cudaSuccess && init_bwd_attributes() == cudaSuccess;
+    if (ok) ok = cudaDeviceSynchronize() == cudaSuccess;
+    if (!ok) {
+        free_ctx(h);
+        return H3ATTN_ERR_CUDA;
+    }
+    *out = h;
+    return H3ATTN_OK;
+}
+
+h3attn_status h3attn_destroy(h3attn_t h) {
+    if (!h) return H3ATTN_OK;
+    cudaDeviceSynchronize();
+    free_ctx(h);
+    return H3ATTN_OK;
+}
+
+h3attn_status h3attn_forward(h3attn_t h, const h3attn_bf16* q, const h3attn_bf16* k, const h3attn_bf16* v,
+                             const float* q_norm_w, const float* k_norm_w, const int32_t* const pos_ids[3],
+                             const int32_t* seg_offsets, int num_samples, int total_tokens, h3attn_bf16* out,
+                             float* lse, void* stream) {
+    h3attn_status st = check_common(h, q, k, v, q_norm_w, k_norm_w, pos_ids, seg_offsets, num_samples, total_tokens);
+    if (st != H3ATTN_OK || total_tokens == 0) return st;
+    if (!aligned16(out) || (lse && !aligned4(lse))) return H3ATTN_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Problem p = make_problem(h, q, k, v, q_norm_w, k_norm_w, pos_ids, seg_offsets, num_samples, total_tokens);
+    Workspace& ws = h->ws;
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out);
+    if (stage(h, kStagePlan, s, [&] { return launch_plan(p, ws, s); }) != cudaSuccess ||
+        stage(h, kStagePrologue, s, [&] { return launch_prologue(p, ws, &h->rope, s); }) != cudaSuccess ||
+        stage(h, kStageFwd, s, [&] { return launch_fwd(p, ws, o, lse, s); }) != cudaSuccess)
+        return H3ATTN_ERR_CUDA;
+    return H3ATTN_OK;
+}
+
+h3attn_status h3attn_backward(h3attn_t h, const h3attn_bf16* q, const h3attn_bf16* k, const h3attn_bf16* v,
+                              const float* q_norm_w, const float* k_norm_w, const int32_t* const pos_ids[3],
+                              const int32_t* seg_offsets, int num_samples, int total_tokens, const h3attn_bf16* out,
+                              const float* lse, const h3attn_bf16* dout, h3attn_bf16* dq, h3attn_bf16* dk,
+                              h3attn_bf16* dv, float* dq_norm_w, float* dk_norm_w, float* dq_norm_w_per_sample,
+                              float* dk_norm_w_per_sample, void* stream) {
+    h3attn_status st = check_common(h, q, k, v, q_norm_w, k_norm_w, pos_ids, seg_offsets, num_samples, total_tokens);
+    if (st != H3ATTN_OK) return st;
+    if (!aligned4(dq_norm_w) || !aligned4(dk_norm_w)) return H3ATTN_ERR_INVALID_ARG;
+    if ((dq_norm_w_per_sample && !aligned4(dq_norm_w_per_sample)) ||
+        (dk_norm_w_per_sample && !aligned4(dk_norm_w_per_sample)))
+        return H3ATTN_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (total_tokens == 0) {  // empty batch: the weight gradients are zero
+        if (cudaMemsetAsync(dq_norm_w, 0, kD * 4, s) != cudaSuccess ||
+            cudaMemsetAsync(dk_norm_w, 0, kD * 4, s) != cudaSuccess)
+            return H3ATTN_ERR_CUDA;
+        return H3ATTN_OK;
+    }
+    if (!aligned16(out) || !aligned4(lse) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return H3ATTN_ERR_INVALID_ARG;
+    Problem p = make_problem(h, q, k, v, q_norm_w, k_norm_w, pos_ids, seg_offsets, num_samples, total_tokens);
+    Workspace& ws = h->ws;
+    const __nv_bfloat16* o = reinterpret_cast<const __nv_bfloat16*>(out);
+    const __nv_bfloat16* dO = reinterpret_cast<const __nv_bfloat16*>(dout);
+    __nv_bfloat16* gq = reinterpret_cast<__nv_bfloat16*>(dq);
+    __nv_bfloat16* gk = reinterpret_cast<__nv_bfloat16*>(dk);
+    __nv_bfloat16* gv = reinterpret_cast<__nv_bfloat16*>(dv);
+    if (stage(h, kStagePlan, s, [&] { return launch_plan(p, ws, s); }) != cudaSuccess ||
+        stage(h, kStagePrologue, s, [&] { return launch_prologue(p, ws, &h->rope, s); }) != cudaSuccess ||
+        stage(h, kStageDelta, s, [&] { return launch_bwd_delta(p, ws, o, dO, s); }) != cudaSuccess ||
+        stage(h, kStageDkdv, s, [&] { return launch_bwd_dkdv(p, ws, &h->rope, lse, dO, gk, gv, s); }) != cudaSuccess ||
+        stage(h, kStageDq, s, [&] { return launch_bwd_dq(p, ws, &h->rope, lse, dO, gq, s); }) != cudaSuccess ||
+        stage(h, kStageDw, s, [&] {
+            return launch_bwd_dw(p, ws, dq_norm_w, dk_norm_w, dq_norm_w_per_sample, dk_norm_w_per_sample, s);
+        }) != cudaSuccess)
+        return H3ATTN_ERR_CUDA;
+    return H3ATTN_OK;
+}
+
+h3attn_status h3attn_set_stage_timing(h3attn_t h, int enable) {
+    if (!h) return H3ATTN_ERR_INVALID_ARG;
+    if (enable && !h->events) {
+        h->events = static_cast<cudaEvent_t*>(calloc(kMaxEvents, sizeof(cudaEvent_t)));
+        if (!h->events) return H3ATTN_ERR_CUDA;
+        for (int i = 0; i < kMaxEvents; ++i)
+            if (cudaEventCreate(&h->events[i]) != cudaSuccess) return H3ATTN_ERR_CUDA;
+    }
+    h->timing = enable ? 1 : 0;
+    return H3ATTN_OK;
+}
+
+h3attn_status h3attn_stage_times(h3attn_t h, float* total_ms, int* launches, int n_stages) {
+    if (!h || !total_ms || !launches || n_stages < 1) return H3ATTN_ERR_INVALID_ARG;
+    for (int i = 0; i < n_stages; ++i) { total_ms[i] = 0.f; launches[i] = 0; }
+    if (h->ev_used && cudaEventSynchronize(h->events[h->ev_used - 1]) != cudaSuccess) return H3ATTN_ERR_CUDA;
+    for (int k = 0; k < h->ev_used / 2; ++k) {
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, h->events[2 * k], h->events[2 * k + 1]) != cudaSuccess) return H3ATTN_ERR_CUDA;
+        const int st = h->ev_stage[k];
+        if (st < n_stages) { total_ms[st] += ms; launches[st] += 1; }
+    }
+    h->ev_used = 0;
+    return H3ATTN_OK;
+}
+
+h3attn_status h3attn_device_status(h3attn_t h, void* stream) {
+    if (!h) return H3ATTN_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(h->host_err, h->ws.plan.err, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return H3ATTN_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return H3ATTN_ERR_CUDA;
+    const unsigned e = *h->host_err;
+    if (e) {
+        if (cudaMemsetAsync(h->ws.plan.err, 0, 4, s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+            return H3ATTN_ERR_CUDA;
+    }
+    if (e & kErrTimeout) return H3ATTN_ERR_TIMEOUT;
+    if (e & kErrBadOffsets) return H3ATTN_ERR_INVALID_ARG;
+    return H3ATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,120 @@
+// rowops.cuh -- per-(token, head) q/k prologue and its backward, one warp per row.
+//
+// Lane l of the warp owns channels 4l..4l+3 of the 128-wide head.
+//
+// Forward (q_norm/k_norm then rope_q/rope_k of an H3 block, "ws1_one_h3_block"
+// page, Bindings table):
+//   n = x / sqrt(mean_c x_c^2 + eps),  z = n * w,
+//   for a rotated pair (u, v) = (z[o+j], z[o+j+n_a/2]) with angle a = p_axis * f_j:
+//   (u, v) -> (u cos a - v sin a, u sin a + v cos a); other channels unchanged.
+// All of it in FP32 with one final rounding to bf16.
+//
+// Backward, for the gradient dy at the rotated output:
+//   g = R(a)^T dy,  dn = g * w,  dx = r (dn - n mean_c(dn_c n_c)),  dw += g * n,
+// with r = 1/sqrt(mean x^2 + eps) recomputed from x.
+#pragma once
+
+#include "common.cuh"
+
+namespace h3 {
+
+struct RowAngles {
+    float c[4], s[4];
+};
+
+// cos/sin of the lane's four channels for one token (identity if not rotated).
+__device__ __forceinline__ RowAngles row_angles(const RopeTable& rt, int lane, int pt, int ph, int pw) {
+    RowAngles a;
+    int ax = rt.axis[lane];
+    if (ax < 0) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) { a.c[e] = 1.f; a.s[e] = 0.f; }
+        return a;
+    }
+    float p = static_cast<float>(ax == 0 ? pt : (ax == 1 ? ph : pw));
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        float ang = p * rt.inv_freq[4 * lane + e];
+        sincosf(ang, &a.s[e], &a.c[e]);
+    }
+    return a;
+}
+
+// 1/sqrt(mean of squares + eps) of the row held 4 channels per lane.
+__device__ __forceinline__ float row_rstd(const float (&x)[4], float eps) {
+    float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
+    ss = warp_sum(ss);
+    return 1.0f / sqrtf(ss * (1.0f / kD) + eps);
+}
+
+// y = RoPE(RMSNorm(x) * w) for one row.
+__device__ __forceinline__ void row_norm_rope(const float (&x)[4], const float (&w)[4], const RowAngles& a,
+                                              const RopeTable& rt, int lane, float eps, float (&y)[4]) {
+    float r = row_rstd(x, eps);
+    float z[4], zp[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) z[e] = (x[e] * r) * w[e];
+    int partner = rt.partner[lane];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) zp[e] = __shfl_sync(0xffffffffu, z[e], partner);
+    if (rt.axis[lane] < 0) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) y[e] = z[e];
+    } else if (!rt.second[lane]) {  // (u, v) = (own, partner): u cos - v sin
+#pragma unroll
+        for (int e = 0; e < 4; ++e) y[e] = z[e] * a.c[e] - zp[e] * a.s[e];
+    } else {                         // (u, v) = (partner, own): u sin + v cos
+#pragma unroll
+        for (int e = 0; e < 4; ++e) y[e] = zp[e] * a.s[e] + z[e] * a.c[e];
+    }
+}
+
+// Backward of row_norm_rope.  dy: gradient at the rotated output; x: the raw
+// input row.  Writes dx and adds g*n into dw_acc.
+__device__ __forceinline__ void row_norm_rope_bwd(const float (&dy)[4], const float (&x)[4], const float (&w)[4],
+                                                  const RowAngles& a, const RopeTable& rt, int lane, float eps,
+                                                  float (&dx)[4], float (&dw_acc)[4]) {
+    float dyp[4], g[4];
+    int partner = rt.partner[lane];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) dyp[e] = __shfl_sync(0xffffffffu, dy[e], partner);
+    if (rt.axis[lane] < 0) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) g[e] = dy[e];
+    } else if (!rt.second[lane]) {  // g_u = dy_u cos + dy_v sin
+#pragma unroll
+        for (int e = 0; e < 4; ++e) g[e] = dy[e] * a.c[e] + dyp[e] * a.s[e];
+    } else {                         // g_v = -dy_u sin + dy_v cos
+#pragma unroll
+        for (int e = 0; e < 4; ++e) g[e] = dy[e] * a.c[e] - dyp[e] * a.s[e];
+    }
+    float r = row_rstd(x, eps);
+    float n[4], dn[4];
+    float t = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        n[e] = x[e] * r;
+        dn[e] = g[e] * w[e];
+        t += dn[e] * n[e];
+    }
+    t = warp_sum(t) * (1.0f / kD);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        dx[e] = r * (dn[e] - n[e] * t);
+        dw_acc[e] += g[e] * n[e];
+    }
+}
+
+__device__ __forceinline__ void load_row4(const __nv_bfloat16* p, float (&x)[4]) {
+    uint2 u = *reinterpret_cast<const uint2*>(p);
+    x[0] = bf16_lo(u.x); x[1] = bf16_hi(u.x); x[2] = bf16_lo(u.y); x[3] = bf16_hi(u.y);
+}
+
+__device__ __forceinline__ void store_row4(__nv_bfloat16* p, const float (&y)[4]) {
+    uint2 u;
+    u.x = pack_bf16(y[0], y[1]);
+    u.y = pack_bf16(y[2], y[3]);
+    *reinterpret_cast<uint2*>(p) = u;
+}
+
+}  // namespace h3

@@ -1,0 +1,193 @@
+"""Python binding of libh3attn.so (include/h3attn.h): argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels; this module
+passes device pointers of torch tensors and the current CUDA stream, and turns
+non-OK status codes into exceptions.  There is no fallback: if the library is
+missing or the device is not an sm_103 GPU, calls raise.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libh3attn.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CAPACITY, ERR_CUDA, ERR_TIMEOUT = range(6)
+
+# Entry points declared in include/h3attn.h.
+EXPORTS = ("h3attn_create", "h3attn_destroy", "h3attn_forward", "h3attn_backward",
+           "h3attn_device_status", "h3attn_set_stage_timing", "h3attn_stage_times", "h3attn_status_string")
+
+STAGES = ("plan", "prologue", "fwd", "bwd_delta", "bwd_dkdv", "bwd_dq", "bwd_dw")
+
+
+class H3AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("num_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("eps", ctypes.c_float),
+                ("rope_theta", ctypes.c_float), ("rope_sections", ctypes.c_int * 3),
+                ("rope_pairing", ctypes.c_int), ("softmax_scale", ctypes.c_float),
+                ("max_tokens", ctypes.c_int), ("max_samples", ctypes.c_int)]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Loads libh3attn.so (built by invariant_dit_attention_gb300.build)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"libh3attn.so not built at {path}; run invariant_dit_attention_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    vp, i32 = ctypes.c_void_p, ctypes.c_int
+    lib.h3attn_create.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(vp)]
+    lib.h3attn_create.restype = i32
+    lib.h3attn_destroy.argtypes = [vp]
+    lib.h3attn_destroy.restype = i32
+    lib.h3attn_forward.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.POINTER(vp), vp, i32, i32, vp, vp, vp]
+    lib.h3attn_forward.restype = i32
+    lib.h3attn_backward.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.POINTER(vp), vp, i32, i32, vp, vp, vp,
+                                    vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.h3attn_backward.restype = i32
+    lib.h3attn_device_status.argtypes = [vp, vp]
+    lib.h3attn_device_status.restype = i32
+    lib.h3attn_set_stage_timing.argtypes = [vp, i32]
+    lib.h3attn_set_stage_timing.restype = i32
+    lib.h3attn_stage_times.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(i32), i32]
+    lib.h3attn_stage_times.restype = i32
+    lib.h3attn_status_string.argtypes = [i32]
+    lib.h3attn_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().h3attn_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise H3AttnError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _pos_array(pos):
+    arr = (ctypes.c_void_p * 3)()
+    for a in range(3):
+        arr[a] = pos[a].data_ptr()
+    return arr
+
+
+class H3Attn:
+    """A handle of the library: configuration plus its bounded device workspace."""
+
+    def __init__(self, num_heads: int, max_tokens: int, max_samples: int = 64, eps: float = 1e-6,
+                 rope_theta: float = 10000.0, rope_sections=(16, 24, 24), softmax_scale: float = 0.0):
+        lib = load_library()
+        cfg = Config()
+        cfg.num_heads, cfg.head_dim, cfg.eps, cfg.rope_theta = num_heads, 128, eps, rope_theta
+        cfg.rope_sections[:] = list(rope_sections)
+        cfg.rope_pairing, cfg.softmax_scale = 0, softmax_scale
+        cfg.max_tokens, cfg.max_samples = max_tokens, max_samples
+        h = ctypes.c_void_p()
+        _check(lib.h3attn_create(ctypes.byref(cfg), ctypes.byref(h)), "h3attn_create")
+        self._h = h
+        self._lib = lib
+        self.num_heads = num_heads
+        self.scale = softmax_scale if softmax_scale else 1.0 / math.sqrt(128)
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            self._lib.h3attn_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def forward(self, q, k, v, q_norm_w, k_norm_w, pos, seg_offsets, num_samples=None,
+                out=None, lse=None, want_lse=True, stream=None):
+        """out = attention core forward; returns (out, lse or None). Tensors on the device."""
+        S, H = q.shape[0], q.shape[1]
+        n = int(seg_offsets.numel() - 1) if num_samples is None else num_samples
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None and want_lse:
+            lse = torch.empty((H, S), dtype=torch.float32, device=q.device)
+        st = self._lib.h3attn_forward(self._h, _ptr(q), _ptr(k), _ptr(v), _ptr(q_norm_w), _ptr(k_norm_w),
+                                      _pos_array(pos), _ptr(seg_offsets), n, S, _ptr(out), _ptr(lse),
+                                      _stream(stream))
+        _check(st, "h3attn_forward")
+        return out, lse
+
+    def backward(self, q, k, v, q_norm_w, k_norm_w, pos, seg_offsets, out, lse, dout, num_samples=None,
+                 grads=None, per_sample=True, stream=None):
+        """Returns a dict: dq, dk, dv, dq_norm_w, dk_norm_w (+ per-sample weight gradients)."""
+        S = q.shape[0]
+        n = int(seg_offsets.numel() - 1) if num_samples is None else num_samples
+        dev = q.device
+        if grads is None:
+            grads = {"dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
+                     "dq_norm_w": torch.empty(128, dtype=torch.float32, device=dev),
+                     "dk_norm_w": torch.empty(128, dtype=torch.float32, device=dev)}
+            if per_sample:
+                grads["dq_norm_w_per_sample"] = torch.empty((max(n, 1), 128), dtype=torch.float32, device=dev)
+                grads["dk_norm_w_per_sample"] = torch.empty((max(n, 1), 128), dtype=torch.float32, device=dev)
+        st = self._lib.h3attn_backward(self._h, _ptr(q), _ptr(k), _ptr(v), _ptr(q_norm_w), _ptr(k_norm_w),
+                                       _pos_array(pos), _ptr(seg_offsets), n, S, _ptr(out), _ptr(lse),
+                                       _ptr(dout), _ptr(grads["dq"]), _ptr(grads["dk"]), _ptr(grads["dv"]),
+                                       _ptr(grads["dq_norm_w"]), _ptr(grads["dk_norm_w"]),
+                                       _ptr(grads.get("dq_norm_w_per_sample")),
+                                       _ptr(grads.get("dk_norm_w_per_sample")), _stream(stream))
+        _check(st, "h3attn_backward")
+        return grads
+
+    def set_stage_timing(self, enable: bool):
+        _check(self._lib.h3attn_set_stage_timing(self._h, 1 if enable else 0), "h3attn_set_stage_timing")
+
+    def stage_times(self) -> dict:
+        """{stage: (total_ms, launches)} since the last read; waits for the recorded events."""
+        n = len(STAGES)
+        ms = (ctypes.c_float * n)()
+        cnt = (ctypes.c_int * n)()
+        _check(self._lib.h3attn_stage_times(self._h, ms, cnt, n), "h3attn_stage_times")
+        return {STAGES[i]: (float(ms[i]), int(cnt[i])) for i in range(n)}
+
+    def device_status(self, stream=None) -> int:
+        """Waits for the stream; returns (and clears) errors recorded on the device."""
+        return int(self._lib.h3attn_device_status(self._h, _stream(stream)))
+
+    def check(self, stream=None):
+        _check(self.device_status(stream), "device")
+
+
+def to_device(inp, device="cuda"):
+    """Moves a workloads.Inputs to the device (pos as three int32 arrays)."""
+    d = {"q": inp.q.to(device), "k": inp.k.to(device), "v": inp.v.to(device),
+         "q_norm_w": inp.q_norm_w.to(device), "k_norm_w": inp.k_norm_w.to(device),
+         "pos": [inp.pos[a].contiguous().to(device) for a in range(3)],
+         "seg_offsets": inp.seg_offsets.to(device)}
+    if inp.dout is not None:
+        d["dout"] = inp.dout.to(device)
+    return d
