@@ -310,10 +310,12 @@ def run_ours(args):
 
 
 def cpu_baseline(H):
-    """The FP64 oracle on the host cores: forward + backward of one 925-token sample."""
+    """The FP64 oracle on the host cores: forward + backward of one 4253-token
+    sample of the workload with a third of its heads (about 10-20 s of CPU work)."""
     import oracle
     w = W.WORKLOADS[WORKLOAD]
-    inp = W.make_inputs([W.S925], H, seed=w.seed + 1, with_grad=True)
+    H = max(1, H // 3)
+    inp = W.make_inputs([W.S4253], H, seed=w.seed + 1, with_grad=True)
     L = inp.total_tokens
     flops = 3.5 * 4.0 * H * 128 * L * L
     t0 = time.perf_counter()

@@ -10,8 +10,11 @@
 //   dq^_i = scale sum_j dS_ij k^_j                                  (K5, per query tile)
 // then the RoPE and RMSNorm backward in the epilogues of K4/K5, with per-tile
 // partial sums of the norm-weight gradients reduced in a fixed order (K6).
-// No atomics: K4 and K5 each recompute S and P, and every sum runs over tiles
-// anchored at the sample start in ascending order.
+// No atomics in any sum: K4 and K5 each recompute S and P, and every sum runs
+// over tiles anchored at the sample start in ascending order.  Operand types:
+// S = q^ k^T on fp16 (the prologue's rounding), dS rounded to fp16 for the
+// dq^ = dS k^ and dk^ = dS^T q^ products, P and dO (bf16) for dV, dO and v
+// (bf16) for dP.
 #include "common.cuh"
 #include "mma.cuh"
 #include "rowops.cuh"
@@ -81,7 +84,7 @@ __device__ __forceinline__ void norm_rope_bwd_tile(const float* stage, const __n
 // ------------------------------------------------------------------ K5: dQ
 
 __global__ void __launch_bounds__(bwdm::kThreads)
-dq_kernel(const __nv_bfloat16* __restrict__ qhat, const __nv_bfloat16* __restrict__ khat,
+dq_kernel(const __half* __restrict__ qhat, const __half* __restrict__ khat,
           const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ dout,
           const __nv_bfloat16* __restrict__ q, const float* __restrict__ wq,
           const float* __restrict__ lse, const float* __restrict__ delta, Seq seq, Plan plan, int H,
@@ -118,6 +121,7 @@ dq_kernel(const __nv_bfloat16* __restrict__ qhat, const __nv_bfloat16* __restric
 #pragma unroll
     for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     uint32_t qa[8][4], oa[8][4];
+    bool range_ok = true;
 
     for (int j = 0; j < nkv; ++j) {
         const int buf = j & 1;
@@ -146,8 +150,8 @@ dq_kernel(const __nv_bfloat16* __restrict__ qhat, const __nv_bfloat16* __restric
             for (int np = 0; np < 2; ++np) {
                 uint32_t b[4];
                 ldsm_b_nk(b, sK[buf], np * 16, kk, lane);
-                mma16816(s[2 * np], qa[kk], b[0], b[1]);
-                mma16816(s[2 * np + 1], qa[kk], b[2], b[3]);
+                mma16816_f16(s[2 * np], qa[kk], b[0], b[1]);
+                mma16816_f16(s[2 * np + 1], qa[kk], b[2], b[3]);
                 ldsm_b_nk(b, sV[buf], np * 16, kk, lane);
                 mma16816(dp[2 * np], oa[kk], b[0], b[1]);
                 mma16816(dp[2 * np + 1], oa[kk], b[2], b[3]);
@@ -164,9 +168,10 @@ dq_kernel(const __nv_bfloat16* __restrict__ qhat, const __nv_bfloat16* __restric
                 float p = ex2(fmaf(s[nt][e], scale_log2, -lse2[r]));
                 p = key < row_end ? p : 0.f;
                 ds[e] = p * (dp[nt][e] - dlt[r]);
+                range_ok &= !(fabsf(ds[e]) > 65504.f);
             }
-            da[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16(ds[0], ds[1]);
-            da[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16(ds[2], ds[3]);
+            da[nt >> 1][(nt & 1) * 2 + 0] = pack_f16(ds[0], ds[1]);
+            da[nt >> 1][(nt & 1) * 2 + 1] = pack_f16(ds[2], ds[3]);
         }
 #pragma unroll
         for (int kc = 0; kc < 2; ++kc)
@@ -174,8 +179,8 @@ dq_kernel(const __nv_bfloat16* __restrict__ qhat, const __nv_bfloat16* __restric
             for (int dpi = 0; dpi < 8; ++dpi) {
                 uint32_t b[4];
                 ldsm_b_kn(b, sK[buf], kc * 16, dpi * 16, lane);
-                mma16816(acc[2 * dpi], da[kc], b[0], b[1]);
-                mma16816(acc[2 * dpi + 1], da[kc], b[2], b[3]);
+                mma16816_f16(acc[2 * dpi], da[kc], b[0], b[1]);
+                mma16816_f16(acc[2 * dpi + 1], da[kc], b[2], b[3]);
             }
         __syncthreads();
     }
@@ -196,12 +201,13 @@ dq_kernel(const __nv_bfloat16* __restrict__ qhat, const __nv_bfloat16* __restric
     __syncthreads();
     norm_rope_bwd_tile(stage, q, wq, seq, H, h, row0, row_end, eps, rt, dq,
                        dw_part + ((size_t)blockIdx.x * H + h) * kD, red);
+    if (!range_ok) atomicOr(plan.err, kErrRange);
 }
 
 // ------------------------------------------------------------- K4: dK, dV
 
 __global__ void __launch_bounds__(bwdm::kThreads)
-dkdv_kernel(const __nv_bfloat16* __restrict__ qhat, const __nv_bfloat16* __restrict__ khat,
+dkdv_kernel(const __half* __restrict__ qhat, const __half* __restrict__ khat,
             const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ dout,
             const __nv_bfloat16* __restrict__ k, const float* __restrict__ wk,
             const float* __restrict__ lse, const float* __restrict__ delta, Seq seq, Plan plan, int H,
@@ -238,6 +244,7 @@ dkdv_kernel(const __nv_bfloat16* __restrict__ qhat, const __nv_bfloat16* __restr
     cp_async_commit();
 
     float adv[16][4], adk[16][4];
+    bool range_ok = true;
 #pragma unroll
     for (int i = 0; i < 16; ++i)
 #pragma unroll
@@ -266,8 +273,8 @@ dkdv_kernel(const __nv_bfloat16* __restrict__ qhat, const __nv_bfloat16* __restr
             for (int np = 0; np < 2; ++np) {
                 uint32_t b[4];
                 ldsm_b_nk(b, sQ[buf], np * 16, kk, lane);
-                mma16816(s[2 * np], ka, b[0], b[1]);
-                mma16816(s[2 * np + 1], ka, b[2], b[3]);
+                mma16816_f16(s[2 * np], ka, b[0], b[1]);
+                mma16816_f16(s[2 * np + 1], ka, b[2], b[3]);
                 ldsm_b_nk(b, sO[buf], np * 16, kk, lane);
                 mma16816(dp[2 * np], va, b[0], b[1]);
                 mma16816(dp[2 * np + 1], va, b[2], b[3]);
@@ -285,11 +292,12 @@ dkdv_kernel(const __nv_bfloat16* __restrict__ qhat, const __nv_bfloat16* __restr
                 pe = q0 + c < row_end ? pe : 0.f;
                 p[e] = pe;
                 ds[e] = pe * (dp[nt][e] - sL[2 * kStep + buf * kStep + c]);
+                range_ok &= !(fabsf(ds[e]) > 65504.f);
             }
             pa[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16(p[0], p[1]);
             pa[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16(p[2], p[3]);
-            da[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16(ds[0], ds[1]);
-            da[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16(ds[2], ds[3]);
+            da[nt >> 1][(nt & 1) * 2 + 0] = pack_f16(ds[0], ds[1]);
+            da[nt >> 1][(nt & 1) * 2 + 1] = pack_f16(ds[2], ds[3]);
         }
 #pragma unroll
         for (int kc = 0; kc < 2; ++kc)
@@ -300,8 +308,8 @@ dkdv_kernel(const __nv_bfloat16* __restrict__ qhat, const __nv_bfloat16* __restr
                 mma16816(adv[2 * dpi], pa[kc], b[0], b[1]);
                 mma16816(adv[2 * dpi + 1], pa[kc], b[2], b[3]);
                 ldsm_b_kn(b, sQ[buf], kc * 16, dpi * 16, lane);
-                mma16816(adk[2 * dpi], da[kc], b[0], b[1]);
-                mma16816(adk[2 * dpi + 1], da[kc], b[2], b[3]);
+                mma16816_f16(adk[2 * dpi], da[kc], b[0], b[1]);
+                mma16816_f16(adk[2 * dpi + 1], da[kc], b[2], b[3]);
             }
     }
     cp_async_wait<0>();
@@ -330,6 +338,7 @@ dkdv_kernel(const __nv_bfloat16* __restrict__ qhat, const __nv_bfloat16* __restr
     __syncthreads();
     norm_rope_bwd_tile(stage, k, wk, seq, H, h, row0, row_end, eps, rt, dk,
                        dw_part + ((size_t)blockIdx.x * H + h) * kD, red);
+    if (!range_ok) atomicOr(plan.err, kErrRange);
 }
 
 // ------------------------------------------------------------------ K6

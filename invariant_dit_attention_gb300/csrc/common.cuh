@@ -8,6 +8,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -18,6 +19,7 @@ constexpr int kD = 128;  // head dim
 // Bits of the device error word.
 constexpr unsigned kErrBadOffsets = 1u;
 constexpr unsigned kErrTimeout = 2u;
+constexpr unsigned kErrRange = 4u;  // a rotated q^/k^ or dS value left the fp16 range
 
 // Rotary layout, per channel group of 4 (lane l of a warp owns channels 4l..4l+3).
 // A section of n channels pairs channel o+j with o+j+n/2, so with n a multiple
@@ -55,6 +57,11 @@ __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v 
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);  // round to nearest even
+    return *reinterpret_cast<uint32_t*>(&r);
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 r = __floats2half2_rn(lo, hi);  // round to nearest even
     return *reinterpret_cast<uint32_t*>(&r);
 }
 
@@ -100,8 +107,8 @@ __device__ __forceinline__ bool plan_tile(const int* __restrict__ cum, const int
 // ------------------------------------------------------- launch interface
 
 struct Workspace {
-    __nv_bfloat16* qhat;     // [max_tokens, H, 128]
-    __nv_bfloat16* khat;     // [max_tokens, H, 128]
+    __half* qhat;            // [max_tokens, H, 128] rotated, normalised q (fp16)
+    __half* khat;            // [max_tokens, H, 128] rotated, normalised k (fp16)
     float* delta;            // [H, max_tokens]
     float* dwq_part;         // [max_tiles64, H, 128]
     float* dwk_part;         // [max_tiles64, H, 128]

@@ -3,7 +3,8 @@
 // One CTA = one (sample, 64-query tile, head).  Four warps own 16 query rows
 // each.  Key/value tiles of 64 tokens anchored at the sample start are streamed
 // in ascending order with cp.async (double buffered); rows past the sample end
-// are zero-filled and their scores replaced (select, not add) by -inf.  Online
+// are zero-filled and their scores replaced (select, not add) by -inf.  S = q^ k^T
+// runs on fp16 operands (the prologue's rounding), PV on bf16 P and v.  Online
 // softmax keeps a running max m and sum l per row in FP32; P is rounded once to
 // bf16 for the PV product; O accumulates in FP32 and is rounded once at the end.
 //
@@ -24,7 +25,7 @@ constexpr int kSmem = kTileBytes * 5;     // Q + 2 x (K, V)
 }  // namespace fwdm
 
 __global__ void __launch_bounds__(fwdm::kThreads)
-fwd_mma_kernel(const __nv_bfloat16* __restrict__ qhat, const __nv_bfloat16* __restrict__ khat,
+fwd_mma_kernel(const __half* __restrict__ qhat, const __half* __restrict__ khat,
                const __nv_bfloat16* __restrict__ v, Seq seq, Plan plan, int H, float scale_log2,
                __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
     using namespace fwdm;
@@ -73,8 +74,8 @@ fwd_mma_kernel(const __nv_bfloat16* __restrict__ qhat, const __nv_bfloat16* __re
             for (int np = 0; np < 4; ++np) {
                 uint32_t b[4];
                 ldsm_b_nk(b, sK[buf], np * 16, kk, lane);
-                mma16816(s[2 * np], qa[kk], b[0], b[1]);
-                mma16816(s[2 * np + 1], qa[kk], b[2], b[3]);
+                mma16816_f16(s[2 * np], qa[kk], b[0], b[1]);
+                mma16816_f16(s[2 * np + 1], qa[kk], b[2], b[3]);
             }
         }
         // mask keys past the sample end

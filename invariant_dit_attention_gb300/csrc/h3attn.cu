@@ -296,7 +296,7 @@ h3attn_status h3attn_device_status(h3attn_t h, void* stream) {
             return H3ATTN_ERR_CUDA;
     }
     if (e & kErrTimeout) return H3ATTN_ERR_TIMEOUT;
-    if (e & kErrBadOffsets) return H3ATTN_ERR_INVALID_ARG;
+    if (e & (kErrBadOffsets | kErrRange)) return H3ATTN_ERR_INVALID_ARG;
     return H3ATTN_OK;
 }
 

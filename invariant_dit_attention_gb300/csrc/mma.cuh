@@ -1,4 +1,4 @@
-// mma.cuh -- warp-level bf16 MMA (m16n8k16), ldmatrix and cp.async helpers
+// mma.cuh -- warp-level bf16/fp16 MMA (m16n8k16), ldmatrix and cp.async helpers
 // with a 128-byte XOR swizzle for [rows][128] bf16 tiles in shared memory.
 #pragma once
 
@@ -14,6 +14,14 @@ __device__ __forceinline__ uint32_t swz(int r, int ch) { return (uint32_t)(r * 2
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma16816_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};\n"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
@@ -40,15 +48,16 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // Loads rows [row0, row0 + ROWS) of head h of a [S, H, 128] tensor into a
 // swizzled tile; rows at or past row_end are zero-filled.  All threads of the
 // block take part.
-template <int ROWS, int THREADS>
-__device__ __forceinline__ void load_tile_async(uint32_t tile, const __nv_bfloat16* __restrict__ g, int H, int h,
+template <int ROWS, int THREADS, class T>
+__device__ __forceinline__ void load_tile_async(uint32_t tile, const T* __restrict__ g, int H, int h,
                                                 int row0, int row_end, int tid) {
+    static_assert(sizeof(T) == 2, "16-bit elements");
 #pragma unroll
     for (int i = tid; i < ROWS * 16; i += THREADS) {
         int r = i >> 4, ch = i & 15;
         int row = row0 + r;
         bool ok = row < row_end;
-        const __nv_bfloat16* src = g + ((size_t)(ok ? row : row0) * H + h) * kD + ch * 8;
+        const T* src = g + ((size_t)(ok ? row : row0) * H + h) * kD + ch * 8;
         cp_async16(tile + swz(r, ch), src, ok ? 16 : 0);
     }
 }

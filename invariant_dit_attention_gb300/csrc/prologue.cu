@@ -5,7 +5,7 @@
 // first); the order only decides which CTA runs a tile, never the arithmetic.
 //
 // The prologue rotates and normalises q and k once per (token, head) into the
-// bf16 workspaces q^ and k^ that the attention kernels stream with TMA or
+// fp16 workspaces q^ and k^ that the attention kernels stream with TMA or
 // cp.async.  It is bound by HBM bandwidth: 8 bytes moved per q/k element pair
 // read + written (2 B read and 2 B written for each of q and k).
 #include "common.cuh"
@@ -90,8 +90,8 @@ constexpr int kProWarps = 8;
 constexpr int kProBatch = 4;  // heads loaded ahead per warp
 
 __global__ void __launch_bounds__(kProWarps * 32)
-prologue_kernel(Problem p, __nv_bfloat16* __restrict__ qhat, __nv_bfloat16* __restrict__ khat,
-                const __grid_constant__ RopeTable rt) {
+prologue_kernel(Problem p, __half* __restrict__ qhat, __half* __restrict__ khat,
+                const __grid_constant__ RopeTable rt, unsigned* err) {
     const int lane = threadIdx.x & 31;
     const int tok = blockIdx.x * kProWarps + (threadIdx.x >> 5);
     if (tok >= p.seq.S) return;
@@ -102,6 +102,7 @@ prologue_kernel(Problem p, __nv_bfloat16* __restrict__ qhat, __nv_bfloat16* __re
     const __nv_bfloat16* __restrict__ q = p.q;
     const __nv_bfloat16* __restrict__ k = p.k;
     const size_t base = (size_t)tok * p.H * kD + 4 * lane;
+    bool ok = true;
     for (int h0 = 0; h0 < p.H; h0 += kProBatch) {
         float xq[kProBatch][4], xk[kProBatch][4];
 #pragma unroll
@@ -115,17 +116,18 @@ prologue_kernel(Problem p, __nv_bfloat16* __restrict__ qhat, __nv_bfloat16* __re
             if (h0 + b < p.H) {
                 float y[4];
                 row_norm_rope(xq[b], wq, ang, rt, lane, p.eps, y);
-                store_row4(qhat + base + (size_t)(h0 + b) * kD, y);
+                ok &= store_row4_f16(qhat + base + (size_t)(h0 + b) * kD, y);
                 row_norm_rope(xk[b], wk, ang, rt, lane, p.eps, y);
-                store_row4(khat + base + (size_t)(h0 + b) * kD, y);
+                ok &= store_row4_f16(khat + base + (size_t)(h0 + b) * kD, y);
             }
     }
+    if (!ok) atomicOr(err, kErrRange);
 }
 
 cudaError_t launch_prologue(const Problem& p, const Workspace& ws, const RopeTable* rope, cudaStream_t st) {
     if (p.seq.S == 0) return cudaSuccess;
     int blocks = (p.seq.S + kProWarps - 1) / kProWarps;
-    prologue_kernel<<<blocks, kProWarps * 32, 0, st>>>(p, ws.qhat, ws.khat, *rope);
+    prologue_kernel<<<blocks, kProWarps * 32, 0, st>>>(p, ws.qhat, ws.khat, *rope, ws.plan.err);
     return cudaGetLastError();
 }
 

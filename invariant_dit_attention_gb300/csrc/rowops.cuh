@@ -7,7 +7,8 @@
 //   n = x / sqrt(mean_c x_c^2 + eps),  z = n * w,
 //   for a rotated pair (u, v) = (z[o+j], z[o+j+n_a/2]) with angle a = p_axis * f_j:
 //   (u, v) -> (u cos a - v sin a, u sin a + v cos a); other channels unchanged.
-// All of it in FP32 with one final rounding to bf16.
+// All of it in FP32 with one final rounding to fp16 (11-bit significand: the
+// rotated rows are bounded by sqrt(128) * max|w|, far inside fp16's range).
 //
 // Backward, for the gradient dy at the rotated output:
 //   g = R(a)^T dy,  dn = g * w,  dx = r (dn - n mean_c(dn_c n_c)),  dw += g * n,
@@ -108,6 +109,17 @@ __device__ __forceinline__ void row_norm_rope_bwd(const float (&dy)[4], const fl
 __device__ __forceinline__ void load_row4(const __nv_bfloat16* p, float (&x)[4]) {
     uint2 u = *reinterpret_cast<const uint2*>(p);
     x[0] = bf16_lo(u.x); x[1] = bf16_hi(u.x); x[2] = bf16_lo(u.y); x[3] = bf16_hi(u.y);
+}
+
+// Rounds the row to fp16 and stores it; returns false if a value overflowed.
+__device__ __forceinline__ bool store_row4_f16(__half* p, const float (&y)[4]) {
+    uint2 u;
+    u.x = pack_f16(y[0], y[1]);
+    u.y = pack_f16(y[2], y[3]);
+    *reinterpret_cast<uint2*>(p) = u;
+    const bool ok = fabsf(y[0]) <= 65504.f && fabsf(y[1]) <= 65504.f && fabsf(y[2]) <= 65504.f &&
+                    fabsf(y[3]) <= 65504.f;
+    return ok || !(isfinite(y[0]) && isfinite(y[1]) && isfinite(y[2]) && isfinite(y[3]));
 }
 
 __device__ __forceinline__ void store_row4(__nv_bfloat16* p, const float (&y)[4]) {

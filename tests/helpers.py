@@ -10,12 +10,15 @@ import torch
 import oracle
 from invariant_dit_attention_gb300 import workloads as W
 
-# Tolerances against the FP64 oracle (bf16 outputs; see the parity section of
-# the design notes): forward rel-L2 and max-abs, backward rel-L2.
+# Tolerances against the FP64 oracle: forward rel-L2 <= 5e-3 and max-abs <= 2e-2
+# on the bf16 outputs, backward rel-L2 <= 1e-2.  The lse bound follows from
+# rounding q^ and k^ to bf16 (2^-9 relative per element): a score moves by at
+# most about 2^-8 |q^||k^| scale, a few 1e-3 for unit-RMS heads, and lse moves
+# by no more than the largest score shift.
 FWD_REL_L2 = 5e-3
 FWD_MAX_ABS = 2e-2
 BWD_REL_L2 = 1e-2
-LSE_MAX_ABS = 2e-3
+LSE_MAX_ABS = 1e-2
 
 
 def rel_l2(x, ref):
