@@ -37,6 +37,7 @@ struct Plan {
     int* order;      // [max_samples] sample index of rank r
     int* cum64;      // [max_samples + 1] tiles of 64 tokens before rank r
     int* cum128;     // [max_samples + 1] tiles of 128 tokens before rank r
+    int* cum256;     // [max_samples + 1] blocks of 256 tokens before rank r
     int* rank_of;    // [max_samples] rank of sample s
     unsigned* err;   // device error word
 };
@@ -132,7 +133,7 @@ struct Problem {
 // Stages of one call, in launch order (timed separately when stage timing is on).
 enum Stage { kStagePlan = 0, kStagePrologue, kStageFwd, kStageDelta, kStageDkdv, kStageDq, kStageDw, kStages };
 
-cudaError_t init_fwd_attributes();
+cudaError_t init_fwd_tc();
 cudaError_t init_bwd_attributes();
 cudaError_t launch_plan(const Problem& p, const Workspace& ws, cudaStream_t st);
 cudaError_t launch_prologue(const Problem& p, const Workspace& ws, const RopeTable* rope, cudaStream_t st);

@@ -1,0 +1,457 @@
+// fwd_tc.cu -- forward attention (K2) on the 5th-generation tensor cores.
+//
+// Non-causal attention inside each packed sample (the attention node of the
+// "ws1_one_h3_block" page of RL-Kernel, PR #539, Bindings table), computed as
+// S = q^ k^T (fp16 operands) -> online softmax -> O += P v (bf16 operands),
+// FP32 accumulation in tensor memory, one rounding of O at the end.
+//
+// Persistent kernel, one CTA per SM.  A work item is (sample, head, block of
+// 256 query rows anchored at the sample start) = two 128-row subtiles A and B
+// that share every K/V tile.  Warp roles (384 threads):
+//   warp 0      TMA producer: q^ tiles, then K and V tiles (128 keys each, from
+//               the sample start, ascending) through a 4-stage ring;
+//   warp 1      tcgen05 issuer: S_X = Q_X K^T into TMEM, then O_X += P_X V with
+//               P_X read from TMEM (it overwrites S_X's first 64 columns);
+//   warps 4-7   softmax of subtile A, warps 8-11 softmax of subtile B: one
+//               thread per query row (TMEM lane), the row max and sum are
+//               sequential in that thread, P rounded once to bf16.
+// TMEM: S_A cols [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
+//
+// The running max is only moved when it grows by more than 8 (log2 units);
+// P = 2^((s - m) c) <= 2^8 then, and O / l are rescaled exactly when m moves.
+// Every row's arithmetic depends only on its sample's data and on tiles
+// anchored at the sample start, so a sample gives the same bits alone or
+// packed.  Key rows past the sample end are masked by select in S and zeroed in
+// shared memory in V (a neighbour's Inf/NaN never reaches the PV product).
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "tc.cuh"
+
+namespace h3 {
+
+namespace fwdt {
+constexpr int kThreads = 384;
+constexpr int kNST = 4;                      // K/V ring stages
+constexpr int kTile = 128 * 128 * 2;         // one 128 x 128 16-bit tile: 32 KB
+constexpr int kHalf = 128 * 64 * 2;          // one 64-channel half (the TMA box): 16 KB
+constexpr int kOffQ = 0;                     // Q_A, Q_B
+constexpr int kOffKV = 2 * kTile;            // ring
+constexpr int kOffBar = kOffKV + kNST * kTile;
+constexpr int kSmem = kOffBar + 512 + 1024;  // barriers + 1 KB alignment slack
+constexpr uint32_t kColS0 = 0, kColO0 = 256;
+constexpr float kMaxStale = 8.0f;            // log2 growth of the max tolerated before rescaling
+
+// barrier indices (8 bytes each)
+enum {
+    bQFull = 0, bQEmpty, bKVFull, bKVEmpty = bKVFull + kNST, bSFull = bKVEmpty + kNST, bPFull = bSFull + 2,
+    bPVDone = bPFull + 2, bOFree = bPVDone + 2, bTail = bOFree + 2, bDone, bCount
+};
+}  // namespace fwdt
+
+struct FwdTcParams {
+    Seq seq;
+    Plan plan;
+    int H;
+    float scale_log2;
+    __nv_bfloat16* out;
+    float* lse;
+};
+
+struct FwdItem {
+    int h, seg0, L, row0, nkv;
+    bool hasB;
+};
+
+__device__ __forceinline__ bool fwd_item(const FwdTcParams& p, int i, FwdItem& it) {
+    const int n = p.seq.n;
+    const int* cum = p.plan.cum256;
+    if (i >= p.H * cum[n]) return false;
+    int lo = 0, hi = n;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (p.H * cum[mid] <= i) lo = mid; else hi = mid;
+    }
+    const int nb = cum[lo + 1] - cum[lo];
+    const int local = i - p.H * cum[lo];
+    const int b = local % nb;
+    const int s = p.plan.order[lo];
+    it.h = local / nb;
+    it.seg0 = p.seq.seg[s];
+    it.L = p.seq.seg[s + 1] - it.seg0;
+    it.row0 = it.seg0 + 256 * b;
+    it.hasB = 256 * b + 128 < it.L;
+    it.nkv = (it.L + 127) / 128;
+    return true;
+}
+
+__global__ void __launch_bounds__(fwdt::kThreads, 1)
+fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+              const __grid_constant__ CUtensorMap mv, const FwdTcParams p) {
+    using namespace fwdt;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bars = sbase + kOffBar;
+    auto bar = [&](int i) { return bars + 8u * i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * bCount);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 8 * bCount + 4);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid == 0) {
+        tc::mbar_init(bar(bQFull), 1);
+        tc::mbar_init(bar(bQEmpty), 1);
+        for (int i = 0; i < kNST; ++i) {
+            tc::mbar_init(bar(bKVFull + i), 1);
+            tc::mbar_init(bar(bKVEmpty + i), 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            tc::mbar_init(bar(bSFull + x), 1);
+            tc::mbar_init(bar(bPFull + x), 4);
+            tc::mbar_init(bar(bPVDone + x), 1);
+            tc::mbar_init(bar(bOFree + x), 4);
+        }
+        tc::mbar_init(bar(bTail), 1);
+        tc::mbar_init(bar(bDone), 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+        tc::prefetch_map(&mq);
+        tc::prefetch_map(&mk);
+        tc::prefetch_map(&mv);
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(smem_u32(tmem_slot), 512);
+        tc::tmem_relinquish();
+        tc::fence_before_sync();
+    }
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    bool failed = false;
+    auto fail = [&]() {
+        failed = true;
+        *abort_flag = 1;
+        atomicOr(p.plan.err, kErrTimeout);
+    };
+
+    // Register split: the producer/issuer warpgroup gives registers to the two
+    // softmax warpgroups (launch: 384 x 168 = 128 x 56 + 256 x 224).
+    if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 152;");
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 176;");
+    }
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        uint32_t kv_it = 0, items = 0, tails = 0;
+        for (int i = blockIdx.x; !failed; i += gridDim.x) {
+            FwdItem it;
+            if (!fwd_item(p, i, it)) break;
+            const int x0 = it.h * 128;
+            if (lane == 0) {
+                if (items > 0 && !tc::mbar_wait(bar(bQEmpty), (items - 1) & 1, abort_flag)) fail();
+                if (!failed) {
+                    tc::mbar_expect_tx(bar(bQFull), it.hasB ? 2 * kTile : kTile);
+                    for (int x = 0; x < (it.hasB ? 2 : 1); ++x)
+                        for (int hf = 0; hf < 2; ++hf)
+                            tc::tma_load_2d(sbase + kOffQ + x * kTile + hf * kHalf, &mq, x0 + 64 * hf,
+                                            it.row0 + 128 * x, bar(bQFull));
+                }
+            }
+            failed = __shfl_sync(0xffffffffu, failed, 0);
+            ++items;
+            for (int j = 0; j < it.nkv && !failed; ++j) {
+                for (int kv = 0; kv < 2 && !failed; ++kv) {
+                    const uint32_t slot = kv_it % kNST, ph = (kv_it / kNST) & 1;
+                    const uint32_t dst = sbase + kOffKV + slot * kTile;
+                    const int y = it.seg0 + 128 * j;
+                    const int valid = it.L - 128 * j;
+                    const bool tail = kv == 1 && valid < 128;
+                    const CUtensorMap* map = kv == 0 ? &mk : &mv;
+                    if (lane == 0) {
+                        if (!tc::mbar_wait(bar(bKVEmpty + slot), ph ^ 1, abort_flag)) fail();
+                        if (!failed) {
+                            const uint32_t b = tail ? bar(bTail) : bar(bKVFull + slot);
+                            tc::mbar_expect_tx(b, kTile);
+                            tc::tma_load_2d(dst, map, x0, y, b);
+                            tc::tma_load_2d(dst + kHalf, map, x0 + 64, y, b);
+                            if (tail && !tc::mbar_wait(bar(bTail), tails & 1, abort_flag)) fail();
+                        }
+                    }
+                    failed = __shfl_sync(0xffffffffu, failed, 0);
+                    if (tail && !failed) {
+                        ++tails;
+                        // zero V rows [valid, 128) of both halves (whole 128-byte rows,
+                        // so the swizzle inside a row does not matter)
+                        for (int r = valid + (lane >> 3); r < 128; r += 4) {
+                            const uint32_t off = (uint32_t)r * 128 + (lane & 7) * 16;
+                            asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" :: "r"(dst + off), "r"(0) : "memory");
+                            asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" :: "r"(dst + kHalf + off), "r"(0)
+                                         : "memory");
+                        }
+                        tc::fence_proxy_async();
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(bar(bKVFull + slot));
+                    }
+                    ++kv_it;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ----------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idS = tc::idesc_f16(false, false, 128, 128);  // fp16 x fp16, K-major B
+            constexpr uint32_t idP = tc::idesc_f16(true, true, 128, 128);    // bf16 x bf16, MN-major B
+            uint32_t kv_it = 0, items = 0, cntPV[2] = {0, 0}, itemsX[2] = {0, 0};
+            for (int i = blockIdx.x; !failed; i += gridDim.x) {
+                FwdItem it;
+                if (!fwd_item(p, i, it)) break;
+                const int nX = it.hasB ? 2 : 1;
+                if (!tc::mbar_wait(bar(bQFull), items & 1, abort_flag)) { fail(); break; }
+                ++items;
+                for (int j = 0; j < it.nkv && !failed; ++j) {
+                    // ---- S_X = Q_X K_j^T
+                    uint32_t slot = kv_it % kNST;
+                    if (!tc::mbar_wait(bar(bKVFull + slot), (kv_it / kNST) & 1, abort_flag)) { fail(); break; }
+                    ++kv_it;
+                    const uint32_t kaddr = sbase + kOffKV + slot * kTile;
+                    for (int x = 0; x < nX && !failed; ++x) {
+                        if (cntPV[x] > 0 && !tc::mbar_wait(bar(bPVDone + x), (cntPV[x] - 1) & 1, abort_flag)) {
+                            fail();
+                            break;
+                        }
+                        tc::fence_after_sync();
+                        const uint32_t qaddr = sbase + kOffQ + x * kTile;
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
+                            tc::mma_ss(tmem + kColS0 + 128 * x, tc::smem_desc_sw128(qaddr + koff, 16, 1024),
+                                       tc::smem_desc_sw128(kaddr + koff, 16, 1024), idS, kk > 0);
+                        }
+                        tc::mma_commit(bar(bSFull + x));
+                    }
+                    if (failed) break;
+                    tc::mma_commit(bar(bKVEmpty + slot));
+                    if (j == it.nkv - 1) tc::mma_commit(bar(bQEmpty));
+                    // ---- O_X += P_X V_j
+                    slot = kv_it % kNST;
+                    if (!tc::mbar_wait(bar(bKVFull + slot), (kv_it / kNST) & 1, abort_flag)) { fail(); break; }
+                    ++kv_it;
+                    const uint32_t vaddr = sbase + kOffKV + slot * kTile;
+                    for (int x = 0; x < nX && !failed; ++x) {
+                        if (j == 0 && itemsX[x] > 0 &&
+                            !tc::mbar_wait(bar(bOFree + x), (itemsX[x] - 1) & 1, abort_flag)) {
+                            fail();
+                            break;
+                        }
+                        if (!tc::mbar_wait(bar(bPFull + x), cntPV[x] & 1, abort_flag)) { fail(); break; }
+                        tc::fence_after_sync();
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            tc::mma_ts(tmem + kColO0 + 128 * x, tmem + kColS0 + 128 * x + 8 * kk,
+                                       tc::smem_desc_sw128(vaddr + kk * 2048, kHalf, 1024), idP, (j > 0) || (kk > 0));
+                        tc::mma_commit(bar(bPVDone + x));
+                        ++cntPV[x];
+                    }
+                    if (failed) break;
+                    tc::mma_commit(bar(bKVEmpty + slot));
+                }
+                for (int x = 0; x < nX; ++x) ++itemsX[x];
+            }
+            // every issued MMA has completed before TMEM is released
+            tc::mma_commit(bar(bDone));
+            if (!tc::mbar_wait(bar(bDone), 0, abort_flag) && !failed) fail();
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------------- softmax
+        const int x = (warp - 4) >> 2;          // subtile
+        const int tx = tid - 128 * (1 + x);     // row in subtile == TMEM lane
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        const uint32_t tS = tmem + lane_base + kColS0 + 128 * x;
+        const uint32_t tO = tmem + lane_base + kColO0 + 128 * x;
+        const float c = p.scale_log2;
+        uint32_t cntS = 0, cntPV = 0;
+        for (int i = blockIdx.x; !failed; i += gridDim.x) {
+            FwdItem it;
+            if (!fwd_item(p, i, it)) break;
+            if (x == 1 && !it.hasB) continue;
+            float m = -INFINITY, l = 0.f;
+            for (int j = 0; j < it.nkv; ++j) {
+                bool ok = true;
+                if (lane == 0) ok = tc::mbar_wait(bar(bSFull + x), cntS & 1, abort_flag);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) { fail(); break; }
+                ++cntS;
+                tc::fence_after_sync();
+                float s[128];
+                {
+                    uint32_t r[4][32];
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) tc::tmem_ld32(tS + 32 * q4, r[q4]);
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        tc::tmem_wait_ld_dep(r[q4]);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) s[32 * q4 + e] = __uint_as_float(r[q4][e]);
+                    }
+                }
+                const int valid = it.L - 128 * j;
+                if (valid < 128) {
+#pragma unroll
+                    for (int e = 0; e < 128; ++e) s[e] = e < valid ? s[e] : -INFINITY;
+                }
+                float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+                for (int e = 4; e < 128; e += 4) {
+                    mx0 = fmaxf(mx0, s[e]);
+                    mx1 = fmaxf(mx1, s[e + 1]);
+                    mx2 = fmaxf(mx2, s[e + 2]);
+                    mx3 = fmaxf(mx3, s[e + 3]);
+                }
+                const float m_new = fmaxf(fmaxf(m, fmaxf(mx0, mx1)), fmaxf(mx2, mx3));
+                const bool need = j == 0 || (m_new - m) * c > kMaxStale;
+                float factor = 1.f;
+                if (need) {
+                    factor = j == 0 ? 0.f : ex2((m - m_new) * c);
+                    m = m_new;
+                    l *= factor;
+                }
+                const float neg = -m * c;
+                float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; e += 2) {
+                        const float p0 = ex2(fmaf(s[32 * q4 + 2 * e], c, neg));
+                        const float p1 = ex2(fmaf(s[32 * q4 + 2 * e + 1], c, neg));
+                        const float p2 = ex2(fmaf(s[32 * q4 + 2 * e + 2], c, neg));
+                        const float p3 = ex2(fmaf(s[32 * q4 + 2 * e + 3], c, neg));
+                        rs0 += p0; rs1 += p1; rs2 += p2; rs3 += p3;
+                        pk[e] = pack_bf16(p0, p1);
+                        pk[e + 1] = pack_bf16(p2, p3);
+                    }
+                    tc::tmem_st16(tS + 16 * q4, pk);
+                }
+                l += (rs0 + rs1) + (rs2 + rs3);
+                // O_X was last written by PV_X(j-1), complete before S_X(j) was issued
+                if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint32_t r[32];
+                        tc::tmem_ld32(tO + 32 * q4, r);
+                        tc::tmem_wait_ld_dep(r);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * factor);
+                        tc::tmem_st32(tO + 32 * q4, r);
+                    }
+                }
+                tc::tmem_wait_st();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(bar(bPFull + x));
+            }
+            if (failed) break;
+            // ---- epilogue: O / l -> bf16 rows, lse
+            cntPV += it.nkv;
+            bool ok = true;
+            if (lane == 0) ok = tc::mbar_wait(bar(bPVDone + x), (cntPV - 1) & 1, abort_flag);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) { fail(); break; }
+            tc::fence_after_sync();
+            const int r_in = 256 * ((it.row0 - it.seg0) / 256) + 128 * x + tx;  // row within the sample
+            const int row = it.seg0 + r_in;
+            const bool store = r_in < it.L;
+            const float inv = 1.0f / l;
+            __nv_bfloat16* dst = p.out + ((size_t)row * p.H + it.h) * kD;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t r[32];
+                tc::tmem_ld32(tO + 32 * q4, r);
+                tc::tmem_wait_ld_dep(r);
+                if (store) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        uint4 u;
+                        u.x = pack_bf16(__uint_as_float(r[e]) * inv, __uint_as_float(r[e + 1]) * inv);
+                        u.y = pack_bf16(__uint_as_float(r[e + 2]) * inv, __uint_as_float(r[e + 3]) * inv);
+                        u.z = pack_bf16(__uint_as_float(r[e + 4]) * inv, __uint_as_float(r[e + 5]) * inv);
+                        u.w = pack_bf16(__uint_as_float(r[e + 6]) * inv, __uint_as_float(r[e + 7]) * inv);
+                        *reinterpret_cast<uint4*>(dst + 32 * q4 + e) = u;
+                    }
+                }
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(bar(bOFree + x));
+            if (store && p.lse) p.lse[(size_t)it.h * p.seq.S + row] = (m * c + log2f(l)) * 0.69314718055994531f;
+        }
+    }
+
+    __syncthreads();
+    if (warp == 0 && lane == 0 && *abort_flag) {
+        // let any TMA still in flight land before the CTA's shared memory goes away
+        const long long t0 = clock64();
+        while (clock64() - t0 < 20000000LL) {
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------------ host
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+int g_num_sms = 0;
+
+bool encode_rows(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int H, int S) {
+    const cuuint64_t dims[2] = {(cuuint64_t)H * kD, (cuuint64_t)S};
+    const cuuint64_t strides[1] = {(cuuint64_t)H * kD * 2};
+    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t es[2] = {1, 1};
+    return g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
+cudaError_t init_fwd_tc() {
+    if (!g_encode) {
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", reinterpret_cast<void**>(&g_encode),
+                                                         12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !g_encode) return cudaErrorNotSupported;
+    }
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, fwdt::kSmem);
+    return e;
+}
+
+cudaError_t launch_fwd(const Problem& p, const Workspace& ws, __nv_bfloat16* out, float* lse, cudaStream_t st) {
+    CUtensorMap mq, mk, mv;
+    if (!encode_rows(&mq, ws.qhat, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.H, p.seq.S) ||
+        !encode_rows(&mk, ws.khat, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.H, p.seq.S) ||
+        !encode_rows(&mv, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.H, p.seq.S))
+        return cudaErrorInvalidValue;
+    FwdTcParams prm;
+    prm.seq = p.seq;
+    prm.plan = ws.plan;
+    prm.H = p.H;
+    prm.scale_log2 = p.scale * 1.4426950408889634f;
+    prm.out = out;
+    prm.lse = lse;
+    fwd_tc_kernel<<<g_num_sms, fwdt::kThreads, fwdt::kSmem, st>>>(mq, mk, mv, prm);
+    return cudaGetLastError();
+}
+
+}  // namespace h3

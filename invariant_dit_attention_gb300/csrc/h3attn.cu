@@ -21,7 +21,7 @@ struct h3attn_ctx {
     Workspace ws;
     int max_tiles64;
     unsigned* host_err;  // pinned
-    void* allocs[16];
+    void* allocs[24];
     int nalloc;
     // stage timing (instrumentation)
     int timing;
@@ -180,10 +180,11 @@ h3attn_status h3attn_create(const h3attn_config* cfg, h3attn_t* out) {
               ws_alloc(h, &ws.dwq_sample, N * kD * 4) && ws_alloc(h, &ws.dwk_sample, N * kD * 4) &&
               ws_alloc(h, &ws.plan.order, N * 4) && ws_alloc(h, &ws.plan.rank_of, N * 4) &&
               ws_alloc(h, &ws.plan.cum64, (N + 1) * 4) && ws_alloc(h, &ws.plan.cum128, (N + 1) * 4) &&
+              ws_alloc(h, &ws.plan.cum256, (N + 1) * 4) &&
               ws_alloc(h, &ws.plan.err, 4);
     if (ok) ok = cudaMemset(ws.plan.err, 0, 4) == cudaSuccess;
     if (ok) ok = cudaMallocHost(&h->host_err, 4) == cudaSuccess;
-    if (ok) ok = init_fwd_attributes() == cudaSuccess && init_bwd_attributes() == cudaSuccess;
+    if (ok) ok = init_fwd_tc() == cudaSuccess && init_bwd_attributes() == cudaSuccess;
     if (ok) ok = cudaDeviceSynchronize() == cudaSuccess;
     if (!ok) {
         free_ctx(h);
