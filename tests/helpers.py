@@ -27,6 +27,14 @@ def rel_l2(x, ref):
     return float(np.linalg.norm((x - ref).ravel()) / max(np.linalg.norm(ref.ravel()), 1e-300))
 
 
+def max_abs_scaled(x, ref):
+    """max |x - ref| / max(1, |ref|): the absolute error where outputs are O(1),
+    relative beyond (a bf16 output of magnitude 8 is quantised in steps of 1/16)."""
+    x = np.asarray(x, np.float64)
+    ref = np.asarray(ref, np.float64)
+    return float(np.max(np.abs(x - ref) / np.maximum(1.0, np.abs(ref))))
+
+
 def max_abs(x, ref):
     return float(np.max(np.abs(np.asarray(x, np.float64) - np.asarray(ref, np.float64))))
 
