@@ -156,6 +156,45 @@ enum {
 h3attn_status h3attn_set_stage_timing(h3attn_t h, int enable);
 h3attn_status h3attn_stage_times(h3attn_t h, float *total_ms, int *launches, int n_stages);
 
+/*
+ * h3attn_forward_static: the forward for callers that cannot allocate device
+ * memory (there is no counterpart on the pages; it is a deployment aid).
+ *
+ * Hosts such as inference servers that hand a plugin a fixed memory pool, or
+ * processes that run under a device-memory budget, may not call cudaMalloc once
+ * they are serving; h3attn_create's workspace is then out of reach.  This entry
+ * point takes no handle and allocates nothing (no cudaMalloc, no cudaFree, no
+ * allocating library call): its scratch - rotated q^/k^ rows, the sample plan
+ * and an error word, 64 MiB + 64 KiB in all - is one static __device__ array
+ * of the library, which every GPU that loads the library holds until the
+ * process exits.
+ *
+ * Arguments are those of h3attn_forward with the configuration passed directly
+ * (cfg->max_tokens and cfg->max_samples are ignored), plus device_error_flags:
+ * a device uint32 (may be NULL) that receives this call's device-side error
+ * bits (0 = none; 1 = invalid seg_offsets, 2 = a bounded wait timed out, 4 = a
+ * value beyond the fp16 operand range), written on `stream` after the kernels.
+ * Limits: total_tokens * num_heads <= H3ATTN_STATIC_MAX_TOKEN_HEADS and
+ * num_samples <= H3ATTN_STATIC_MAX_SAMPLES, else H3ATTN_ERR_CAPACITY.
+ * The first call on a device resolves the array's device address and prepares
+ * the kernels for that device (make that first call before any stream
+ * capture).  Every call on a device shares the one array and leaves its
+ * contents behind; the call clears what must start at zero.  Two calls whose
+ * work overlaps on the GPU (different streams, or different host threads)
+ * race on the array: serialise them.  Results are bitwise those of
+ * h3attn_forward for the same inputs.
+ * Errors: INVALID_ARG, UNSUPPORTED, CAPACITY, CUDA.
+ */
+#define H3ATTN_STATIC_MAX_TOKEN_HEADS 131072
+#define H3ATTN_STATIC_MAX_SAMPLES 2048
+h3attn_status h3attn_forward_static(const h3attn_config *cfg,
+                                    const h3attn_bf16 *q, const h3attn_bf16 *k, const h3attn_bf16 *v,
+                                    const float *q_norm_w, const float *k_norm_w,
+                                    const int32_t *const pos_ids[3], const int32_t *seg_offsets,
+                                    int num_samples, int total_tokens,
+                                    h3attn_bf16 *out, float *lse, uint32_t *device_error_flags,
+                                    void *stream);
+
 /* Static, human-readable name of a status code. */
 const char *h3attn_status_string(h3attn_status s);
 

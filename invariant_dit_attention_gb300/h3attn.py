@@ -21,7 +21,12 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CAPACITY, ERR_CUDA, ERR_TIMEOUT = rang
 
 # Entry points declared in include/h3attn.h.
 EXPORTS = ("h3attn_create", "h3attn_destroy", "h3attn_forward", "h3attn_backward",
-           "h3attn_device_status", "h3attn_set_stage_timing", "h3attn_stage_times", "h3attn_status_string")
+           "h3attn_device_status", "h3attn_set_stage_timing", "h3attn_stage_times", "h3attn_forward_static",
+           "h3attn_status_string")
+
+# Limits of h3attn_forward_static's built-in scratch (include/h3attn.h).
+STATIC_MAX_TOKEN_HEADS = 131072
+STATIC_MAX_SAMPLES = 2048
 
 STAGES = ("plan", "prologue", "fwd", "bwd_delta", "bwd_dkdv", "bwd_dq", "bwd_dw")
 
@@ -66,6 +71,9 @@ def load_library(path: str = LIB_PATH):
     lib.h3attn_set_stage_timing.restype = i32
     lib.h3attn_stage_times.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(i32), i32]
     lib.h3attn_stage_times.restype = i32
+    lib.h3attn_forward_static.argtypes = [ctypes.POINTER(Config), vp, vp, vp, vp, vp, ctypes.POINTER(vp), vp,
+                                          i32, i32, vp, vp, vp, vp]
+    lib.h3attn_forward_static.restype = i32
     lib.h3attn_status_string.argtypes = [i32]
     lib.h3attn_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -180,6 +188,31 @@ class H3Attn:
 
     def check(self, stream=None):
         _check(self.device_status(stream), "device")
+
+
+def forward_static(q, k, v, q_norm_w, k_norm_w, pos, seg_offsets, num_heads=None, eps=1e-6,
+                   rope_theta=10000.0, rope_sections=(16, 24, 24), softmax_scale=0.0, num_samples=None,
+                   out=None, lse=None, error_flags=None, stream=None):
+    """h3attn_forward_static: the forward with no handle and no device allocation
+    inside the library (for hosts that forbid cudaMalloc while serving).
+
+    ``out``/``lse``/``error_flags`` are caller-owned device tensors; they are
+    created here with torch when not given.  Returns (out, lse).
+    """
+    lib = load_library()
+    S, H = q.shape[0], q.shape[1] if num_heads is None else num_heads
+    cfg = Config()
+    cfg.num_heads, cfg.head_dim, cfg.eps, cfg.rope_theta = H, 128, eps, rope_theta
+    cfg.rope_sections[:] = list(rope_sections)
+    cfg.rope_pairing, cfg.softmax_scale, cfg.max_tokens, cfg.max_samples = 0, softmax_scale, 0, 0
+    n = int(seg_offsets.numel() - 1) if num_samples is None else num_samples
+    if out is None:
+        out = torch.empty_like(q)
+    st = lib.h3attn_forward_static(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(q_norm_w), _ptr(k_norm_w),
+                                   _pos_array(pos), _ptr(seg_offsets), n, S, _ptr(out), _ptr(lse),
+                                   _ptr(error_flags), _stream(stream))
+    _check(st, "h3attn_forward_static")
+    return out, lse
 
 
 def to_device(inp, device="cuda"):
