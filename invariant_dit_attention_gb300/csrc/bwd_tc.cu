@@ -1,0 +1,846 @@
+// bwd_tc.cu -- backward of the attention core on the 5th-generation tensor cores.
+//
+// Gradients of sum(out * dout) (the per-leaf gradient checks of the
+// "ws1_one_h3_block" page of RL-Kernel, PR #539, Results and Tests; the
+// 128-element norm-weight gradient of its Status section):
+//   Delta_i = sum_c dO_ic O_ic                                         (delta_kernel)
+//   P_ij = exp(scale q^_i.k^_j - lse_i),  dP_ij = dO_i . v_j,  dS_ij = P_ij (dP_ij - Delta_i)
+//   dV_j = sum_i P_ij dO_i,  dk^_j = scale sum_i dS_ij q^_i              (dkdv_tc_kernel)
+//   dq^_i = scale sum_j dS_ij k^_j                                       (dq_tc_kernel)
+// then RoPE^-1 and the RMSNorm backward per row in the epilogues, and the
+// norm-weight gradients reduced per 128-token tile, per sample, then over
+// samples, always in the same order (dw_sample_kernel, dw_total_kernel).
+//
+// No atomics anywhere: dkdv and dq each recompute S and P (7 tile products for
+// the 5 of the algorithm) and every sum runs over tiles anchored at the sample
+// start in ascending order, so a sample's gradients are the same bits alone or
+// packed.
+//
+// Both main kernels are persistent (one CTA per SM) with the forward's roles:
+// warp 0 TMA producer, warp 1 single-thread tcgen05 issuer, warps 4-7 and 8-11
+// two warpgroups that split the 128 columns of each 128 x 128 score tile
+// (thread = TMEM lane = one row).  Operands: S on fp16 q^/k^, dP on bf16 dO/v,
+// P (bf16) and dS (fp16) written back into tensor memory over the columns
+// their warpgroup just read, and fed to the accumulating MMAs as the
+// TMEM-resident A operand.
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "rowops.cuh"
+#include "tc.cuh"
+
+namespace h3 {
+
+namespace bwdt {
+constexpr int kThreads = 384;
+constexpr int kTile = 128 * 128 * 2;   // 32 KB
+constexpr int kHalf = 128 * 64 * 2;    // 16 KB
+constexpr int kPair = 2 * kTile;       // two tiles (q^ + dO, or k^ + v): 64 KB
+constexpr int kOffFixed = 0;           // the tile pair loaded once per item (also the epilogue stage)
+constexpr int kOffRing = kPair;        // 2-stage ring of tile pairs
+constexpr int kOffLse = kOffRing + 2 * kPair;  // [2 wg][2 buf][2][64] floats
+constexpr int kOffRed = kOffLse + 2 * 2 * 2 * 64 * 4;  // [8 warps][128] floats
+constexpr int kOffBar = kOffRed + 8 * 128 * 4;
+constexpr int kSmem = kOffBar + 256 + 1024;
+constexpr float kLog2e = 1.4426950408889634f;
+enum { bFixedFull = 0, bItemFree, bRingFull, bRingEmpty = bRingFull + 2, bSFull = bRingEmpty + 2, bPFull,
+       bMmaDone, bTail, bDone, bCount };
+// TMEM columns
+constexpr uint32_t cS = 0, cDP = 128, cA0 = 256, cA1 = 384;
+}  // namespace bwdt
+
+struct BwdTcParams {
+    Seq seq;
+    Plan plan;
+    int H;
+    float scale;
+    float eps;
+    const float* lse;
+    const float* delta;
+    const __nv_bfloat16* x;  // raw q (dq kernel) or k (dkdv kernel)
+    const float* w;          // q_norm_w or k_norm_w
+    __nv_bfloat16* dx;       // dq or dk
+    __nv_bfloat16* dv;       // dkdv kernel only
+    float* dw_part;          // [tiles128, H, 128]
+};
+
+struct BwdItem {
+    int h, seg0, L, tile, row0, n_other, tile_global;
+};
+
+// Item i over (rank, head, 128-token tile), samples longest first.
+__device__ __forceinline__ bool bwd_item(const BwdTcParams& p, int i, BwdItem& it) {
+    const int n = p.seq.n;
+    const int* cum = p.plan.cum128;
+    if (i >= p.H * cum[n]) return false;
+    int lo = 0, hi = n;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (p.H * cum[mid] <= i) lo = mid; else hi = mid;
+    }
+    const int nb = cum[lo + 1] - cum[lo];
+    const int local = i - p.H * cum[lo];
+    const int s = p.plan.order[lo];
+    it.h = local / nb;
+    it.tile = local % nb;
+    it.seg0 = p.seq.seg[s];
+    it.L = p.seq.seg[s + 1] - it.seg0;
+    it.row0 = it.seg0 + 128 * it.tile;
+    it.n_other = nb;
+    it.tile_global = cum[lo] + it.tile;
+    return true;
+}
+
+__device__ __forceinline__ void named_bar(int id, int count) {
+    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
+}
+
+// Byte offset of float4 chunk c4 (0..31) of fp32 row r in a [128][128] staging
+// tile; chunks are XOR-swizzled by the row so that both row-per-thread writes
+// and warp-per-row reads are free of bank conflicts.
+__device__ __forceinline__ uint32_t stage_off(int r, int c4) { return (uint32_t)(r * 512 + ((c4 ^ (r & 7)) << 4)); }
+
+// Zeroes rows [valid, 128) of a 64-channel-half tile (whole 128-byte rows).
+__device__ __forceinline__ void zero_rows(uint32_t half, int valid, int lane) {
+    for (int r = valid + (lane >> 3); r < 128; r += 4)
+        asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" :: "r"(half + (uint32_t)r * 128 + (lane & 7) * 16),
+                     "r"(0) : "memory");
+}
+
+// Row epilogue over a staged tile of d(x^) (already scaled): RoPE^-1 and the
+// RMSNorm backward per row (one warp per row, 8 warps), dx rows in bf16, and
+// the tile's norm-weight partial (fixed order: rows by warp, then warps).
+__device__ __forceinline__ void rows_epilogue(const uint8_t* stage, float* red, const BwdTcParams& p,
+                                              const BwdItem& it, const RopeTable& rt, int w8, int lane) {
+    const LaneRope lr = lane_rope(rt, lane);
+    float wl[4], acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) wl[e] = p.w[4 * lane + e];
+    const int nvalid = min(128, it.L - 128 * it.tile);
+    for (int r = w8; r < nvalid; r += 8) {
+        const int row = it.row0 + r;
+        const float4 s4 = *reinterpret_cast<const float4*>(stage + stage_off(r, lane));
+        float dy[4] = {s4.x, s4.y, s4.z, s4.w}, xr[4], d[4];
+        load_row4(p.x + ((size_t)row * p.H + it.h) * kD + 4 * lane, xr);
+        const RowAngles a = row_angles(lr, p.seq.pos_t[row], p.seq.pos_h[row], p.seq.pos_w[row]);
+        row_norm_rope_bwd(dy, xr, wl, a, lr, p.eps, d, acc);
+        store_row4(p.dx + ((size_t)row * p.H + it.h) * kD + 4 * lane, d);
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) red[w8 * kD + 4 * lane + e] = acc[e];
+    named_bar(3, 256);
+    const int t = w8 * 32 + lane;
+    if (t < kD) {
+        float s = 0.f;
+#pragma unroll
+        for (int wi = 0; wi < 8; ++wi) s += red[wi * kD + t];
+        p.dw_part[((size_t)it.tile_global * p.H + it.h) * kD + t] = s;
+    }
+}
+
+// Column of the TMEM A operand for K-step kk (16 columns of the score tile):
+// warpgroup 0 wrote columns 0..63 of the tile at TMEM [0, 32), warpgroup 1
+// columns 64..127 at [64, 96).
+__device__ __forceinline__ uint32_t a_col(int kk) { return kk < 4 ? 8 * kk : 64 + 8 * (kk - 4); }
+
+// ------------------------------------------------------------------ dK, dV
+
+__global__ void __launch_bounds__(bwdt::kThreads, 1)
+dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+               const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
+               const __grid_constant__ RopeTable rt, const BwdTcParams p) {
+    using namespace bwdt;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    auto bar = [&](int i) { return sbase + kOffBar + 8u * i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * bCount);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 8 * bCount + 4);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid == 0) {
+        tc::mbar_init(bar(bFixedFull), 1);
+        tc::mbar_init(bar(bItemFree), 8);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(bar(bRingFull + i), 1);
+            tc::mbar_init(bar(bRingEmpty + i), 1);
+        }
+        tc::mbar_init(bar(bSFull), 1);
+        tc::mbar_init(bar(bPFull), 8);
+        tc::mbar_init(bar(bMmaDone), 1);
+        tc::mbar_init(bar(bTail), 1);
+        tc::mbar_init(bar(bDone), 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(smem_u32(tmem_slot), 512);
+        tc::tmem_relinquish();
+        tc::fence_before_sync();
+    }
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    bool failed = false;
+    auto fail = [&]() {
+        failed = true;
+        *abort_flag = 1;
+        atomicOr(p.plan.err, kErrTimeout);
+    };
+    if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 152;");
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 176;");
+    }
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        uint32_t it_ring = 0, items = 0, tails = 0;
+        for (int i = blockIdx.x; !failed; i += gridDim.x) {
+            BwdItem it;
+            if (!bwd_item(p, i, it)) break;
+            const int x0 = it.h * 128;
+            if (lane == 0) {
+                if (items > 0 && !tc::mbar_wait(bar(bItemFree), (items - 1) & 1, abort_flag)) fail();
+                if (!failed) {
+                    tc::fence_proxy_async();
+                    tc::mbar_expect_tx(bar(bFixedFull), kPair);
+                    for (int hf = 0; hf < 2; ++hf) {
+                        tc::tma_load_2d(sbase + kOffFixed + hf * kHalf, &mk, x0 + 64 * hf, it.row0, bar(bFixedFull));
+                        tc::tma_load_2d(sbase + kOffFixed + kTile + hf * kHalf, &mv, x0 + 64 * hf, it.row0,
+                                        bar(bFixedFull));
+                    }
+                }
+            }
+            failed = __shfl_sync(0xffffffffu, failed, 0);
+            ++items;
+            const int nq = (it.L + 127) / 128;
+            for (int qi = 0; qi < nq && !failed; ++qi) {
+                const uint32_t slot = it_ring & 1, ph = (it_ring >> 1) & 1;
+                const uint32_t dst = sbase + kOffRing + slot * kPair;
+                const int y = it.seg0 + 128 * qi;
+                const int valid = it.L - 128 * qi;
+                const bool tail = valid < 128;
+                if (lane == 0) {
+                    if (!tc::mbar_wait(bar(bRingEmpty + slot), ph ^ 1, abort_flag)) fail();
+                    if (!failed) {
+                        const uint32_t b = tail ? bar(bTail) : bar(bRingFull + slot);
+                        tc::mbar_expect_tx(b, kPair);
+                        for (int hf = 0; hf < 2; ++hf) {
+                            tc::tma_load_2d(dst + hf * kHalf, &mq, x0 + 64 * hf, y, b);
+                            tc::tma_load_2d(dst + kTile + hf * kHalf, &mdo, x0 + 64 * hf, y, b);
+                        }
+                        if (tail && !tc::mbar_wait(bar(bTail), tails & 1, abort_flag)) fail();
+                    }
+                }
+                failed = __shfl_sync(0xffffffffu, failed, 0);
+                if (tail && !failed) {
+                    ++tails;
+                    // query rows past the sample end: zero q^ and dO so no neighbour
+                    // value reaches the dV and dK products
+                    for (int hf = 0; hf < 2; ++hf) {
+                        zero_rows(dst + hf * kHalf, valid, lane);
+                        zero_rows(dst + kTile + hf * kHalf, valid, lane);
+                    }
+                    tc::fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(bar(bRingFull + slot));
+                }
+                ++it_ring;
+            }
+        }
+    } else if (warp == 1) {
+        // ----------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idS16 = tc::idesc_f16(false, false, 128, 128);
+            constexpr uint32_t idSbf = tc::idesc_f16(true, false, 128, 128);
+            constexpr uint32_t idAbf = tc::idesc_f16(true, true, 128, 128);
+            constexpr uint32_t idA16 = tc::idesc_f16(false, true, 128, 128);
+            uint32_t it_ring = 0, items = 0, cntP = 0, cntDone = 0;
+            for (int i = blockIdx.x; !failed; i += gridDim.x) {
+                BwdItem it;
+                if (!bwd_item(p, i, it)) break;
+                if (!tc::mbar_wait(bar(bFixedFull), items & 1, abort_flag)) { fail(); break; }
+                ++items;
+                const uint32_t kaddr = sbase + kOffFixed, vaddr = kaddr + kTile;
+                const int nq = (it.L + 127) / 128;
+                for (int qi = 0; qi < nq; ++qi) {
+                    const uint32_t slot = it_ring & 1;
+                    if (!tc::mbar_wait(bar(bRingFull + slot), (it_ring >> 1) & 1, abort_flag)) { fail(); break; }
+                    ++it_ring;
+                    if (cntDone > 0 && !tc::mbar_wait(bar(bMmaDone), (cntDone - 1) & 1, abort_flag)) { fail(); break; }
+                    tc::fence_after_sync();
+                    const uint32_t qaddr = sbase + kOffRing + slot * kPair, doaddr = qaddr + kTile;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
+                        tc::mma_ss(tmem + cS, tc::smem_desc_sw128(kaddr + koff, 16, 1024),
+                                   tc::smem_desc_sw128(qaddr + koff, 16, 1024), idS16, kk > 0);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
+                        tc::mma_ss(tmem + cDP, tc::smem_desc_sw128(vaddr + koff, 16, 1024),
+                                   tc::smem_desc_sw128(doaddr + koff, 16, 1024), idSbf, kk > 0);
+                    }
+                    tc::mma_commit(bar(bSFull));
+                    if (!tc::mbar_wait(bar(bPFull), cntP & 1, abort_flag)) { fail(); break; }
+                    ++cntP;
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        tc::mma_ts(tmem + cA0, tmem + cS + a_col(kk),
+                                   tc::smem_desc_sw128(doaddr + kk * 2048, kHalf, 1024), idAbf, (qi > 0) || (kk > 0));
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        tc::mma_ts(tmem + cA1, tmem + cDP + a_col(kk),
+                                   tc::smem_desc_sw128(qaddr + kk * 2048, kHalf, 1024), idA16, (qi > 0) || (kk > 0));
+                    tc::mma_commit(bar(bMmaDone));
+                    ++cntDone;
+                    tc::mma_commit(bar(bRingEmpty + slot));
+                }
+                if (failed) break;
+            }
+            tc::mma_commit(bar(bDone));
+            if (!tc::mbar_wait(bar(bDone), 0, abort_flag) && !failed) fail();
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------- softmax gradient + epilogue
+        const int wg = (warp - 4) >> 2;                 // column half of the score tile
+        const int w8 = warp - 4;                        // 0..7
+        const int t = tid - 128 * (1 + wg);             // thread in warpgroup == TMEM lane == key row
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        const float c = p.scale * kLog2e;
+        float* lsebuf = reinterpret_cast<float*>(smem + kOffLse) + wg * 256;  // [2 buf][lse2 64 | delta 64]
+        float* red = reinterpret_cast<float*>(smem + kOffRed);
+        uint32_t cntS = 0, cntDone = 0;
+        bool range_ok = true;
+        for (int i = blockIdx.x; !failed; i += gridDim.x) {
+            BwdItem it;
+            if (!bwd_item(p, i, it)) break;
+            const int nq = (it.L + 127) / 128;
+            const bool key_ok = 128 * it.tile + t < it.L;
+            for (int qi = 0; qi < nq; ++qi) {
+                float* lb = lsebuf + (qi & 1) * 128;
+                if (t < 64) {
+                    const int q = 128 * qi + 64 * wg + t;
+                    const bool v = q < it.L;
+                    const size_t idx = (size_t)it.h * p.seq.S + it.seg0 + (v ? q : 0);
+                    lb[t] = v ? p.lse[idx] * kLog2e : 0.f;
+                    lb[64 + t] = v ? p.delta[idx] : 0.f;
+                }
+                named_bar(1 + wg, 128);
+                bool ok = true;
+                if (lane == 0) ok = tc::mbar_wait(bar(bSFull), cntS & 1, abort_flag);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) { fail(); break; }
+                ++cntS;
+                tc::fence_after_sync();
+                uint32_t sr[2][32], dr[2][32];
+                tc::tmem_ld32(tmem + lane_base + cS + 64 * wg, sr[0]);
+                tc::tmem_ld32(tmem + lane_base + cS + 64 * wg + 32, sr[1]);
+                tc::tmem_ld32(tmem + lane_base + cDP + 64 * wg, dr[0]);
+                tc::tmem_ld32(tmem + lane_base + cDP + 64 * wg + 32, dr[1]);
+                tc::tmem_wait_ld_dep(sr[0]);
+                tc::tmem_wait_ld_dep(sr[1]);
+                tc::tmem_wait_ld_dep(dr[0]);
+                tc::tmem_wait_ld_dep(dr[1]);
+                const int validq = it.L - 128 * qi - 64 * wg;  // columns of this half inside the sample
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t pk[16], dk[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        float pv[2], dsv[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int col = 32 * hh + e + u;
+                            const float pe = ex2(fmaf(__uint_as_float(sr[hh][e + u]), c, -lb[col]));
+                            const float ds = pe * (__uint_as_float(dr[hh][e + u]) - lb[64 + col]);
+                            const bool v = col < validq;
+                            pv[u] = v ? pe : 0.f;
+                            dsv[u] = v ? ds : 0.f;
+                            range_ok &= !(key_ok && fabsf(dsv[u]) > 65504.f);
+                        }
+                        pk[e >> 1] = pack_bf16(pv[0], pv[1]);
+                        dk[e >> 1] = pack_f16(dsv[0], dsv[1]);
+                    }
+                    tc::tmem_st16(tmem + lane_base + cS + 64 * wg + 16 * hh, pk);
+                    tc::tmem_st16(tmem + lane_base + cDP + 64 * wg + 16 * hh, dk);
+                }
+                tc::tmem_wait_st();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(bar(bPFull));
+            }
+            if (failed) break;
+            // ---- epilogue: dV rows (warpgroup 0), staged dK rows (warpgroup 1), then rows
+            cntDone += nq;
+            bool ok = true;
+            if (lane == 0) ok = tc::mbar_wait(bar(bMmaDone), (cntDone - 1) & 1, abort_flag);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) { fail(); break; }
+            tc::fence_after_sync();
+            const int krow = it.row0 + t;
+            if (wg == 0) {
+                __nv_bfloat16* dst = p.dv + ((size_t)krow * p.H + it.h) * kD;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t r[32];
+                    tc::tmem_ld32(tmem + lane_base + cA0 + 32 * q4, r);
+                    tc::tmem_wait_ld_dep(r);
+                    if (key_ok) {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 8) {
+                            uint4 u;
+                            u.x = pack_bf16(__uint_as_float(r[e]), __uint_as_float(r[e + 1]));
+                            u.y = pack_bf16(__uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
+                            u.z = pack_bf16(__uint_as_float(r[e + 4]), __uint_as_float(r[e + 5]));
+                            u.w = pack_bf16(__uint_as_float(r[e + 6]), __uint_as_float(r[e + 7]));
+                            *reinterpret_cast<uint4*>(dst + 32 * q4 + e) = u;
+                        }
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t r[32];
+                    tc::tmem_ld32(tmem + lane_base + cA1 + 32 * q4, r);
+                    tc::tmem_wait_ld_dep(r);
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4) {
+                        const float4 v4 = make_float4(__uint_as_float(r[e]) * p.scale, __uint_as_float(r[e + 1]) * p.scale,
+                                                      __uint_as_float(r[e + 2]) * p.scale,
+                                                      __uint_as_float(r[e + 3]) * p.scale);
+                        *reinterpret_cast<float4*>(smem + kOffFixed + stage_off(t, 8 * q4 + e / 4)) = v4;
+                    }
+                }
+            }
+            named_bar(3, 256);
+            rows_epilogue(smem + kOffFixed, red, p, it, rt, w8, lane);
+            tc::fence_before_sync();
+            tc::fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(bar(bItemFree));
+        }
+        if (!range_ok) atomicOr(p.plan.err, kErrRange);
+    }
+
+    __syncthreads();
+    if (warp == 0 && lane == 0 && *abort_flag) {
+        const long long t0 = clock64();
+        while (clock64() - t0 < 20000000LL) {
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------------ dQ
+
+__global__ void __launch_bounds__(bwdt::kThreads, 1)
+dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+             const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
+             const __grid_constant__ RopeTable rt, const BwdTcParams p) {
+    using namespace bwdt;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    auto bar = [&](int i) { return sbase + kOffBar + 8u * i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * bCount);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 8 * bCount + 4);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid == 0) {
+        tc::mbar_init(bar(bFixedFull), 1);
+        tc::mbar_init(bar(bItemFree), 8);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(bar(bRingFull + i), 1);
+            tc::mbar_init(bar(bRingEmpty + i), 1);
+        }
+        tc::mbar_init(bar(bSFull), 1);
+        tc::mbar_init(bar(bPFull), 8);
+        tc::mbar_init(bar(bMmaDone), 1);
+        tc::mbar_init(bar(bTail), 1);
+        tc::mbar_init(bar(bDone), 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(smem_u32(tmem_slot), 512);
+        tc::tmem_relinquish();
+        tc::fence_before_sync();
+    }
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    bool failed = false;
+    auto fail = [&]() {
+        failed = true;
+        *abort_flag = 1;
+        atomicOr(p.plan.err, kErrTimeout);
+    };
+    if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 152;");
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 176;");
+    }
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        uint32_t it_ring = 0, items = 0, tails = 0;
+        for (int i = blockIdx.x; !failed; i += gridDim.x) {
+            BwdItem it;
+            if (!bwd_item(p, i, it)) break;
+            const int x0 = it.h * 128;
+            if (lane == 0) {
+                if (items > 0 && !tc::mbar_wait(bar(bItemFree), (items - 1) & 1, abort_flag)) fail();
+                if (!failed) {
+                    tc::fence_proxy_async();
+                    tc::mbar_expect_tx(bar(bFixedFull), kPair);
+                    for (int hf = 0; hf < 2; ++hf) {
+                        tc::tma_load_2d(sbase + kOffFixed + hf * kHalf, &mq, x0 + 64 * hf, it.row0, bar(bFixedFull));
+                        tc::tma_load_2d(sbase + kOffFixed + kTile + hf * kHalf, &mdo, x0 + 64 * hf, it.row0,
+                                        bar(bFixedFull));
+                    }
+                }
+            }
+            failed = __shfl_sync(0xffffffffu, failed, 0);
+            ++items;
+            const int nk = (it.L + 127) / 128;
+            for (int kj = 0; kj < nk && !failed; ++kj) {
+                const uint32_t slot = it_ring & 1, ph = (it_ring >> 1) & 1;
+                const uint32_t dst = sbase + kOffRing + slot * kPair;
+                const int y = it.seg0 + 128 * kj;
+                const int valid = it.L - 128 * kj;
+                const bool tail = valid < 128;
+                if (lane == 0) {
+                    if (!tc::mbar_wait(bar(bRingEmpty + slot), ph ^ 1, abort_flag)) fail();
+                    if (!failed) {
+                        const uint32_t b = tail ? bar(bTail) : bar(bRingFull + slot);
+                        tc::mbar_expect_tx(b, kPair);
+                        for (int hf = 0; hf < 2; ++hf) {
+                            tc::tma_load_2d(dst + hf * kHalf, &mk, x0 + 64 * hf, y, b);
+                            tc::tma_load_2d(dst + kTile + hf * kHalf, &mv, x0 + 64 * hf, y, b);
+                        }
+                        if (tail && !tc::mbar_wait(bar(bTail), tails & 1, abort_flag)) fail();
+                    }
+                }
+                failed = __shfl_sync(0xffffffffu, failed, 0);
+                if (tail && !failed) {
+                    ++tails;
+                    // key rows past the sample end: zero k^ (dS is 0 there, k^ may not be finite)
+                    for (int hf = 0; hf < 2; ++hf) zero_rows(dst + hf * kHalf, valid, lane);
+                    tc::fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(bar(bRingFull + slot));
+                }
+                ++it_ring;
+            }
+        }
+    } else if (warp == 1) {
+        // ----------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idS16 = tc::idesc_f16(false, false, 128, 128);
+            constexpr uint32_t idSbf = tc::idesc_f16(true, false, 128, 128);
+            constexpr uint32_t idA16 = tc::idesc_f16(false, true, 128, 128);
+            uint32_t it_ring = 0, items = 0, cntP = 0, cntDone = 0;
+            for (int i = blockIdx.x; !failed; i += gridDim.x) {
+                BwdItem it;
+                if (!bwd_item(p, i, it)) break;
+                if (!tc::mbar_wait(bar(bFixedFull), items & 1, abort_flag)) { fail(); break; }
+                ++items;
+                const uint32_t qaddr = sbase + kOffFixed, doaddr = qaddr + kTile;
+                const int nk = (it.L + 127) / 128;
+                for (int kj = 0; kj < nk; ++kj) {
+                    const uint32_t slot = it_ring & 1;
+                    if (!tc::mbar_wait(bar(bRingFull + slot), (it_ring >> 1) & 1, abort_flag)) { fail(); break; }
+                    ++it_ring;
+                    if (cntDone > 0 && !tc::mbar_wait(bar(bMmaDone), (cntDone - 1) & 1, abort_flag)) { fail(); break; }
+                    tc::fence_after_sync();
+                    const uint32_t kaddr = sbase + kOffRing + slot * kPair, vaddr = kaddr + kTile;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
+                        tc::mma_ss(tmem + cS, tc::smem_desc_sw128(qaddr + koff, 16, 1024),
+                                   tc::smem_desc_sw128(kaddr + koff, 16, 1024), idS16, kk > 0);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
+                        tc::mma_ss(tmem + cDP, tc::smem_desc_sw128(doaddr + koff, 16, 1024),
+                                   tc::smem_desc_sw128(vaddr + koff, 16, 1024), idSbf, kk > 0);
+                    }
+                    tc::mma_commit(bar(bSFull));
+                    if (!tc::mbar_wait(bar(bPFull), cntP & 1, abort_flag)) { fail(); break; }
+                    ++cntP;
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        tc::mma_ts(tmem + cA0, tmem + cS + a_col(kk),
+                                   tc::smem_desc_sw128(kaddr + kk * 2048, kHalf, 1024), idA16, (kj > 0) || (kk > 0));
+                    tc::mma_commit(bar(bMmaDone));
+                    ++cntDone;
+                    tc::mma_commit(bar(bRingEmpty + slot));
+                }
+                if (failed) break;
+            }
+            tc::mma_commit(bar(bDone));
+            if (!tc::mbar_wait(bar(bDone), 0, abort_flag) && !failed) fail();
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------- softmax gradient + epilogue
+        const int wg = (warp - 4) >> 2;
+        const int w8 = warp - 4;
+        const int t = tid - 128 * (1 + wg);             // query row of the tile
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        const float c = p.scale * kLog2e;
+        float* red = reinterpret_cast<float*>(smem + kOffRed);
+        uint32_t cntS = 0, cntDone = 0;
+        bool range_ok = true;
+        for (int i = blockIdx.x; !failed; i += gridDim.x) {
+            BwdItem it;
+            if (!bwd_item(p, i, it)) break;
+            const int nk = (it.L + 127) / 128;
+            const bool row_ok = 128 * it.tile + t < it.L;
+            const size_t idx = (size_t)it.h * p.seq.S + (row_ok ? it.row0 + t : it.seg0);
+            const float lse2 = row_ok ? p.lse[idx] * kLog2e : 0.f;
+            const float dlt = row_ok ? p.delta[idx] : 0.f;
+            for (int kj = 0; kj < nk; ++kj) {
+                bool ok = true;
+                if (lane == 0) ok = tc::mbar_wait(bar(bSFull), cntS & 1, abort_flag);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) { fail(); break; }
+                ++cntS;
+                tc::fence_after_sync();
+                uint32_t sr[2][32], dr[2][32];
+                tc::tmem_ld32(tmem + lane_base + cS + 64 * wg, sr[0]);
+                tc::tmem_ld32(tmem + lane_base + cS + 64 * wg + 32, sr[1]);
+                tc::tmem_ld32(tmem + lane_base + cDP + 64 * wg, dr[0]);
+                tc::tmem_ld32(tmem + lane_base + cDP + 64 * wg + 32, dr[1]);
+                tc::tmem_wait_ld_dep(sr[0]);
+                tc::tmem_wait_ld_dep(sr[1]);
+                tc::tmem_wait_ld_dep(dr[0]);
+                tc::tmem_wait_ld_dep(dr[1]);
+                const int validk = it.L - 128 * kj - 64 * wg;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t dk[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        float dsv[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int col = 32 * hh + e + u;
+                            const float pe = ex2(fmaf(__uint_as_float(sr[hh][e + u]), c, -lse2));
+                            const float ds = pe * (__uint_as_float(dr[hh][e + u]) - dlt);
+                            dsv[u] = col < validk ? ds : 0.f;
+                            range_ok &= !(row_ok && fabsf(dsv[u]) > 65504.f);
+                        }
+                        dk[e >> 1] = pack_f16(dsv[0], dsv[1]);
+                    }
+                    tc::tmem_st16(tmem + lane_base + cS + 64 * wg + 16 * hh, dk);
+                }
+                tc::tmem_wait_st();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(bar(bPFull));
+            }
+            if (failed) break;
+            // ---- epilogue: stage scale * dq^ (each warpgroup its 64 channels), then rows
+            cntDone += nk;
+            bool ok = true;
+            if (lane == 0) ok = tc::mbar_wait(bar(bMmaDone), (cntDone - 1) & 1, abort_flag);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) { fail(); break; }
+            tc::fence_after_sync();
+#pragma unroll
+            for (int q2 = 0; q2 < 2; ++q2) {
+                uint32_t r[32];
+                tc::tmem_ld32(tmem + lane_base + cA0 + 64 * wg + 32 * q2, r);
+                tc::tmem_wait_ld_dep(r);
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    const float4 v4 = make_float4(__uint_as_float(r[e]) * p.scale, __uint_as_float(r[e + 1]) * p.scale,
+                                                  __uint_as_float(r[e + 2]) * p.scale,
+                                                  __uint_as_float(r[e + 3]) * p.scale);
+                    *reinterpret_cast<float4*>(smem + kOffFixed + stage_off(t, 16 * wg + 8 * q2 + e / 4)) = v4;
+                }
+            }
+            named_bar(3, 256);
+            rows_epilogue(smem + kOffFixed, red, p, it, rt, w8, lane);
+            tc::fence_before_sync();
+            tc::fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(bar(bItemFree));
+        }
+        if (!range_ok) atomicOr(p.plan.err, kErrRange);
+    }
+
+    __syncthreads();
+    if (warp == 0 && lane == 0 && *abort_flag) {
+        const long long t0 = clock64();
+        while (clock64() - t0 < 20000000LL) {
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------------ Delta
+
+__global__ void __launch_bounds__(256) delta_kernel(const __nv_bfloat16* __restrict__ out,
+                                                    const __nv_bfloat16* __restrict__ dout, int S, int H,
+                                                    float* __restrict__ delta) {
+    const int lane = threadIdx.x & 31;
+    const long row = (long)blockIdx.x * 8 + (threadIdx.x >> 5);  // (token, head)
+    if (row >= (long)S * H) return;
+    float o[4], d[4];
+    load_row4(out + row * kD + 4 * lane, o);
+    load_row4(dout + row * kD + 4 * lane, d);
+    float acc = o[0] * d[0] + o[1] * d[1] + o[2] * d[2] + o[3] * d[3];
+    acc = warp_sum(acc);
+    if (lane == 0) delta[(long)(row % H) * S + row / H] = acc;
+}
+
+// -------------------------------------------------------- weight gradients
+
+// Per-sample weight gradient: the sample's 128-token tiles in ascending order
+// (two fixed interleaved halves, then added), heads ascending inside.
+__global__ void __launch_bounds__(256)
+dw_sample_kernel(const float* __restrict__ part_q, const float* __restrict__ part_k, Seq seq, Plan plan, int H,
+                 float* __restrict__ dwq_s, float* __restrict__ dwk_s) {
+    const int s = blockIdx.x;
+    const float* part = blockIdx.y == 0 ? part_q : part_k;
+    float* dst = blockIdx.y == 0 ? dwq_s : dwk_s;
+    const int c = threadIdx.x & 127, grp = threadIdx.x >> 7;
+    __shared__ float half[128];
+    const int r = plan.rank_of[s];
+    const int t0 = plan.cum128[r], t1 = plan.cum128[r + 1];
+    float acc = 0.f;
+    for (int tt = t0 + grp; tt < t1; tt += 2)
+        for (int h = 0; h < H; ++h) acc += part[((size_t)tt * H + h) * kD + c];
+    if (grp == 1) half[c] = acc;
+    __syncthreads();
+    if (grp == 0) dst[(size_t)s * kD + c] = acc + half[c];
+}
+
+__global__ void dw_total_kernel(const float* __restrict__ dwq_s, const float* __restrict__ dwk_s, int n,
+                                float* __restrict__ dwq, float* __restrict__ dwk) {
+    const int c = threadIdx.x & 127;
+    const float* src = threadIdx.x < 128 ? dwq_s : dwk_s;
+    float acc = 0.f;
+    for (int s = 0; s < n; ++s) acc += src[(size_t)s * kD + c];
+    (threadIdx.x < 128 ? dwq : dwk)[c] = acc;
+}
+
+// ------------------------------------------------------------------ host
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 g_encode_b = nullptr;
+int g_sms_b = 0;
+
+bool encode_rows_b(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int H, int S) {
+    const cuuint64_t dims[2] = {(cuuint64_t)H * kD, (cuuint64_t)S};
+    const cuuint64_t strides[1] = {(cuuint64_t)H * kD * 2};
+    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t es[2] = {1, 1};
+    return g_encode_b(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct BwdMaps {
+    CUtensorMap q, k, v, dout;
+};
+
+bool encode_all(BwdMaps& m, const Problem& p, const Workspace& ws, const __nv_bfloat16* dout) {
+    return encode_rows_b(&m.q, ws.qhat, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.H, p.seq.S) &&
+           encode_rows_b(&m.k, ws.khat, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.H, p.seq.S) &&
+           encode_rows_b(&m.v, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.H, p.seq.S) &&
+           encode_rows_b(&m.dout, dout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.H, p.seq.S);
+}
+}  // namespace
+
+cudaError_t init_bwd_attributes() {
+    if (!g_encode_b) {
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", reinterpret_cast<void**>(&g_encode_b),
+                                                         12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !g_encode_b) return cudaErrorNotSupported;
+    }
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_sms_b, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bwdt::kSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bwdt::kSmem);
+    return e;
+}
+
+cudaError_t launch_bwd_delta(const Problem& p, const Workspace& ws, const __nv_bfloat16* out,
+                             const __nv_bfloat16* dout, cudaStream_t st) {
+    const long rows = (long)p.seq.S * p.H;
+    delta_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(out, dout, p.seq.S, p.H, ws.delta);
+    return cudaGetLastError();
+}
+
+static BwdTcParams bwd_params(const Problem& p, const Workspace& ws, const float* lse) {
+    BwdTcParams b;
+    b.seq = p.seq;
+    b.plan = ws.plan;
+    b.H = p.H;
+    b.scale = p.scale;
+    b.eps = p.eps;
+    b.lse = lse;
+    b.delta = ws.delta;
+    return b;
+}
+
+cudaError_t launch_bwd_dkdv(const Problem& p, const Workspace& ws, const RopeTable* rope, const float* lse,
+                            const __nv_bfloat16* dout, __nv_bfloat16* dk, __nv_bfloat16* dv, cudaStream_t st) {
+    BwdMaps m;
+    if (!encode_all(m, p, ws, dout)) return cudaErrorInvalidValue;
+    BwdTcParams b = bwd_params(p, ws, lse);
+    b.x = p.k;
+    b.w = p.wk;
+    b.dx = dk;
+    b.dv = dv;
+    b.dw_part = ws.dwk_part;
+    dkdv_tc_kernel<<<g_sms_b, bwdt::kThreads, bwdt::kSmem, st>>>(m.q, m.k, m.v, m.dout, *rope, b);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dq(const Problem& p, const Workspace& ws, const RopeTable* rope, const float* lse,
+                          const __nv_bfloat16* dout, __nv_bfloat16* dq, cudaStream_t st) {
+    BwdMaps m;
+    if (!encode_all(m, p, ws, dout)) return cudaErrorInvalidValue;
+    BwdTcParams b = bwd_params(p, ws, lse);
+    b.x = p.q;
+    b.w = p.wq;
+    b.dx = dq;
+    b.dv = nullptr;
+    b.dw_part = ws.dwq_part;
+    dq_tc_kernel<<<g_sms_b, bwdt::kThreads, bwdt::kSmem, st>>>(m.q, m.k, m.v, m.dout, *rope, b);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dw(const Problem& p, const Workspace& ws, float* dwq, float* dwk, float* dwq_s,
+                          float* dwk_s, cudaStream_t st) {
+    float* qs = dwq_s ? dwq_s : ws.dwq_sample;
+    float* ks = dwk_s ? dwk_s : ws.dwk_sample;
+    dw_sample_kernel<<<dim3(p.seq.n, 2), 256, 0, st>>>(ws.dwq_part, ws.dwk_part, p.seq, ws.plan, p.H, qs, ks);
+    dw_total_kernel<<<1, 256, 0, st>>>(qs, ks, p.seq.n, dwq, dwk);
+    return cudaGetLastError();
+}
+
+}  // namespace h3

@@ -103,7 +103,8 @@ prologue_kernel(Problem p, __half* __restrict__ qhat, __half* __restrict__ khat,
     const int lane = threadIdx.x & 31;
     const int tok = blockIdx.x * kProWarps + (threadIdx.x >> 5);
     if (tok >= p.seq.S) return;
-    const RowAngles ang = row_angles(rt, lane, p.seq.pos_t[tok], p.seq.pos_h[tok], p.seq.pos_w[tok]);
+    const LaneRope lr = lane_rope(rt, lane);
+    const RowAngles ang = row_angles(lr, p.seq.pos_t[tok], p.seq.pos_h[tok], p.seq.pos_w[tok]);
     float wq[4], wk[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) { wq[e] = p.wq[4 * lane + e]; wk[e] = p.wk[4 * lane + e]; }
@@ -123,9 +124,9 @@ prologue_kernel(Problem p, __half* __restrict__ qhat, __half* __restrict__ khat,
         for (int b = 0; b < kProBatch; ++b)
             if (h0 + b < p.H) {
                 float y[4];
-                row_norm_rope(xq[b], wq, ang, rt, lane, p.eps, y);
+                row_norm_rope(xq[b], wq, ang, lr, p.eps, y);
                 ok &= store_row4_f16(qhat + base + (size_t)(h0 + b) * kD, y);
-                row_norm_rope(xk[b], wk, ang, rt, lane, p.eps, y);
+                row_norm_rope(xk[b], wk, ang, lr, p.eps, y);
                 ok &= store_row4_f16(khat + base + (size_t)(h0 + b) * kD, y);
             }
     }

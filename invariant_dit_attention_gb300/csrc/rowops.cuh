@@ -23,21 +23,36 @@ struct RowAngles {
     float c[4], s[4];
 };
 
+// The lane's view of the rotary table, read once (the table lives in the
+// constant bank, where lanes reading different entries would serialise).
+struct LaneRope {
+    float f[4];   // frequencies of the lane's four channels
+    int axis;     // 0/1/2 = t/h/w, -1 = not rotated
+    int partner;  // lane holding the paired channels
+    int second;   // 1 if the lane's channels are the second half of their section
+};
+
+__device__ __forceinline__ LaneRope lane_rope(const RopeTable& rt, int lane) {
+    LaneRope r;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) r.f[e] = rt.inv_freq[4 * lane + e];
+    r.axis = rt.axis[lane];
+    r.partner = rt.partner[lane];
+    r.second = rt.second[lane];
+    return r;
+}
+
 // cos/sin of the lane's four channels for one token (identity if not rotated).
-__device__ __forceinline__ RowAngles row_angles(const RopeTable& rt, int lane, int pt, int ph, int pw) {
+__device__ __forceinline__ RowAngles row_angles(const LaneRope& lr, int pt, int ph, int pw) {
     RowAngles a;
-    int ax = rt.axis[lane];
-    if (ax < 0) {
+    if (lr.axis < 0) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) { a.c[e] = 1.f; a.s[e] = 0.f; }
         return a;
     }
-    float p = static_cast<float>(ax == 0 ? pt : (ax == 1 ? ph : pw));
+    const float p = static_cast<float>(lr.axis == 0 ? pt : (lr.axis == 1 ? ph : pw));
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        float ang = p * rt.inv_freq[4 * lane + e];
-        sincosf(ang, &a.s[e], &a.c[e]);
-    }
+    for (int e = 0; e < 4; ++e) sincosf(p * lr.f[e], &a.s[e], &a.c[e]);
     return a;
 }
 
@@ -50,18 +65,17 @@ __device__ __forceinline__ float row_rstd(const float (&x)[4], float eps) {
 
 // y = RoPE(RMSNorm(x) * w) for one row.
 __device__ __forceinline__ void row_norm_rope(const float (&x)[4], const float (&w)[4], const RowAngles& a,
-                                              const RopeTable& rt, int lane, float eps, float (&y)[4]) {
+                                              const LaneRope& lr, float eps, float (&y)[4]) {
     float r = row_rstd(x, eps);
     float z[4], zp[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) z[e] = (x[e] * r) * w[e];
-    int partner = rt.partner[lane];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) zp[e] = __shfl_sync(0xffffffffu, z[e], partner);
-    if (rt.axis[lane] < 0) {
+    for (int e = 0; e < 4; ++e) zp[e] = __shfl_sync(0xffffffffu, z[e], lr.partner);
+    if (lr.axis < 0) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) y[e] = z[e];
-    } else if (!rt.second[lane]) {  // (u, v) = (own, partner): u cos - v sin
+    } else if (!lr.second) {  // (u, v) = (own, partner): u cos - v sin
 #pragma unroll
         for (int e = 0; e < 4; ++e) y[e] = z[e] * a.c[e] - zp[e] * a.s[e];
     } else {                         // (u, v) = (partner, own): u sin + v cos
@@ -73,16 +87,15 @@ __device__ __forceinline__ void row_norm_rope(const float (&x)[4], const float (
 // Backward of row_norm_rope.  dy: gradient at the rotated output; x: the raw
 // input row.  Writes dx and adds g*n into dw_acc.
 __device__ __forceinline__ void row_norm_rope_bwd(const float (&dy)[4], const float (&x)[4], const float (&w)[4],
-                                                  const RowAngles& a, const RopeTable& rt, int lane, float eps,
+                                                  const RowAngles& a, const LaneRope& lr, float eps,
                                                   float (&dx)[4], float (&dw_acc)[4]) {
     float dyp[4], g[4];
-    int partner = rt.partner[lane];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) dyp[e] = __shfl_sync(0xffffffffu, dy[e], partner);
-    if (rt.axis[lane] < 0) {
+    for (int e = 0; e < 4; ++e) dyp[e] = __shfl_sync(0xffffffffu, dy[e], lr.partner);
+    if (lr.axis < 0) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) g[e] = dy[e];
-    } else if (!rt.second[lane]) {  // g_u = dy_u cos + dy_v sin
+    } else if (!lr.second) {  // g_u = dy_u cos + dy_v sin
 #pragma unroll
         for (int e = 0; e < 4; ++e) g[e] = dy[e] * a.c[e] + dyp[e] * a.s[e];
     } else {                         // g_v = -dy_u sin + dy_v cos
