@@ -40,7 +40,8 @@ constexpr int kOffFixed = 0;           // the tile pair loaded once per item (al
 constexpr int kOffRing = kPair;        // 2-stage ring of tile pairs
 constexpr int kOffLse = kOffRing + 2 * kPair;  // [2 wg][2 buf][2][64] floats
 constexpr int kOffRed = kOffLse + 2 * 2 * 2 * 64 * 4;  // [8 warps][128] floats
-constexpr int kOffBar = kOffRed + 8 * 128 * 4;
+constexpr int kOffRope = kOffRed + 8 * 128 * 4;  // shared copy of the rotary table
+constexpr int kOffBar = kOffRope + 768;
 constexpr int kSmem = kOffBar + 256 + 1024;
 constexpr float kLog2e = 1.4426950408889634f;
 enum { bFixedFull = 0, bItemFree, bRingFull, bRingEmpty = bRingFull + 2, bSFull = bRingEmpty + 2, bPFull,
@@ -111,8 +112,8 @@ __device__ __forceinline__ void zero_rows(uint32_t half, int valid, int lane) {
 // RMSNorm backward per row (one warp per row, 8 warps), dx rows in bf16, and
 // the tile's norm-weight partial (fixed order: rows by warp, then warps).
 __device__ __forceinline__ void rows_epilogue(const uint8_t* stage, float* red, const BwdTcParams& p,
-                                              const BwdItem& it, const RopeTable& rt, int w8, int lane) {
-    const LaneRope lr = lane_rope(rt, lane);
+                                              const BwdItem& it, const RopeTable& srt, int w8, int lane) {
+    const LaneRope lr = lane_rope(srt, lane);
     float wl[4], acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int e = 0; e < 4; ++e) wl[e] = p.w[4 * lane + e];
@@ -178,6 +179,8 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         tc::tmem_relinquish();
         tc::fence_before_sync();
     }
+    RopeTable& srt = *reinterpret_cast<RopeTable*>(smem + kOffRope);
+    rope_to_smem(rt, srt, tid, kThreads);
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
@@ -256,7 +259,24 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             constexpr uint32_t idSbf = tc::idesc_f16(true, false, 128, 128);
             constexpr uint32_t idAbf = tc::idesc_f16(true, true, 128, 128);
             constexpr uint32_t idA16 = tc::idesc_f16(false, true, 128, 128);
-            uint32_t it_ring = 0, items = 0, cntP = 0, cntDone = 0;
+            uint32_t it_ring = 0, items = 0, cntP = 0;
+            // S^T(i+1), dP^T(i+1) are issued right behind dV(i), dK(i): the thread's
+            // MMAs run in order, so P^T(i), dS^T(i) are read before being overwritten.
+            auto issue_s = [&](uint32_t kaddr, uint32_t vaddr, uint32_t qaddr, uint32_t doaddr) {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
+                    tc::mma_ss(tmem + cS, tc::smem_desc_sw128(kaddr + koff, 16, 1024),
+                               tc::smem_desc_sw128(qaddr + koff, 16, 1024), idS16, kk > 0);
+                }
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
+                    tc::mma_ss(tmem + cDP, tc::smem_desc_sw128(vaddr + koff, 16, 1024),
+                               tc::smem_desc_sw128(doaddr + koff, 16, 1024), idSbf, kk > 0);
+                }
+                tc::mma_commit(bar(bSFull));
+            };
             for (int i = blockIdx.x; !failed; i += gridDim.x) {
                 BwdItem it;
                 if (!bwd_item(p, i, it)) break;
@@ -264,29 +284,16 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 ++items;
                 const uint32_t kaddr = sbase + kOffFixed, vaddr = kaddr + kTile;
                 const int nq = (it.L + 127) / 128;
+                uint32_t slot = it_ring & 1;
+                if (!tc::mbar_wait(bar(bRingFull + slot), (it_ring >> 1) & 1, abort_flag)) { fail(); break; }
+                ++it_ring;
+                tc::fence_after_sync();
+                issue_s(kaddr, vaddr, sbase + kOffRing + slot * kPair, sbase + kOffRing + slot * kPair + kTile);
                 for (int qi = 0; qi < nq; ++qi) {
-                    const uint32_t slot = it_ring & 1;
-                    if (!tc::mbar_wait(bar(bRingFull + slot), (it_ring >> 1) & 1, abort_flag)) { fail(); break; }
-                    ++it_ring;
-                    if (cntDone > 0 && !tc::mbar_wait(bar(bMmaDone), (cntDone - 1) & 1, abort_flag)) { fail(); break; }
-                    tc::fence_after_sync();
-                    const uint32_t qaddr = sbase + kOffRing + slot * kPair, doaddr = qaddr + kTile;
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
-                        tc::mma_ss(tmem + cS, tc::smem_desc_sw128(kaddr + koff, 16, 1024),
-                                   tc::smem_desc_sw128(qaddr + koff, 16, 1024), idS16, kk > 0);
-                    }
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
-                        tc::mma_ss(tmem + cDP, tc::smem_desc_sw128(vaddr + koff, 16, 1024),
-                                   tc::smem_desc_sw128(doaddr + koff, 16, 1024), idSbf, kk > 0);
-                    }
-                    tc::mma_commit(bar(bSFull));
                     if (!tc::mbar_wait(bar(bPFull), cntP & 1, abort_flag)) { fail(); break; }
                     ++cntP;
                     tc::fence_after_sync();
+                    const uint32_t qaddr = sbase + kOffRing + slot * kPair, doaddr = qaddr + kTile;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
                         tc::mma_ts(tmem + cA0, tmem + cS + a_col(kk),
@@ -296,8 +303,13 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                         tc::mma_ts(tmem + cA1, tmem + cDP + a_col(kk),
                                    tc::smem_desc_sw128(qaddr + kk * 2048, kHalf, 1024), idA16, (qi > 0) || (kk > 0));
                     tc::mma_commit(bar(bMmaDone));
-                    ++cntDone;
                     tc::mma_commit(bar(bRingEmpty + slot));
+                    if (qi + 1 < nq) {
+                        slot = it_ring & 1;
+                        if (!tc::mbar_wait(bar(bRingFull + slot), (it_ring >> 1) & 1, abort_flag)) { fail(); break; }
+                        ++it_ring;
+                        issue_s(kaddr, vaddr, sbase + kOffRing + slot * kPair, sbase + kOffRing + slot * kPair + kTile);
+                    }
                 }
                 if (failed) break;
             }
@@ -418,7 +430,7 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 }
             }
             named_bar(3, 256);
-            rows_epilogue(smem + kOffFixed, red, p, it, rt, w8, lane);
+            rows_epilogue(smem + kOffFixed, red, p, it, srt, w8, lane);
             tc::fence_before_sync();
             tc::fence_proxy_async();
             __syncwarp();
@@ -475,6 +487,8 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         tc::tmem_relinquish();
         tc::fence_before_sync();
     }
+    RopeTable& srt = *reinterpret_cast<RopeTable*>(smem + kOffRope);
+    rope_to_smem(rt, srt, tid, kThreads);
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
@@ -548,7 +562,24 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
             constexpr uint32_t idS16 = tc::idesc_f16(false, false, 128, 128);
             constexpr uint32_t idSbf = tc::idesc_f16(true, false, 128, 128);
             constexpr uint32_t idA16 = tc::idesc_f16(false, true, 128, 128);
-            uint32_t it_ring = 0, items = 0, cntP = 0, cntDone = 0;
+            uint32_t it_ring = 0, items = 0, cntP = 0;
+            // S(j+1), dP(j+1) are issued right behind dQ(j) (in-order MMAs: dS(j) is
+            // read before it is overwritten).
+            auto issue_s = [&](uint32_t qaddr, uint32_t doaddr, uint32_t kaddr, uint32_t vaddr) {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
+                    tc::mma_ss(tmem + cS, tc::smem_desc_sw128(qaddr + koff, 16, 1024),
+                               tc::smem_desc_sw128(kaddr + koff, 16, 1024), idS16, kk > 0);
+                }
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
+                    tc::mma_ss(tmem + cDP, tc::smem_desc_sw128(doaddr + koff, 16, 1024),
+                               tc::smem_desc_sw128(vaddr + koff, 16, 1024), idSbf, kk > 0);
+                }
+                tc::mma_commit(bar(bSFull));
+            };
             for (int i = blockIdx.x; !failed; i += gridDim.x) {
                 BwdItem it;
                 if (!bwd_item(p, i, it)) break;
@@ -556,36 +587,28 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                 ++items;
                 const uint32_t qaddr = sbase + kOffFixed, doaddr = qaddr + kTile;
                 const int nk = (it.L + 127) / 128;
+                uint32_t slot = it_ring & 1;
+                if (!tc::mbar_wait(bar(bRingFull + slot), (it_ring >> 1) & 1, abort_flag)) { fail(); break; }
+                ++it_ring;
+                tc::fence_after_sync();
+                issue_s(qaddr, doaddr, sbase + kOffRing + slot * kPair, sbase + kOffRing + slot * kPair + kTile);
                 for (int kj = 0; kj < nk; ++kj) {
-                    const uint32_t slot = it_ring & 1;
-                    if (!tc::mbar_wait(bar(bRingFull + slot), (it_ring >> 1) & 1, abort_flag)) { fail(); break; }
-                    ++it_ring;
-                    if (cntDone > 0 && !tc::mbar_wait(bar(bMmaDone), (cntDone - 1) & 1, abort_flag)) { fail(); break; }
-                    tc::fence_after_sync();
-                    const uint32_t kaddr = sbase + kOffRing + slot * kPair, vaddr = kaddr + kTile;
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
-                        tc::mma_ss(tmem + cS, tc::smem_desc_sw128(qaddr + koff, 16, 1024),
-                                   tc::smem_desc_sw128(kaddr + koff, 16, 1024), idS16, kk > 0);
-                    }
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
-                        tc::mma_ss(tmem + cDP, tc::smem_desc_sw128(doaddr + koff, 16, 1024),
-                                   tc::smem_desc_sw128(vaddr + koff, 16, 1024), idSbf, kk > 0);
-                    }
-                    tc::mma_commit(bar(bSFull));
                     if (!tc::mbar_wait(bar(bPFull), cntP & 1, abort_flag)) { fail(); break; }
                     ++cntP;
                     tc::fence_after_sync();
+                    const uint32_t kaddr = sbase + kOffRing + slot * kPair;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
                         tc::mma_ts(tmem + cA0, tmem + cS + a_col(kk),
                                    tc::smem_desc_sw128(kaddr + kk * 2048, kHalf, 1024), idA16, (kj > 0) || (kk > 0));
                     tc::mma_commit(bar(bMmaDone));
-                    ++cntDone;
                     tc::mma_commit(bar(bRingEmpty + slot));
+                    if (kj + 1 < nk) {
+                        slot = it_ring & 1;
+                        if (!tc::mbar_wait(bar(bRingFull + slot), (it_ring >> 1) & 1, abort_flag)) { fail(); break; }
+                        ++it_ring;
+                        issue_s(qaddr, doaddr, sbase + kOffRing + slot * kPair, sbase + kOffRing + slot * kPair + kTile);
+                    }
                 }
                 if (failed) break;
             }
@@ -673,7 +696,7 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                 }
             }
             named_bar(3, 256);
-            rows_epilogue(smem + kOffFixed, red, p, it, rt, w8, lane);
+            rows_epilogue(smem + kOffFixed, red, p, it, srt, w8, lane);
             tc::fence_before_sync();
             tc::fence_proxy_async();
             __syncwarp();

@@ -29,6 +29,7 @@ struct RopeTable {
     int8_t axis[32];          // 0/1/2 = t/h/w, -1 = not rotated
     int8_t partner[32];       // lane holding the paired channels
     int8_t second[32];        // 1 if this group is the second half of its section
+    int8_t pad[32];           // keeps the size a multiple of 16 bytes
 };
 
 // Per-call plan written on the device from seg_offsets: samples ordered by

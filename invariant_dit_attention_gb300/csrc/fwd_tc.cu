@@ -205,41 +205,45 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             constexpr uint32_t idS = tc::idesc_f16(false, false, 128, 128);  // fp16 x fp16, K-major B
             constexpr uint32_t idP = tc::idesc_f16(true, true, 128, 128);    // bf16 x bf16, MN-major B
             uint32_t kv_it = 0, items = 0, cntPV[2] = {0, 0}, itemsX[2] = {0, 0};
+            // S_X(j+1) is issued right behind PV_X(j): tcgen05 MMAs of one thread run in
+            // order, so PV_X(j) has read P_X(j) before S_X(j+1) overwrites those columns,
+            // and S_X(j+1) completing implies PV_X(j) completed (the softmax relies on
+            // that before it rescales O_X).
+            auto issue_s = [&](int x, uint32_t kaddr) {
+                const uint32_t qaddr = sbase + kOffQ + x * kTile;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
+                    tc::mma_ss(tmem + kColS0 + 128 * x, tc::smem_desc_sw128(qaddr + koff, 16, 1024),
+                               tc::smem_desc_sw128(kaddr + koff, 16, 1024), idS, kk > 0);
+                }
+                tc::mma_commit(bar(bSFull + x));
+            };
             for (int i = blockIdx.x; !failed; i += gridDim.x) {
                 FwdItem it;
                 if (!fwd_item(p, i, it)) break;
                 const int nX = it.hasB ? 2 : 1;
                 if (!tc::mbar_wait(bar(bQFull), items & 1, abort_flag)) { fail(); break; }
                 ++items;
+                // ---- S_X(0) = Q_X K_0^T
+                uint32_t kslot = kv_it % kNST;
+                if (!tc::mbar_wait(bar(bKVFull + kslot), (kv_it / kNST) & 1, abort_flag)) { fail(); break; }
+                ++kv_it;
+                tc::fence_after_sync();
+                for (int x = 0; x < nX; ++x) issue_s(x, sbase + kOffKV + kslot * kTile);
+                tc::mma_commit(bar(bKVEmpty + kslot));
+                if (it.nkv == 1) tc::mma_commit(bar(bQEmpty));
                 for (int j = 0; j < it.nkv && !failed; ++j) {
-                    // ---- S_X = Q_X K_j^T
-                    uint32_t slot = kv_it % kNST;
-                    if (!tc::mbar_wait(bar(bKVFull + slot), (kv_it / kNST) & 1, abort_flag)) { fail(); break; }
+                    const uint32_t vslot = kv_it % kNST;
+                    if (!tc::mbar_wait(bar(bKVFull + vslot), (kv_it / kNST) & 1, abort_flag)) { fail(); break; }
                     ++kv_it;
-                    const uint32_t kaddr = sbase + kOffKV + slot * kTile;
-                    for (int x = 0; x < nX && !failed; ++x) {
-                        if (cntPV[x] > 0 && !tc::mbar_wait(bar(bPVDone + x), (cntPV[x] - 1) & 1, abort_flag)) {
-                            fail();
-                            break;
-                        }
-                        tc::fence_after_sync();
-                        const uint32_t qaddr = sbase + kOffQ + x * kTile;
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
-                            tc::mma_ss(tmem + kColS0 + 128 * x, tc::smem_desc_sw128(qaddr + koff, 16, 1024),
-                                       tc::smem_desc_sw128(kaddr + koff, 16, 1024), idS, kk > 0);
-                        }
-                        tc::mma_commit(bar(bSFull + x));
+                    const bool more = j + 1 < it.nkv;
+                    if (more) {
+                        kslot = kv_it % kNST;
+                        if (!tc::mbar_wait(bar(bKVFull + kslot), (kv_it / kNST) & 1, abort_flag)) { fail(); break; }
+                        ++kv_it;
                     }
-                    if (failed) break;
-                    tc::mma_commit(bar(bKVEmpty + slot));
-                    if (j == it.nkv - 1) tc::mma_commit(bar(bQEmpty));
-                    // ---- O_X += P_X V_j
-                    slot = kv_it % kNST;
-                    if (!tc::mbar_wait(bar(bKVFull + slot), (kv_it / kNST) & 1, abort_flag)) { fail(); break; }
-                    ++kv_it;
-                    const uint32_t vaddr = sbase + kOffKV + slot * kTile;
+                    const uint32_t vaddr = sbase + kOffKV + vslot * kTile;
                     for (int x = 0; x < nX && !failed; ++x) {
                         if (j == 0 && itemsX[x] > 0 &&
                             !tc::mbar_wait(bar(bOFree + x), (itemsX[x] - 1) & 1, abort_flag)) {
@@ -248,15 +252,22 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                         }
                         if (!tc::mbar_wait(bar(bPFull + x), cntPV[x] & 1, abort_flag)) { fail(); break; }
                         tc::fence_after_sync();
+                        // ---- O_X += P_X V_j
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
                             tc::mma_ts(tmem + kColO0 + 128 * x, tmem + kColS0 + 128 * x + 8 * kk,
                                        tc::smem_desc_sw128(vaddr + kk * 2048, kHalf, 1024), idP, (j > 0) || (kk > 0));
                         tc::mma_commit(bar(bPVDone + x));
                         ++cntPV[x];
+                        // ---- S_X(j+1) = Q_X K_{j+1}^T
+                        if (more) issue_s(x, sbase + kOffKV + kslot * kTile);
                     }
                     if (failed) break;
-                    tc::mma_commit(bar(bKVEmpty + slot));
+                    tc::mma_commit(bar(bKVEmpty + vslot));
+                    if (more) {
+                        tc::mma_commit(bar(bKVEmpty + kslot));
+                        if (j + 2 == it.nkv) tc::mma_commit(bar(bQEmpty));
+                    }
                 }
                 for (int x = 0; x < nX; ++x) ++itemsX[x];
             }

@@ -100,10 +100,13 @@ constexpr int kProBatch = 4;  // heads loaded ahead per warp
 __global__ void __launch_bounds__(kProWarps * 32)
 prologue_kernel(Problem p, __half* __restrict__ qhat, __half* __restrict__ khat,
                 const __grid_constant__ RopeTable rt, unsigned* err) {
+    __shared__ RopeTable srt;
+    rope_to_smem(rt, srt, threadIdx.x, blockDim.x);
+    __syncthreads();
     const int lane = threadIdx.x & 31;
     const int tok = blockIdx.x * kProWarps + (threadIdx.x >> 5);
     if (tok >= p.seq.S) return;
-    const LaneRope lr = lane_rope(rt, lane);
+    const LaneRope lr = lane_rope(srt, lane);
     const RowAngles ang = row_angles(lr, p.seq.pos_t[tok], p.seq.pos_h[tok], p.seq.pos_w[tok]);
     float wq[4], wk[4];
 #pragma unroll

@@ -32,6 +32,15 @@ struct LaneRope {
     int second;   // 1 if the lane's channels are the second half of their section
 };
 
+// Copies the rotary table into shared memory (call with the whole block, then
+// __syncthreads); lanes then read their entries from there instead of issuing
+// per-lane indexed reads of the kernel-parameter bank.
+__device__ __forceinline__ void rope_to_smem(const RopeTable& rt, RopeTable& dst, int tid, int nthreads) {
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(&rt);
+    uint32_t* d = reinterpret_cast<uint32_t*>(&dst);
+    for (int i = tid; i < (int)(sizeof(RopeTable) / 4); i += nthreads) d[i] = src[i];
+}
+
 __device__ __forceinline__ LaneRope lane_rope(const RopeTable& rt, int lane) {
     LaneRope r;
 #pragma unroll
