@@ -18,11 +18,12 @@
 //
 // Both main kernels are persistent (one CTA per SM) with the forward's roles:
 // warp 0 TMA producer, warp 1 single-thread tcgen05 issuer, warps 4-7 and 8-11
-// two warpgroups that split the 128 columns of each 128 x 128 score tile
-// (thread = TMEM lane = one row).  Operands: S on fp16 q^/k^, dP on bf16 dO/v,
-// P (bf16) and dS (fp16) written back into tensor memory over the columns
-// their warpgroup just read, and fed to the accumulating MMAs as the
-// TMEM-resident A operand.
+// two warpgroups that ping-pong over the 64-row blocks streamed against the
+// CTA's 128-row tile (thread = TMEM lane = one row of the tile), so the tensor
+// pipe computes one block's products while the other block's softmax
+// gradient runs.  Operands: S on fp16 q^/k^, dP on bf16 dO/v, P (bf16) and dS
+// (fp16) written back into tensor memory over the columns their warpgroup
+// just read, and fed to the accumulating MMAs as the TMEM-resident A operand.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -36,18 +37,22 @@ constexpr int kThreads = 384;
 constexpr int kTile = 128 * 128 * 2;   // 32 KB
 constexpr int kHalf = 128 * 64 * 2;    // 16 KB
 constexpr int kPair = 2 * kTile;       // two tiles (q^ + dO, or k^ + v): 64 KB
-constexpr int kOffFixed = 0;           // the tile pair loaded once per item (also the epilogue stage)
-constexpr int kOffRing = kPair;        // 2-stage ring of tile pairs
-constexpr int kOffLse = kOffRing + 2 * kPair;  // [2 wg][2 buf][2][64] floats
+constexpr int kBlk = 64 * 128 * 2;    // one streamed 64-row block: 16 KB
+constexpr int kBlkHalf = 64 * 64 * 2;  // its 64-channel half (the TMA box): 8 KB
+constexpr int kBlkPair = 2 * kBlk;     // q^ + dO block, or k^ + v block: 32 KB
+constexpr int kRing = 3;               // ring stages of block pairs
+constexpr int kOffFixed = 0;           // the 128-row tile pair loaded once per item (also the epilogue stage)
+constexpr int kOffRing = kPair;        // ring of block pairs
+constexpr int kOffDs = kOffRing + kRing * kBlkPair;  // dq: dS of the two blocks in flight, [128][64] fp16 each
+constexpr int kDsBytes = 128 * 64 * 2;
+constexpr int kOffLse = kOffDs + 2 * kDsBytes;  // [2 wg][2 buf][2][64] floats
 constexpr int kOffRed = kOffLse + 2 * 2 * 2 * 64 * 4;  // [8 warps][128] floats
 constexpr int kOffRope = kOffRed + 8 * 128 * 4;  // shared copy of the rotary table
 constexpr int kOffBar = kOffRope + 768;
 constexpr int kSmem = kOffBar + 256 + 1024;
 constexpr float kLog2e = 1.4426950408889634f;
-enum { bFixedFull = 0, bItemFree, bRingFull, bRingEmpty = bRingFull + 2, bSFull = bRingEmpty + 2, bPFull,
-       bMmaDone, bTail, bDone, bCount };
-// TMEM columns
-constexpr uint32_t cS = 0, cDP = 128, cA0 = 256, cA1 = 384;
+enum { bFixedFull = 0, bItemFree, bRingFull, bRingEmpty = bRingFull + kRing, bSFull = bRingEmpty + kRing,
+       bPFull = bSFull + 2, bSUsed = bPFull + 2, bDsFree = bSUsed + 2, bAccDone = bDsFree + 2, bTail, bDone, bCount };
 }  // namespace bwdt
 
 struct BwdTcParams {
@@ -101,11 +106,34 @@ __device__ __forceinline__ void named_bar(int id, int count) {
 // and warp-per-row reads are free of bank conflicts.
 __device__ __forceinline__ uint32_t stage_off(int r, int c4) { return (uint32_t)(r * 512 + ((c4 ^ (r & 7)) << 4)); }
 
-// Zeroes rows [valid, 128) of a 64-channel-half tile (whole 128-byte rows).
-__device__ __forceinline__ void zero_rows(uint32_t half, int valid, int lane) {
-    for (int r = valid + (lane >> 3); r < 128; r += 4)
+// Zeroes rows [valid, rows) of a 64-channel-half tile (whole 128-byte rows).
+__device__ __forceinline__ void zero_rows(uint32_t half, int valid, int rows, int lane) {
+    for (int r = valid + (lane >> 3); r < rows; r += 4)
         asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" :: "r"(half + (uint32_t)r * 128 + (lane & 7) * 16),
                      "r"(0) : "memory");
+}
+
+__device__ __forceinline__ void init_bars(uint32_t sbase) {
+    using namespace bwdt;
+    auto bar = [&](int i) { return sbase + kOffBar + 8u * i; };
+    tc::mbar_init(bar(bFixedFull), 1);
+    tc::mbar_init(bar(bItemFree), 8);
+    for (int i = 0; i < kRing; ++i) {
+        tc::mbar_init(bar(bRingFull + i), 1);
+        tc::mbar_init(bar(bRingEmpty + i), 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+        tc::mbar_init(bar(bSFull + x), 1);
+        tc::mbar_init(bar(bPFull + x), 4);
+    }
+    for (int x = 0; x < 2; ++x) {
+        tc::mbar_init(bar(bSUsed + x), 4);
+        tc::mbar_init(bar(bDsFree + x), 1);
+    }
+    tc::mbar_init(bar(bAccDone), 1);
+    tc::mbar_init(bar(bTail), 1);
+    tc::mbar_init(bar(bDone), 1);
+    tc::fence_mbar_init();
 }
 
 // Row epilogue over a staged tile of d(x^) (already scaled): RoPE^-1 and the
@@ -118,14 +146,31 @@ __device__ __forceinline__ void rows_epilogue(const uint8_t* stage, float* red, 
 #pragma unroll
     for (int e = 0; e < 4; ++e) wl[e] = p.w[4 * lane + e];
     const int nvalid = min(128, it.L - 128 * it.tile);
-    for (int r = w8; r < nvalid; r += 8) {
-        const int row = it.row0 + r;
-        const float4 s4 = *reinterpret_cast<const float4*>(stage + stage_off(r, lane));
-        float dy[4] = {s4.x, s4.y, s4.z, s4.w}, xr[4], d[4];
-        load_row4(p.x + ((size_t)row * p.H + it.h) * kD + 4 * lane, xr);
-        const RowAngles a = row_angles(lr, p.seq.pos_t[row], p.seq.pos_h[row], p.seq.pos_w[row]);
-        row_norm_rope_bwd(dy, xr, wl, a, lr, p.eps, d, acc);
-        store_row4(p.dx + ((size_t)row * p.H + it.h) * kD + 4 * lane, d);
+    // rows w8, w8 + 8, ...: four rows per batch so their loads overlap
+    for (int r0 = w8; r0 < nvalid; r0 += 32) {
+        float dy[4][4], xr[4][4];
+        int pos[4][3];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int r = min(r0 + 8 * u, nvalid - 1);
+            const int row = it.row0 + r;
+            const float4 s4 = *reinterpret_cast<const float4*>(stage + stage_off(r, lane));
+            dy[u][0] = s4.x; dy[u][1] = s4.y; dy[u][2] = s4.z; dy[u][3] = s4.w;
+            load_row4(p.x + ((size_t)row * p.H + it.h) * kD + 4 * lane, xr[u]);
+            pos[u][0] = p.seq.pos_t[row];
+            pos[u][1] = p.seq.pos_h[row];
+            pos[u][2] = p.seq.pos_w[row];
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int r = r0 + 8 * u;
+            if (r >= nvalid) break;
+            const int row = it.row0 + r;
+            float d[4];
+            const RowAngles a = row_angles(lr, pos[u][0], pos[u][1], pos[u][2]);
+            row_norm_rope_bwd(dy[u], xr[u], wl, a, lr, p.eps, d, acc);
+            store_row4(p.dx + ((size_t)row * p.H + it.h) * kD + 4 * lane, d);
+        }
     }
 #pragma unroll
     for (int e = 0; e < 4; ++e) red[w8 * kD + 4 * lane + e] = acc[e];
@@ -139,16 +184,23 @@ __device__ __forceinline__ void rows_epilogue(const uint8_t* stage, float* red, 
     }
 }
 
-// Column of the TMEM A operand for K-step kk (16 columns of the score tile):
-// warpgroup 0 wrote columns 0..63 of the tile at TMEM [0, 32), warpgroup 1
-// columns 64..127 at [64, 96).
-__device__ __forceinline__ uint32_t a_col(int kk) { return kk < 4 ? 8 * kk : 64 + 8 * (kk - 4); }
+// Streamed blocks are 64 rows (queries in dkdv, keys in dq), so two score
+// buffers fit beside the accumulators in TMEM: buffer X (X = block parity)
+// holds S at cols [128X, 128X+64) and dP at [128X+64, 128X+128); warpgroup X
+// handles the blocks of parity X.
+//   dkdv: P^T (bf16) is written over S's first 32 columns and dS^T (fp16) over
+//         dP's; accumulators dV [256, 384), dK [384, 512).  Buffer X is refilled
+//         with block b+2 right behind block b's dV/dK MMAs (in-order MMAs).
+//   dq:   dS (fp16) goes to a 128-byte-swizzled shared-memory tile X, so buffer X
+//         is refilled with block b+2 as soon as warpgroup X has loaded block b;
+//         the tile is rewritten only after block b's dQ MMAs completed.
+//         Accumulator dQ [256, 384).
 
 // ------------------------------------------------------------------ dK, dV
 
 __global__ void __launch_bounds__(bwdt::kThreads, 1)
-dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-               const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
+dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq64, const __grid_constant__ CUtensorMap mk,
+               const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo64,
                const __grid_constant__ RopeTable rt, const BwdTcParams p) {
     using namespace bwdt;
     extern __shared__ uint8_t smem_raw[];
@@ -159,21 +211,7 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 8 * bCount + 4);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    if (tid == 0) {
-        tc::mbar_init(bar(bFixedFull), 1);
-        tc::mbar_init(bar(bItemFree), 8);
-        for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(bar(bRingFull + i), 1);
-            tc::mbar_init(bar(bRingEmpty + i), 1);
-        }
-        tc::mbar_init(bar(bSFull), 1);
-        tc::mbar_init(bar(bPFull), 8);
-        tc::mbar_init(bar(bMmaDone), 1);
-        tc::mbar_init(bar(bTail), 1);
-        tc::mbar_init(bar(bDone), 1);
-        *abort_flag = 0;
-        tc::fence_mbar_init();
-    }
+    if (tid == 0) init_bars(sbase);
     if (warp == 1) {
         tc::tmem_alloc(smem_u32(tmem_slot), 512);
         tc::tmem_relinquish();
@@ -181,6 +219,7 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
     }
     RopeTable& srt = *reinterpret_cast<RopeTable*>(smem + kOffRope);
     rope_to_smem(rt, srt, tid, kThreads);
+    if (tid == 0) *abort_flag = 0;
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
@@ -198,7 +237,7 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
-        uint32_t it_ring = 0, items = 0, tails = 0;
+        uint32_t ring = 0, items = 0, tails = 0;
         for (int i = blockIdx.x; !failed; i += gridDim.x) {
             BwdItem it;
             if (!bwd_item(p, i, it)) break;
@@ -217,21 +256,21 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             }
             failed = __shfl_sync(0xffffffffu, failed, 0);
             ++items;
-            const int nq = (it.L + 127) / 128;
-            for (int qi = 0; qi < nq && !failed; ++qi) {
-                const uint32_t slot = it_ring & 1, ph = (it_ring >> 1) & 1;
-                const uint32_t dst = sbase + kOffRing + slot * kPair;
-                const int y = it.seg0 + 128 * qi;
-                const int valid = it.L - 128 * qi;
-                const bool tail = valid < 128;
+            const int nb = (it.L + 63) / 64;
+            for (int b = 0; b < nb && !failed; ++b) {
+                const uint32_t slot = ring % kRing, ph = (ring / kRing) & 1;
+                const uint32_t dst = sbase + kOffRing + slot * kBlkPair;
+                const int y = it.seg0 + 64 * b;
+                const int valid = it.L - 64 * b;
+                const bool tail = valid < 64;
                 if (lane == 0) {
                     if (!tc::mbar_wait(bar(bRingEmpty + slot), ph ^ 1, abort_flag)) fail();
                     if (!failed) {
-                        const uint32_t b = tail ? bar(bTail) : bar(bRingFull + slot);
-                        tc::mbar_expect_tx(b, kPair);
+                        const uint32_t bb = tail ? bar(bTail) : bar(bRingFull + slot);
+                        tc::mbar_expect_tx(bb, kBlkPair);
                         for (int hf = 0; hf < 2; ++hf) {
-                            tc::tma_load_2d(dst + hf * kHalf, &mq, x0 + 64 * hf, y, b);
-                            tc::tma_load_2d(dst + kTile + hf * kHalf, &mdo, x0 + 64 * hf, y, b);
+                            tc::tma_load_2d(dst + hf * kBlkHalf, &mq64, x0 + 64 * hf, y, bb);
+                            tc::tma_load_2d(dst + kBlk + hf * kBlkHalf, &mdo64, x0 + 64 * hf, y, bb);
                         }
                         if (tail && !tc::mbar_wait(bar(bTail), tails & 1, abort_flag)) fail();
                     }
@@ -242,76 +281,86 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                     // query rows past the sample end: zero q^ and dO so no neighbour
                     // value reaches the dV and dK products
                     for (int hf = 0; hf < 2; ++hf) {
-                        zero_rows(dst + hf * kHalf, valid, lane);
-                        zero_rows(dst + kTile + hf * kHalf, valid, lane);
+                        zero_rows(dst + hf * kBlkHalf, valid, 64, lane);
+                        zero_rows(dst + kBlk + hf * kBlkHalf, valid, 64, lane);
                     }
                     tc::fence_proxy_async();
                     __syncwarp();
                     if (lane == 0) tc::mbar_arrive(bar(bRingFull + slot));
                 }
-                ++it_ring;
+                ++ring;
             }
         }
     } else if (warp == 1) {
         // ----------------------------------------------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idS16 = tc::idesc_f16(false, false, 128, 128);
-            constexpr uint32_t idSbf = tc::idesc_f16(true, false, 128, 128);
+            constexpr uint32_t idS16 = tc::idesc_f16(false, false, 128, 64);
+            constexpr uint32_t idSbf = tc::idesc_f16(true, false, 128, 64);
             constexpr uint32_t idAbf = tc::idesc_f16(true, true, 128, 128);
             constexpr uint32_t idA16 = tc::idesc_f16(false, true, 128, 128);
-            uint32_t it_ring = 0, items = 0, cntP = 0;
-            // S^T(i+1), dP^T(i+1) are issued right behind dV(i), dK(i): the thread's
-            // MMAs run in order, so P^T(i), dS^T(i) are read before being overwritten.
-            auto issue_s = [&](uint32_t kaddr, uint32_t vaddr, uint32_t qaddr, uint32_t doaddr) {
+            // descriptors are built once; per MMA only the 16-byte start address moves
+            const uint64_t dK = tc::smem_desc_sw128(sbase + kOffFixed, 16, 1024);
+            const uint64_t dV = dK + (kTile >> 4);
+            const uint64_t dRing = tc::smem_desc_sw128(sbase + kOffRing, 16, 1024);          // K-major blocks
+            const uint64_t dRingMN = tc::smem_desc_sw128(sbase + kOffRing, kBlkHalf, 1024);  // MN-major blocks
+            uint32_t ring = 0, items = 0, cntP[2] = {0, 0};
+            // S^T(b) = k^ q^(b)^T and dP^T(b) = v dO(b)^T into buffer b & 1
+            auto issue_s = [&](int x, uint32_t slot) {
+                const uint64_t bq = dRing + ((slot * kBlkPair) >> 4), bdo = bq + (kBlk >> 4);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    tc::mma_ss(tmem + cS, tc::smem_desc_sw128(kaddr + koff, 16, 1024),
-                               tc::smem_desc_sw128(qaddr + koff, 16, 1024), idS16, kk > 0);
+                    const uint32_t aoff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+                    const uint32_t boff = ((kk >> 2) * kBlkHalf + (kk & 3) * 32) >> 4;
+                    tc::mma_ss(tmem + 128 * x, dK + aoff, bq + boff, idS16, kk > 0);
                 }
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    tc::mma_ss(tmem + cDP, tc::smem_desc_sw128(vaddr + koff, 16, 1024),
-                               tc::smem_desc_sw128(doaddr + koff, 16, 1024), idSbf, kk > 0);
+                    const uint32_t aoff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+                    const uint32_t boff = ((kk >> 2) * kBlkHalf + (kk & 3) * 32) >> 4;
+                    tc::mma_ss(tmem + 128 * x + 64, dV + aoff, bdo + boff, idSbf, kk > 0);
                 }
-                tc::mma_commit(bar(bSFull));
+                tc::mma_commit(bar(bSFull + x));
             };
             for (int i = blockIdx.x; !failed; i += gridDim.x) {
                 BwdItem it;
                 if (!bwd_item(p, i, it)) break;
                 if (!tc::mbar_wait(bar(bFixedFull), items & 1, abort_flag)) { fail(); break; }
                 ++items;
-                const uint32_t kaddr = sbase + kOffFixed, vaddr = kaddr + kTile;
-                const int nq = (it.L + 127) / 128;
-                uint32_t slot = it_ring & 1;
-                if (!tc::mbar_wait(bar(bRingFull + slot), (it_ring >> 1) & 1, abort_flag)) { fail(); break; }
-                ++it_ring;
-                tc::fence_after_sync();
-                issue_s(kaddr, vaddr, sbase + kOffRing + slot * kPair, sbase + kOffRing + slot * kPair + kTile);
-                for (int qi = 0; qi < nq; ++qi) {
-                    if (!tc::mbar_wait(bar(bPFull), cntP & 1, abort_flag)) { fail(); break; }
-                    ++cntP;
+                const int nb = (it.L + 63) / 64;
+                const uint32_t ring0 = ring;
+                for (int b = 0; b < 2 && b < nb; ++b) {
+                    const uint32_t slot = ring % kRing;
+                    if (!tc::mbar_wait(bar(bRingFull + slot), (ring / kRing) & 1, abort_flag)) { fail(); break; }
+                    ++ring;
                     tc::fence_after_sync();
-                    const uint32_t qaddr = sbase + kOffRing + slot * kPair, doaddr = qaddr + kTile;
+                    issue_s(b, slot);
+                }
+                for (int b = 0; b < nb && !failed; ++b) {
+                    const int x = b & 1;
+                    const uint32_t slot = (ring0 + b) % kRing;
+                    if (!tc::mbar_wait(bar(bPFull + x), cntP[x] & 1, abort_flag)) { fail(); break; }
+                    ++cntP[x];
+                    tc::fence_after_sync();
+                    const uint64_t bq = dRingMN + ((slot * kBlkPair) >> 4), bdo = bq + (kBlk >> 4);
+                    // dV += P^T(b) dO(b), dK += dS^T(b) q^(b): K = the block's 64 queries
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        tc::mma_ts(tmem + cA0, tmem + cS + a_col(kk),
-                                   tc::smem_desc_sw128(doaddr + kk * 2048, kHalf, 1024), idAbf, (qi > 0) || (kk > 0));
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc::mma_ts(tmem + 256, tmem + 128 * x + 8 * kk, bdo + ((kk * 2048) >> 4), idAbf,
+                                   (b > 0) || (kk > 0));
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        tc::mma_ts(tmem + cA1, tmem + cDP + a_col(kk),
-                                   tc::smem_desc_sw128(qaddr + kk * 2048, kHalf, 1024), idA16, (qi > 0) || (kk > 0));
-                    tc::mma_commit(bar(bMmaDone));
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc::mma_ts(tmem + 384, tmem + 128 * x + 64 + 8 * kk, bq + ((kk * 2048) >> 4), idA16,
+                                   (b > 0) || (kk > 0));
                     tc::mma_commit(bar(bRingEmpty + slot));
-                    if (qi + 1 < nq) {
-                        slot = it_ring & 1;
-                        if (!tc::mbar_wait(bar(bRingFull + slot), (it_ring >> 1) & 1, abort_flag)) { fail(); break; }
-                        ++it_ring;
-                        issue_s(kaddr, vaddr, sbase + kOffRing + slot * kPair, sbase + kOffRing + slot * kPair + kTile);
+                    if (b + 2 < nb) {
+                        const uint32_t ns = ring % kRing;
+                        if (!tc::mbar_wait(bar(bRingFull + ns), (ring / kRing) & 1, abort_flag)) { fail(); break; }
+                        ++ring;
+                        issue_s(x, ns);
                     }
                 }
                 if (failed) break;
+                tc::mma_commit(bar(bAccDone));
             }
             tc::mma_commit(bar(bDone));
             if (!tc::mbar_wait(bar(bDone), 0, abort_flag) && !failed) fail();
@@ -319,80 +368,105 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------- softmax gradient + epilogue
-        const int wg = (warp - 4) >> 2;                 // column half of the score tile
+        const int wg = (warp - 4) >> 2;                 // block parity handled
         const int w8 = warp - 4;                        // 0..7
-        const int t = tid - 128 * (1 + wg);             // thread in warpgroup == TMEM lane == key row
+        const int t = tid - 128 * (1 + wg);             // key row == TMEM lane
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        const uint32_t tS = tmem + lane_base + 128 * wg, tDP = tS + 64;  // this warpgroup's buffer
         const float c = p.scale * kLog2e;
         float* lsebuf = reinterpret_cast<float*>(smem + kOffLse) + wg * 256;  // [2 buf][lse2 64 | delta 64]
         float* red = reinterpret_cast<float*>(smem + kOffRed);
-        uint32_t cntS = 0, cntDone = 0;
+        uint32_t cntS = 0, items = 0;
         bool range_ok = true;
         for (int i = blockIdx.x; !failed; i += gridDim.x) {
             BwdItem it;
             if (!bwd_item(p, i, it)) break;
-            const int nq = (it.L + 127) / 128;
+            const int nb = (it.L + 63) / 64;
             const bool key_ok = 128 * it.tile + t < it.L;
-            for (int qi = 0; qi < nq; ++qi) {
-                float* lb = lsebuf + (qi & 1) * 128;
-                if (t < 64) {
-                    const int q = 128 * qi + 64 * wg + t;
-                    const bool v = q < it.L;
-                    const size_t idx = (size_t)it.h * p.seq.S + it.seg0 + (v ? q : 0);
-                    lb[t] = v ? p.lse[idx] * kLog2e : 0.f;
-                    lb[64 + t] = v ? p.delta[idx] : 0.f;
+            // lse2 / Delta of the warpgroup's next block, loaded one block ahead
+            float nl = 0.f, nd = 0.f;
+            auto fetch = [&](int b) {
+                const int q = 64 * b + t;
+                nl = 0.f;
+                nd = 0.f;
+                if (t < 64 && b < nb && q < it.L) {
+                    const size_t idx = (size_t)it.h * p.seq.S + it.seg0 + q;
+                    nl = p.lse[idx] * kLog2e;
+                    nd = p.delta[idx];
                 }
+            };
+            fetch(wg);
+            int k = 0;
+            for (int b = wg; b < nb; b += 2, ++k) {
+                float* lb = lsebuf + (k & 1) * 128;
+                if (t < 64) {
+                    lb[t] = nl;
+                    lb[64 + t] = nd;
+                }
+                fetch(b + 2);
                 named_bar(1 + wg, 128);
                 bool ok = true;
-                if (lane == 0) ok = tc::mbar_wait(bar(bSFull), cntS & 1, abort_flag);
+                if (lane == 0) ok = tc::mbar_wait(bar(bSFull + wg), cntS & 1, abort_flag);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) { fail(); break; }
                 ++cntS;
                 tc::fence_after_sync();
-                uint32_t sr[2][32], dr[2][32];
-                tc::tmem_ld32(tmem + lane_base + cS + 64 * wg, sr[0]);
-                tc::tmem_ld32(tmem + lane_base + cS + 64 * wg + 32, sr[1]);
-                tc::tmem_ld32(tmem + lane_base + cDP + 64 * wg, dr[0]);
-                tc::tmem_ld32(tmem + lane_base + cDP + 64 * wg + 32, dr[1]);
-                tc::tmem_wait_ld_dep(sr[0]);
-                tc::tmem_wait_ld_dep(sr[1]);
-                tc::tmem_wait_ld_dep(dr[0]);
-                tc::tmem_wait_ld_dep(dr[1]);
-                const int validq = it.L - 128 * qi - 64 * wg;  // columns of this half inside the sample
+                const int validq = it.L - 64 * b;  // columns of the block inside the sample
+                const float4* lb4 = reinterpret_cast<const float4*>(lb);
+                float amax = 0.f;
+                // two halves of 32 columns: S and dP of a half in registers at a time
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t sr[32], dr[32];
+                    tc::tmem_ld32(tS + 32 * hh, sr);
+                    tc::tmem_ld32(tDP + 32 * hh, dr);
+                    tc::tmem_wait_ld_dep(sr);
+                    tc::tmem_wait_ld_dep(dr);
                     uint32_t pk[16], dk[16];
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        float pv[2], dsv[2];
+                    for (int e = 0; e < 32; e += 4) {
+                        const float4 l4 = lb4[(32 * hh + e) >> 2];
+                        const float4 d4 = lb4[(64 + 32 * hh + e) >> 2];
+                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+                        float pv[4], dsv[4];
 #pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const int col = 32 * hh + e + u;
-                            const float pe = ex2(fmaf(__uint_as_float(sr[hh][e + u]), c, -lb[col]));
-                            const float ds = pe * (__uint_as_float(dr[hh][e + u]) - lb[64 + col]);
-                            const bool v = col < validq;
-                            pv[u] = v ? pe : 0.f;
-                            dsv[u] = v ? ds : 0.f;
-                            range_ok &= !(key_ok && fabsf(dsv[u]) > 65504.f);
+                        for (int u = 0; u < 4; ++u) {
+                            pv[u] = ex2(fmaf(__uint_as_float(sr[e + u]), c, -lv[u]));
+                            dsv[u] = pv[u] * (__uint_as_float(dr[e + u]) - dv[u]);
                         }
+                        if (validq < 64) {  // tail block: columns past the sample end are exact zeros
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const bool v = 32 * hh + e + u < validq;
+                                pv[u] = v ? pv[u] : 0.f;
+                                dsv[u] = v ? dsv[u] : 0.f;
+                            }
+                        }
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) amax = fmaxf(amax, fabsf(dsv[u]));
                         pk[e >> 1] = pack_bf16(pv[0], pv[1]);
+                        pk[(e >> 1) + 1] = pack_bf16(pv[2], pv[3]);
                         dk[e >> 1] = pack_f16(dsv[0], dsv[1]);
+                        dk[(e >> 1) + 1] = pack_f16(dsv[2], dsv[3]);
                     }
-                    tc::tmem_st16(tmem + lane_base + cS + 64 * wg + 16 * hh, pk);
-                    tc::tmem_st16(tmem + lane_base + cDP + 64 * wg + 16 * hh, dk);
+                    // P^T over S's columns [0, 32), dS^T over dP's: this half's 32 values are
+                    // already in registers, and the second half reads columns [32, 64)
+                    tc::tmem_st16(tS + 16 * hh, pk);
+                    tc::tmem_st16(tDP + 16 * hh, dk);
                 }
+                range_ok &= !(key_ok && amax > 65504.f);
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(bar(bPFull));
+                if (lane == 0) tc::mbar_arrive(bar(bPFull + wg));
             }
             if (failed) break;
             // ---- epilogue: dV rows (warpgroup 0), staged dK rows (warpgroup 1), then rows
-            cntDone += nq;
             bool ok = true;
-            if (lane == 0) ok = tc::mbar_wait(bar(bMmaDone), (cntDone - 1) & 1, abort_flag);
+            if (lane == 0) ok = tc::mbar_wait(bar(bAccDone), items & 1, abort_flag);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) { fail(); break; }
+            ++items;
             tc::fence_after_sync();
             const int krow = it.row0 + t;
             if (wg == 0) {
@@ -400,7 +474,7 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     uint32_t r[32];
-                    tc::tmem_ld32(tmem + lane_base + cA0 + 32 * q4, r);
+                    tc::tmem_ld32(tmem + lane_base + 256 + 32 * q4, r);
                     tc::tmem_wait_ld_dep(r);
                     if (key_ok) {
 #pragma unroll
@@ -418,7 +492,7 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     uint32_t r[32];
-                    tc::tmem_ld32(tmem + lane_base + cA1 + 32 * q4, r);
+                    tc::tmem_ld32(tmem + lane_base + 384 + 32 * q4, r);
                     tc::tmem_wait_ld_dep(r);
 #pragma unroll
                     for (int e = 0; e < 32; e += 4) {
@@ -455,8 +529,8 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
 // ------------------------------------------------------------------ dQ
 
 __global__ void __launch_bounds__(bwdt::kThreads, 1)
-dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-             const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
+dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk64,
+             const __grid_constant__ CUtensorMap mv64, const __grid_constant__ CUtensorMap mdo,
              const __grid_constant__ RopeTable rt, const BwdTcParams p) {
     using namespace bwdt;
     extern __shared__ uint8_t smem_raw[];
@@ -467,21 +541,7 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 8 * bCount + 4);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    if (tid == 0) {
-        tc::mbar_init(bar(bFixedFull), 1);
-        tc::mbar_init(bar(bItemFree), 8);
-        for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(bar(bRingFull + i), 1);
-            tc::mbar_init(bar(bRingEmpty + i), 1);
-        }
-        tc::mbar_init(bar(bSFull), 1);
-        tc::mbar_init(bar(bPFull), 8);
-        tc::mbar_init(bar(bMmaDone), 1);
-        tc::mbar_init(bar(bTail), 1);
-        tc::mbar_init(bar(bDone), 1);
-        *abort_flag = 0;
-        tc::fence_mbar_init();
-    }
+    if (tid == 0) init_bars(sbase);
     if (warp == 1) {
         tc::tmem_alloc(smem_u32(tmem_slot), 512);
         tc::tmem_relinquish();
@@ -489,6 +549,7 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     }
     RopeTable& srt = *reinterpret_cast<RopeTable*>(smem + kOffRope);
     rope_to_smem(rt, srt, tid, kThreads);
+    if (tid == 0) *abort_flag = 0;
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
@@ -506,7 +567,7 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
-        uint32_t it_ring = 0, items = 0, tails = 0;
+        uint32_t ring = 0, items = 0, tails = 0;
         for (int i = blockIdx.x; !failed; i += gridDim.x) {
             BwdItem it;
             if (!bwd_item(p, i, it)) break;
@@ -525,21 +586,21 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
             }
             failed = __shfl_sync(0xffffffffu, failed, 0);
             ++items;
-            const int nk = (it.L + 127) / 128;
-            for (int kj = 0; kj < nk && !failed; ++kj) {
-                const uint32_t slot = it_ring & 1, ph = (it_ring >> 1) & 1;
-                const uint32_t dst = sbase + kOffRing + slot * kPair;
-                const int y = it.seg0 + 128 * kj;
-                const int valid = it.L - 128 * kj;
-                const bool tail = valid < 128;
+            const int nb = (it.L + 63) / 64;
+            for (int b = 0; b < nb && !failed; ++b) {
+                const uint32_t slot = ring % kRing, ph = (ring / kRing) & 1;
+                const uint32_t dst = sbase + kOffRing + slot * kBlkPair;
+                const int y = it.seg0 + 64 * b;
+                const int valid = it.L - 64 * b;
+                const bool tail = valid < 64;
                 if (lane == 0) {
                     if (!tc::mbar_wait(bar(bRingEmpty + slot), ph ^ 1, abort_flag)) fail();
                     if (!failed) {
-                        const uint32_t b = tail ? bar(bTail) : bar(bRingFull + slot);
-                        tc::mbar_expect_tx(b, kPair);
+                        const uint32_t bb = tail ? bar(bTail) : bar(bRingFull + slot);
+                        tc::mbar_expect_tx(bb, kBlkPair);
                         for (int hf = 0; hf < 2; ++hf) {
-                            tc::tma_load_2d(dst + hf * kHalf, &mk, x0 + 64 * hf, y, b);
-                            tc::tma_load_2d(dst + kTile + hf * kHalf, &mv, x0 + 64 * hf, y, b);
+                            tc::tma_load_2d(dst + hf * kBlkHalf, &mk64, x0 + 64 * hf, y, bb);
+                            tc::tma_load_2d(dst + kBlk + hf * kBlkHalf, &mv64, x0 + 64 * hf, y, bb);
                         }
                         if (tail && !tc::mbar_wait(bar(bTail), tails & 1, abort_flag)) fail();
                     }
@@ -548,69 +609,112 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                 if (tail && !failed) {
                     ++tails;
                     // key rows past the sample end: zero k^ (dS is 0 there, k^ may not be finite)
-                    for (int hf = 0; hf < 2; ++hf) zero_rows(dst + hf * kHalf, valid, lane);
+                    for (int hf = 0; hf < 2; ++hf) zero_rows(dst + hf * kBlkHalf, valid, 64, lane);
                     tc::fence_proxy_async();
                     __syncwarp();
                     if (lane == 0) tc::mbar_arrive(bar(bRingFull + slot));
                 }
-                ++it_ring;
+                ++ring;
             }
         }
     } else if (warp == 1) {
         // ----------------------------------------------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idS16 = tc::idesc_f16(false, false, 128, 128);
-            constexpr uint32_t idSbf = tc::idesc_f16(true, false, 128, 128);
+            constexpr uint32_t idS16 = tc::idesc_f16(false, false, 128, 64);
+            constexpr uint32_t idSbf = tc::idesc_f16(true, false, 128, 64);
             constexpr uint32_t idA16 = tc::idesc_f16(false, true, 128, 128);
-            uint32_t it_ring = 0, items = 0, cntP = 0;
-            // S(j+1), dP(j+1) are issued right behind dQ(j) (in-order MMAs: dS(j) is
-            // read before it is overwritten).
-            auto issue_s = [&](uint32_t qaddr, uint32_t doaddr, uint32_t kaddr, uint32_t vaddr) {
+            // descriptors are built once; per MMA only the 16-byte start address moves
+            const uint64_t dQ = tc::smem_desc_sw128(sbase + kOffFixed, 16, 1024);
+            const uint64_t dO = dQ + (kTile >> 4);
+            const uint64_t dRing = tc::smem_desc_sw128(sbase + kOffRing, 16, 1024);          // K-major blocks
+            const uint64_t dRingMN = tc::smem_desc_sw128(sbase + kOffRing, kBlkHalf, 1024);  // MN-major blocks
+            const uint64_t dDs = tc::smem_desc_sw128(sbase + kOffDs, 16, 1024);
+            uint32_t ring = 0, items = 0, cntP[2] = {0, 0}, cntUsed[2] = {0, 0};
+            // S(b) = q^ k^(b)^T and dP(b) = dO v(b)^T into buffer b & 1
+            auto issue_s = [&](int x, uint32_t slot) {
+                const uint64_t bk = dRing + ((slot * kBlkPair) >> 4), bv = bk + (kBlk >> 4);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    tc::mma_ss(tmem + cS, tc::smem_desc_sw128(qaddr + koff, 16, 1024),
-                               tc::smem_desc_sw128(kaddr + koff, 16, 1024), idS16, kk > 0);
+                    const uint32_t aoff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+                    const uint32_t boff = ((kk >> 2) * kBlkHalf + (kk & 3) * 32) >> 4;
+                    tc::mma_ss(tmem + 128 * x, dQ + aoff, bk + boff, idS16, kk > 0);
                 }
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    tc::mma_ss(tmem + cDP, tc::smem_desc_sw128(doaddr + koff, 16, 1024),
-                               tc::smem_desc_sw128(vaddr + koff, 16, 1024), idSbf, kk > 0);
+                    const uint32_t aoff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+                    const uint32_t boff = ((kk >> 2) * kBlkHalf + (kk & 3) * 32) >> 4;
+                    tc::mma_ss(tmem + 128 * x + 64, dO + aoff, bv + boff, idSbf, kk > 0);
                 }
-                tc::mma_commit(bar(bSFull));
+                tc::mma_commit(bar(bSFull + x));
             };
             for (int i = blockIdx.x; !failed; i += gridDim.x) {
                 BwdItem it;
                 if (!bwd_item(p, i, it)) break;
                 if (!tc::mbar_wait(bar(bFixedFull), items & 1, abort_flag)) { fail(); break; }
                 ++items;
-                const uint32_t qaddr = sbase + kOffFixed, doaddr = qaddr + kTile;
-                const int nk = (it.L + 127) / 128;
-                uint32_t slot = it_ring & 1;
-                if (!tc::mbar_wait(bar(bRingFull + slot), (it_ring >> 1) & 1, abort_flag)) { fail(); break; }
-                ++it_ring;
-                tc::fence_after_sync();
-                issue_s(qaddr, doaddr, sbase + kOffRing + slot * kPair, sbase + kOffRing + slot * kPair + kTile);
-                for (int kj = 0; kj < nk; ++kj) {
-                    if (!tc::mbar_wait(bar(bPFull), cntP & 1, abort_flag)) { fail(); break; }
-                    ++cntP;
+                const int nb = (it.L + 63) / 64;
+                const uint32_t ring0 = ring;
+                for (int b = 0; b < 2 && b < nb; ++b) {
+                    const uint32_t slot = ring % kRing;
+                    if (!tc::mbar_wait(bar(bRingFull + slot), (ring / kRing) & 1, abort_flag)) { fail(); break; }
+                    ++ring;
                     tc::fence_after_sync();
-                    const uint32_t kaddr = sbase + kOffRing + slot * kPair;
+                    issue_s(b, slot);
+                }
+                // Event loop: refill buffer b & 1 with block b (b >= 2) as soon as
+                // warpgroup b & 1 has loaded block b - 2, and accumulate dQ(b) in block
+                // order as soon as dS(b) is written; neither waits for the other.
+                int next_s = nb < 2 ? nb : 2, next_q = 0;
+                long long idle0 = clock64();
+                while (next_q < nb && !failed) {
+                    bool did = false;
+                    if (next_s < nb) {
+                        const int x = next_s & 1;
+                        const uint32_t ns = ring % kRing;
+                        if (tc::mbar_try(bar(bSUsed + x), cntUsed[x] & 1) &&
+                            tc::mbar_try(bar(bRingFull + ns), (ring / kRing) & 1)) {
+                            ++cntUsed[x];
+                            ++ring;
+                            tc::fence_after_sync();
+                            issue_s(x, ns);
+                            ++next_s;
+                            did = true;
+                        }
+                    }
+                    {
+                        const int x = next_q & 1;
+                        if (tc::mbar_try(bar(bPFull + x), cntP[x] & 1)) {
+                            ++cntP[x];
+                            tc::fence_after_sync();
+                            const uint32_t slot = (ring0 + next_q) % kRing;
+                            const uint64_t bk = dRingMN + ((slot * kBlkPair) >> 4);
+                            const uint64_t ads = dDs + ((uint32_t)(x * kDsBytes) >> 4);
+                            // dQ += dS(b) k^(b): K = the block's 64 keys; dS from shared memory
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        tc::mma_ts(tmem + cA0, tmem + cS + a_col(kk),
-                                   tc::smem_desc_sw128(kaddr + kk * 2048, kHalf, 1024), idA16, (kj > 0) || (kk > 0));
-                    tc::mma_commit(bar(bMmaDone));
-                    tc::mma_commit(bar(bRingEmpty + slot));
-                    if (kj + 1 < nk) {
-                        slot = it_ring & 1;
-                        if (!tc::mbar_wait(bar(bRingFull + slot), (it_ring >> 1) & 1, abort_flag)) { fail(); break; }
-                        ++it_ring;
-                        issue_s(qaddr, doaddr, sbase + kOffRing + slot * kPair, sbase + kOffRing + slot * kPair + kTile);
+                            for (int kk = 0; kk < 4; ++kk)
+                                tc::mma_ss(tmem + 256, ads + ((kk * 32) >> 4), bk + ((kk * 2048) >> 4), idA16,
+                                           (next_q > 0) || (kk > 0));
+                            tc::mma_commit(bar(bDsFree + x));
+                            tc::mma_commit(bar(bRingEmpty + slot));
+                            ++next_q;
+                            did = true;
+                        }
+                    }
+                    if (did) {
+                        idle0 = clock64();
+                    } else if (*abort_flag || clock64() - idle0 > tc::kWaitBudget) {
+                        fail();
                     }
                 }
+                // the loads of the last two blocks were not needed as refill gates: consume them
+                for (int b = nb - 2; b < nb && !failed; ++b) {
+                    if (b < 0) continue;
+                    const int x = b & 1;
+                    if (!tc::mbar_wait(bar(bSUsed + x), cntUsed[x] & 1, abort_flag)) { fail(); break; }
+                    ++cntUsed[x];
+                }
                 if (failed) break;
+                tc::mma_commit(bar(bAccDone));
             }
             tc::mma_commit(bar(bDone));
             if (!tc::mbar_wait(bar(bDone), 0, abort_flag) && !failed) fail();
@@ -622,70 +726,90 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         const int w8 = warp - 4;
         const int t = tid - 128 * (1 + wg);             // query row of the tile
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        const uint32_t tS = tmem + lane_base + 128 * wg, tDP = tS + 64;  // this warpgroup's buffer
         const float c = p.scale * kLog2e;
         float* red = reinterpret_cast<float*>(smem + kOffRed);
-        uint32_t cntS = 0, cntDone = 0;
+        uint32_t cntS = 0, items = 0;
         bool range_ok = true;
         for (int i = blockIdx.x; !failed; i += gridDim.x) {
             BwdItem it;
             if (!bwd_item(p, i, it)) break;
-            const int nk = (it.L + 127) / 128;
+            const int nb = (it.L + 63) / 64;
             const bool row_ok = 128 * it.tile + t < it.L;
             const size_t idx = (size_t)it.h * p.seq.S + (row_ok ? it.row0 + t : it.seg0);
             const float lse2 = row_ok ? p.lse[idx] * kLog2e : 0.f;
             const float dlt = row_ok ? p.delta[idx] : 0.f;
-            for (int kj = 0; kj < nk; ++kj) {
+            for (int b = wg; b < nb; b += 2) {
                 bool ok = true;
-                if (lane == 0) ok = tc::mbar_wait(bar(bSFull), cntS & 1, abort_flag);
+                if (lane == 0) ok = tc::mbar_wait(bar(bSFull + wg), cntS & 1, abort_flag);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) { fail(); break; }
                 ++cntS;
                 tc::fence_after_sync();
                 uint32_t sr[2][32], dr[2][32];
-                tc::tmem_ld32(tmem + lane_base + cS + 64 * wg, sr[0]);
-                tc::tmem_ld32(tmem + lane_base + cS + 64 * wg + 32, sr[1]);
-                tc::tmem_ld32(tmem + lane_base + cDP + 64 * wg, dr[0]);
-                tc::tmem_ld32(tmem + lane_base + cDP + 64 * wg + 32, dr[1]);
+                tc::tmem_ld32(tS, sr[0]);
+                tc::tmem_ld32(tS + 32, sr[1]);
+                tc::tmem_ld32(tDP, dr[0]);
+                tc::tmem_ld32(tDP + 32, dr[1]);
                 tc::tmem_wait_ld_dep(sr[0]);
                 tc::tmem_wait_ld_dep(sr[1]);
                 tc::tmem_wait_ld_dep(dr[0]);
                 tc::tmem_wait_ld_dep(dr[1]);
-                const int validk = it.L - 128 * kj - 64 * wg;
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t dk[16];
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        float dsv[2];
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const int col = 32 * hh + e + u;
-                            const float pe = ex2(fmaf(__uint_as_float(sr[hh][e + u]), c, -lse2));
-                            const float ds = pe * (__uint_as_float(dr[hh][e + u]) - dlt);
-                            dsv[u] = col < validk ? ds : 0.f;
-                            range_ok &= !(row_ok && fabsf(dsv[u]) > 65504.f);
-                        }
-                        dk[e >> 1] = pack_f16(dsv[0], dsv[1]);
-                    }
-                    tc::tmem_st16(tmem + lane_base + cS + 64 * wg + 16 * hh, dk);
-                }
-                tc::tmem_wait_st();
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(bar(bPFull));
+                if (lane == 0) tc::mbar_arrive(bar(bSUsed + wg));
+                // the dS tile is rewritten only after the dQ MMAs of this warpgroup's
+                // previous block have read it
+                if (cntS >= 2) {
+                    bool fr = true;
+                    if (lane == 0) fr = tc::mbar_wait(bar(bDsFree + wg), (cntS - 2) & 1, abort_flag);
+                    fr = __shfl_sync(0xffffffffu, fr, 0);
+                    if (!fr) { fail(); break; }
+                }
+                const int validk = it.L - 64 * b;
+                float amax = 0.f;
+                // dS row (64 keys, fp16) into the warpgroup's K-major 128-byte-swizzled tile
+                uint8_t* dsrow = smem + kOffDs + wg * kDsBytes + t * 128;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8) {
+                        uint32_t dk[4];
+#pragma unroll
+                        for (int e = 0; e < 8; e += 2) {
+                            float dsv[2];
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const int col = 32 * hh + 8 * c8 + e + u;
+                                const float pe = ex2(fmaf(__uint_as_float(sr[hh][8 * c8 + e + u]), c, -lse2));
+                                dsv[u] = pe * (__uint_as_float(dr[hh][8 * c8 + e + u]) - dlt);
+                                if (validk < 64) dsv[u] = col < validk ? dsv[u] : 0.f;
+                            }
+                            amax = fmaxf(amax, fmaxf(fabsf(dsv[0]), fabsf(dsv[1])));
+                            dk[e >> 1] = pack_f16(dsv[0], dsv[1]);
+                        }
+                        const int chunk = 4 * hh + c8;
+                        *reinterpret_cast<uint4*>(dsrow + ((chunk ^ (t & 7)) << 4)) = make_uint4(dk[0], dk[1], dk[2], dk[3]);
+                    }
+                }
+                range_ok &= !(row_ok && amax > 65504.f);
+                tc::fence_proxy_async();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(bar(bPFull + wg));
             }
             if (failed) break;
             // ---- epilogue: stage scale * dq^ (each warpgroup its 64 channels), then rows
-            cntDone += nk;
             bool ok = true;
-            if (lane == 0) ok = tc::mbar_wait(bar(bMmaDone), (cntDone - 1) & 1, abort_flag);
+            if (lane == 0) ok = tc::mbar_wait(bar(bAccDone), items & 1, abort_flag);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) { fail(); break; }
+            ++items;
             tc::fence_after_sync();
 #pragma unroll
             for (int q2 = 0; q2 < 2; ++q2) {
                 uint32_t r[32];
-                tc::tmem_ld32(tmem + lane_base + cA0 + 64 * wg + 32 * q2, r);
+                tc::tmem_ld32(tmem + lane_base + 256 + 64 * wg + 32 * q2, r);
                 tc::tmem_wait_ld_dep(r);
 #pragma unroll
                 for (int e = 0; e < 32; e += 4) {
@@ -771,10 +895,10 @@ namespace {
 PFN_cuTensorMapEncodeTiled_v12000 g_encode_b = nullptr;
 int g_sms_b = 0;
 
-bool encode_rows_b(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int H, int S) {
+bool encode_rows_b(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int H, int S, int rows) {
     const cuuint64_t dims[2] = {(cuuint64_t)H * kD, (cuuint64_t)S};
     const cuuint64_t strides[1] = {(cuuint64_t)H * kD * 2};
-    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t box[2] = {64, (cuuint32_t)rows};
     const cuuint32_t es[2] = {1, 1};
     return g_encode_b(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -785,11 +909,13 @@ struct BwdMaps {
     CUtensorMap q, k, v, dout;
 };
 
-bool encode_all(BwdMaps& m, const Problem& p, const Workspace& ws, const __nv_bfloat16* dout) {
-    return encode_rows_b(&m.q, ws.qhat, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.H, p.seq.S) &&
-           encode_rows_b(&m.k, ws.khat, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.H, p.seq.S) &&
-           encode_rows_b(&m.v, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.H, p.seq.S) &&
-           encode_rows_b(&m.dout, dout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.H, p.seq.S);
+// q^ and dO streamed in 64-row blocks with k^, v as 128-row tiles (dkdv), or
+// the other way round (dq).
+bool encode_all(BwdMaps& m, const Problem& p, const Workspace& ws, const __nv_bfloat16* dout, int qrows, int krows) {
+    return encode_rows_b(&m.q, ws.qhat, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.H, p.seq.S, qrows) &&
+           encode_rows_b(&m.k, ws.khat, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.H, p.seq.S, krows) &&
+           encode_rows_b(&m.v, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.H, p.seq.S, krows) &&
+           encode_rows_b(&m.dout, dout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.H, p.seq.S, qrows);
 }
 }  // namespace
 
@@ -832,7 +958,7 @@ static BwdTcParams bwd_params(const Problem& p, const Workspace& ws, const float
 cudaError_t launch_bwd_dkdv(const Problem& p, const Workspace& ws, const RopeTable* rope, const float* lse,
                             const __nv_bfloat16* dout, __nv_bfloat16* dk, __nv_bfloat16* dv, cudaStream_t st) {
     BwdMaps m;
-    if (!encode_all(m, p, ws, dout)) return cudaErrorInvalidValue;
+    if (!encode_all(m, p, ws, dout, 64, 128)) return cudaErrorInvalidValue;
     BwdTcParams b = bwd_params(p, ws, lse);
     b.x = p.k;
     b.w = p.wk;
@@ -846,7 +972,7 @@ cudaError_t launch_bwd_dkdv(const Problem& p, const Workspace& ws, const RopeTab
 cudaError_t launch_bwd_dq(const Problem& p, const Workspace& ws, const RopeTable* rope, const float* lse,
                           const __nv_bfloat16* dout, __nv_bfloat16* dq, cudaStream_t st) {
     BwdMaps m;
-    if (!encode_all(m, p, ws, dout)) return cudaErrorInvalidValue;
+    if (!encode_all(m, p, ws, dout, 128, 64)) return cudaErrorInvalidValue;
     BwdTcParams b = bwd_params(p, ws, lse);
     b.x = p.q;
     b.w = p.wq;

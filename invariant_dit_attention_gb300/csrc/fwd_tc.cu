@@ -209,13 +209,16 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             // order, so PV_X(j) has read P_X(j) before S_X(j+1) overwrites those columns,
             // and S_X(j+1) completing implies PV_X(j) completed (the softmax relies on
             // that before it rescales O_X).
-            auto issue_s = [&](int x, uint32_t kaddr) {
-                const uint32_t qaddr = sbase + kOffQ + x * kTile;
+            // descriptors are built once; per MMA only the 16-byte start address moves
+            const uint64_t dQ = tc::smem_desc_sw128(sbase + kOffQ, 16, 1024);
+            const uint64_t dK = tc::smem_desc_sw128(sbase + kOffKV, 16, 1024);
+            const uint64_t dV = tc::smem_desc_sw128(sbase + kOffKV, kHalf, 1024);
+            auto issue_s = [&](int x, uint32_t kslot) {
+                const uint64_t a0 = dQ + ((uint32_t)(x * kTile) >> 4), b0 = dK + ((kslot * kTile) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t koff = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    tc::mma_ss(tmem + kColS0 + 128 * x, tc::smem_desc_sw128(qaddr + koff, 16, 1024),
-                               tc::smem_desc_sw128(kaddr + koff, 16, 1024), idS, kk > 0);
+                    const uint32_t koff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+                    tc::mma_ss(tmem + kColS0 + 128 * x, a0 + koff, b0 + koff, idS, kk > 0);
                 }
                 tc::mma_commit(bar(bSFull + x));
             };
@@ -230,7 +233,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                 if (!tc::mbar_wait(bar(bKVFull + kslot), (kv_it / kNST) & 1, abort_flag)) { fail(); break; }
                 ++kv_it;
                 tc::fence_after_sync();
-                for (int x = 0; x < nX; ++x) issue_s(x, sbase + kOffKV + kslot * kTile);
+                for (int x = 0; x < nX; ++x) issue_s(x, kslot);
                 tc::mma_commit(bar(bKVEmpty + kslot));
                 if (it.nkv == 1) tc::mma_commit(bar(bQEmpty));
                 for (int j = 0; j < it.nkv && !failed; ++j) {
@@ -243,7 +246,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                         if (!tc::mbar_wait(bar(bKVFull + kslot), (kv_it / kNST) & 1, abort_flag)) { fail(); break; }
                         ++kv_it;
                     }
-                    const uint32_t vaddr = sbase + kOffKV + vslot * kTile;
+                    const uint64_t bv0 = dV + ((vslot * kTile) >> 4);
                     for (int x = 0; x < nX && !failed; ++x) {
                         if (j == 0 && itemsX[x] > 0 &&
                             !tc::mbar_wait(bar(bOFree + x), (itemsX[x] - 1) & 1, abort_flag)) {
@@ -256,11 +259,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
                             tc::mma_ts(tmem + kColO0 + 128 * x, tmem + kColS0 + 128 * x + 8 * kk,
-                                       tc::smem_desc_sw128(vaddr + kk * 2048, kHalf, 1024), idP, (j > 0) || (kk > 0));
+                                       bv0 + ((kk * 2048) >> 4), idP, (j > 0) || (kk > 0));
                         tc::mma_commit(bar(bPVDone + x));
                         ++cntPV[x];
                         // ---- S_X(j+1) = Q_X K_{j+1}^T
-                        if (more) issue_s(x, sbase + kOffKV + kslot * kTile);
+                        if (more) issue_s(x, kslot);
                     }
                     if (failed) break;
                     tc::mma_commit(bar(bKVEmpty + vslot));
