@@ -113,6 +113,10 @@ __device__ __forceinline__ void zero_rows(uint32_t half, int valid, int rows, in
                      "r"(0) : "memory");
 }
 
+// TMEM column of the A operand for K-step kk of a 128-wide score tile split
+// between two warpgroups: columns 0..63 were packed at [0, 32), 64..127 at [64, 96).
+__device__ __forceinline__ uint32_t a_col(int kk) { return kk < 4 ? 8 * kk : 64 + 8 * (kk - 4); }
+
 __device__ __forceinline__ void init_bars(uint32_t sbase) {
     using namespace bwdt;
     auto bar = [&](int i) { return sbase + kOffBar + 8u * i; };
@@ -197,21 +201,65 @@ __device__ __forceinline__ void rows_epilogue(const uint8_t* stage, float* red, 
 //         Accumulator dQ [256, 384).
 
 // ------------------------------------------------------------------ dK, dV
+//
+// 128-query blocks (N = 128 MMAs run at the full rate).  TMEM: S^T [0, 128),
+// dP^T [128, 256), dV [256, 384), dK [384, 512).  The two warpgroups split each
+// block's 128 query columns (thread = key row).  P^T (bf16) is written over
+// the S^T columns its warpgroup read (A operand of dV from TMEM); dS^T (fp16)
+// goes to a 128 x 128 shared-memory tile (A operand of dK), so the dP^T buffer
+// is refilled with block j+1 as soon as both warpgroups have loaded block j.
+// S^T(j+1) follows dV(j) (in-order MMAs: P^T(j) is read before it is overwritten).
+namespace kvt {
+constexpr int kOffFixed = 0;                        // k^ + v tiles (also the epilogue stage)
+constexpr int kOffRing = bwdt::kPair;               // 2 stages of q^ + dO tiles
+constexpr int kOffDs = kOffRing + 2 * bwdt::kPair;  // dS^T tile (two 64-column halves); also the epilogue's red
+constexpr int kOffLse = kOffDs + bwdt::kTile;       // [2 wg][2 buf][lse2 64 | delta 64] floats
+constexpr int kOffRope = kOffLse + 2 * 2 * 128 * 4;
+constexpr int kOffBar = kOffRope + 640;
+constexpr int kSmem = kOffBar + 256;                // the dynamic shared memory base is 1024-aligned (checked)
+enum { bFixedFull = 0, bItemFree, bRingFull, bRingEmpty = bRingFull + 2, bSFull = bRingEmpty + 2, bDpUsed, bPFull,
+       bDsFree, bAccDone, bTail, bDone, bCount };
+}  // namespace kvt
 
 __global__ void __launch_bounds__(bwdt::kThreads, 1)
-dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq64, const __grid_constant__ CUtensorMap mk,
-               const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo64,
+dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+               const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
                const __grid_constant__ RopeTable rt, const BwdTcParams p) {
-    using namespace bwdt;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    using namespace kvt;
+    using bwdt::kHalf;
+    using bwdt::kLog2e;
+    using bwdt::kPair;
+    using bwdt::kThreads;
+    using bwdt::kTile;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if (smem_u32(smem_raw) & 1023u) {  // the layout below needs a 1024-byte aligned base
+        if (threadIdx.x == 0) atomicOr(p.plan.err, kErrTimeout);
+        return;
+    }
+    uint8_t* smem = smem_raw;
     const uint32_t sbase = smem_u32(smem);
     auto bar = [&](int i) { return sbase + kOffBar + 8u * i; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * bCount);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 8 * bCount + 4);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    if (tid == 0) init_bars(sbase);
+    if (tid == 0) {
+        tc::mbar_init(bar(bFixedFull), 1);
+        tc::mbar_init(bar(bItemFree), 8);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(bar(bRingFull + i), 1);
+            tc::mbar_init(bar(bRingEmpty + i), 1);
+        }
+        tc::mbar_init(bar(bSFull), 1);
+        tc::mbar_init(bar(bDpUsed), 8);
+        tc::mbar_init(bar(bPFull), 8);
+        tc::mbar_init(bar(bDsFree), 1);
+        tc::mbar_init(bar(bAccDone), 1);
+        tc::mbar_init(bar(bTail), 1);
+        tc::mbar_init(bar(bDone), 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
     if (warp == 1) {
         tc::tmem_alloc(smem_u32(tmem_slot), 512);
         tc::tmem_relinquish();
@@ -219,7 +267,6 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq64, const __grid_constant__
     }
     RopeTable& srt = *reinterpret_cast<RopeTable*>(smem + kOffRope);
     rope_to_smem(rt, srt, tid, kThreads);
-    if (tid == 0) *abort_flag = 0;
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
@@ -256,21 +303,21 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq64, const __grid_constant__
             }
             failed = __shfl_sync(0xffffffffu, failed, 0);
             ++items;
-            const int nb = (it.L + 63) / 64;
-            for (int b = 0; b < nb && !failed; ++b) {
-                const uint32_t slot = ring % kRing, ph = (ring / kRing) & 1;
-                const uint32_t dst = sbase + kOffRing + slot * kBlkPair;
-                const int y = it.seg0 + 64 * b;
-                const int valid = it.L - 64 * b;
-                const bool tail = valid < 64;
+            const int nq = (it.L + 127) / 128;
+            for (int qj = 0; qj < nq && !failed; ++qj) {
+                const uint32_t slot = ring & 1, ph = (ring >> 1) & 1;
+                const uint32_t dst = sbase + kOffRing + slot * kPair;
+                const int y = it.seg0 + 128 * qj;
+                const int valid = it.L - 128 * qj;
+                const bool tail = valid < 128;
                 if (lane == 0) {
                     if (!tc::mbar_wait(bar(bRingEmpty + slot), ph ^ 1, abort_flag)) fail();
                     if (!failed) {
-                        const uint32_t bb = tail ? bar(bTail) : bar(bRingFull + slot);
-                        tc::mbar_expect_tx(bb, kBlkPair);
+                        const uint32_t b = tail ? bar(bTail) : bar(bRingFull + slot);
+                        tc::mbar_expect_tx(b, kPair);
                         for (int hf = 0; hf < 2; ++hf) {
-                            tc::tma_load_2d(dst + hf * kBlkHalf, &mq64, x0 + 64 * hf, y, bb);
-                            tc::tma_load_2d(dst + kBlk + hf * kBlkHalf, &mdo64, x0 + 64 * hf, y, bb);
+                            tc::tma_load_2d(dst + hf * kHalf, &mq, x0 + 64 * hf, y, b);
+                            tc::tma_load_2d(dst + kTile + hf * kHalf, &mdo, x0 + 64 * hf, y, b);
                         }
                         if (tail && !tc::mbar_wait(bar(bTail), tails & 1, abort_flag)) fail();
                     }
@@ -281,8 +328,8 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq64, const __grid_constant__
                     // query rows past the sample end: zero q^ and dO so no neighbour
                     // value reaches the dV and dK products
                     for (int hf = 0; hf < 2; ++hf) {
-                        zero_rows(dst + hf * kBlkHalf, valid, 64, lane);
-                        zero_rows(dst + kBlk + hf * kBlkHalf, valid, 64, lane);
+                        zero_rows(dst + hf * kHalf, valid, 128, lane);
+                        zero_rows(dst + kTile + hf * kHalf, valid, 128, lane);
                     }
                     tc::fence_proxy_async();
                     __syncwarp();
@@ -294,69 +341,80 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq64, const __grid_constant__
     } else if (warp == 1) {
         // ----------------------------------------------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idS16 = tc::idesc_f16(false, false, 128, 64);
-            constexpr uint32_t idSbf = tc::idesc_f16(true, false, 128, 64);
+            constexpr uint32_t idS16 = tc::idesc_f16(false, false, 128, 128);
+            constexpr uint32_t idSbf = tc::idesc_f16(true, false, 128, 128);
             constexpr uint32_t idAbf = tc::idesc_f16(true, true, 128, 128);
             constexpr uint32_t idA16 = tc::idesc_f16(false, true, 128, 128);
             // descriptors are built once; per MMA only the 16-byte start address moves
             const uint64_t dK = tc::smem_desc_sw128(sbase + kOffFixed, 16, 1024);
             const uint64_t dV = dK + (kTile >> 4);
-            const uint64_t dRing = tc::smem_desc_sw128(sbase + kOffRing, 16, 1024);          // K-major blocks
-            const uint64_t dRingMN = tc::smem_desc_sw128(sbase + kOffRing, kBlkHalf, 1024);  // MN-major blocks
-            uint32_t ring = 0, items = 0, cntP[2] = {0, 0};
-            // S^T(b) = k^ q^(b)^T and dP^T(b) = v dO(b)^T into buffer b & 1
-            auto issue_s = [&](int x, uint32_t slot) {
-                const uint64_t bq = dRing + ((slot * kBlkPair) >> 4), bdo = bq + (kBlk >> 4);
+            const uint64_t dRing = tc::smem_desc_sw128(sbase + kOffRing, 16, 1024);
+            const uint64_t dRingMN = tc::smem_desc_sw128(sbase + kOffRing, kHalf, 1024);
+            const uint64_t dDs = tc::smem_desc_sw128(sbase + kOffDs, 16, 1024);
+            uint32_t ring = 0, items = 0, cntB = 0;
+            auto issue_st = [&](uint32_t slot) {  // S^T(j) = k^ q^(j)^T
+                const uint64_t bq = dRing + ((slot * kPair) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t aoff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
-                    const uint32_t boff = ((kk >> 2) * kBlkHalf + (kk & 3) * 32) >> 4;
-                    tc::mma_ss(tmem + 128 * x, dK + aoff, bq + boff, idS16, kk > 0);
+                    const uint32_t koff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+                    tc::mma_ss(tmem + 0, dK + koff, bq + koff, idS16, kk > 0);
                 }
+            };
+            auto issue_dpt = [&](uint32_t slot) {  // dP^T(j) = v dO(j)^T
+                const uint64_t bdo = dRing + ((slot * kPair + kTile) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t aoff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
-                    const uint32_t boff = ((kk >> 2) * kBlkHalf + (kk & 3) * 32) >> 4;
-                    tc::mma_ss(tmem + 128 * x + 64, dV + aoff, bdo + boff, idSbf, kk > 0);
+                    const uint32_t koff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+                    tc::mma_ss(tmem + 128, dV + koff, bdo + koff, idSbf, kk > 0);
                 }
-                tc::mma_commit(bar(bSFull + x));
             };
             for (int i = blockIdx.x; !failed; i += gridDim.x) {
                 BwdItem it;
                 if (!bwd_item(p, i, it)) break;
                 if (!tc::mbar_wait(bar(bFixedFull), items & 1, abort_flag)) { fail(); break; }
                 ++items;
-                const int nb = (it.L + 63) / 64;
+                const int nq = (it.L + 127) / 128;
                 const uint32_t ring0 = ring;
-                for (int b = 0; b < 2 && b < nb; ++b) {
-                    const uint32_t slot = ring % kRing;
-                    if (!tc::mbar_wait(bar(bRingFull + slot), (ring / kRing) & 1, abort_flag)) { fail(); break; }
+                {
+                    const uint32_t slot = ring & 1;
+                    if (!tc::mbar_wait(bar(bRingFull + slot), (ring >> 1) & 1, abort_flag)) { fail(); break; }
                     ++ring;
                     tc::fence_after_sync();
-                    issue_s(b, slot);
+                    issue_dpt(slot);
+                    issue_st(slot);
+                    tc::mma_commit(bar(bSFull));
                 }
-                for (int b = 0; b < nb && !failed; ++b) {
-                    const int x = b & 1;
-                    const uint32_t slot = (ring0 + b) % kRing;
-                    if (!tc::mbar_wait(bar(bPFull + x), cntP[x] & 1, abort_flag)) { fail(); break; }
-                    ++cntP[x];
-                    tc::fence_after_sync();
-                    const uint64_t bq = dRingMN + ((slot * kBlkPair) >> 4), bdo = bq + (kBlk >> 4);
-                    // dV += P^T(b) dO(b), dK += dS^T(b) q^(b): K = the block's 64 queries
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc::mma_ts(tmem + 256, tmem + 128 * x + 8 * kk, bdo + ((kk * 2048) >> 4), idAbf,
-                                   (b > 0) || (kk > 0));
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc::mma_ts(tmem + 384, tmem + 128 * x + 64 + 8 * kk, bq + ((kk * 2048) >> 4), idA16,
-                                   (b > 0) || (kk > 0));
-                    tc::mma_commit(bar(bRingEmpty + slot));
-                    if (b + 2 < nb) {
-                        const uint32_t ns = ring % kRing;
-                        if (!tc::mbar_wait(bar(bRingFull + ns), (ring / kRing) & 1, abort_flag)) { fail(); break; }
+                for (int qj = 0; qj < nq && !failed; ++qj) {
+                    const uint32_t slot = (ring0 + qj) & 1;
+                    const bool more = qj + 1 < nq;
+                    uint32_t ns = 0;
+                    // block qj's dP^T is in registers: refill that buffer with block qj+1
+                    if (!tc::mbar_wait(bar(bDpUsed), cntB & 1, abort_flag)) { fail(); break; }
+                    if (more) {
+                        ns = ring & 1;
+                        if (!tc::mbar_wait(bar(bRingFull + ns), (ring >> 1) & 1, abort_flag)) { fail(); break; }
                         ++ring;
-                        issue_s(x, ns);
+                        tc::fence_after_sync();
+                        issue_dpt(ns);
+                    }
+                    if (!tc::mbar_wait(bar(bPFull), cntB & 1, abort_flag)) { fail(); break; }
+                    ++cntB;
+                    tc::fence_after_sync();
+                    const uint64_t bq = dRingMN + ((slot * kPair) >> 4), bdo = bq + (kTile >> 4);
+                    // dV += P^T(j) dO(j) (P^T from TMEM), dK += dS^T(j) q^(j) (dS^T from shared memory)
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        tc::mma_ts(tmem + 256, tmem + a_col(kk), bdo + ((kk * 2048) >> 4), idAbf, (qj > 0) || (kk > 0));
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t aoff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+                        tc::mma_ss(tmem + 384, dDs + aoff, bq + ((kk * 2048) >> 4), idA16, (qj > 0) || (kk > 0));
+                    }
+                    tc::mma_commit(bar(bDsFree));
+                    tc::mma_commit(bar(bRingEmpty + slot));
+                    if (more) {
+                        issue_st(ns);
+                        tc::mma_commit(bar(bSFull));
                     }
                 }
                 if (failed) break;
@@ -368,97 +426,118 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq64, const __grid_constant__
         __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------- softmax gradient + epilogue
-        const int wg = (warp - 4) >> 2;                 // block parity handled
-        const int w8 = warp - 4;                        // 0..7
+        const int wg = (warp - 4) >> 2;                 // query half of the score tile
+        const int w8 = warp - 4;
         const int t = tid - 128 * (1 + wg);             // key row == TMEM lane
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-        const uint32_t tS = tmem + lane_base + 128 * wg, tDP = tS + 64;  // this warpgroup's buffer
+        const uint32_t tS = tmem + lane_base + 64 * wg, tDP = tmem + lane_base + 128 + 64 * wg;
         const float c = p.scale * kLog2e;
         float* lsebuf = reinterpret_cast<float*>(smem + kOffLse) + wg * 256;  // [2 buf][lse2 64 | delta 64]
-        float* red = reinterpret_cast<float*>(smem + kOffRed);
-        uint32_t cntS = 0, items = 0;
+        float* red = reinterpret_cast<float*>(smem + kOffDs);                  // epilogue only
+        uint8_t* dsrow = smem + kOffDs + wg * kHalf + t * 128;
+        uint32_t cntS = 0, items = 0, nds = 0;
         bool range_ok = true;
         for (int i = blockIdx.x; !failed; i += gridDim.x) {
             BwdItem it;
             if (!bwd_item(p, i, it)) break;
-            const int nb = (it.L + 63) / 64;
+            const int nq = (it.L + 127) / 128;
             const bool key_ok = 128 * it.tile + t < it.L;
-            // lse2 / Delta of the warpgroup's next block, loaded one block ahead
+            // lse2 / Delta of this warpgroup's 64 queries of the next block, one block ahead
             float nl = 0.f, nd = 0.f;
-            auto fetch = [&](int b) {
-                const int q = 64 * b + t;
+            auto fetch = [&](int qj) {
+                const int q = 128 * qj + 64 * wg + t;
                 nl = 0.f;
                 nd = 0.f;
-                if (t < 64 && b < nb && q < it.L) {
+                if (t < 64 && qj < nq && q < it.L) {
                     const size_t idx = (size_t)it.h * p.seq.S + it.seg0 + q;
                     nl = p.lse[idx] * kLog2e;
                     nd = p.delta[idx];
                 }
             };
-            fetch(wg);
-            int k = 0;
-            for (int b = wg; b < nb; b += 2, ++k) {
-                float* lb = lsebuf + (k & 1) * 128;
+            fetch(0);
+            for (int qj = 0; qj < nq; ++qj) {
+                float* lb = lsebuf + (qj & 1) * 128;
                 if (t < 64) {
                     lb[t] = nl;
                     lb[64 + t] = nd;
                 }
-                fetch(b + 2);
+                fetch(qj + 1);
                 named_bar(1 + wg, 128);
                 bool ok = true;
-                if (lane == 0) ok = tc::mbar_wait(bar(bSFull + wg), cntS & 1, abort_flag);
+                if (lane == 0) ok = tc::mbar_wait(bar(bSFull), cntS & 1, abort_flag);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) { fail(); break; }
                 ++cntS;
                 tc::fence_after_sync();
-                const int validq = it.L - 64 * b;  // columns of the block inside the sample
+                uint32_t dr[2][32];
+                tc::tmem_ld32(tDP, dr[0]);
+                tc::tmem_ld32(tDP + 32, dr[1]);
+                tc::tmem_wait_ld_dep(dr[0]);
+                tc::tmem_wait_ld_dep(dr[1]);
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(bar(bDpUsed));
+                // the dS^T tile is rewritten only after the previous block's dK MMAs read it
+                if (nds > 0) {
+                    bool fr = true;
+                    if (lane == 0) fr = tc::mbar_wait(bar(bDsFree), (nds - 1) & 1, abort_flag);
+                    fr = __shfl_sync(0xffffffffu, fr, 0);
+                    if (!fr) { fail(); break; }
+                }
+                ++nds;
+                const int validq = it.L - 128 * qj - 64 * wg;  // columns of this half inside the sample
                 const float4* lb4 = reinterpret_cast<const float4*>(lb);
                 float amax = 0.f;
-                // two halves of 32 columns: S and dP of a half in registers at a time
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t sr[32], dr[32];
+                    uint32_t sr[32];
                     tc::tmem_ld32(tS + 32 * hh, sr);
-                    tc::tmem_ld32(tDP + 32 * hh, dr);
                     tc::tmem_wait_ld_dep(sr);
-                    tc::tmem_wait_ld_dep(dr);
-                    uint32_t pk[16], dk[16];
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        const float4 l4 = lb4[(32 * hh + e) >> 2];
-                        const float4 d4 = lb4[(64 + 32 * hh + e) >> 2];
-                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
-                        float pv[4], dsv[4];
+                    for (int c8 = 0; c8 < 4; ++c8) {
+                        uint32_t dk[4];
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            pv[u] = ex2(fmaf(__uint_as_float(sr[e + u]), c, -lv[u]));
-                            dsv[u] = pv[u] * (__uint_as_float(dr[e + u]) - dv[u]);
-                        }
-                        if (validq < 64) {  // tail block: columns past the sample end are exact zeros
+                        for (int e = 0; e < 8; e += 4) {
+                            const int col = 32 * hh + 8 * c8 + e;
+                            const float4 l4 = lb4[col >> 2];
+                            const float4 d4 = lb4[(64 + col) >> 2];
+                            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+                            float pv[4], dsv[4];
 #pragma unroll
                             for (int u = 0; u < 4; ++u) {
-                                const bool v = 32 * hh + e + u < validq;
-                                pv[u] = v ? pv[u] : 0.f;
-                                dsv[u] = v ? dsv[u] : 0.f;
+                                pv[u] = ex2(fmaf(__uint_as_float(sr[8 * c8 + e + u]), c, -lv[u]));
+                                dsv[u] = pv[u] * (__uint_as_float(dr[hh][8 * c8 + e + u]) - dv[u]);
                             }
-                        }
+                            if (validq < 64) {  // tail block: columns past the sample end are exact zeros
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) amax = fmaxf(amax, fabsf(dsv[u]));
-                        pk[e >> 1] = pack_bf16(pv[0], pv[1]);
-                        pk[(e >> 1) + 1] = pack_bf16(pv[2], pv[3]);
-                        dk[e >> 1] = pack_f16(dsv[0], dsv[1]);
-                        dk[(e >> 1) + 1] = pack_f16(dsv[2], dsv[3]);
+                                for (int u = 0; u < 4; ++u) {
+                                    const bool v = col + u < validq;
+                                    pv[u] = v ? pv[u] : 0.f;
+                                    dsv[u] = v ? dsv[u] : 0.f;
+                                }
+                            }
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) amax = fmaxf(amax, fabsf(dsv[u]));
+                            pk[(8 * c8 + e) >> 1] = pack_bf16(pv[0], pv[1]);
+                            pk[((8 * c8 + e) >> 1) + 1] = pack_bf16(pv[2], pv[3]);
+                            dk[e >> 1] = pack_f16(dsv[0], dsv[1]);
+                            dk[(e >> 1) + 1] = pack_f16(dsv[2], dsv[3]);
+                        }
+                        const int chunk = 4 * hh + c8;
+                        *reinterpret_cast<uint4*>(dsrow + ((chunk ^ (t & 7)) << 4)) =
+                            make_uint4(dk[0], dk[1], dk[2], dk[3]);
                     }
-                    // P^T over S's columns [0, 32), dS^T over dP's: this half's 32 values are
-                    // already in registers, and the second half reads columns [32, 64)
+                    // P^T over the S^T columns [64wg, 64wg + 32): half 0 writes [0, 16), half 1
+                    // [16, 32) while it reads [32, 64)
                     tc::tmem_st16(tS + 16 * hh, pk);
-                    tc::tmem_st16(tDP + 16 * hh, dk);
                 }
                 range_ok &= !(key_ok && amax > 65504.f);
                 tc::tmem_wait_st();
+                tc::fence_proxy_async();
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(bar(bPFull + wg));
+                if (lane == 0) tc::mbar_arrive(bar(bPFull));
             }
             if (failed) break;
             // ---- epilogue: dV rows (warpgroup 0), staged dK rows (warpgroup 1), then rows
@@ -527,12 +606,33 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq64, const __grid_constant__
 }
 
 // ------------------------------------------------------------------ dQ
+//
+// 128-key blocks (N = 128 MMAs run at the full rate), one score buffer in TMEM
+// (S cols [0, 128), dP cols [128, 256)) and dQ at [256, 384).  The two
+// warpgroups split each block's 128 columns (thread = query row).  dS goes to
+// a 128 x 128 fp16 shared-memory tile, so the score buffer is refilled with
+// block j+1 as soon as both warpgroups have loaded block j; dQ(j) follows.
+namespace dqt {
+constexpr int kOffFixed = 0;                    // q^ + dO tiles (also the epilogue stage)
+constexpr int kOffRing = bwdt::kPair;           // 2 stages of k^ + v tiles
+constexpr int kOffDs = kOffRing + 2 * bwdt::kPair;  // dS tile (two 64-column halves); also the epilogue's red
+constexpr int kOffRope = kOffDs + bwdt::kTile;
+constexpr int kOffBar = kOffRope + 768;
+constexpr int kSmem = kOffBar + 256 + 1024;
+enum { bFixedFull = 0, bItemFree, bRingFull, bRingEmpty = bRingFull + 2, bSFull = bRingEmpty + 2, bSUsed, bPFull,
+       bDsFree, bAccDone, bTail, bDone, bCount };
+}  // namespace dqt
 
 __global__ void __launch_bounds__(bwdt::kThreads, 1)
-dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk64,
-             const __grid_constant__ CUtensorMap mv64, const __grid_constant__ CUtensorMap mdo,
+dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+             const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
              const __grid_constant__ RopeTable rt, const BwdTcParams p) {
-    using namespace bwdt;
+    using namespace dqt;
+    using bwdt::kHalf;
+    using bwdt::kLog2e;
+    using bwdt::kPair;
+    using bwdt::kThreads;
+    using bwdt::kTile;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -541,7 +641,23 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 8 * bCount + 4);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    if (tid == 0) init_bars(sbase);
+    if (tid == 0) {
+        tc::mbar_init(bar(bFixedFull), 1);
+        tc::mbar_init(bar(bItemFree), 8);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(bar(bRingFull + i), 1);
+            tc::mbar_init(bar(bRingEmpty + i), 1);
+        }
+        tc::mbar_init(bar(bSFull), 1);
+        tc::mbar_init(bar(bSUsed), 8);
+        tc::mbar_init(bar(bPFull), 8);
+        tc::mbar_init(bar(bDsFree), 1);
+        tc::mbar_init(bar(bAccDone), 1);
+        tc::mbar_init(bar(bTail), 1);
+        tc::mbar_init(bar(bDone), 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
     if (warp == 1) {
         tc::tmem_alloc(smem_u32(tmem_slot), 512);
         tc::tmem_relinquish();
@@ -549,7 +665,6 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     }
     RopeTable& srt = *reinterpret_cast<RopeTable*>(smem + kOffRope);
     rope_to_smem(rt, srt, tid, kThreads);
-    if (tid == 0) *abort_flag = 0;
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
@@ -586,21 +701,21 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
             }
             failed = __shfl_sync(0xffffffffu, failed, 0);
             ++items;
-            const int nb = (it.L + 63) / 64;
-            for (int b = 0; b < nb && !failed; ++b) {
-                const uint32_t slot = ring % kRing, ph = (ring / kRing) & 1;
-                const uint32_t dst = sbase + kOffRing + slot * kBlkPair;
-                const int y = it.seg0 + 64 * b;
-                const int valid = it.L - 64 * b;
-                const bool tail = valid < 64;
+            const int nk = (it.L + 127) / 128;
+            for (int kj = 0; kj < nk && !failed; ++kj) {
+                const uint32_t slot = ring & 1, ph = (ring >> 1) & 1;
+                const uint32_t dst = sbase + kOffRing + slot * kPair;
+                const int y = it.seg0 + 128 * kj;
+                const int valid = it.L - 128 * kj;
+                const bool tail = valid < 128;
                 if (lane == 0) {
                     if (!tc::mbar_wait(bar(bRingEmpty + slot), ph ^ 1, abort_flag)) fail();
                     if (!failed) {
-                        const uint32_t bb = tail ? bar(bTail) : bar(bRingFull + slot);
-                        tc::mbar_expect_tx(bb, kBlkPair);
+                        const uint32_t b = tail ? bar(bTail) : bar(bRingFull + slot);
+                        tc::mbar_expect_tx(b, kPair);
                         for (int hf = 0; hf < 2; ++hf) {
-                            tc::tma_load_2d(dst + hf * kBlkHalf, &mk64, x0 + 64 * hf, y, bb);
-                            tc::tma_load_2d(dst + kBlk + hf * kBlkHalf, &mv64, x0 + 64 * hf, y, bb);
+                            tc::tma_load_2d(dst + hf * kHalf, &mk, x0 + 64 * hf, y, b);
+                            tc::tma_load_2d(dst + kTile + hf * kHalf, &mv, x0 + 64 * hf, y, b);
                         }
                         if (tail && !tc::mbar_wait(bar(bTail), tails & 1, abort_flag)) fail();
                     }
@@ -609,7 +724,7 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                 if (tail && !failed) {
                     ++tails;
                     // key rows past the sample end: zero k^ (dS is 0 there, k^ may not be finite)
-                    for (int hf = 0; hf < 2; ++hf) zero_rows(dst + hf * kBlkHalf, valid, 64, lane);
+                    for (int hf = 0; hf < 2; ++hf) zero_rows(dst + hf * kHalf, valid, 128, lane);
                     tc::fence_proxy_async();
                     __syncwarp();
                     if (lane == 0) tc::mbar_arrive(bar(bRingFull + slot));
@@ -620,98 +735,68 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     } else if (warp == 1) {
         // ----------------------------------------------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idS16 = tc::idesc_f16(false, false, 128, 64);
-            constexpr uint32_t idSbf = tc::idesc_f16(true, false, 128, 64);
+            constexpr uint32_t idS16 = tc::idesc_f16(false, false, 128, 128);
+            constexpr uint32_t idSbf = tc::idesc_f16(true, false, 128, 128);
             constexpr uint32_t idA16 = tc::idesc_f16(false, true, 128, 128);
             // descriptors are built once; per MMA only the 16-byte start address moves
             const uint64_t dQ = tc::smem_desc_sw128(sbase + kOffFixed, 16, 1024);
             const uint64_t dO = dQ + (kTile >> 4);
-            const uint64_t dRing = tc::smem_desc_sw128(sbase + kOffRing, 16, 1024);          // K-major blocks
-            const uint64_t dRingMN = tc::smem_desc_sw128(sbase + kOffRing, kBlkHalf, 1024);  // MN-major blocks
+            const uint64_t dRing = tc::smem_desc_sw128(sbase + kOffRing, 16, 1024);
+            const uint64_t dRingMN = tc::smem_desc_sw128(sbase + kOffRing, kHalf, 1024);
             const uint64_t dDs = tc::smem_desc_sw128(sbase + kOffDs, 16, 1024);
-            uint32_t ring = 0, items = 0, cntP[2] = {0, 0}, cntUsed[2] = {0, 0};
-            // S(b) = q^ k^(b)^T and dP(b) = dO v(b)^T into buffer b & 1
-            auto issue_s = [&](int x, uint32_t slot) {
-                const uint64_t bk = dRing + ((slot * kBlkPair) >> 4), bv = bk + (kBlk >> 4);
+            uint32_t ring = 0, items = 0, cntS = 0;
+            // S(j) = q^ k^(j)^T and dP(j) = dO v(j)^T into the score buffer
+            auto issue_s = [&](uint32_t slot) {
+                const uint64_t bk = dRing + ((slot * kPair) >> 4), bv = bk + (kTile >> 4);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t aoff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
-                    const uint32_t boff = ((kk >> 2) * kBlkHalf + (kk & 3) * 32) >> 4;
-                    tc::mma_ss(tmem + 128 * x, dQ + aoff, bk + boff, idS16, kk > 0);
+                    const uint32_t koff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+                    tc::mma_ss(tmem + 0, dQ + koff, bk + koff, idS16, kk > 0);
                 }
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t aoff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
-                    const uint32_t boff = ((kk >> 2) * kBlkHalf + (kk & 3) * 32) >> 4;
-                    tc::mma_ss(tmem + 128 * x + 64, dO + aoff, bv + boff, idSbf, kk > 0);
+                    const uint32_t koff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+                    tc::mma_ss(tmem + 128, dO + koff, bv + koff, idSbf, kk > 0);
                 }
-                tc::mma_commit(bar(bSFull + x));
+                tc::mma_commit(bar(bSFull));
             };
             for (int i = blockIdx.x; !failed; i += gridDim.x) {
                 BwdItem it;
                 if (!bwd_item(p, i, it)) break;
                 if (!tc::mbar_wait(bar(bFixedFull), items & 1, abort_flag)) { fail(); break; }
                 ++items;
-                const int nb = (it.L + 63) / 64;
+                const int nk = (it.L + 127) / 128;
                 const uint32_t ring0 = ring;
-                for (int b = 0; b < 2 && b < nb; ++b) {
-                    const uint32_t slot = ring % kRing;
-                    if (!tc::mbar_wait(bar(bRingFull + slot), (ring / kRing) & 1, abort_flag)) { fail(); break; }
+                {
+                    const uint32_t slot = ring & 1;
+                    if (!tc::mbar_wait(bar(bRingFull + slot), (ring >> 1) & 1, abort_flag)) { fail(); break; }
                     ++ring;
                     tc::fence_after_sync();
-                    issue_s(b, slot);
+                    issue_s(slot);
                 }
-                // Event loop: refill buffer b & 1 with block b (b >= 2) as soon as
-                // warpgroup b & 1 has loaded block b - 2, and accumulate dQ(b) in block
-                // order as soon as dS(b) is written; neither waits for the other.
-                int next_s = nb < 2 ? nb : 2, next_q = 0;
-                long long idle0 = clock64();
-                while (next_q < nb && !failed) {
-                    bool did = false;
-                    if (next_s < nb) {
-                        const int x = next_s & 1;
-                        const uint32_t ns = ring % kRing;
-                        if (tc::mbar_try(bar(bSUsed + x), cntUsed[x] & 1) &&
-                            tc::mbar_try(bar(bRingFull + ns), (ring / kRing) & 1)) {
-                            ++cntUsed[x];
-                            ++ring;
-                            tc::fence_after_sync();
-                            issue_s(x, ns);
-                            ++next_s;
-                            did = true;
-                        }
+                for (int kj = 0; kj < nk && !failed; ++kj) {
+                    const uint32_t slot = (ring0 + kj) & 1;
+                    // block kj's scores are in registers: refill the buffer with block kj+1
+                    if (!tc::mbar_wait(bar(bSUsed), cntS & 1, abort_flag)) { fail(); break; }
+                    ++cntS;
+                    if (kj + 1 < nk) {
+                        const uint32_t ns = ring & 1;
+                        if (!tc::mbar_wait(bar(bRingFull + ns), (ring >> 1) & 1, abort_flag)) { fail(); break; }
+                        ++ring;
+                        tc::fence_after_sync();
+                        issue_s(ns);
                     }
-                    {
-                        const int x = next_q & 1;
-                        if (tc::mbar_try(bar(bPFull + x), cntP[x] & 1)) {
-                            ++cntP[x];
-                            tc::fence_after_sync();
-                            const uint32_t slot = (ring0 + next_q) % kRing;
-                            const uint64_t bk = dRingMN + ((slot * kBlkPair) >> 4);
-                            const uint64_t ads = dDs + ((uint32_t)(x * kDsBytes) >> 4);
-                            // dQ += dS(b) k^(b): K = the block's 64 keys; dS from shared memory
+                    if (!tc::mbar_wait(bar(bPFull), (cntS - 1) & 1, abort_flag)) { fail(); break; }
+                    tc::fence_after_sync();
+                    const uint64_t bk = dRingMN + ((slot * kPair) >> 4);
+                    // dQ += dS(j) k^(j): K = the block's 128 keys; dS from shared memory
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                tc::mma_ss(tmem + 256, ads + ((kk * 32) >> 4), bk + ((kk * 2048) >> 4), idA16,
-                                           (next_q > 0) || (kk > 0));
-                            tc::mma_commit(bar(bDsFree + x));
-                            tc::mma_commit(bar(bRingEmpty + slot));
-                            ++next_q;
-                            did = true;
-                        }
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t aoff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+                        tc::mma_ss(tmem + 256, dDs + aoff, bk + ((kk * 2048) >> 4), idA16, (kj > 0) || (kk > 0));
                     }
-                    if (did) {
-                        idle0 = clock64();
-                    } else if (*abort_flag || clock64() - idle0 > tc::kWaitBudget) {
-                        fail();
-                    }
-                }
-                // the loads of the last two blocks were not needed as refill gates: consume them
-                for (int b = nb - 2; b < nb && !failed; ++b) {
-                    if (b < 0) continue;
-                    const int x = b & 1;
-                    if (!tc::mbar_wait(bar(bSUsed + x), cntUsed[x] & 1, abort_flag)) { fail(); break; }
-                    ++cntUsed[x];
+                    tc::mma_commit(bar(bDsFree));
+                    tc::mma_commit(bar(bRingEmpty + slot));
                 }
                 if (failed) break;
                 tc::mma_commit(bar(bAccDone));
@@ -722,26 +807,27 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------- softmax gradient + epilogue
-        const int wg = (warp - 4) >> 2;
+        const int wg = (warp - 4) >> 2;                 // column half of the score tile
         const int w8 = warp - 4;
         const int t = tid - 128 * (1 + wg);             // query row of the tile
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-        const uint32_t tS = tmem + lane_base + 128 * wg, tDP = tS + 64;  // this warpgroup's buffer
+        const uint32_t tS = tmem + lane_base + 64 * wg, tDP = tmem + lane_base + 128 + 64 * wg;
         const float c = p.scale * kLog2e;
-        float* red = reinterpret_cast<float*>(smem + kOffRed);
-        uint32_t cntS = 0, items = 0;
+        float* red = reinterpret_cast<float*>(smem + kOffDs);  // epilogue only (all dQ MMAs done)
+        uint8_t* dsrow = smem + kOffDs + wg * bwdt::kHalf + t * 128;
+        uint32_t cntS = 0, items = 0, nds = 0;
         bool range_ok = true;
         for (int i = blockIdx.x; !failed; i += gridDim.x) {
             BwdItem it;
             if (!bwd_item(p, i, it)) break;
-            const int nb = (it.L + 63) / 64;
+            const int nk = (it.L + 127) / 128;
             const bool row_ok = 128 * it.tile + t < it.L;
             const size_t idx = (size_t)it.h * p.seq.S + (row_ok ? it.row0 + t : it.seg0);
             const float lse2 = row_ok ? p.lse[idx] * kLog2e : 0.f;
             const float dlt = row_ok ? p.delta[idx] : 0.f;
-            for (int b = wg; b < nb; b += 2) {
+            for (int kj = 0; kj < nk; ++kj) {
                 bool ok = true;
-                if (lane == 0) ok = tc::mbar_wait(bar(bSFull + wg), cntS & 1, abort_flag);
+                if (lane == 0) ok = tc::mbar_wait(bar(bSFull), cntS & 1, abort_flag);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) { fail(); break; }
                 ++cntS;
@@ -757,19 +843,17 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                 tc::tmem_wait_ld_dep(dr[1]);
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(bar(bSUsed + wg));
-                // the dS tile is rewritten only after the dQ MMAs of this warpgroup's
-                // previous block have read it
-                if (cntS >= 2) {
+                if (lane == 0) tc::mbar_arrive(bar(bSUsed));
+                // the dS tile is rewritten only after the previous block's dQ MMAs read it
+                if (nds > 0) {
                     bool fr = true;
-                    if (lane == 0) fr = tc::mbar_wait(bar(bDsFree + wg), (cntS - 2) & 1, abort_flag);
+                    if (lane == 0) fr = tc::mbar_wait(bar(bDsFree), (nds - 1) & 1, abort_flag);
                     fr = __shfl_sync(0xffffffffu, fr, 0);
                     if (!fr) { fail(); break; }
                 }
-                const int validk = it.L - 64 * b;
+                ++nds;
+                const int validk = it.L - 128 * kj - 64 * wg;  // keys of this half inside the sample
                 float amax = 0.f;
-                // dS row (64 keys, fp16) into the warpgroup's K-major 128-byte-swizzled tile
-                uint8_t* dsrow = smem + kOffDs + wg * kDsBytes + t * 128;
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
@@ -789,14 +873,15 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                             dk[e >> 1] = pack_f16(dsv[0], dsv[1]);
                         }
                         const int chunk = 4 * hh + c8;
-                        *reinterpret_cast<uint4*>(dsrow + ((chunk ^ (t & 7)) << 4)) = make_uint4(dk[0], dk[1], dk[2], dk[3]);
+                        *reinterpret_cast<uint4*>(dsrow + ((chunk ^ (t & 7)) << 4)) =
+                            make_uint4(dk[0], dk[1], dk[2], dk[3]);
                     }
                 }
                 range_ok &= !(row_ok && amax > 65504.f);
                 tc::fence_proxy_async();
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(bar(bPFull + wg));
+                if (lane == 0) tc::mbar_arrive(bar(bPFull));
             }
             if (failed) break;
             // ---- epilogue: stage scale * dq^ (each warpgroup its 64 channels), then rows
@@ -930,9 +1015,9 @@ cudaError_t init_bwd_attributes() {
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_sms_b, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bwdt::kSmem);
+        e = cudaFuncSetAttribute(dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kvt::kSmem);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bwdt::kSmem);
+        e = cudaFuncSetAttribute(dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dqt::kSmem);
     return e;
 }
 
@@ -958,28 +1043,28 @@ static BwdTcParams bwd_params(const Problem& p, const Workspace& ws, const float
 cudaError_t launch_bwd_dkdv(const Problem& p, const Workspace& ws, const RopeTable* rope, const float* lse,
                             const __nv_bfloat16* dout, __nv_bfloat16* dk, __nv_bfloat16* dv, cudaStream_t st) {
     BwdMaps m;
-    if (!encode_all(m, p, ws, dout, 64, 128)) return cudaErrorInvalidValue;
+    if (!encode_all(m, p, ws, dout, 128, 128)) return cudaErrorInvalidValue;
     BwdTcParams b = bwd_params(p, ws, lse);
     b.x = p.k;
     b.w = p.wk;
     b.dx = dk;
     b.dv = dv;
     b.dw_part = ws.dwk_part;
-    dkdv_tc_kernel<<<g_sms_b, bwdt::kThreads, bwdt::kSmem, st>>>(m.q, m.k, m.v, m.dout, *rope, b);
+    dkdv_tc_kernel<<<g_sms_b, bwdt::kThreads, kvt::kSmem, st>>>(m.q, m.k, m.v, m.dout, *rope, b);
     return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dq(const Problem& p, const Workspace& ws, const RopeTable* rope, const float* lse,
                           const __nv_bfloat16* dout, __nv_bfloat16* dq, cudaStream_t st) {
     BwdMaps m;
-    if (!encode_all(m, p, ws, dout, 128, 64)) return cudaErrorInvalidValue;
+    if (!encode_all(m, p, ws, dout, 128, 128)) return cudaErrorInvalidValue;
     BwdTcParams b = bwd_params(p, ws, lse);
     b.x = p.q;
     b.w = p.wq;
     b.dx = dq;
     b.dv = nullptr;
     b.dw_part = ws.dwq_part;
-    dq_tc_kernel<<<g_sms_b, bwdt::kThreads, bwdt::kSmem, st>>>(m.q, m.k, m.v, m.dout, *rope, b);
+    dq_tc_kernel<<<g_sms_b, bwdt::kThreads, dqt::kSmem, st>>>(m.q, m.k, m.v, m.dout, *rope, b);
     return cudaGetLastError();
 }
 
