@@ -122,6 +122,21 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def measured_traffic(kernel_key):
+    """DRAM bytes (read + write) of one launch from the committed ncu summary, or
+    None if the kernel's source changed since the counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        k = json.load(open(path))["kernels"][kernel_key]
+        src = os.path.join(ROOT, k["source"])
+        if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != k["sha256_16"]:
+            return None
+        return int(k["dram_read_bytes"]) + int(k["dram_write_bytes"])
+    except Exception:
+        return None
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -278,13 +293,18 @@ def run_ours(args):
     kms = stages[kern][0] / max(stages[kern][1], 1)
     ach = algo[kern] / (kms * 1e-3) / 1e12
     roof = {"kernel": kern, "bound": "tensor", "achieved": round(ach, 2), "peak": pk["bf16_tflops"],
-            "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops"], 4), "traffic": None,
+            "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops"], 4), "traffic": measured_traffic(kern),
             "peak_source": f"{pk['source']} bf16 burst",
             "frac_of_sustained": round(ach / pk["bf16_tflops_sustained"], 4)}
+    fwd_ms_launch = stages["fwd"][0] / max(stages["fwd"][1], 1)
+    fwd_ach = algo["fwd"] / (fwd_ms_launch * 1e-3) / 1e12
+    fwd_roof = {"kernel": "fwd", "bound": "tensor", "achieved": round(fwd_ach, 2), "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(fwd_ach / pk["bf16_tflops"], 4), "traffic": measured_traffic("fwd")}
     pro_ms = stages["prologue"][0] / max(stages["prologue"][1], 1)
     pro_bytes = 8.0 * S * H * 128  # q, k read (bf16) + q^, k^ written (bf16)
-    prologue = {"achieved_gbs": round(pro_bytes / (pro_ms * 1e-3) / 1e9, 1), "peak_gbs": pk["hbm_gbs"],
-                "frac": round(pro_bytes / (pro_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4), "ms": round(pro_ms, 4)}
+    prologue = {"bound": "hbm", "achieved": round(pro_bytes / (pro_ms * 1e-3) / 1e9, 1), "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": round(pro_bytes / (pro_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+                "traffic": measured_traffic("prologue"), "ms": round(pro_ms, 4)}
     launches_per_step = 3 + 7
 
     # ---- CPU baseline: the oracle as it stands, bounded sample, rank 0 only
@@ -303,7 +323,7 @@ def run_ours(args):
         "fwd_tflops_batch": round(fwd_flops / (fwd_ms / args.steps * 1e-3) / 1e12, 2) if fwd_ms else None,
         "fwd_per_sample": per_sample,
         "stages_ms_per_step": {k: round(v[0] / args.steps, 4) for k, v in stages.items()},
-        "roofline": roof, "prologue_roofline": prologue,
+        "roofline": roof, "fwd_roofline": fwd_roof, "prologue_roofline": prologue,
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / args.steps, 4)},
         "gpu_launches": launches_per_step * args.steps,
