@@ -127,9 +127,10 @@ h3attn_status h3attn_backward(h3attn_t h,
 /*
  * Waits for `stream`, then returns and clears the errors the device recorded
  * since the last call: INVALID_ARG (seg_offsets not 0 / increasing / ending at
- * total_tokens, or a finite rotated q^/k^ value or softmax gradient dS beyond
- * the fp16 range of the tensor-core operands, |x| > 65504; outputs of that call
- * are unspecified), TIMEOUT (a bounded wait
+ * total_tokens; or a finite rotated q^/k^ value beyond the fp16 range of the
+ * tensor-core operands, |x| > 65504; or a non-finite dq/dk row, which from
+ * finite inputs means the fp16 softmax gradient dS overflowed; outputs of that
+ * call are unspecified), TIMEOUT (a bounded wait
  * expired; outputs unspecified), CUDA (an asynchronous CUDA error), else OK.
  */
 h3attn_status h3attn_device_status(h3attn_t h, void *stream);

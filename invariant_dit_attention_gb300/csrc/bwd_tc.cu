@@ -150,6 +150,7 @@ __device__ __forceinline__ void rows_epilogue(const uint8_t* stage, float* red, 
 #pragma unroll
     for (int e = 0; e < 4; ++e) wl[e] = p.w[4 * lane + e];
     const int nvalid = min(128, it.L - 128 * it.tile);
+    bool nonfinite = false;
     // rows w8, w8 + 8, ...: four rows per batch so their loads overlap
     for (int r0 = w8; r0 < nvalid; r0 += 32) {
         float dy[4][4], xr[4][4];
@@ -173,9 +174,12 @@ __device__ __forceinline__ void rows_epilogue(const uint8_t* stage, float* red, 
             float d[4];
             const RowAngles a = row_angles(lr, pos[u][0], pos[u][1], pos[u][2]);
             row_norm_rope_bwd(dy[u], xr[u], wl, a, lr, p.eps, d, acc);
+            nonfinite |= !(isfinite(d[0]) && isfinite(d[1]) && isfinite(d[2]) && isfinite(d[3]));
             store_row4(p.dx + ((size_t)row * p.H + it.h) * kD + 4 * lane, d);
         }
     }
+    // a non-finite gradient row from finite inputs means an fp16 operand (dS) overflowed
+    if (nonfinite) atomicOr(p.plan.err, kErrRange);
 #pragma unroll
     for (int e = 0; e < 4; ++e) red[w8 * kD + 4 * lane + e] = acc[e];
     named_bar(3, 256);
@@ -436,7 +440,6 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         float* red = reinterpret_cast<float*>(smem + kOffDs);                  // epilogue only
         uint8_t* dsrow = smem + kOffDs + wg * kHalf + t * 128;
         uint32_t cntS = 0, items = 0, nds = 0;
-        bool range_ok = true;
         for (int i = blockIdx.x; !failed; i += gridDim.x) {
             BwdItem it;
             if (!bwd_item(p, i, it)) break;
@@ -450,8 +453,8 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 nd = 0.f;
                 if (t < 64 && qj < nq && q < it.L) {
                     const size_t idx = (size_t)it.h * p.seq.S + it.seg0 + q;
-                    nl = p.lse[idx] * kLog2e;
-                    nd = p.delta[idx];
+                    nl = -p.lse[idx] * kLog2e;  // staged negated: the loop adds them
+                    nd = -p.delta[idx];
                 }
             };
             fetch(0);
@@ -486,8 +489,8 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 }
                 ++nds;
                 const int validq = it.L - 128 * qj - 64 * wg;  // columns of this half inside the sample
-                const float4* lb4 = reinterpret_cast<const float4*>(lb);
-                float amax = 0.f;
+                const uint64_t* lb2 = reinterpret_cast<const uint64_t*>(lb);  // (-lse2, -lse2') pairs, then -Delta pairs
+                const uint64_t c2 = f2pack(c, c);
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     uint32_t sr[32];
@@ -498,31 +501,26 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                     for (int c8 = 0; c8 < 4; ++c8) {
                         uint32_t dk[4];
 #pragma unroll
-                        for (int e = 0; e < 8; e += 4) {
-                            const int col = 32 * hh + 8 * c8 + e;
-                            const float4 l4 = lb4[col >> 2];
-                            const float4 d4 = lb4[(64 + col) >> 2];
-                            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
-                            float pv[4], dsv[4];
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                pv[u] = ex2(fmaf(__uint_as_float(sr[8 * c8 + e + u]), c, -lv[u]));
-                                dsv[u] = pv[u] * (__uint_as_float(dr[hh][8 * c8 + e + u]) - dv[u]);
-                            }
+                        for (int e = 0; e < 8; e += 2) {
+                            const int k0 = 8 * c8 + e, col = 32 * hh + k0;
+                            float a0, a1, p0, p1, d0, d1;
+                            // P = 2^(s c - lse2_col); dS = P (dP - Delta_col), two columns per instruction
+                            f2unpack(f2fma(f2pack(__uint_as_float(sr[k0]), __uint_as_float(sr[k0 + 1])), c2, lb2[col >> 1]),
+                                     a0, a1);
+                            p0 = ex2(a0);
+                            p1 = ex2(a1);
+                            f2unpack(f2mul(f2pack(p0, p1),
+                                           f2add(f2pack(__uint_as_float(dr[hh][k0]), __uint_as_float(dr[hh][k0 + 1])),
+                                                 lb2[(64 + col) >> 1])),
+                                     d0, d1);
                             if (validq < 64) {  // tail block: columns past the sample end are exact zeros
-#pragma unroll
-                                for (int u = 0; u < 4; ++u) {
-                                    const bool v = col + u < validq;
-                                    pv[u] = v ? pv[u] : 0.f;
-                                    dsv[u] = v ? dsv[u] : 0.f;
-                                }
+                                p0 = col < validq ? p0 : 0.f;
+                                p1 = col + 1 < validq ? p1 : 0.f;
+                                d0 = col < validq ? d0 : 0.f;
+                                d1 = col + 1 < validq ? d1 : 0.f;
                             }
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) amax = fmaxf(amax, fabsf(dsv[u]));
-                            pk[(8 * c8 + e) >> 1] = pack_bf16(pv[0], pv[1]);
-                            pk[((8 * c8 + e) >> 1) + 1] = pack_bf16(pv[2], pv[3]);
-                            dk[e >> 1] = pack_f16(dsv[0], dsv[1]);
-                            dk[(e >> 1) + 1] = pack_f16(dsv[2], dsv[3]);
+                            pk[k0 >> 1] = pack_bf16(p0, p1);
+                            dk[e >> 1] = pack_f16(d0, d1);
                         }
                         const int chunk = 4 * hh + c8;
                         *reinterpret_cast<uint4*>(dsrow + ((chunk ^ (t & 7)) << 4)) =
@@ -532,7 +530,6 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                     // [16, 32) while it reads [32, 64)
                     tc::tmem_st16(tS + 16 * hh, pk);
                 }
-                range_ok &= !(key_ok && amax > 65504.f);
                 tc::tmem_wait_st();
                 tc::fence_proxy_async();
                 tc::fence_before_sync();
@@ -589,7 +586,6 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(bar(bItemFree));
         }
-        if (!range_ok) atomicOr(p.plan.err, kErrRange);
     }
 
     __syncthreads();
@@ -816,7 +812,6 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         float* red = reinterpret_cast<float*>(smem + kOffDs);  // epilogue only (all dQ MMAs done)
         uint8_t* dsrow = smem + kOffDs + wg * bwdt::kHalf + t * 128;
         uint32_t cntS = 0, items = 0, nds = 0;
-        bool range_ok = true;
         for (int i = blockIdx.x; !failed; i += gridDim.x) {
             BwdItem it;
             if (!bwd_item(p, i, it)) break;
@@ -853,7 +848,7 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                 }
                 ++nds;
                 const int validk = it.L - 128 * kj - 64 * wg;  // keys of this half inside the sample
-                float amax = 0.f;
+                const uint64_t c2 = f2pack(c, c), nl2 = f2pack(-lse2, -lse2), nd2 = f2pack(-dlt, -dlt);
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
@@ -861,23 +856,29 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                         uint32_t dk[4];
 #pragma unroll
                         for (int e = 0; e < 8; e += 2) {
-                            float dsv[2];
-#pragma unroll
-                            for (int u = 0; u < 2; ++u) {
-                                const int col = 32 * hh + 8 * c8 + e + u;
-                                const float pe = ex2(fmaf(__uint_as_float(sr[hh][8 * c8 + e + u]), c, -lse2));
-                                dsv[u] = pe * (__uint_as_float(dr[hh][8 * c8 + e + u]) - dlt);
-                                if (validk < 64) dsv[u] = col < validk ? dsv[u] : 0.f;
+                            const int k0 = 8 * c8 + e;
+                            float a0, a1, p0, p1, d0, d1;
+                            // P = 2^(s c - lse2); dS = P (dP - Delta), two columns per instruction
+                            f2unpack(f2fma(f2pack(__uint_as_float(sr[hh][k0]), __uint_as_float(sr[hh][k0 + 1])), c2, nl2),
+                                     a0, a1);
+                            p0 = ex2(a0);
+                            p1 = ex2(a1);
+                            f2unpack(f2mul(f2pack(p0, p1),
+                                           f2add(f2pack(__uint_as_float(dr[hh][k0]), __uint_as_float(dr[hh][k0 + 1])),
+                                                 nd2)),
+                                     d0, d1);
+                            if (validk < 64) {  // tail block: keys past the sample end give exact zeros
+                                const int col = 32 * hh + k0;
+                                d0 = col < validk ? d0 : 0.f;
+                                d1 = col + 1 < validk ? d1 : 0.f;
                             }
-                            amax = fmaxf(amax, fmaxf(fabsf(dsv[0]), fabsf(dsv[1])));
-                            dk[e >> 1] = pack_f16(dsv[0], dsv[1]);
+                            dk[e >> 1] = pack_f16(d0, d1);
                         }
                         const int chunk = 4 * hh + c8;
                         *reinterpret_cast<uint4*>(dsrow + ((chunk ^ (t & 7)) << 4)) =
                             make_uint4(dk[0], dk[1], dk[2], dk[3]);
                     }
                 }
-                range_ok &= !(row_ok && amax > 65504.f);
                 tc::fence_proxy_async();
                 tc::fence_before_sync();
                 __syncwarp();
@@ -911,7 +912,6 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(bar(bItemFree));
         }
-        if (!range_ok) atomicOr(p.plan.err, kErrRange);
     }
 
     __syncthreads();
