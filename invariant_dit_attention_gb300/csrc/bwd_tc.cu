@@ -37,22 +37,7 @@ constexpr int kThreads = 384;
 constexpr int kTile = 128 * 128 * 2;   // 32 KB
 constexpr int kHalf = 128 * 64 * 2;    // 16 KB
 constexpr int kPair = 2 * kTile;       // two tiles (q^ + dO, or k^ + v): 64 KB
-constexpr int kBlk = 64 * 128 * 2;    // one streamed 64-row block: 16 KB
-constexpr int kBlkHalf = 64 * 64 * 2;  // its 64-channel half (the TMA box): 8 KB
-constexpr int kBlkPair = 2 * kBlk;     // q^ + dO block, or k^ + v block: 32 KB
-constexpr int kRing = 3;               // ring stages of block pairs
-constexpr int kOffFixed = 0;           // the 128-row tile pair loaded once per item (also the epilogue stage)
-constexpr int kOffRing = kPair;        // ring of block pairs
-constexpr int kOffDs = kOffRing + kRing * kBlkPair;  // dq: dS of the two blocks in flight, [128][64] fp16 each
-constexpr int kDsBytes = 128 * 64 * 2;
-constexpr int kOffLse = kOffDs + 2 * kDsBytes;  // [2 wg][2 buf][2][64] floats
-constexpr int kOffRed = kOffLse + 2 * 2 * 2 * 64 * 4;  // [8 warps][128] floats
-constexpr int kOffRope = kOffRed + 8 * 128 * 4;  // shared copy of the rotary table
-constexpr int kOffBar = kOffRope + 768;
-constexpr int kSmem = kOffBar + 256 + 1024;
 constexpr float kLog2e = 1.4426950408889634f;
-enum { bFixedFull = 0, bItemFree, bRingFull, bRingEmpty = bRingFull + kRing, bSFull = bRingEmpty + kRing,
-       bPFull = bSFull + 2, bSUsed = bPFull + 2, bDsFree = bSUsed + 2, bAccDone = bDsFree + 2, bTail, bDone, bCount };
 }  // namespace bwdt
 
 struct BwdTcParams {
@@ -117,29 +102,6 @@ __device__ __forceinline__ void zero_rows(uint32_t half, int valid, int rows, in
 // between two warpgroups: columns 0..63 were packed at [0, 32), 64..127 at [64, 96).
 __device__ __forceinline__ uint32_t a_col(int kk) { return kk < 4 ? 8 * kk : 64 + 8 * (kk - 4); }
 
-__device__ __forceinline__ void init_bars(uint32_t sbase) {
-    using namespace bwdt;
-    auto bar = [&](int i) { return sbase + kOffBar + 8u * i; };
-    tc::mbar_init(bar(bFixedFull), 1);
-    tc::mbar_init(bar(bItemFree), 8);
-    for (int i = 0; i < kRing; ++i) {
-        tc::mbar_init(bar(bRingFull + i), 1);
-        tc::mbar_init(bar(bRingEmpty + i), 1);
-    }
-    for (int x = 0; x < 2; ++x) {
-        tc::mbar_init(bar(bSFull + x), 1);
-        tc::mbar_init(bar(bPFull + x), 4);
-    }
-    for (int x = 0; x < 2; ++x) {
-        tc::mbar_init(bar(bSUsed + x), 4);
-        tc::mbar_init(bar(bDsFree + x), 1);
-    }
-    tc::mbar_init(bar(bAccDone), 1);
-    tc::mbar_init(bar(bTail), 1);
-    tc::mbar_init(bar(bDone), 1);
-    tc::fence_mbar_init();
-}
-
 // Row epilogue over a staged tile of d(x^) (already scaled): RoPE^-1 and the
 // RMSNorm backward per row (one warp per row, 8 warps), dx rows in bf16, and
 // the tile's norm-weight partial (fixed order: rows by warp, then warps).
@@ -191,18 +153,6 @@ __device__ __forceinline__ void rows_epilogue(const uint8_t* stage, float* red, 
         p.dw_part[((size_t)it.tile_global * p.H + it.h) * kD + t] = s;
     }
 }
-
-// Streamed blocks are 64 rows (queries in dkdv, keys in dq), so two score
-// buffers fit beside the accumulators in TMEM: buffer X (X = block parity)
-// holds S at cols [128X, 128X+64) and dP at [128X+64, 128X+128); warpgroup X
-// handles the blocks of parity X.
-//   dkdv: P^T (bf16) is written over S's first 32 columns and dS^T (fp16) over
-//         dP's; accumulators dV [256, 384), dK [384, 512).  Buffer X is refilled
-//         with block b+2 right behind block b's dV/dK MMAs (in-order MMAs).
-//   dq:   dS (fp16) goes to a 128-byte-swizzled shared-memory tile X, so buffer X
-//         is refilled with block b+2 as soon as warpgroup X has loaded block b;
-//         the tile is rewritten only after block b's dQ MMAs completed.
-//         Accumulator dQ [256, 384).
 
 // ------------------------------------------------------------------ dK, dV
 //
@@ -603,21 +553,84 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
 
 // ------------------------------------------------------------------ dQ
 //
-// 128-key blocks (N = 128 MMAs run at the full rate), one score buffer in TMEM
-// (S cols [0, 128), dP cols [128, 256)) and dQ at [256, 384).  The two
-// warpgroups split each block's 128 columns (thread = query row).  dS goes to
-// a 128 x 128 fp16 shared-memory tile, so the score buffer is refilled with
-// block j+1 as soon as both warpgroups have loaded block j; dQ(j) follows.
+// 128-key blocks (N = 128 MMAs run at the full rate).  TMEM: S [0, 128),
+// dP [128, 256), dQ [256, 384), dS [384, 448).  The two warpgroups split each
+// block's 128 key columns (thread = query row).  The score buffer is refilled
+// with block j+1 as soon as both warpgroups have loaded block j; dS (fp16) is
+// written to its own TMEM columns and read by the dQ MMAs from there, and is
+// rewritten for block j+1 only after dQ(j) completed.  k^ tiles stream through
+// a 3-slot ring (held until dQ(j)), v tiles through a 2-slot ring (released
+// as soon as dP(j) completed), so the next tiles load while a block is used.
 namespace dqt {
-constexpr int kOffFixed = 0;                    // q^ + dO tiles (also the epilogue stage)
-constexpr int kOffRing = bwdt::kPair;           // 2 stages of k^ + v tiles
-constexpr int kOffDs = kOffRing + 2 * bwdt::kPair;  // dS tile (two 64-column halves); also the epilogue's red
-constexpr int kOffRope = kOffDs + bwdt::kTile;
-constexpr int kOffBar = kOffRope + 768;
-constexpr int kSmem = kOffBar + 256 + 1024;
-enum { bFixedFull = 0, bItemFree, bRingFull, bRingEmpty = bRingFull + 2, bSFull = bRingEmpty + 2, bSUsed, bPFull,
-       bDsFree, bAccDone, bTail, bDone, bCount };
+constexpr int kOffFixed = 0;                       // q^ + dO tiles (also the epilogue stage)
+constexpr int kKSlots = 3, kVSlots = 2;
+constexpr int kOffK = bwdt::kPair;                 // k^ ring
+constexpr int kOffV = kOffK + kKSlots * bwdt::kTile;  // v ring
+constexpr int kOffRed = kOffV + kVSlots * bwdt::kTile;  // [8 warps][64] floats, two passes
+constexpr int kOffRope = kOffRed + 8 * 64 * 4;
+constexpr int kOffBar = kOffRope + 640;
+constexpr int kSmem = kOffBar + 256;               // the dynamic shared memory base is 1024-aligned (checked)
+enum { bFixedFull = 0, bItemFree, bKFull, bKEmpty = bKFull + kKSlots, bVFull = bKEmpty + kKSlots,
+       bVEmpty = bVFull + kVSlots, bSFull = bVEmpty + kVSlots, bSUsed, bPFull, bDsFree, bAccDone, bTail, bDone,
+       bCount };
+constexpr uint32_t cDs = 384;
 }  // namespace dqt
+
+// Row epilogue of the dq kernel: as rows_epilogue, with the tile's weight
+// partial reduced across the 8 warps in two passes of 64 channels through a
+// 2 KB buffer (same fixed order).
+__device__ __forceinline__ void rows_epilogue_2pass(const uint8_t* stage, float* red, const BwdTcParams& p,
+                                                    const BwdItem& it, const RopeTable& srt, int w8, int lane) {
+    const LaneRope lr = lane_rope(srt, lane);
+    float wl[4], acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) wl[e] = p.w[4 * lane + e];
+    const int nvalid = min(128, it.L - 128 * it.tile);
+    bool nonfinite = false;
+    for (int r0 = w8; r0 < nvalid; r0 += 32) {
+        float dy[4][4], xr[4][4];
+        int pos[4][3];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int r = min(r0 + 8 * u, nvalid - 1);
+            const int row = it.row0 + r;
+            const float4 s4 = *reinterpret_cast<const float4*>(stage + stage_off(r, lane));
+            dy[u][0] = s4.x; dy[u][1] = s4.y; dy[u][2] = s4.z; dy[u][3] = s4.w;
+            load_row4(p.x + ((size_t)row * p.H + it.h) * kD + 4 * lane, xr[u]);
+            pos[u][0] = p.seq.pos_t[row];
+            pos[u][1] = p.seq.pos_h[row];
+            pos[u][2] = p.seq.pos_w[row];
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int r = r0 + 8 * u;
+            if (r >= nvalid) break;
+            const int row = it.row0 + r;
+            float d[4];
+            const RowAngles a = row_angles(lr, pos[u][0], pos[u][1], pos[u][2]);
+            row_norm_rope_bwd(dy[u], xr[u], wl, a, lr, p.eps, d, acc);
+            nonfinite |= !(isfinite(d[0]) && isfinite(d[1]) && isfinite(d[2]) && isfinite(d[3]));
+            store_row4(p.dx + ((size_t)row * p.H + it.h) * kD + 4 * lane, d);
+        }
+    }
+    if (nonfinite) atomicOr(p.plan.err, kErrRange);
+    const int t = w8 * 32 + lane;
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+        if ((lane >> 4) == pass) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) red[w8 * 64 + 4 * (lane & 15) + e] = acc[e];
+        }
+        named_bar(3, 256);
+        if (t < 64) {
+            float s = 0.f;
+#pragma unroll
+            for (int wi = 0; wi < 8; ++wi) s += red[wi * 64 + t];
+            p.dw_part[((size_t)it.tile_global * p.H + it.h) * kD + 64 * pass + t] = s;
+        }
+        named_bar(3, 256);
+    }
+}
 
 __global__ void __launch_bounds__(bwdt::kThreads, 1)
 dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
@@ -629,8 +642,12 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     using bwdt::kPair;
     using bwdt::kThreads;
     using bwdt::kTile;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if (smem_u32(smem_raw) & 1023u) {  // the layout below needs a 1024-byte aligned base
+        if (threadIdx.x == 0) atomicOr(p.plan.err, kErrTimeout);
+        return;
+    }
+    uint8_t* smem = smem_raw;
     const uint32_t sbase = smem_u32(smem);
     auto bar = [&](int i) { return sbase + kOffBar + 8u * i; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * bCount);
@@ -640,9 +657,13 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     if (tid == 0) {
         tc::mbar_init(bar(bFixedFull), 1);
         tc::mbar_init(bar(bItemFree), 8);
-        for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(bar(bRingFull + i), 1);
-            tc::mbar_init(bar(bRingEmpty + i), 1);
+        for (int i = 0; i < kKSlots; ++i) {
+            tc::mbar_init(bar(bKFull + i), 1);
+            tc::mbar_init(bar(bKEmpty + i), 1);
+        }
+        for (int i = 0; i < kVSlots; ++i) {
+            tc::mbar_init(bar(bVFull + i), 1);
+            tc::mbar_init(bar(bVEmpty + i), 1);
         }
         tc::mbar_init(bar(bSFull), 1);
         tc::mbar_init(bar(bSUsed), 8);
@@ -678,7 +699,7 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
-        uint32_t ring = 0, items = 0, tails = 0;
+        uint32_t kr = 0, vr = 0, items = 0, tails = 0;
         for (int i = blockIdx.x; !failed; i += gridDim.x) {
             BwdItem it;
             if (!bwd_item(p, i, it)) break;
@@ -699,20 +720,24 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
             ++items;
             const int nk = (it.L + 127) / 128;
             for (int kj = 0; kj < nk && !failed; ++kj) {
-                const uint32_t slot = ring & 1, ph = (ring >> 1) & 1;
-                const uint32_t dst = sbase + kOffRing + slot * kPair;
                 const int y = it.seg0 + 128 * kj;
                 const int valid = it.L - 128 * kj;
                 const bool tail = valid < 128;
+                const uint32_t ks = kr % kKSlots, vs = vr % kVSlots;
+                const uint32_t kdst = sbase + kOffK + ks * kTile, vdst = sbase + kOffV + vs * kTile;
                 if (lane == 0) {
-                    if (!tc::mbar_wait(bar(bRingEmpty + slot), ph ^ 1, abort_flag)) fail();
+                    // v first: its slot frees early, and S(j) waits for both anyway
+                    if (!tc::mbar_wait(bar(bVEmpty + vs), ((vr / kVSlots) & 1) ^ 1, abort_flag)) fail();
                     if (!failed) {
-                        const uint32_t b = tail ? bar(bTail) : bar(bRingFull + slot);
-                        tc::mbar_expect_tx(b, kPair);
-                        for (int hf = 0; hf < 2; ++hf) {
-                            tc::tma_load_2d(dst + hf * kHalf, &mk, x0 + 64 * hf, y, b);
-                            tc::tma_load_2d(dst + kTile + hf * kHalf, &mv, x0 + 64 * hf, y, b);
-                        }
+                        tc::mbar_expect_tx(bar(bVFull + vs), kTile);
+                        for (int hf = 0; hf < 2; ++hf)
+                            tc::tma_load_2d(vdst + hf * kHalf, &mv, x0 + 64 * hf, y, bar(bVFull + vs));
+                    }
+                    if (!failed && !tc::mbar_wait(bar(bKEmpty + ks), ((kr / kKSlots) & 1) ^ 1, abort_flag)) fail();
+                    if (!failed) {
+                        const uint32_t b = tail ? bar(bTail) : bar(bKFull + ks);
+                        tc::mbar_expect_tx(b, kTile);
+                        for (int hf = 0; hf < 2; ++hf) tc::tma_load_2d(kdst + hf * kHalf, &mk, x0 + 64 * hf, y, b);
                         if (tail && !tc::mbar_wait(bar(bTail), tails & 1, abort_flag)) fail();
                     }
                 }
@@ -720,12 +745,13 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                 if (tail && !failed) {
                     ++tails;
                     // key rows past the sample end: zero k^ (dS is 0 there, k^ may not be finite)
-                    for (int hf = 0; hf < 2; ++hf) zero_rows(dst + hf * kHalf, valid, 128, lane);
+                    for (int hf = 0; hf < 2; ++hf) zero_rows(kdst + hf * kHalf, valid, 128, lane);
                     tc::fence_proxy_async();
                     __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(bar(bRingFull + slot));
+                    if (lane == 0) tc::mbar_arrive(bar(bKFull + ks));
                 }
-                ++ring;
+                ++kr;
+                ++vr;
             }
         }
     } else if (warp == 1) {
@@ -737,13 +763,17 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
             // descriptors are built once; per MMA only the 16-byte start address moves
             const uint64_t dQ = tc::smem_desc_sw128(sbase + kOffFixed, 16, 1024);
             const uint64_t dO = dQ + (kTile >> 4);
-            const uint64_t dRing = tc::smem_desc_sw128(sbase + kOffRing, 16, 1024);
-            const uint64_t dRingMN = tc::smem_desc_sw128(sbase + kOffRing, kHalf, 1024);
-            const uint64_t dDs = tc::smem_desc_sw128(sbase + kOffDs, 16, 1024);
-            uint32_t ring = 0, items = 0, cntS = 0;
+            const uint64_t dKr = tc::smem_desc_sw128(sbase + kOffK, 16, 1024);
+            const uint64_t dKrMN = tc::smem_desc_sw128(sbase + kOffK, kHalf, 1024);
+            const uint64_t dVr = tc::smem_desc_sw128(sbase + kOffV, 16, 1024);
+            uint32_t kr = 0, vr = 0, items = 0, cntS = 0;
             // S(j) = q^ k^(j)^T and dP(j) = dO v(j)^T into the score buffer
-            auto issue_s = [&](uint32_t slot) {
-                const uint64_t bk = dRing + ((slot * kPair) >> 4), bv = bk + (kTile >> 4);
+            auto issue_s = [&]() -> bool {
+                const uint32_t ks = kr % kKSlots, vs = vr % kVSlots;
+                if (!tc::mbar_wait(bar(bKFull + ks), (kr / kKSlots) & 1, abort_flag)) return false;
+                if (!tc::mbar_wait(bar(bVFull + vs), (vr / kVSlots) & 1, abort_flag)) return false;
+                tc::fence_after_sync();
+                const uint64_t bk = dKr + ((ks * kTile) >> 4), bv = dVr + ((vs * kTile) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t koff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
@@ -755,6 +785,9 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                     tc::mma_ss(tmem + 128, dO + koff, bv + koff, idSbf, kk > 0);
                 }
                 tc::mma_commit(bar(bSFull));
+                tc::mma_commit(bar(bVEmpty + vs));  // v(j) is free once dP(j) completed
+                ++vr;
+                return true;
             };
             for (int i = blockIdx.x; !failed; i += gridDim.x) {
                 BwdItem it;
@@ -762,37 +795,28 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                 if (!tc::mbar_wait(bar(bFixedFull), items & 1, abort_flag)) { fail(); break; }
                 ++items;
                 const int nk = (it.L + 127) / 128;
-                const uint32_t ring0 = ring;
-                {
-                    const uint32_t slot = ring & 1;
-                    if (!tc::mbar_wait(bar(bRingFull + slot), (ring >> 1) & 1, abort_flag)) { fail(); break; }
-                    ++ring;
-                    tc::fence_after_sync();
-                    issue_s(slot);
-                }
+                uint32_t kcur = kr;  // ring index of the k^ tile of block kj
+                if (!issue_s()) { fail(); break; }
+                ++kr;
                 for (int kj = 0; kj < nk && !failed; ++kj) {
-                    const uint32_t slot = (ring0 + kj) & 1;
                     // block kj's scores are in registers: refill the buffer with block kj+1
                     if (!tc::mbar_wait(bar(bSUsed), cntS & 1, abort_flag)) { fail(); break; }
                     ++cntS;
                     if (kj + 1 < nk) {
-                        const uint32_t ns = ring & 1;
-                        if (!tc::mbar_wait(bar(bRingFull + ns), (ring >> 1) & 1, abort_flag)) { fail(); break; }
-                        ++ring;
-                        tc::fence_after_sync();
-                        issue_s(ns);
+                        if (!issue_s()) { fail(); break; }
+                        ++kr;
                     }
                     if (!tc::mbar_wait(bar(bPFull), (cntS - 1) & 1, abort_flag)) { fail(); break; }
                     tc::fence_after_sync();
-                    const uint64_t bk = dRingMN + ((slot * kPair) >> 4);
-                    // dQ += dS(j) k^(j): K = the block's 128 keys; dS from shared memory
+                    const uint32_t ks = kcur % kKSlots;
+                    const uint64_t bk = dKrMN + ((ks * kTile) >> 4);
+                    // dQ += dS(j) k^(j): K = the block's 128 keys, dS from TMEM
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t aoff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
-                        tc::mma_ss(tmem + 256, dDs + aoff, bk + ((kk * 2048) >> 4), idA16, (kj > 0) || (kk > 0));
-                    }
+                    for (int kk = 0; kk < 8; ++kk)
+                        tc::mma_ts(tmem + 256, tmem + cDs + 8 * kk, bk + ((kk * 2048) >> 4), idA16, (kj > 0) || (kk > 0));
                     tc::mma_commit(bar(bDsFree));
-                    tc::mma_commit(bar(bRingEmpty + slot));
+                    tc::mma_commit(bar(bKEmpty + ks));
+                    ++kcur;
                 }
                 if (failed) break;
                 tc::mma_commit(bar(bAccDone));
@@ -803,14 +827,14 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------- softmax gradient + epilogue
-        const int wg = (warp - 4) >> 2;                 // column half of the score tile
+        const int wg = (warp - 4) >> 2;                 // key half of the score tile
         const int w8 = warp - 4;
         const int t = tid - 128 * (1 + wg);             // query row of the tile
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         const uint32_t tS = tmem + lane_base + 64 * wg, tDP = tmem + lane_base + 128 + 64 * wg;
+        const uint32_t tDs = tmem + lane_base + cDs + 32 * wg;
         const float c = p.scale * kLog2e;
-        float* red = reinterpret_cast<float*>(smem + kOffDs);  // epilogue only (all dQ MMAs done)
-        uint8_t* dsrow = smem + kOffDs + wg * bwdt::kHalf + t * 128;
+        float* red = reinterpret_cast<float*>(smem + kOffRed);
         uint32_t cntS = 0, items = 0, nds = 0;
         for (int i = blockIdx.x; !failed; i += gridDim.x) {
             BwdItem it;
@@ -820,6 +844,7 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
             const size_t idx = (size_t)it.h * p.seq.S + (row_ok ? it.row0 + t : it.seg0);
             const float lse2 = row_ok ? p.lse[idx] * kLog2e : 0.f;
             const float dlt = row_ok ? p.delta[idx] : 0.f;
+            const uint64_t c2 = f2pack(c, c), nl2 = f2pack(-lse2, -lse2), nd2 = f2pack(-dlt, -dlt);
             for (int kj = 0; kj < nk; ++kj) {
                 bool ok = true;
                 if (lane == 0) ok = tc::mbar_wait(bar(bSFull), cntS & 1, abort_flag);
@@ -839,47 +864,39 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                 tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(bar(bSUsed));
-                // the dS tile is rewritten only after the previous block's dQ MMAs read it
+                // dS of the previous block must have been read by its dQ MMAs
                 if (nds > 0) {
                     bool fr = true;
                     if (lane == 0) fr = tc::mbar_wait(bar(bDsFree), (nds - 1) & 1, abort_flag);
                     fr = __shfl_sync(0xffffffffu, fr, 0);
                     if (!fr) { fail(); break; }
+                    tc::fence_after_sync();
                 }
                 ++nds;
                 const int validk = it.L - 128 * kj - 64 * wg;  // keys of this half inside the sample
-                const uint64_t c2 = f2pack(c, c), nl2 = f2pack(-lse2, -lse2), nd2 = f2pack(-dlt, -dlt);
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t dk[16];
 #pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8) {
-                        uint32_t dk[4];
-#pragma unroll
-                        for (int e = 0; e < 8; e += 2) {
-                            const int k0 = 8 * c8 + e;
-                            float a0, a1, p0, p1, d0, d1;
-                            // P = 2^(s c - lse2); dS = P (dP - Delta), two columns per instruction
-                            f2unpack(f2fma(f2pack(__uint_as_float(sr[hh][k0]), __uint_as_float(sr[hh][k0 + 1])), c2, nl2),
-                                     a0, a1);
-                            p0 = ex2(a0);
-                            p1 = ex2(a1);
-                            f2unpack(f2mul(f2pack(p0, p1),
-                                           f2add(f2pack(__uint_as_float(dr[hh][k0]), __uint_as_float(dr[hh][k0 + 1])),
-                                                 nd2)),
-                                     d0, d1);
-                            if (validk < 64) {  // tail block: keys past the sample end give exact zeros
-                                const int col = 32 * hh + k0;
-                                d0 = col < validk ? d0 : 0.f;
-                                d1 = col + 1 < validk ? d1 : 0.f;
-                            }
-                            dk[e >> 1] = pack_f16(d0, d1);
+                    for (int e = 0; e < 32; e += 2) {
+                        float a0, a1, p0, p1, d0, d1;
+                        // P = 2^(s c - lse2); dS = P (dP - Delta), two columns per instruction
+                        f2unpack(f2fma(f2pack(__uint_as_float(sr[hh][e]), __uint_as_float(sr[hh][e + 1])), c2, nl2), a0, a1);
+                        p0 = ex2(a0);
+                        p1 = ex2(a1);
+                        f2unpack(f2mul(f2pack(p0, p1),
+                                       f2add(f2pack(__uint_as_float(dr[hh][e]), __uint_as_float(dr[hh][e + 1])), nd2)),
+                                 d0, d1);
+                        if (validk < 64) {  // tail block: keys past the sample end give exact zeros
+                            const int col = 32 * hh + e;
+                            d0 = col < validk ? d0 : 0.f;
+                            d1 = col + 1 < validk ? d1 : 0.f;
                         }
-                        const int chunk = 4 * hh + c8;
-                        *reinterpret_cast<uint4*>(dsrow + ((chunk ^ (t & 7)) << 4)) =
-                            make_uint4(dk[0], dk[1], dk[2], dk[3]);
+                        dk[e >> 1] = pack_f16(d0, d1);
                     }
+                    tc::tmem_st16(tDs + 16 * hh, dk);
                 }
-                tc::fence_proxy_async();
+                tc::tmem_wait_st();
                 tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(bar(bPFull));
@@ -906,7 +923,7 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                 }
             }
             named_bar(3, 256);
-            rows_epilogue(smem + kOffFixed, red, p, it, srt, w8, lane);
+            rows_epilogue_2pass(smem + kOffFixed, red, p, it, srt, w8, lane);
             tc::fence_before_sync();
             tc::fence_proxy_async();
             __syncwarp();
