@@ -77,7 +77,8 @@ typedef struct {
 
 /*
  * Creates a handle on the current CUDA device and allocates its workspace
- * (rotated q^/k^ buffers of max_tokens * H * 128 bf16 each, softmax row terms,
+ * (rotated q^/k^ buffers of max_tokens * H * 128 fp16 each, the backward's FP32
+ * dq^/dk^ rows of max_tokens * H * 128 floats each, softmax row terms,
  * weight-gradient partials, a small per-call plan).  The workspace is bounded
  * by the config, never by the inputs.  *out receives the handle.
  * Errors: INVALID_ARG (null pointer, sizes < 1), UNSUPPORTED (head_dim,
@@ -152,7 +153,8 @@ enum {
     H3ATTN_STAGE_BWD_DKDV = 4,  /* dK (through RoPE/RMSNorm), dV               */
     H3ATTN_STAGE_BWD_DQ = 5,    /* dQ (through RoPE/RMSNorm)                   */
     H3ATTN_STAGE_BWD_DW = 6,    /* fixed-order norm-weight gradient reduction  */
-    H3ATTN_NUM_STAGES = 7
+    H3ATTN_STAGE_BWD_ROWS = 7,  /* RoPE^-1 + RMSNorm backward of dq^, dk^ rows */
+    H3ATTN_NUM_STAGES = 8
 };
 h3attn_status h3attn_set_stage_timing(h3attn_t h, int enable);
 h3attn_status h3attn_stage_times(h3attn_t h, float *total_ms, int *launches, int n_stages);

@@ -7,9 +7,10 @@
 //   P_ij = exp(scale q^_i.k^_j - lse_i),  dP_ij = dO_i . v_j,  dS_ij = P_ij (dP_ij - Delta_i)
 //   dV_j = sum_i P_ij dO_i,  dk^_j = scale sum_i dS_ij q^_i              (dkdv_tc_kernel)
 //   dq^_i = scale sum_j dS_ij k^_j                                       (dq_tc_kernel)
-// then RoPE^-1 and the RMSNorm backward per row in the epilogues, and the
-// norm-weight gradients reduced per 128-token tile, per sample, then over
-// samples, always in the same order (dw_sample_kernel, dw_total_kernel).
+// The main kernels leave scale * dk^ and scale * dq^ in FP32 rows; rows_bwd_kernel
+// then applies RoPE^-1 and the RMSNorm backward per row and reduces the
+// norm-weight gradient per 128-token tile, then per sample, then over samples,
+// always in the same order (dw_sample_kernel, dw_total_kernel).
 //
 // No atomics anywhere: dkdv and dq each recompute S and P (7 tile products for
 // the 5 of the algorithm) and every sum runs over tiles anchored at the sample
@@ -18,12 +19,11 @@
 //
 // Both main kernels are persistent (one CTA per SM) with the forward's roles:
 // warp 0 TMA producer, warp 1 single-thread tcgen05 issuer, warps 4-7 and 8-11
-// two warpgroups that ping-pong over the 64-row blocks streamed against the
-// CTA's 128-row tile (thread = TMEM lane = one row of the tile), so the tensor
-// pipe computes one block's products while the other block's softmax
-// gradient runs.  Operands: S on fp16 q^/k^, dP on bf16 dO/v, P (bf16) and dS
-// (fp16) written back into tensor memory over the columns their warpgroup
-// just read, and fed to the accumulating MMAs as the TMEM-resident A operand.
+// two warpgroups that split each 128 x 128 score block by columns (thread =
+// TMEM lane = one row of the CTA's 128-row tile).  Operands: S on fp16 q^/k^,
+// dP on bf16 dO/v, P (bf16) and dS (fp16) for the accumulating products.  An
+// item's accumulators are drained to HBM as soon as its last MMA completed, so
+// the next item's loads and products start right away.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -45,14 +45,10 @@ struct BwdTcParams {
     Plan plan;
     int H;
     float scale;
-    float eps;
     const float* lse;
     const float* delta;
-    const __nv_bfloat16* x;  // raw q (dq kernel) or k (dkdv kernel)
-    const float* w;          // q_norm_w or k_norm_w
-    __nv_bfloat16* dx;       // dq or dk
-    __nv_bfloat16* dv;       // dkdv kernel only
-    float* dw_part;          // [tiles128, H, 128]
+    __nv_bfloat16* dv;  // dkdv kernel only
+    float* dyhat;       // scale * dk^ (dkdv) or scale * dq^ (dq): FP32 [S, H, 128]
 };
 
 struct BwdItem {
@@ -86,11 +82,6 @@ __device__ __forceinline__ void named_bar(int id, int count) {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
 }
 
-// Byte offset of float4 chunk c4 (0..31) of fp32 row r in a [128][128] staging
-// tile; chunks are XOR-swizzled by the row so that both row-per-thread writes
-// and warp-per-row reads are free of bank conflicts.
-__device__ __forceinline__ uint32_t stage_off(int r, int c4) { return (uint32_t)(r * 512 + ((c4 ^ (r & 7)) << 4)); }
-
 // Zeroes rows [valid, rows) of a 64-channel-half tile (whole 128-byte rows).
 __device__ __forceinline__ void zero_rows(uint32_t half, int valid, int rows, int lane) {
     for (int r = valid + (lane >> 3); r < rows; r += 4)
@@ -102,88 +93,43 @@ __device__ __forceinline__ void zero_rows(uint32_t half, int valid, int rows, in
 // between two warpgroups: columns 0..63 were packed at [0, 32), 64..127 at [64, 96).
 __device__ __forceinline__ uint32_t a_col(int kk) { return kk < 4 ? 8 * kk : 64 + 8 * (kk - 4); }
 
-// Row epilogue over a staged tile of d(x^) (already scaled): RoPE^-1 and the
-// RMSNorm backward per row (one warp per row, 8 warps), dx rows in bf16, and
-// the tile's norm-weight partial (fixed order: rows by warp, then warps).
-__device__ __forceinline__ void rows_epilogue(const uint8_t* stage, float* red, const BwdTcParams& p,
-                                              const BwdItem& it, const RopeTable& srt, int w8, int lane) {
-    const LaneRope lr = lane_rope(srt, lane);
-    float wl[4], acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) wl[e] = p.w[4 * lane + e];
-    const int nvalid = min(128, it.L - 128 * it.tile);
-    bool nonfinite = false;
-    // rows w8, w8 + 8, ...: four rows per batch so their loads overlap
-    for (int r0 = w8; r0 < nvalid; r0 += 32) {
-        float dy[4][4], xr[4][4];
-        int pos[4][3];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int r = min(r0 + 8 * u, nvalid - 1);
-            const int row = it.row0 + r;
-            const float4 s4 = *reinterpret_cast<const float4*>(stage + stage_off(r, lane));
-            dy[u][0] = s4.x; dy[u][1] = s4.y; dy[u][2] = s4.z; dy[u][3] = s4.w;
-            load_row4(p.x + ((size_t)row * p.H + it.h) * kD + 4 * lane, xr[u]);
-            pos[u][0] = p.seq.pos_t[row];
-            pos[u][1] = p.seq.pos_h[row];
-            pos[u][2] = p.seq.pos_w[row];
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int r = r0 + 8 * u;
-            if (r >= nvalid) break;
-            const int row = it.row0 + r;
-            float d[4];
-            const RowAngles a = row_angles(lr, pos[u][0], pos[u][1], pos[u][2]);
-            row_norm_rope_bwd(dy[u], xr[u], wl, a, lr, p.eps, d, acc);
-            nonfinite |= !(isfinite(d[0]) && isfinite(d[1]) && isfinite(d[2]) && isfinite(d[3]));
-            store_row4(p.dx + ((size_t)row * p.H + it.h) * kD + 4 * lane, d);
-        }
-    }
-    // a non-finite gradient row from finite inputs means an fp16 operand (dS) overflowed
-    if (nonfinite) atomicOr(p.plan.err, kErrRange);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) red[w8 * kD + 4 * lane + e] = acc[e];
-    named_bar(3, 256);
-    const int t = w8 * 32 + lane;
-    if (t < kD) {
-        float s = 0.f;
-#pragma unroll
-        for (int wi = 0; wi < 8; ++wi) s += red[wi * kD + t];
-        p.dw_part[((size_t)it.tile_global * p.H + it.h) * kD + t] = s;
-    }
-}
+// The same for a tile split between four warpgroups: columns 32w..32w+31 were
+// packed at [32w, 32w + 16).
+__device__ __forceinline__ uint32_t a_col4(int kk) { return 32 * (kk >> 1) + 8 * (kk & 1); }
 
 // ------------------------------------------------------------------ dK, dV
 //
 // 128-query blocks (N = 128 MMAs run at the full rate).  TMEM: S^T [0, 128),
 // dP^T [128, 256), dV [256, 384), dK [384, 512).  The two warpgroups split each
-// block's 128 query columns (thread = key row).  P^T (bf16) is written over
-// the S^T columns its warpgroup read (A operand of dV from TMEM); dS^T (fp16)
-// goes to a 128 x 128 shared-memory tile (A operand of dK), so the dP^T buffer
-// is refilled with block j+1 as soon as both warpgroups have loaded block j.
-// S^T(j+1) follows dV(j) (in-order MMAs: P^T(j) is read before it is overwritten).
+// block's 128 query columns (thread = key row).  The softmax gradient of a
+// block runs in two phases: P^T (bf16) first, written over the S^T columns its
+// warpgroup read (A operand of dV from TMEM), then dS^T (fp16) to a 128 x 128
+// shared-memory tile (A operand of dK).  So dV(j) and S^T(j+1) run on the
+// tensor cores while dS^T(j) is computed, and dK(j) while P^T(j+1) is; dP^T(j+1)
+// is issued as soon as both warpgroups have loaded dP^T(j).  q^ and dO stream
+// through separate 2-slot rings: a dO slot is released after dV(j), a q^ slot
+// after dK(j).
 namespace kvt {
-constexpr int kOffFixed = 0;                        // k^ + v tiles (also the epilogue stage)
-constexpr int kOffRing = bwdt::kPair;               // 2 stages of q^ + dO tiles
-constexpr int kOffDs = kOffRing + 2 * bwdt::kPair;  // dS^T tile (two 64-column halves); also the epilogue's red
-constexpr int kOffLse = kOffDs + bwdt::kTile;       // [2 wg][2 buf][lse2 64 | delta 64] floats
-constexpr int kOffRope = kOffLse + 2 * 2 * 128 * 4;
-constexpr int kOffBar = kOffRope + 640;
+constexpr int kThreads = 640;                       // warps 0-3: producer, MMA issuer; 4-19: four warpgroups
+constexpr int kOffFixed = 0;                        // k^ + v tiles
+constexpr int kOffQ = bwdt::kPair;                  // q^ ring, 2 slots
+constexpr int kOffO = kOffQ + 2 * bwdt::kTile;      // dO ring, 2 slots
+constexpr int kOffDs = kOffO + 2 * bwdt::kTile;     // dS^T tile (two 64-column halves)
+constexpr int kOffLse = kOffDs + bwdt::kTile;       // [4 wg][2 buf][lse2 32 | delta 32] floats
+constexpr int kOffBar = kOffLse + 2 * 2 * 128 * 4;
 constexpr int kSmem = kOffBar + 256;                // the dynamic shared memory base is 1024-aligned (checked)
-enum { bFixedFull = 0, bItemFree, bRingFull, bRingEmpty = bRingFull + 2, bSFull = bRingEmpty + 2, bDpUsed, bPFull,
-       bDsFree, bAccDone, bTail, bDone, bCount };
+enum { bFixedFull = 0, bQFull, bQEmpty = bQFull + 2, bOFull = bQEmpty + 2, bOEmpty = bOFull + 2,
+       bSFull = bOEmpty + 2, bDpUsed, bPtFull, bDsFull, bDsFree, bAccDone, bTail, bDone, bCount };
 }  // namespace kvt
 
-__global__ void __launch_bounds__(bwdt::kThreads, 1)
+__global__ void __launch_bounds__(kvt::kThreads, 1)
 dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
-               const __grid_constant__ RopeTable rt, const BwdTcParams p) {
+               const BwdTcParams p) {
     using namespace kvt;
     using bwdt::kHalf;
     using bwdt::kLog2e;
     using bwdt::kPair;
-    using bwdt::kThreads;
     using bwdt::kTile;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if (smem_u32(smem_raw) & 1023u) {  // the layout below needs a 1024-byte aligned base
@@ -199,14 +145,16 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
 
     if (tid == 0) {
         tc::mbar_init(bar(bFixedFull), 1);
-        tc::mbar_init(bar(bItemFree), 8);
         for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(bar(bRingFull + i), 1);
-            tc::mbar_init(bar(bRingEmpty + i), 1);
+            tc::mbar_init(bar(bQFull + i), 1);
+            tc::mbar_init(bar(bQEmpty + i), 1);
+            tc::mbar_init(bar(bOFull + i), 1);
+            tc::mbar_init(bar(bOEmpty + i), 1);
         }
         tc::mbar_init(bar(bSFull), 1);
-        tc::mbar_init(bar(bDpUsed), 8);
-        tc::mbar_init(bar(bPFull), 8);
+        tc::mbar_init(bar(bDpUsed), 16);
+        tc::mbar_init(bar(bPtFull), 16);
+        tc::mbar_init(bar(bDsFull), 16);
         tc::mbar_init(bar(bDsFree), 1);
         tc::mbar_init(bar(bAccDone), 1);
         tc::mbar_init(bar(bTail), 1);
@@ -219,8 +167,6 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         tc::tmem_relinquish();
         tc::fence_before_sync();
     }
-    RopeTable& srt = *reinterpret_cast<RopeTable*>(smem + kOffRope);
-    rope_to_smem(rt, srt, tid, kThreads);
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
@@ -230,21 +176,20 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         *abort_flag = 1;
         atomicOr(p.plan.err, kErrTimeout);
     };
-    if (warp < 4) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 152;");
-    } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 176;");
-    }
+    // 640 threads x 96 registers: the MMA issuer and the softmax warps both need about 96,
+    // so no setmaxnreg split
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
-        uint32_t ring = 0, items = 0, tails = 0;
+        // blk counts streamed blocks; both rings have two slots: slot blk & 1, phase (blk >> 1) & 1
+        uint32_t blk = 0, items = 0, tails = 0;
         for (int i = blockIdx.x; !failed; i += gridDim.x) {
             BwdItem it;
             if (!bwd_item(p, i, it)) break;
             const int x0 = it.h * 128;
             if (lane == 0) {
-                if (items > 0 && !tc::mbar_wait(bar(bItemFree), (items - 1) & 1, abort_flag)) fail();
+                // the fixed tiles are reloaded once the previous item's last MMA completed
+                if (items > 0 && !tc::mbar_wait(bar(bAccDone), (items - 1) & 1, abort_flag)) fail();
                 if (!failed) {
                     tc::fence_proxy_async();
                     tc::mbar_expect_tx(bar(bFixedFull), kPair);
@@ -259,19 +204,26 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             ++items;
             const int nq = (it.L + 127) / 128;
             for (int qj = 0; qj < nq && !failed; ++qj) {
-                const uint32_t slot = ring & 1, ph = (ring >> 1) & 1;
-                const uint32_t dst = sbase + kOffRing + slot * kPair;
+                const uint32_t slot = blk & 1, ph = (blk >> 1) & 1;
+                const uint32_t qdst = sbase + kOffQ + slot * kTile, odst = sbase + kOffO + slot * kTile;
                 const int y = it.seg0 + 128 * qj;
                 const int valid = it.L - 128 * qj;
                 const bool tail = valid < 128;
                 if (lane == 0) {
-                    if (!tc::mbar_wait(bar(bRingEmpty + slot), ph ^ 1, abort_flag)) fail();
+                    // dO first: its slot frees earlier (after dV) and dP^T needs it first
+                    if (!tc::mbar_wait(bar(bOEmpty + slot), ph ^ 1, abort_flag)) fail();
+                    if (!failed && !tail) {
+                        tc::mbar_expect_tx(bar(bOFull + slot), kTile);
+                        for (int hf = 0; hf < 2; ++hf)
+                            tc::tma_load_2d(odst + hf * kHalf, &mdo, x0 + 64 * hf, y, bar(bOFull + slot));
+                    }
+                    if (!failed && !tc::mbar_wait(bar(bQEmpty + slot), ph ^ 1, abort_flag)) fail();
                     if (!failed) {
-                        const uint32_t b = tail ? bar(bTail) : bar(bRingFull + slot);
-                        tc::mbar_expect_tx(b, kPair);
+                        const uint32_t b = tail ? bar(bTail) : bar(bQFull + slot);
+                        tc::mbar_expect_tx(b, tail ? kPair : kTile);
                         for (int hf = 0; hf < 2; ++hf) {
-                            tc::tma_load_2d(dst + hf * kHalf, &mq, x0 + 64 * hf, y, b);
-                            tc::tma_load_2d(dst + kTile + hf * kHalf, &mdo, x0 + 64 * hf, y, b);
+                            tc::tma_load_2d(qdst + hf * kHalf, &mq, x0 + 64 * hf, y, b);
+                            if (tail) tc::tma_load_2d(odst + hf * kHalf, &mdo, x0 + 64 * hf, y, b);
                         }
                         if (tail && !tc::mbar_wait(bar(bTail), tails & 1, abort_flag)) fail();
                     }
@@ -282,14 +234,17 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                     // query rows past the sample end: zero q^ and dO so no neighbour
                     // value reaches the dV and dK products
                     for (int hf = 0; hf < 2; ++hf) {
-                        zero_rows(dst + hf * kHalf, valid, 128, lane);
-                        zero_rows(dst + kTile + hf * kHalf, valid, 128, lane);
+                        zero_rows(qdst + hf * kHalf, valid, 128, lane);
+                        zero_rows(odst + hf * kHalf, valid, 128, lane);
                     }
                     tc::fence_proxy_async();
                     __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(bar(bRingFull + slot));
+                    if (lane == 0) {
+                        tc::mbar_arrive(bar(bQFull + slot));
+                        tc::mbar_arrive(bar(bOFull + slot));
+                    }
                 }
-                ++ring;
+                ++blk;
             }
         }
     } else if (warp == 1) {
@@ -302,25 +257,35 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             // descriptors are built once; per MMA only the 16-byte start address moves
             const uint64_t dK = tc::smem_desc_sw128(sbase + kOffFixed, 16, 1024);
             const uint64_t dV = dK + (kTile >> 4);
-            const uint64_t dRing = tc::smem_desc_sw128(sbase + kOffRing, 16, 1024);
-            const uint64_t dRingMN = tc::smem_desc_sw128(sbase + kOffRing, kHalf, 1024);
+            const uint64_t dQr = tc::smem_desc_sw128(sbase + kOffQ, 16, 1024);
+            const uint64_t dOr = tc::smem_desc_sw128(sbase + kOffO, 16, 1024);
+            const uint64_t dQrMN = tc::smem_desc_sw128(sbase + kOffQ, kHalf, 1024);
+            const uint64_t dOrMN = tc::smem_desc_sw128(sbase + kOffO, kHalf, 1024);
             const uint64_t dDs = tc::smem_desc_sw128(sbase + kOffDs, 16, 1024);
-            uint32_t ring = 0, items = 0, cntB = 0;
-            auto issue_st = [&](uint32_t slot) {  // S^T(j) = k^ q^(j)^T
-                const uint64_t bq = dRing + ((slot * kPair) >> 4);
+            uint32_t blk = 0, items = 0, cnt = 0;
+            // dP^T(b) = v dO(b)^T into [128, 256)
+            auto issue_dpt = [&](uint32_t b) -> bool {
+                if (!tc::mbar_wait(bar(bOFull + (b & 1)), (b >> 1) & 1, abort_flag)) return false;
+                tc::fence_after_sync();
+                const uint64_t bo = dOr + (((b & 1) * kTile) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t koff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+                    tc::mma_ss(tmem + 128, dV + koff, bo + koff, idSbf, kk > 0);
+                }
+                return true;
+            };
+            // S^T(b) = k^ q^(b)^T into [0, 128)
+            auto issue_st = [&](uint32_t b) -> bool {
+                if (!tc::mbar_wait(bar(bQFull + (b & 1)), (b >> 1) & 1, abort_flag)) return false;
+                tc::fence_after_sync();
+                const uint64_t bq = dQr + (((b & 1) * kTile) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t koff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
                     tc::mma_ss(tmem + 0, dK + koff, bq + koff, idS16, kk > 0);
                 }
-            };
-            auto issue_dpt = [&](uint32_t slot) {  // dP^T(j) = v dO(j)^T
-                const uint64_t bdo = dRing + ((slot * kPair + kTile) >> 4);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t koff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
-                    tc::mma_ss(tmem + 128, dV + koff, bdo + koff, idSbf, kk > 0);
-                }
+                return true;
             };
             for (int i = blockIdx.x; !failed; i += gridDim.x) {
                 BwdItem it;
@@ -328,50 +293,43 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 if (!tc::mbar_wait(bar(bFixedFull), items & 1, abort_flag)) { fail(); break; }
                 ++items;
                 const int nq = (it.L + 127) / 128;
-                const uint32_t ring0 = ring;
-                {
-                    const uint32_t slot = ring & 1;
-                    if (!tc::mbar_wait(bar(bRingFull + slot), (ring >> 1) & 1, abort_flag)) { fail(); break; }
-                    ++ring;
-                    tc::fence_after_sync();
-                    issue_dpt(slot);
-                    issue_st(slot);
-                    tc::mma_commit(bar(bSFull));
-                }
+                const uint32_t b0 = blk;
+                if (!issue_dpt(b0) || !issue_st(b0)) { fail(); break; }
+                tc::mma_commit(bar(bSFull));
                 for (int qj = 0; qj < nq && !failed; ++qj) {
-                    const uint32_t slot = (ring0 + qj) & 1;
+                    const uint32_t b = b0 + qj, slot = b & 1;
                     const bool more = qj + 1 < nq;
-                    uint32_t ns = 0;
-                    // block qj's dP^T is in registers: refill that buffer with block qj+1
-                    if (!tc::mbar_wait(bar(bDpUsed), cntB & 1, abort_flag)) { fail(); break; }
-                    if (more) {
-                        ns = ring & 1;
-                        if (!tc::mbar_wait(bar(bRingFull + ns), (ring >> 1) & 1, abort_flag)) { fail(); break; }
-                        ++ring;
-                        tc::fence_after_sync();
-                        issue_dpt(ns);
-                    }
-                    if (!tc::mbar_wait(bar(bPFull), cntB & 1, abort_flag)) { fail(); break; }
-                    ++cntB;
+                    // block b's dP^T is in registers: refill that buffer with block b+1
+                    if (!tc::mbar_wait(bar(bDpUsed), cnt & 1, abort_flag)) { fail(); break; }
+                    if (more && !issue_dpt(b + 1)) { fail(); break; }
+                    // dV += P^T(b) dO(b), P^T from TMEM
+                    if (!tc::mbar_wait(bar(bPtFull), cnt & 1, abort_flag)) { fail(); break; }
                     tc::fence_after_sync();
-                    const uint64_t bq = dRingMN + ((slot * kPair) >> 4), bdo = bq + (kTile >> 4);
-                    // dV += P^T(j) dO(j) (P^T from TMEM), dK += dS^T(j) q^(j) (dS^T from shared memory)
+                    const uint64_t bo = dOrMN + ((slot * kTile) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        tc::mma_ts(tmem + 256, tmem + a_col(kk), bdo + ((kk * 2048) >> 4), idAbf, (qj > 0) || (kk > 0));
+                        tc::mma_ts(tmem + 256, tmem + a_col4(kk), bo + ((kk * 2048) >> 4), idAbf, (qj > 0) || (kk > 0));
+                    tc::mma_commit(bar(bOEmpty + slot));
+                    // S^T(b+1) overwrites P^T(b): in-order MMAs, dV has read it
+                    if (more) {
+                        if (!issue_st(b + 1)) { fail(); break; }
+                        tc::mma_commit(bar(bSFull));
+                    }
+                    // dK += dS^T(b) q^(b), dS^T from shared memory
+                    if (!tc::mbar_wait(bar(bDsFull), cnt & 1, abort_flag)) { fail(); break; }
+                    tc::fence_after_sync();
+                    const uint64_t bq = dQrMN + ((slot * kTile) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint32_t aoff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
                         tc::mma_ss(tmem + 384, dDs + aoff, bq + ((kk * 2048) >> 4), idA16, (qj > 0) || (kk > 0));
                     }
                     tc::mma_commit(bar(bDsFree));
-                    tc::mma_commit(bar(bRingEmpty + slot));
-                    if (more) {
-                        issue_st(ns);
-                        tc::mma_commit(bar(bSFull));
-                    }
+                    tc::mma_commit(bar(bQEmpty + slot));
+                    ++cnt;
                 }
                 if (failed) break;
+                blk = b0 + nq;
                 tc::mma_commit(bar(bAccDone));
             }
             tc::mma_commit(bar(bDone));
@@ -380,28 +338,28 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------- softmax gradient + epilogue
-        const int wg = (warp - 4) >> 2;                 // query half of the score tile
-        const int w8 = warp - 4;
+        const int wg = (warp - 4) >> 2;                 // query quarter of the score tile
         const int t = tid - 128 * (1 + wg);             // key row == TMEM lane
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-        const uint32_t tS = tmem + lane_base + 64 * wg, tDP = tmem + lane_base + 128 + 64 * wg;
+        const uint32_t tS = tmem + lane_base + 32 * wg, tDP = tmem + lane_base + 128 + 32 * wg;
         const float c = p.scale * kLog2e;
-        float* lsebuf = reinterpret_cast<float*>(smem + kOffLse) + wg * 256;  // [2 buf][lse2 64 | delta 64]
-        float* red = reinterpret_cast<float*>(smem + kOffDs);                  // epilogue only
-        uint8_t* dsrow = smem + kOffDs + wg * kHalf + t * 128;
+        float* lsebuf = reinterpret_cast<float*>(smem + kOffLse) + wg * 128;  // [2 buf][lse2 32 | delta 32]
+        // this warpgroup's 32 query columns are 16-byte chunks 4 (wg & 1) .. +3 of half wg >> 1
+        uint8_t* dsrow = smem + kOffDs + (wg >> 1) * kHalf + t * 128;
+        const int chunk0 = 4 * (wg & 1);
         uint32_t cntS = 0, items = 0, nds = 0;
         for (int i = blockIdx.x; !failed; i += gridDim.x) {
             BwdItem it;
             if (!bwd_item(p, i, it)) break;
             const int nq = (it.L + 127) / 128;
             const bool key_ok = 128 * it.tile + t < it.L;
-            // lse2 / Delta of this warpgroup's 64 queries of the next block, one block ahead
+            // lse2 / Delta of this warpgroup's 32 queries of the next block, one block ahead
             float nl = 0.f, nd = 0.f;
             auto fetch = [&](int qj) {
-                const int q = 128 * qj + 64 * wg + t;
+                const int q = 128 * qj + 32 * wg + t;
                 nl = 0.f;
                 nd = 0.f;
-                if (t < 64 && qj < nq && q < it.L) {
+                if (t < 32 && qj < nq && q < it.L) {
                     const size_t idx = (size_t)it.h * p.seq.S + it.seg0 + q;
                     nl = -p.lse[idx] * kLog2e;  // staged negated: the loop adds them
                     nd = -p.delta[idx];
@@ -409,10 +367,10 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             };
             fetch(0);
             for (int qj = 0; qj < nq; ++qj) {
-                float* lb = lsebuf + (qj & 1) * 128;
-                if (t < 64) {
+                float* lb = lsebuf + (qj & 1) * 64;
+                if (t < 32) {
                     lb[t] = nl;
-                    lb[64 + t] = nd;
+                    lb[32 + t] = nd;
                 }
                 fetch(qj + 1);
                 named_bar(1 + wg, 128);
@@ -422,15 +380,44 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 if (!ok) { fail(); break; }
                 ++cntS;
                 tc::fence_after_sync();
-                uint32_t dr[2][32];
-                tc::tmem_ld32(tDP, dr[0]);
-                tc::tmem_ld32(tDP + 32, dr[1]);
-                tc::tmem_wait_ld_dep(dr[0]);
-                tc::tmem_wait_ld_dep(dr[1]);
+                uint32_t dr[32], sr[32];
+                tc::tmem_ld32(tDP, dr);
+                tc::tmem_ld32(tS, sr);
+                tc::tmem_wait_ld_dep(dr);
+                tc::tmem_wait_ld_dep(sr);
                 tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(bar(bDpUsed));
-                // the dS^T tile is rewritten only after the previous block's dK MMAs read it
+                const int validq = it.L - 128 * qj - 32 * wg;  // columns of this quarter inside the sample
+                const uint64_t* lb2 = reinterpret_cast<const uint64_t*>(lb);  // (-lse2, -lse2') pairs, then -Delta pairs
+                const uint64_t c2 = f2pack(c, c);
+                // ---- phase 1: P = 2^(s c - lse2_col), kept in FP32 (sr), P^T as bf16 into TMEM
+                {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        float a0, a1, p0, p1;
+                        f2unpack(f2fma(f2pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, lb2[e >> 1]),
+                                 a0, a1);
+                        p0 = ex2(a0);
+                        p1 = ex2(a1);
+                        if (validq < 32) {  // tail block: columns past the sample end are exact zeros
+                            p0 = e < validq ? p0 : 0.f;
+                            p1 = e + 1 < validq ? p1 : 0.f;
+                        }
+                        sr[e] = __float_as_uint(p0);
+                        sr[e + 1] = __float_as_uint(p1);
+                        pk[e >> 1] = pack_bf16(p0, p1);
+                    }
+                    // P^T over the S^T columns [32wg, 32wg + 16) (already read)
+                    tc::tmem_st16(tS, pk);
+                }
+                tc::tmem_wait_st();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(bar(bPtFull));
+                // ---- phase 2: dS = P (dP - Delta_col) as fp16 into the dS^T tile, rewritten
+                // only after the previous block's dK MMAs read it
                 if (nds > 0) {
                     bool fr = true;
                     if (lane == 0) fr = tc::mbar_wait(bar(bDsFree), (nds - 1) & 1, abort_flag);
@@ -438,103 +425,72 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                     if (!fr) { fail(); break; }
                 }
                 ++nds;
-                const int validq = it.L - 128 * qj - 64 * wg;  // columns of this half inside the sample
-                const uint64_t* lb2 = reinterpret_cast<const uint64_t*>(lb);  // (-lse2, -lse2') pairs, then -Delta pairs
-                const uint64_t c2 = f2pack(c, c);
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t sr[32];
-                    tc::tmem_ld32(tS + 32 * hh, sr);
-                    tc::tmem_wait_ld_dep(sr);
-                    uint32_t pk[16];
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    uint32_t dk[4];
 #pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8) {
-                        uint32_t dk[4];
-#pragma unroll
-                        for (int e = 0; e < 8; e += 2) {
-                            const int k0 = 8 * c8 + e, col = 32 * hh + k0;
-                            float a0, a1, p0, p1, d0, d1;
-                            // P = 2^(s c - lse2_col); dS = P (dP - Delta_col), two columns per instruction
-                            f2unpack(f2fma(f2pack(__uint_as_float(sr[k0]), __uint_as_float(sr[k0 + 1])), c2, lb2[col >> 1]),
-                                     a0, a1);
-                            p0 = ex2(a0);
-                            p1 = ex2(a1);
-                            f2unpack(f2mul(f2pack(p0, p1),
-                                           f2add(f2pack(__uint_as_float(dr[hh][k0]), __uint_as_float(dr[hh][k0 + 1])),
-                                                 lb2[(64 + col) >> 1])),
-                                     d0, d1);
-                            if (validq < 64) {  // tail block: columns past the sample end are exact zeros
-                                p0 = col < validq ? p0 : 0.f;
-                                p1 = col + 1 < validq ? p1 : 0.f;
-                                d0 = col < validq ? d0 : 0.f;
-                                d1 = col + 1 < validq ? d1 : 0.f;
-                            }
-                            pk[k0 >> 1] = pack_bf16(p0, p1);
-                            dk[e >> 1] = pack_f16(d0, d1);
+                    for (int e = 0; e < 8; e += 2) {
+                        const int col = 8 * c8 + e;
+                        float d0, d1;
+                        f2unpack(f2mul(f2pack(__uint_as_float(sr[col]), __uint_as_float(sr[col + 1])),
+                                       f2add(f2pack(__uint_as_float(dr[col]), __uint_as_float(dr[col + 1])),
+                                             lb2[(32 + col) >> 1])),
+                                 d0, d1);
+                        if (validq < 32) {
+                            d0 = col < validq ? d0 : 0.f;
+                            d1 = col + 1 < validq ? d1 : 0.f;
                         }
-                        const int chunk = 4 * hh + c8;
-                        *reinterpret_cast<uint4*>(dsrow + ((chunk ^ (t & 7)) << 4)) =
-                            make_uint4(dk[0], dk[1], dk[2], dk[3]);
+                        dk[e >> 1] = pack_f16(d0, d1);
                     }
-                    // P^T over the S^T columns [64wg, 64wg + 32): half 0 writes [0, 16), half 1
-                    // [16, 32) while it reads [32, 64)
-                    tc::tmem_st16(tS + 16 * hh, pk);
+                    *reinterpret_cast<uint4*>(dsrow + (((chunk0 + c8) ^ (t & 7)) << 4)) =
+                        make_uint4(dk[0], dk[1], dk[2], dk[3]);
                 }
-                tc::tmem_wait_st();
                 tc::fence_proxy_async();
-                tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(bar(bPFull));
+                if (lane == 0) tc::mbar_arrive(bar(bDsFull));
             }
             if (failed) break;
-            // ---- epilogue: dV rows (warpgroup 0), staged dK rows (warpgroup 1), then rows
+            // ---- drain: each warpgroup its 32 channels of dV (bf16 output rows) and of
+            // scale * dk^ (FP32 rows for the RoPE^-1 / RMSNorm backward)
             bool ok = true;
             if (lane == 0) ok = tc::mbar_wait(bar(bAccDone), items & 1, abort_flag);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) { fail(); break; }
             ++items;
             tc::fence_after_sync();
-            const int krow = it.row0 + t;
-            if (wg == 0) {
-                __nv_bfloat16* dst = p.dv + ((size_t)krow * p.H + it.h) * kD;
+            const size_t row_off = ((size_t)(it.row0 + t) * p.H + it.h) * kD + 32 * wg;
+            {
+                uint32_t r[32];
+                tc::tmem_ld32(tmem + lane_base + 256 + 32 * wg, r);
+                tc::tmem_wait_ld_dep(r);
+                if (key_ok) {
+                    __nv_bfloat16* dst = p.dv + row_off;
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    uint32_t r[32];
-                    tc::tmem_ld32(tmem + lane_base + 256 + 32 * q4, r);
-                    tc::tmem_wait_ld_dep(r);
-                    if (key_ok) {
-#pragma unroll
-                        for (int e = 0; e < 32; e += 8) {
-                            uint4 u;
-                            u.x = pack_bf16(__uint_as_float(r[e]), __uint_as_float(r[e + 1]));
-                            u.y = pack_bf16(__uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
-                            u.z = pack_bf16(__uint_as_float(r[e + 4]), __uint_as_float(r[e + 5]));
-                            u.w = pack_bf16(__uint_as_float(r[e + 6]), __uint_as_float(r[e + 7]));
-                            *reinterpret_cast<uint4*>(dst + 32 * q4 + e) = u;
-                        }
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    uint32_t r[32];
-                    tc::tmem_ld32(tmem + lane_base + 384 + 32 * q4, r);
-                    tc::tmem_wait_ld_dep(r);
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        const float4 v4 = make_float4(__uint_as_float(r[e]) * p.scale, __uint_as_float(r[e + 1]) * p.scale,
-                                                      __uint_as_float(r[e + 2]) * p.scale,
-                                                      __uint_as_float(r[e + 3]) * p.scale);
-                        *reinterpret_cast<float4*>(smem + kOffFixed + stage_off(t, 8 * q4 + e / 4)) = v4;
+                    for (int e = 0; e < 32; e += 8) {
+                        uint4 u;
+                        u.x = pack_bf16(__uint_as_float(r[e]), __uint_as_float(r[e + 1]));
+                        u.y = pack_bf16(__uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
+                        u.z = pack_bf16(__uint_as_float(r[e + 4]), __uint_as_float(r[e + 5]));
+                        u.w = pack_bf16(__uint_as_float(r[e + 6]), __uint_as_float(r[e + 7]));
+                        *reinterpret_cast<uint4*>(dst + e) = u;
                     }
                 }
             }
-            named_bar(3, 256);
-            rows_epilogue(smem + kOffFixed, red, p, it, srt, w8, lane);
-            tc::fence_before_sync();
-            tc::fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(bar(bItemFree));
+            {
+                uint32_t r[32];
+                tc::tmem_ld32(tmem + lane_base + 384 + 32 * wg, r);
+                tc::tmem_wait_ld_dep(r);
+                if (key_ok) {
+                    float* dst = p.dyhat + row_off;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4*>(dst + e) =
+                            make_float4(__uint_as_float(r[e]) * p.scale, __uint_as_float(r[e + 1]) * p.scale,
+                                        __uint_as_float(r[e + 2]) * p.scale, __uint_as_float(r[e + 3]) * p.scale);
+                }
+            }
+            // the next item's first dV/dK products overwrite the accumulators only after
+            // this warpgroup's P^T / dS^T of its first block, which follow in program order
         }
     }
 
@@ -562,80 +518,22 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
 // a 3-slot ring (held until dQ(j)), v tiles through a 2-slot ring (released
 // as soon as dP(j) completed), so the next tiles load while a block is used.
 namespace dqt {
-constexpr int kOffFixed = 0;                       // q^ + dO tiles (also the epilogue stage)
+constexpr int kOffFixed = 0;                       // q^ + dO tiles
 constexpr int kKSlots = 3, kVSlots = 2;
 constexpr int kOffK = bwdt::kPair;                 // k^ ring
 constexpr int kOffV = kOffK + kKSlots * bwdt::kTile;  // v ring
-constexpr int kOffRed = kOffV + kVSlots * bwdt::kTile;  // [8 warps][64] floats, two passes
-constexpr int kOffRope = kOffRed + 8 * 64 * 4;
-constexpr int kOffBar = kOffRope + 640;
+constexpr int kOffBar = kOffV + kVSlots * bwdt::kTile;
 constexpr int kSmem = kOffBar + 256;               // the dynamic shared memory base is 1024-aligned (checked)
-enum { bFixedFull = 0, bItemFree, bKFull, bKEmpty = bKFull + kKSlots, bVFull = bKEmpty + kKSlots,
+enum { bFixedFull = 0, bKFull, bKEmpty = bKFull + kKSlots, bVFull = bKEmpty + kKSlots,
        bVEmpty = bVFull + kVSlots, bSFull = bVEmpty + kVSlots, bSUsed, bPFull, bDsFree, bAccDone, bTail, bDone,
        bCount };
 constexpr uint32_t cDs = 384;
 }  // namespace dqt
 
-// Row epilogue of the dq kernel: as rows_epilogue, with the tile's weight
-// partial reduced across the 8 warps in two passes of 64 channels through a
-// 2 KB buffer (same fixed order).
-__device__ __forceinline__ void rows_epilogue_2pass(const uint8_t* stage, float* red, const BwdTcParams& p,
-                                                    const BwdItem& it, const RopeTable& srt, int w8, int lane) {
-    const LaneRope lr = lane_rope(srt, lane);
-    float wl[4], acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) wl[e] = p.w[4 * lane + e];
-    const int nvalid = min(128, it.L - 128 * it.tile);
-    bool nonfinite = false;
-    for (int r0 = w8; r0 < nvalid; r0 += 32) {
-        float dy[4][4], xr[4][4];
-        int pos[4][3];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int r = min(r0 + 8 * u, nvalid - 1);
-            const int row = it.row0 + r;
-            const float4 s4 = *reinterpret_cast<const float4*>(stage + stage_off(r, lane));
-            dy[u][0] = s4.x; dy[u][1] = s4.y; dy[u][2] = s4.z; dy[u][3] = s4.w;
-            load_row4(p.x + ((size_t)row * p.H + it.h) * kD + 4 * lane, xr[u]);
-            pos[u][0] = p.seq.pos_t[row];
-            pos[u][1] = p.seq.pos_h[row];
-            pos[u][2] = p.seq.pos_w[row];
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int r = r0 + 8 * u;
-            if (r >= nvalid) break;
-            const int row = it.row0 + r;
-            float d[4];
-            const RowAngles a = row_angles(lr, pos[u][0], pos[u][1], pos[u][2]);
-            row_norm_rope_bwd(dy[u], xr[u], wl, a, lr, p.eps, d, acc);
-            nonfinite |= !(isfinite(d[0]) && isfinite(d[1]) && isfinite(d[2]) && isfinite(d[3]));
-            store_row4(p.dx + ((size_t)row * p.H + it.h) * kD + 4 * lane, d);
-        }
-    }
-    if (nonfinite) atomicOr(p.plan.err, kErrRange);
-    const int t = w8 * 32 + lane;
-#pragma unroll
-    for (int pass = 0; pass < 2; ++pass) {
-        if ((lane >> 4) == pass) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) red[w8 * 64 + 4 * (lane & 15) + e] = acc[e];
-        }
-        named_bar(3, 256);
-        if (t < 64) {
-            float s = 0.f;
-#pragma unroll
-            for (int wi = 0; wi < 8; ++wi) s += red[wi * 64 + t];
-            p.dw_part[((size_t)it.tile_global * p.H + it.h) * kD + 64 * pass + t] = s;
-        }
-        named_bar(3, 256);
-    }
-}
-
 __global__ void __launch_bounds__(bwdt::kThreads, 1)
 dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
              const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
-             const __grid_constant__ RopeTable rt, const BwdTcParams p) {
+             const BwdTcParams p) {
     using namespace dqt;
     using bwdt::kHalf;
     using bwdt::kLog2e;
@@ -656,7 +554,6 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 
     if (tid == 0) {
         tc::mbar_init(bar(bFixedFull), 1);
-        tc::mbar_init(bar(bItemFree), 8);
         for (int i = 0; i < kKSlots; ++i) {
             tc::mbar_init(bar(bKFull + i), 1);
             tc::mbar_init(bar(bKEmpty + i), 1);
@@ -680,8 +577,6 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         tc::tmem_relinquish();
         tc::fence_before_sync();
     }
-    RopeTable& srt = *reinterpret_cast<RopeTable*>(smem + kOffRope);
-    rope_to_smem(rt, srt, tid, kThreads);
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
@@ -705,7 +600,8 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
             if (!bwd_item(p, i, it)) break;
             const int x0 = it.h * 128;
             if (lane == 0) {
-                if (items > 0 && !tc::mbar_wait(bar(bItemFree), (items - 1) & 1, abort_flag)) fail();
+                // the fixed tiles are reloaded once the previous item's last MMA completed
+                if (items > 0 && !tc::mbar_wait(bar(bAccDone), (items - 1) & 1, abort_flag)) fail();
                 if (!failed) {
                     tc::fence_proxy_async();
                     tc::mbar_expect_tx(bar(bFixedFull), kPair);
@@ -828,13 +724,11 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     } else if (warp >= 4) {
         // ------------------------------------- softmax gradient + epilogue
         const int wg = (warp - 4) >> 2;                 // key half of the score tile
-        const int w8 = warp - 4;
         const int t = tid - 128 * (1 + wg);             // query row of the tile
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         const uint32_t tS = tmem + lane_base + 64 * wg, tDP = tmem + lane_base + 128 + 64 * wg;
         const uint32_t tDs = tmem + lane_base + cDs + 32 * wg;
         const float c = p.scale * kLog2e;
-        float* red = reinterpret_cast<float*>(smem + kOffRed);
         uint32_t cntS = 0, items = 0, nds = 0;
         for (int i = blockIdx.x; !failed; i += gridDim.x) {
             BwdItem it;
@@ -902,7 +796,7 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                 if (lane == 0) tc::mbar_arrive(bar(bPFull));
             }
             if (failed) break;
-            // ---- epilogue: stage scale * dq^ (each warpgroup its 64 channels), then rows
+            // ---- drain: scale * dq^ as FP32 rows, each warpgroup its 64 channels
             bool ok = true;
             if (lane == 0) ok = tc::mbar_wait(bar(bAccDone), items & 1, abort_flag);
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -914,20 +808,15 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                 uint32_t r[32];
                 tc::tmem_ld32(tmem + lane_base + 256 + 64 * wg + 32 * q2, r);
                 tc::tmem_wait_ld_dep(r);
+                if (row_ok) {
+                    float* dst = p.dyhat + ((size_t)(it.row0 + t) * p.H + it.h) * kD + 64 * wg + 32 * q2;
 #pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    const float4 v4 = make_float4(__uint_as_float(r[e]) * p.scale, __uint_as_float(r[e + 1]) * p.scale,
-                                                  __uint_as_float(r[e + 2]) * p.scale,
-                                                  __uint_as_float(r[e + 3]) * p.scale);
-                    *reinterpret_cast<float4*>(smem + kOffFixed + stage_off(t, 16 * wg + 8 * q2 + e / 4)) = v4;
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4*>(dst + e) =
+                            make_float4(__uint_as_float(r[e]) * p.scale, __uint_as_float(r[e + 1]) * p.scale,
+                                        __uint_as_float(r[e + 2]) * p.scale, __uint_as_float(r[e + 3]) * p.scale);
                 }
             }
-            named_bar(3, 256);
-            rows_epilogue_2pass(smem + kOffFixed, red, p, it, srt, w8, lane);
-            tc::fence_before_sync();
-            tc::fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(bar(bItemFree));
         }
     }
 
@@ -958,6 +847,83 @@ __global__ void __launch_bounds__(256) delta_kernel(const __nv_bfloat16* __restr
     float acc = o[0] * d[0] + o[1] * d[1] + o[2] * d[2] + o[3] * d[3];
     acc = warp_sum(acc);
     if (lane == 0) delta[(long)(row % H) * S + row / H] = acc;
+}
+
+// ------------------------------------------- RoPE^-1 + RMSNorm backward rows
+
+struct RowsParams {
+    Seq seq;
+    Plan plan;
+    int H;
+    float eps;
+    const float* dyhat[2];         // scale * dq^, scale * dk^: FP32 [S, H, 128]
+    const __nv_bfloat16* x[2];     // raw q, k
+    const float* w[2];             // q_norm_w, k_norm_w
+    __nv_bfloat16* dx[2];          // dq, dk
+    float* dw_part[2];             // [tiles128, H, 128]
+};
+
+// One CTA per (128-token tile of a sample, head) and per q / k (blockIdx.y):
+// dx = RMSNorm-backward(RoPE^-1(dy)) per row (one warp per row, rows w, w + 8,
+// ... with four rows' loads in flight per warp), and the tile's norm-weight
+// partial sum_rows g * n, reduced rows-by-warp then warps in a fixed order.
+__global__ void __launch_bounds__(256)
+rows_bwd_kernel(const __grid_constant__ RopeTable rt, const RowsParams p) {
+    __shared__ RopeTable srt;
+    __shared__ float red[8 * kD];
+    const int which = blockIdx.y;
+    const int tile = blockIdx.x / p.H, h = blockIdx.x % p.H;
+    const int w8 = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    rope_to_smem(rt, srt, threadIdx.x, 256);
+    __syncthreads();
+    int sample, row0, row_end, local;
+    if (!plan_tile(p.plan.cum128, p.plan.order, p.seq.seg, p.seq.n, 128, tile, sample, row0, row_end, local)) return;
+    const float* dyhat = p.dyhat[which];
+    const __nv_bfloat16* x = p.x[which];
+    __nv_bfloat16* dx = p.dx[which];
+    const LaneRope lr = lane_rope(srt, lane);
+    float wl[4], acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) wl[e] = p.w[which][4 * lane + e];
+    const int nvalid = min(128, row_end - row0);
+    bool nonfinite = false;
+    for (int r0 = w8; r0 < nvalid; r0 += 32) {
+        float dy[4][4], xr[4][4];
+        int pos[4][3];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int row = row0 + min(r0 + 8 * u, nvalid - 1);
+            const size_t off = ((size_t)row * p.H + h) * kD + 4 * lane;
+            const float4 d4 = *reinterpret_cast<const float4*>(dyhat + off);
+            dy[u][0] = d4.x; dy[u][1] = d4.y; dy[u][2] = d4.z; dy[u][3] = d4.w;
+            load_row4(x + off, xr[u]);
+            pos[u][0] = p.seq.pos_t[row];
+            pos[u][1] = p.seq.pos_h[row];
+            pos[u][2] = p.seq.pos_w[row];
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int r = r0 + 8 * u;
+            if (r >= nvalid) break;
+            float d[4];
+            const RowAngles a = row_angles(lr, pos[u][0], pos[u][1], pos[u][2]);
+            row_norm_rope_bwd(dy[u], xr[u], wl, a, lr, p.eps, d, acc);
+            nonfinite |= !(isfinite(d[0]) && isfinite(d[1]) && isfinite(d[2]) && isfinite(d[3]));
+            store_row4(dx + ((size_t)(row0 + r) * p.H + h) * kD + 4 * lane, d);
+        }
+    }
+    // a non-finite gradient row from finite inputs means an fp16 operand (dS) overflowed
+    if (nonfinite) atomicOr(p.plan.err, kErrRange);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) red[w8 * kD + 4 * lane + e] = acc[e];
+    __syncthreads();
+    const int c = threadIdx.x;
+    if (c < kD) {
+        float sum = 0.f;
+#pragma unroll
+        for (int wi = 0; wi < 8; ++wi) sum += red[wi * kD + c];
+        p.dw_part[which][((size_t)tile * p.H + h) * kD + c] = sum;
+    }
 }
 
 // -------------------------------------------------------- weight gradients
@@ -1051,37 +1017,54 @@ static BwdTcParams bwd_params(const Problem& p, const Workspace& ws, const float
     b.plan = ws.plan;
     b.H = p.H;
     b.scale = p.scale;
-    b.eps = p.eps;
     b.lse = lse;
     b.delta = ws.delta;
     return b;
 }
 
-cudaError_t launch_bwd_dkdv(const Problem& p, const Workspace& ws, const RopeTable* rope, const float* lse,
+cudaError_t launch_bwd_dkdv(const Problem& p, const Workspace& ws, const float* lse,
                             const __nv_bfloat16* dout, __nv_bfloat16* dk, __nv_bfloat16* dv, cudaStream_t st) {
     BwdMaps m;
     if (!encode_all(m, p, ws, dout, 128, 128)) return cudaErrorInvalidValue;
     BwdTcParams b = bwd_params(p, ws, lse);
-    b.x = p.k;
-    b.w = p.wk;
-    b.dx = dk;
     b.dv = dv;
-    b.dw_part = ws.dwk_part;
-    dkdv_tc_kernel<<<g_sms_b, bwdt::kThreads, kvt::kSmem, st>>>(m.q, m.k, m.v, m.dout, *rope, b);
+    b.dyhat = ws.dkhat32;
+    dkdv_tc_kernel<<<g_sms_b, kvt::kThreads, kvt::kSmem, st>>>(m.q, m.k, m.v, m.dout, b);
     return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_dq(const Problem& p, const Workspace& ws, const RopeTable* rope, const float* lse,
+cudaError_t launch_bwd_dq(const Problem& p, const Workspace& ws, const float* lse,
                           const __nv_bfloat16* dout, __nv_bfloat16* dq, cudaStream_t st) {
     BwdMaps m;
     if (!encode_all(m, p, ws, dout, 128, 128)) return cudaErrorInvalidValue;
     BwdTcParams b = bwd_params(p, ws, lse);
-    b.x = p.q;
-    b.w = p.wq;
-    b.dx = dq;
     b.dv = nullptr;
-    b.dw_part = ws.dwq_part;
-    dq_tc_kernel<<<g_sms_b, bwdt::kThreads, dqt::kSmem, st>>>(m.q, m.k, m.v, m.dout, *rope, b);
+    b.dyhat = ws.dqhat32;
+    dq_tc_kernel<<<g_sms_b, bwdt::kThreads, dqt::kSmem, st>>>(m.q, m.k, m.v, m.dout, b);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_rows(const Problem& p, const Workspace& ws, const RopeTable* rope, __nv_bfloat16* dq,
+                            __nv_bfloat16* dk, cudaStream_t st) {
+    RowsParams r;
+    r.seq = p.seq;
+    r.plan = ws.plan;
+    r.H = p.H;
+    r.eps = p.eps;
+    r.dyhat[0] = ws.dqhat32;
+    r.dyhat[1] = ws.dkhat32;
+    r.x[0] = p.q;
+    r.x[1] = p.k;
+    r.w[0] = p.wq;
+    r.w[1] = p.wk;
+    r.dx[0] = dq;
+    r.dx[1] = dk;
+    r.dw_part[0] = ws.dwq_part;
+    r.dw_part[1] = ws.dwk_part;
+    // an upper bound of the 128-token tiles (every sample adds at most one partial
+    // tile); CTAs past the plan's last tile return at once
+    const long tiles = (long)(p.seq.S + 127) / 128 + p.seq.n;
+    rows_bwd_kernel<<<dim3((unsigned)(tiles * p.H), 2), 256, 0, st>>>(*rope, r);
     return cudaGetLastError();
 }
 

@@ -138,6 +138,8 @@ struct Workspace {
     __half* qhat;            // [max_tokens, H, 128] rotated, normalised q (fp16)
     __half* khat;            // [max_tokens, H, 128] rotated, normalised k (fp16)
     float* delta;            // [H, max_tokens]
+    float* dqhat32;          // [max_tokens, H, 128] scale * dq^ (FP32), backward only
+    float* dkhat32;          // [max_tokens, H, 128] scale * dk^ (FP32), backward only
     float* dwq_part;         // [max_tiles64, H, 128]
     float* dwk_part;         // [max_tiles64, H, 128]
     float* dwq_sample;       // [max_samples, 128]
@@ -158,7 +160,8 @@ struct Problem {
 };
 
 // Stages of one call, in launch order (timed separately when stage timing is on).
-enum Stage { kStagePlan = 0, kStagePrologue, kStageFwd, kStageDelta, kStageDkdv, kStageDq, kStageDw, kStages };
+// Values match the h3attn_stage enum of the C ABI.
+enum Stage { kStagePlan = 0, kStagePrologue, kStageFwd, kStageDelta, kStageDkdv, kStageDq, kStageDw, kStageRows, kStages };
 
 cudaError_t init_fwd_tc();
 cudaError_t init_bwd_attributes();
@@ -167,10 +170,12 @@ cudaError_t launch_prologue(const Problem& p, const Workspace& ws, const RopeTab
 cudaError_t launch_fwd(const Problem& p, const Workspace& ws, __nv_bfloat16* out, float* lse, cudaStream_t st);
 cudaError_t launch_bwd_delta(const Problem& p, const Workspace& ws, const __nv_bfloat16* out,
                              const __nv_bfloat16* dout, cudaStream_t st);
-cudaError_t launch_bwd_dkdv(const Problem& p, const Workspace& ws, const RopeTable* rope, const float* lse,
+cudaError_t launch_bwd_dkdv(const Problem& p, const Workspace& ws, const float* lse,
                             const __nv_bfloat16* dout, __nv_bfloat16* dk, __nv_bfloat16* dv, cudaStream_t st);
-cudaError_t launch_bwd_dq(const Problem& p, const Workspace& ws, const RopeTable* rope, const float* lse,
+cudaError_t launch_bwd_dq(const Problem& p, const Workspace& ws, const float* lse,
                           const __nv_bfloat16* dout, __nv_bfloat16* dq, cudaStream_t st);
+cudaError_t launch_bwd_rows(const Problem& p, const Workspace& ws, const RopeTable* rope, __nv_bfloat16* dq,
+                            __nv_bfloat16* dk, cudaStream_t st);
 cudaError_t launch_bwd_dw(const Problem& p, const Workspace& ws, float* dwq, float* dwk, float* dwq_s,
                           float* dwk_s, cudaStream_t st);
 

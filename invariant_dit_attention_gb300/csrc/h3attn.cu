@@ -174,7 +174,8 @@ h3attn_status h3attn_create(const h3attn_config* cfg, h3attn_t* out) {
     h->max_tiles64 = (int)((T + 63) / 64 + N);
     Workspace& ws = h->ws;
     bool ok = ws_alloc(h, &ws.qhat, T * H * kD * 2) && ws_alloc(h, &ws.khat, T * H * kD * 2) &&
-              ws_alloc(h, &ws.delta, T * H * 4) &&
+              ws_alloc(h, &ws.delta, T * H * 4) && ws_alloc(h, &ws.dqhat32, T * H * kD * 4) &&
+              ws_alloc(h, &ws.dkhat32, T * H * kD * 4) &&
               ws_alloc(h, &ws.dwq_part, (size_t)h->max_tiles64 * H * kD * 4) &&
               ws_alloc(h, &ws.dwk_part, (size_t)h->max_tiles64 * H * kD * 4) &&
               ws_alloc(h, &ws.dwq_sample, N * kD * 4) && ws_alloc(h, &ws.dwk_sample, N * kD * 4) &&
@@ -250,8 +251,9 @@ h3attn_status h3attn_backward(h3attn_t h, const h3attn_bf16* q, const h3attn_bf1
     if (stage(h, kStagePlan, s, [&] { return launch_plan(p, ws, s); }) != cudaSuccess ||
         stage(h, kStagePrologue, s, [&] { return launch_prologue(p, ws, &h->rope, s); }) != cudaSuccess ||
         stage(h, kStageDelta, s, [&] { return launch_bwd_delta(p, ws, o, dO, s); }) != cudaSuccess ||
-        stage(h, kStageDkdv, s, [&] { return launch_bwd_dkdv(p, ws, &h->rope, lse, dO, gk, gv, s); }) != cudaSuccess ||
-        stage(h, kStageDq, s, [&] { return launch_bwd_dq(p, ws, &h->rope, lse, dO, gq, s); }) != cudaSuccess ||
+        stage(h, kStageDkdv, s, [&] { return launch_bwd_dkdv(p, ws, lse, dO, gk, gv, s); }) != cudaSuccess ||
+        stage(h, kStageDq, s, [&] { return launch_bwd_dq(p, ws, lse, dO, gq, s); }) != cudaSuccess ||
+        stage(h, kStageRows, s, [&] { return launch_bwd_rows(p, ws, &h->rope, gq, gk, s); }) != cudaSuccess ||
         stage(h, kStageDw, s, [&] {
             return launch_bwd_dw(p, ws, dq_norm_w, dk_norm_w, dq_norm_w_per_sample, dk_norm_w_per_sample, s);
         }) != cudaSuccess)

@@ -28,7 +28,7 @@ EXPORTS = ("h3attn_create", "h3attn_destroy", "h3attn_forward", "h3attn_backward
 STATIC_MAX_TOKEN_HEADS = 131072
 STATIC_MAX_SAMPLES = 2048
 
-STAGES = ("plan", "prologue", "fwd", "bwd_delta", "bwd_dkdv", "bwd_dq", "bwd_dw")
+STAGES = ("plan", "prologue", "fwd", "bwd_delta", "bwd_dkdv", "bwd_dq", "bwd_dw", "bwd_rows")
 
 
 class H3AttnError(RuntimeError):
