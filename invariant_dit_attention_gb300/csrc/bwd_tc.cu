@@ -33,7 +33,6 @@
 namespace h3 {
 
 namespace bwdt {
-constexpr int kThreads = 384;
 constexpr int kTile = 128 * 128 * 2;   // 32 KB
 constexpr int kHalf = 128 * 64 * 2;    // 16 KB
 constexpr int kPair = 2 * kTile;       // two tiles (q^ + dO, or k^ + v): 64 KB
@@ -100,27 +99,38 @@ __device__ __forceinline__ uint32_t a_col4(int kk) { return 32 * (kk >> 1) + 8 *
 // ------------------------------------------------------------------ dK, dV
 //
 // 128-query blocks (N = 128 MMAs run at the full rate).  TMEM: S^T [0, 128),
-// dP^T [128, 256), dV [256, 384), dK [384, 512).  The two warpgroups split each
-// block's 128 query columns (thread = key row).  The softmax gradient of a
-// block runs in two phases: P^T (bf16) first, written over the S^T columns its
-// warpgroup read (A operand of dV from TMEM), then dS^T (fp16) to a 128 x 128
-// shared-memory tile (A operand of dK).  So dV(j) and S^T(j+1) run on the
-// tensor cores while dS^T(j) is computed, and dK(j) while P^T(j+1) is; dP^T(j+1)
-// is issued as soon as both warpgroups have loaded dP^T(j).  q^ and dO stream
-// through separate 2-slot rings: a dO slot is released after dV(j), a q^ slot
-// after dK(j).
+// the block buffer B [128, 256), dV [256, 384), dK [384, 512).  Four warpgroups
+// split each block's 128 query columns (thread = key row, 32 columns each).
+// Per block b a warpgroup
+//   loads S^T(b) and computes P (FP32, registers); the S^T buffer is refilled
+//     with S^T(b+1) right away;
+//   loads dP^T(b) from B, then writes P^T(b) (bf16) over the first 16 of its
+//     32 B columns -> dV(b) = P^T(b) dO(b) reads it as the TMEM A operand;
+//   computes dS = P (dP - Delta) and writes dS^T(b) (fp16) over the other 16
+//     -> dK(b) = dS^T(b) q^(b), TMEM A operand as well;
+// and dP^T(b+1) is issued into B right behind dK(b) (in-order MMAs).  So the
+// tensor cores never wait on a whole softmax-gradient pass, and the softmax
+// warps wait on the tensor cores only for dP^T.  q^ streams through a 3-slot
+// ring (a slot is held from S^T(b), one block ahead, to dK(b)), dO through a
+// 2-slot ring (dP^T(b) to dV(b)).
 namespace kvt {
 constexpr int kThreads = 640;                       // warps 0-3: producer, MMA issuer; 4-19: four warpgroups
+constexpr int kQSlots = 3, kOSlots = 2;
 constexpr int kOffFixed = 0;                        // k^ + v tiles
-constexpr int kOffQ = bwdt::kPair;                  // q^ ring, 2 slots
-constexpr int kOffO = kOffQ + 2 * bwdt::kTile;      // dO ring, 2 slots
-constexpr int kOffDs = kOffO + 2 * bwdt::kTile;     // dS^T tile (two 64-column halves)
-constexpr int kOffLse = kOffDs + bwdt::kTile;       // [4 wg][2 buf][lse2 32 | delta 32] floats
-constexpr int kOffBar = kOffLse + 2 * 2 * 128 * 4;
+constexpr int kOffQ = bwdt::kPair;                  // q^ ring
+constexpr int kOffO = kOffQ + kQSlots * bwdt::kTile;  // dO ring
+constexpr int kOffLse = kOffO + kOSlots * bwdt::kTile;  // [4 wg][2 buf][lse2 32 | delta 32] floats
+constexpr int kOffBar = kOffLse + 4 * 2 * 64 * 4;
 constexpr int kSmem = kOffBar + 256;                // the dynamic shared memory base is 1024-aligned (checked)
-enum { bFixedFull = 0, bQFull, bQEmpty = bQFull + 2, bOFull = bQEmpty + 2, bOEmpty = bOFull + 2,
-       bSFull = bOEmpty + 2, bDpUsed, bPtFull, bDsFull, bDsFree, bAccDone, bTail, bDone, bCount };
+enum { bFixedFull = 0, bQFull, bQEmpty = bQFull + kQSlots, bOFull = bQEmpty + kQSlots, bOEmpty = bOFull + kOSlots,
+       bSFull = bOEmpty + kOSlots, bPFull, bSUsed, bPtFull, bDsFull, bAccDone, bTail, bDone, bCount };
+constexpr uint32_t cB = 128;
 }  // namespace kvt
+
+// TMEM column of the A operand for K-step kk (queries 16kk .. 16kk + 15) of P^T
+// (half = 0) or dS^T (half = 1): warpgroup kk / 2 packed its 32 queries at
+// B + 32 (kk / 2) + 16 half.
+__device__ __forceinline__ uint32_t kv_acol(int kk, int half) { return kvt::cB + 32 * (kk >> 1) + 16 * half + 8 * (kk & 1); }
 
 __global__ void __launch_bounds__(kvt::kThreads, 1)
 dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
@@ -145,17 +155,19 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
 
     if (tid == 0) {
         tc::mbar_init(bar(bFixedFull), 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kQSlots; ++i) {
             tc::mbar_init(bar(bQFull + i), 1);
             tc::mbar_init(bar(bQEmpty + i), 1);
+        }
+        for (int i = 0; i < kOSlots; ++i) {
             tc::mbar_init(bar(bOFull + i), 1);
             tc::mbar_init(bar(bOEmpty + i), 1);
         }
         tc::mbar_init(bar(bSFull), 1);
-        tc::mbar_init(bar(bDpUsed), 16);
+        tc::mbar_init(bar(bPFull), 1);
+        tc::mbar_init(bar(bSUsed), 16);
         tc::mbar_init(bar(bPtFull), 16);
         tc::mbar_init(bar(bDsFull), 16);
-        tc::mbar_init(bar(bDsFree), 1);
         tc::mbar_init(bar(bAccDone), 1);
         tc::mbar_init(bar(bTail), 1);
         tc::mbar_init(bar(bDone), 1);
@@ -181,7 +193,7 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
-        // blk counts streamed blocks; both rings have two slots: slot blk & 1, phase (blk >> 1) & 1
+        // blk counts streamed blocks: q^ slot blk % 3, dO slot blk % 2
         uint32_t blk = 0, items = 0, tails = 0;
         for (int i = blockIdx.x; !failed; i += gridDim.x) {
             BwdItem it;
@@ -204,26 +216,26 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             ++items;
             const int nq = (it.L + 127) / 128;
             for (int qj = 0; qj < nq && !failed; ++qj) {
-                const uint32_t slot = blk & 1, ph = (blk >> 1) & 1;
-                const uint32_t qdst = sbase + kOffQ + slot * kTile, odst = sbase + kOffO + slot * kTile;
+                const uint32_t qs = blk % kQSlots, os = blk % kOSlots;
+                const uint32_t qdst = sbase + kOffQ + qs * kTile, odst = sbase + kOffO + os * kTile;
                 const int y = it.seg0 + 128 * qj;
                 const int valid = it.L - 128 * qj;
                 const bool tail = valid < 128;
                 if (lane == 0) {
-                    // dO first: its slot frees earlier (after dV) and dP^T needs it first
-                    if (!tc::mbar_wait(bar(bOEmpty + slot), ph ^ 1, abort_flag)) fail();
+                    // q^ first: S^T(b) runs a block ahead of dP^T(b)
+                    if (!tc::mbar_wait(bar(bQEmpty + qs), ((blk / kQSlots) & 1) ^ 1, abort_flag)) fail();
                     if (!failed && !tail) {
-                        tc::mbar_expect_tx(bar(bOFull + slot), kTile);
+                        tc::mbar_expect_tx(bar(bQFull + qs), kTile);
                         for (int hf = 0; hf < 2; ++hf)
-                            tc::tma_load_2d(odst + hf * kHalf, &mdo, x0 + 64 * hf, y, bar(bOFull + slot));
+                            tc::tma_load_2d(qdst + hf * kHalf, &mq, x0 + 64 * hf, y, bar(bQFull + qs));
                     }
-                    if (!failed && !tc::mbar_wait(bar(bQEmpty + slot), ph ^ 1, abort_flag)) fail();
+                    if (!failed && !tc::mbar_wait(bar(bOEmpty + os), ((blk / kOSlots) & 1) ^ 1, abort_flag)) fail();
                     if (!failed) {
-                        const uint32_t b = tail ? bar(bTail) : bar(bQFull + slot);
+                        const uint32_t b = tail ? bar(bTail) : bar(bOFull + os);
                         tc::mbar_expect_tx(b, tail ? kPair : kTile);
                         for (int hf = 0; hf < 2; ++hf) {
-                            tc::tma_load_2d(qdst + hf * kHalf, &mq, x0 + 64 * hf, y, b);
-                            if (tail) tc::tma_load_2d(odst + hf * kHalf, &mdo, x0 + 64 * hf, y, b);
+                            tc::tma_load_2d(odst + hf * kHalf, &mdo, x0 + 64 * hf, y, b);
+                            if (tail) tc::tma_load_2d(qdst + hf * kHalf, &mq, x0 + 64 * hf, y, b);
                         }
                         if (tail && !tc::mbar_wait(bar(bTail), tails & 1, abort_flag)) fail();
                     }
@@ -240,8 +252,8 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                     tc::fence_proxy_async();
                     __syncwarp();
                     if (lane == 0) {
-                        tc::mbar_arrive(bar(bQFull + slot));
-                        tc::mbar_arrive(bar(bOFull + slot));
+                        tc::mbar_arrive(bar(bQFull + qs));
+                        tc::mbar_arrive(bar(bOFull + os));
                     }
                 }
                 ++blk;
@@ -261,30 +273,33 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             const uint64_t dOr = tc::smem_desc_sw128(sbase + kOffO, 16, 1024);
             const uint64_t dQrMN = tc::smem_desc_sw128(sbase + kOffQ, kHalf, 1024);
             const uint64_t dOrMN = tc::smem_desc_sw128(sbase + kOffO, kHalf, 1024);
-            const uint64_t dDs = tc::smem_desc_sw128(sbase + kOffDs, 16, 1024);
             uint32_t blk = 0, items = 0, cnt = 0;
-            // dP^T(b) = v dO(b)^T into [128, 256)
-            auto issue_dpt = [&](uint32_t b) -> bool {
-                if (!tc::mbar_wait(bar(bOFull + (b & 1)), (b >> 1) & 1, abort_flag)) return false;
-                tc::fence_after_sync();
-                const uint64_t bo = dOr + (((b & 1) * kTile) >> 4);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t koff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
-                    tc::mma_ss(tmem + 128, dV + koff, bo + koff, idSbf, kk > 0);
-                }
-                return true;
-            };
             // S^T(b) = k^ q^(b)^T into [0, 128)
             auto issue_st = [&](uint32_t b) -> bool {
-                if (!tc::mbar_wait(bar(bQFull + (b & 1)), (b >> 1) & 1, abort_flag)) return false;
+                const uint32_t qs = b % kQSlots;
+                if (!tc::mbar_wait(bar(bQFull + qs), (b / kQSlots) & 1, abort_flag)) return false;
                 tc::fence_after_sync();
-                const uint64_t bq = dQr + (((b & 1) * kTile) >> 4);
+                const uint64_t bq = dQr + ((qs * kTile) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t koff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
                     tc::mma_ss(tmem + 0, dK + koff, bq + koff, idS16, kk > 0);
                 }
+                tc::mma_commit(bar(bSFull));
+                return true;
+            };
+            // dP^T(b) = v dO(b)^T into B
+            auto issue_dpt = [&](uint32_t b) -> bool {
+                const uint32_t os = b % kOSlots;
+                if (!tc::mbar_wait(bar(bOFull + os), (b / kOSlots) & 1, abort_flag)) return false;
+                tc::fence_after_sync();
+                const uint64_t bo = dOr + ((os * kTile) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t koff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+                    tc::mma_ss(tmem + cB, dV + koff, bo + koff, idSbf, kk > 0);
+                }
+                tc::mma_commit(bar(bPFull));
                 return true;
             };
             for (int i = blockIdx.x; !failed; i += gridDim.x) {
@@ -294,38 +309,33 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 ++items;
                 const int nq = (it.L + 127) / 128;
                 const uint32_t b0 = blk;
-                if (!issue_dpt(b0) || !issue_st(b0)) { fail(); break; }
-                tc::mma_commit(bar(bSFull));
+                if (!issue_st(b0) || !issue_dpt(b0)) { fail(); break; }
                 for (int qj = 0; qj < nq && !failed; ++qj) {
-                    const uint32_t b = b0 + qj, slot = b & 1;
+                    const uint32_t b = b0 + qj;
                     const bool more = qj + 1 < nq;
-                    // block b's dP^T is in registers: refill that buffer with block b+1
-                    if (!tc::mbar_wait(bar(bDpUsed), cnt & 1, abort_flag)) { fail(); break; }
-                    if (more && !issue_dpt(b + 1)) { fail(); break; }
-                    // dV += P^T(b) dO(b), P^T from TMEM
+                    // S^T(b) is in registers: refill the S^T buffer with block b+1
+                    if (!tc::mbar_wait(bar(bSUsed), cnt & 1, abort_flag)) { fail(); break; }
+                    if (more && !issue_st(b + 1)) { fail(); break; }
+                    // dV += P^T(b) dO(b)
                     if (!tc::mbar_wait(bar(bPtFull), cnt & 1, abort_flag)) { fail(); break; }
                     tc::fence_after_sync();
-                    const uint64_t bo = dOrMN + ((slot * kTile) >> 4);
+                    const uint64_t bo = dOrMN + (((b % kOSlots) * kTile) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        tc::mma_ts(tmem + 256, tmem + a_col4(kk), bo + ((kk * 2048) >> 4), idAbf, (qj > 0) || (kk > 0));
-                    tc::mma_commit(bar(bOEmpty + slot));
-                    // S^T(b+1) overwrites P^T(b): in-order MMAs, dV has read it
-                    if (more) {
-                        if (!issue_st(b + 1)) { fail(); break; }
-                        tc::mma_commit(bar(bSFull));
-                    }
-                    // dK += dS^T(b) q^(b), dS^T from shared memory
+                        tc::mma_ts(tmem + 256, tmem + kv_acol(kk, 0), bo + ((kk * 2048) >> 4), idAbf,
+                                   (qj > 0) || (kk > 0));
+                    tc::mma_commit(bar(bOEmpty + (b % kOSlots)));
+                    // dK += dS^T(b) q^(b)
                     if (!tc::mbar_wait(bar(bDsFull), cnt & 1, abort_flag)) { fail(); break; }
                     tc::fence_after_sync();
-                    const uint64_t bq = dQrMN + ((slot * kTile) >> 4);
+                    const uint64_t bq = dQrMN + (((b % kQSlots) * kTile) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t aoff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
-                        tc::mma_ss(tmem + 384, dDs + aoff, bq + ((kk * 2048) >> 4), idA16, (qj > 0) || (kk > 0));
-                    }
-                    tc::mma_commit(bar(bDsFree));
-                    tc::mma_commit(bar(bQEmpty + slot));
+                    for (int kk = 0; kk < 8; ++kk)
+                        tc::mma_ts(tmem + 384, tmem + kv_acol(kk, 1), bq + ((kk * 2048) >> 4), idA16,
+                                   (qj > 0) || (kk > 0));
+                    tc::mma_commit(bar(bQEmpty + (b % kQSlots)));
+                    // dP^T(b+1) overwrites P^T(b) and dS^T(b): in-order MMAs, dV and dK read them
+                    if (more && !issue_dpt(b + 1)) { fail(); break; }
                     ++cnt;
                 }
                 if (failed) break;
@@ -337,17 +347,14 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         }
         __syncwarp();
     } else if (warp >= 4) {
-        // ------------------------------------- softmax gradient + epilogue
+        // ------------------------------------- softmax gradient + drain
         const int wg = (warp - 4) >> 2;                 // query quarter of the score tile
         const int t = tid - 128 * (1 + wg);             // key row == TMEM lane
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-        const uint32_t tS = tmem + lane_base + 32 * wg, tDP = tmem + lane_base + 128 + 32 * wg;
+        const uint32_t tS = tmem + lane_base + 32 * wg, tB = tmem + lane_base + cB + 32 * wg;
         const float c = p.scale * kLog2e;
         float* lsebuf = reinterpret_cast<float*>(smem + kOffLse) + wg * 128;  // [2 buf][lse2 32 | delta 32]
-        // this warpgroup's 32 query columns are 16-byte chunks 4 (wg & 1) .. +3 of half wg >> 1
-        uint8_t* dsrow = smem + kOffDs + (wg >> 1) * kHalf + t * 128;
-        const int chunk0 = 4 * (wg & 1);
-        uint32_t cntS = 0, items = 0, nds = 0;
+        uint32_t cntS = 0, items = 0;
         for (int i = blockIdx.x; !failed; i += gridDim.x) {
             BwdItem it;
             if (!bwd_item(p, i, it)) break;
@@ -374,78 +381,53 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 }
                 fetch(qj + 1);
                 named_bar(1 + wg, 128);
+                const uint64_t* lb2 = reinterpret_cast<const uint64_t*>(lb);  // (-lse2, -lse2') pairs, then -Delta pairs
+                const int validq = it.L - 128 * qj - 32 * wg;  // columns of this quarter inside the sample
                 bool ok = true;
                 if (lane == 0) ok = tc::mbar_wait(bar(bSFull), cntS & 1, abort_flag);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) { fail(); break; }
-                ++cntS;
                 tc::fence_after_sync();
-                uint32_t dr[32], sr[32];
-                tc::tmem_ld32(tDP, dr);
-                tc::tmem_ld32(tS, sr);
-                tc::tmem_wait_ld_dep(dr);
-                tc::tmem_wait_ld_dep(sr);
+                uint64_t p2[16];  // S^T column pairs, then P in FP32
+                tc::tmem_ld32_pairs(tS, p2);
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(bar(bDpUsed));
-                const int validq = it.L - 128 * qj - 32 * wg;  // columns of this quarter inside the sample
-                const uint64_t* lb2 = reinterpret_cast<const uint64_t*>(lb);  // (-lse2, -lse2') pairs, then -Delta pairs
+                if (lane == 0) tc::mbar_arrive(bar(bSUsed));
+                // ---- P = 2^(s c - lse2_col)
                 const uint64_t c2 = f2pack(c, c);
-                // ---- phase 1: P = 2^(s c - lse2_col), kept in FP32 (sr), P^T as bf16 into TMEM
+#pragma unroll
+                for (int e = 0; e < 16; ++e) p2[e] = exp2_pair(p2[e], c2, lb2[e]);
+                if (validq < 32) {  // tail block: columns past the sample end are exact zeros
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) p2[e] = mask_pair(p2[e], 2 * e, validq);
+                }
+                // ---- dP^T(b) from B, then P^T (bf16) over B's first 16 columns of this quarter
+                if (lane == 0) ok = tc::mbar_wait(bar(bPFull), cntS & 1, abort_flag);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) { fail(); break; }
+                ++cntS;
+                tc::fence_after_sync();
+                uint64_t d2[16];
+                tc::tmem_ld32_pairs(tB, d2);
                 {
                     uint32_t pk[16];
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        float a0, a1, p0, p1;
-                        f2unpack(f2fma(f2pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, lb2[e >> 1]),
-                                 a0, a1);
-                        p0 = ex2(a0);
-                        p1 = ex2(a1);
-                        if (validq < 32) {  // tail block: columns past the sample end are exact zeros
-                            p0 = e < validq ? p0 : 0.f;
-                            p1 = e + 1 < validq ? p1 : 0.f;
-                        }
-                        sr[e] = __float_as_uint(p0);
-                        sr[e + 1] = __float_as_uint(p1);
-                        pk[e >> 1] = pack_bf16(p0, p1);
-                    }
-                    // P^T over the S^T columns [32wg, 32wg + 16) (already read)
-                    tc::tmem_st16(tS, pk);
+                    for (int e = 0; e < 16; ++e) pk[e] = bf16_pair(p2[e]);
+                    tc::tmem_st16(tB, pk);
                 }
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(bar(bPtFull));
-                // ---- phase 2: dS = P (dP - Delta_col) as fp16 into the dS^T tile, rewritten
-                // only after the previous block's dK MMAs read it
-                if (nds > 0) {
-                    bool fr = true;
-                    if (lane == 0) fr = tc::mbar_wait(bar(bDsFree), (nds - 1) & 1, abort_flag);
-                    fr = __shfl_sync(0xffffffffu, fr, 0);
-                    if (!fr) { fail(); break; }
-                }
-                ++nds;
+                // ---- dS = P (dP - Delta_col), fp16, over B's other 16 columns (zero where P is)
+                {
+                    uint32_t dk[16];
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    uint32_t dk[4];
-#pragma unroll
-                    for (int e = 0; e < 8; e += 2) {
-                        const int col = 8 * c8 + e;
-                        float d0, d1;
-                        f2unpack(f2mul(f2pack(__uint_as_float(sr[col]), __uint_as_float(sr[col + 1])),
-                                       f2add(f2pack(__uint_as_float(dr[col]), __uint_as_float(dr[col + 1])),
-                                             lb2[(32 + col) >> 1])),
-                                 d0, d1);
-                        if (validq < 32) {
-                            d0 = col < validq ? d0 : 0.f;
-                            d1 = col + 1 < validq ? d1 : 0.f;
-                        }
-                        dk[e >> 1] = pack_f16(d0, d1);
-                    }
-                    *reinterpret_cast<uint4*>(dsrow + (((chunk0 + c8) ^ (t & 7)) << 4)) =
-                        make_uint4(dk[0], dk[1], dk[2], dk[3]);
+                    for (int e = 0; e < 16; ++e) dk[e] = ds_f16_pair(p2[e], d2[e], lb2[16 + e]);
+                    tc::tmem_st16(tB + 16, dk);
                 }
-                tc::fence_proxy_async();
+                tc::tmem_wait_st();
+                tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(bar(bDsFull));
             }
@@ -510,14 +492,15 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
 // ------------------------------------------------------------------ dQ
 //
 // 128-key blocks (N = 128 MMAs run at the full rate).  TMEM: S [0, 128),
-// dP [128, 256), dQ [256, 384), dS [384, 448).  The two warpgroups split each
-// block's 128 key columns (thread = query row).  The score buffer is refilled
+// dP [128, 256), dQ [256, 384), dS [384, 448).  Four warpgroups split each
+// block's 128 key columns (thread = query row, 32 keys each).  The score buffer is refilled
 // with block j+1 as soon as both warpgroups have loaded block j; dS (fp16) is
 // written to its own TMEM columns and read by the dQ MMAs from there, and is
 // rewritten for block j+1 only after dQ(j) completed.  k^ tiles stream through
 // a 3-slot ring (held until dQ(j)), v tiles through a 2-slot ring (released
 // as soon as dP(j) completed), so the next tiles load while a block is used.
 namespace dqt {
+constexpr int kThreads = 640;                      // warps 0-3: producer, MMA issuer; 4-19: four warpgroups
 constexpr int kOffFixed = 0;                       // q^ + dO tiles
 constexpr int kKSlots = 3, kVSlots = 2;
 constexpr int kOffK = bwdt::kPair;                 // k^ ring
@@ -530,7 +513,7 @@ enum { bFixedFull = 0, bKFull, bKEmpty = bKFull + kKSlots, bVFull = bKEmpty + kK
 constexpr uint32_t cDs = 384;
 }  // namespace dqt
 
-__global__ void __launch_bounds__(bwdt::kThreads, 1)
+__global__ void __launch_bounds__(dqt::kThreads, 1)
 dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
              const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
              const BwdTcParams p) {
@@ -538,7 +521,6 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     using bwdt::kHalf;
     using bwdt::kLog2e;
     using bwdt::kPair;
-    using bwdt::kThreads;
     using bwdt::kTile;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if (smem_u32(smem_raw) & 1023u) {  // the layout below needs a 1024-byte aligned base
@@ -563,8 +545,8 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
             tc::mbar_init(bar(bVEmpty + i), 1);
         }
         tc::mbar_init(bar(bSFull), 1);
-        tc::mbar_init(bar(bSUsed), 8);
-        tc::mbar_init(bar(bPFull), 8);
+        tc::mbar_init(bar(bSUsed), 16);
+        tc::mbar_init(bar(bPFull), 16);
         tc::mbar_init(bar(bDsFree), 1);
         tc::mbar_init(bar(bAccDone), 1);
         tc::mbar_init(bar(bTail), 1);
@@ -586,11 +568,7 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         *abort_flag = 1;
         atomicOr(p.plan.err, kErrTimeout);
     };
-    if (warp < 4) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 152;");
-    } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 176;");
-    }
+    // 640 threads x 96 registers for every role (no setmaxnreg split)
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -722,12 +700,12 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         }
         __syncwarp();
     } else if (warp >= 4) {
-        // ------------------------------------- softmax gradient + epilogue
-        const int wg = (warp - 4) >> 2;                 // key half of the score tile
+        // ------------------------------------- softmax gradient + drain
+        const int wg = (warp - 4) >> 2;                 // key quarter of the score tile
         const int t = tid - 128 * (1 + wg);             // query row of the tile
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-        const uint32_t tS = tmem + lane_base + 64 * wg, tDP = tmem + lane_base + 128 + 64 * wg;
-        const uint32_t tDs = tmem + lane_base + cDs + 32 * wg;
+        const uint32_t tS = tmem + lane_base + 32 * wg, tDP = tmem + lane_base + 128 + 32 * wg;
+        const uint32_t tDs = tmem + lane_base + cDs + 16 * wg;
         const float c = p.scale * kLog2e;
         uint32_t cntS = 0, items = 0, nds = 0;
         for (int i = blockIdx.x; !failed; i += gridDim.x) {
@@ -746,15 +724,9 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                 if (!ok) { fail(); break; }
                 ++cntS;
                 tc::fence_after_sync();
-                uint32_t sr[2][32], dr[2][32];
-                tc::tmem_ld32(tS, sr[0]);
-                tc::tmem_ld32(tS + 32, sr[1]);
-                tc::tmem_ld32(tDP, dr[0]);
-                tc::tmem_ld32(tDP + 32, dr[1]);
-                tc::tmem_wait_ld_dep(sr[0]);
-                tc::tmem_wait_ld_dep(sr[1]);
-                tc::tmem_wait_ld_dep(dr[0]);
-                tc::tmem_wait_ld_dep(dr[1]);
+                uint64_t p2[16], d2[16];  // S then P column pairs; dP column pairs
+                tc::tmem_ld32_pairs(tS, p2);
+                tc::tmem_ld32_pairs(tDP, d2);
                 tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(bar(bSUsed));
@@ -767,28 +739,19 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                     tc::fence_after_sync();
                 }
                 ++nds;
-                const int validk = it.L - 128 * kj - 64 * wg;  // keys of this half inside the sample
+                const int validk = it.L - 128 * kj - 32 * wg;  // keys of this quarter inside the sample
+                // P = 2^(s c - lse2); dS = P (dP - Delta), fp16 into TMEM
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
+                for (int e = 0; e < 16; ++e) p2[e] = exp2_pair(p2[e], c2, nl2);
+                if (validk < 32) {  // tail block: keys past the sample end give exact zeros
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) p2[e] = mask_pair(p2[e], 2 * e, validk);
+                }
+                {
                     uint32_t dk[16];
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        float a0, a1, p0, p1, d0, d1;
-                        // P = 2^(s c - lse2); dS = P (dP - Delta), two columns per instruction
-                        f2unpack(f2fma(f2pack(__uint_as_float(sr[hh][e]), __uint_as_float(sr[hh][e + 1])), c2, nl2), a0, a1);
-                        p0 = ex2(a0);
-                        p1 = ex2(a1);
-                        f2unpack(f2mul(f2pack(p0, p1),
-                                       f2add(f2pack(__uint_as_float(dr[hh][e]), __uint_as_float(dr[hh][e + 1])), nd2)),
-                                 d0, d1);
-                        if (validk < 64) {  // tail block: keys past the sample end give exact zeros
-                            const int col = 32 * hh + e;
-                            d0 = col < validk ? d0 : 0.f;
-                            d1 = col + 1 < validk ? d1 : 0.f;
-                        }
-                        dk[e >> 1] = pack_f16(d0, d1);
-                    }
-                    tc::tmem_st16(tDs + 16 * hh, dk);
+                    for (int e = 0; e < 16; ++e) dk[e] = ds_f16_pair(p2[e], d2[e], nd2);
+                    tc::tmem_st16(tDs, dk);
                 }
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
@@ -796,20 +759,19 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                 if (lane == 0) tc::mbar_arrive(bar(bPFull));
             }
             if (failed) break;
-            // ---- drain: scale * dq^ as FP32 rows, each warpgroup its 64 channels
+            // ---- drain: scale * dq^ as FP32 rows, each warpgroup its 32 channels
             bool ok = true;
             if (lane == 0) ok = tc::mbar_wait(bar(bAccDone), items & 1, abort_flag);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) { fail(); break; }
             ++items;
             tc::fence_after_sync();
-#pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
+            {
                 uint32_t r[32];
-                tc::tmem_ld32(tmem + lane_base + 256 + 64 * wg + 32 * q2, r);
+                tc::tmem_ld32(tmem + lane_base + 256 + 32 * wg, r);
                 tc::tmem_wait_ld_dep(r);
                 if (row_ok) {
-                    float* dst = p.dyhat + ((size_t)(it.row0 + t) * p.H + it.h) * kD + 64 * wg + 32 * q2;
+                    float* dst = p.dyhat + ((size_t)(it.row0 + t) * p.H + it.h) * kD + 32 * wg;
 #pragma unroll
                     for (int e = 0; e < 32; e += 4)
                         *reinterpret_cast<float4*>(dst + e) =
@@ -1040,7 +1002,7 @@ cudaError_t launch_bwd_dq(const Problem& p, const Workspace& ws, const float* ls
     BwdTcParams b = bwd_params(p, ws, lse);
     b.dv = nullptr;
     b.dyhat = ws.dqhat32;
-    dq_tc_kernel<<<g_sms_b, bwdt::kThreads, dqt::kSmem, st>>>(m.q, m.k, m.v, m.dout, b);
+    dq_tc_kernel<<<g_sms_b, dqt::kThreads, dqt::kSmem, st>>>(m.q, m.k, m.v, m.dout, b);
     return cudaGetLastError();
 }
 

@@ -100,6 +100,49 @@ __device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b) {
     return d;
 }
 
+// Column-pair steps of the softmax gradient on 64-bit register pairs (two FP32
+// values), written as single asm blocks so that the halves of a pair are plain
+// register views and no moves are needed between the packed and scalar forms.
+//   p2 = 2^(s2 * c2 + n2) per half (ex2.approx, flush-to-zero below 2^-126)
+__device__ __forceinline__ uint64_t exp2_pair(uint64_t s2, uint64_t c2, uint64_t n2) {
+    uint64_t p2;
+    asm("{\n.reg .b64 t;\n.reg .f32 a0, a1, q0, q1;\n"
+        "fma.rn.f32x2 t, %1, %2, %3;\n"
+        "mov.b64 {a0, a1}, t;\n"
+        "ex2.approx.ftz.f32 q0, a0;\n"
+        "ex2.approx.ftz.f32 q1, a1;\n"
+        "mov.b64 %0, {q0, q1};\n}"
+        : "=l"(p2) : "l"(s2), "l"(c2), "l"(n2));
+    return p2;
+}
+// bf16x2 of a pair, low half first (round to nearest even)
+__device__ __forceinline__ uint32_t bf16_pair(uint64_t p2) {
+    uint32_t r;
+    asm("{\n.reg .f32 a0, a1;\nmov.b64 {a0, a1}, %1;\ncvt.rn.bf16x2.f32 %0, a1, a0;\n}" : "=r"(r) : "l"(p2));
+    return r;
+}
+//   dS = p2 * (d2 + n2) per half, as f16x2, low half first (round to nearest even)
+__device__ __forceinline__ uint32_t ds_f16_pair(uint64_t p2, uint64_t d2, uint64_t n2) {
+    uint32_t r;
+    asm("{\n.reg .b64 t;\n.reg .f32 a0, a1;\n"
+        "add.rn.f32x2 t, %2, %3;\n"
+        "mul.rn.f32x2 t, %1, t;\n"
+        "mov.b64 {a0, a1}, t;\n"
+        "cvt.rn.f16x2.f32 %0, a1, a0;\n}"
+        : "=r"(r) : "l"(p2), "l"(d2), "l"(n2));
+    return r;
+}
+// Zeroes the halves of a pair whose column (col, col + 1) is not below `valid`.
+__device__ __forceinline__ uint64_t mask_pair(uint64_t p2, int col, int valid) {
+    float a, b;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(p2));
+    a = col < valid ? a : 0.f;
+    b = col + 1 < valid ? b : 0.f;
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
     // fixed butterfly: every lane ends with the same, order-fixed sum
     v += __shfl_xor_sync(0xffffffffu, v, 16);

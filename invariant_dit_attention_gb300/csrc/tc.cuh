@@ -35,12 +35,22 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
         : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
     return ok != 0;
 }
+// As mbar_try, but a thread whose phase is not complete yet is suspended by the
+// hardware until it completes or about `ns` nanoseconds pass, instead of
+// returning at once: waiting warps then issue (almost) no instructions.
+__device__ __forceinline__ bool mbar_try_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\nselp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok) : "r"(bar), "r"(parity), "r"(ns) : "memory");
+    return ok != 0;
+}
 // Waits for the phase of the given parity to complete; false on timeout or abort.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort) {
     if (mbar_try(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
-        if (mbar_try(bar, parity)) return true;
+        if (mbar_try_sleep(bar, parity, 20000u)) return true;
         if (*abort) return false;
         if (clock64() - t0 > kWaitBudget) return false;
     }
@@ -93,6 +103,32 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(bar) : "memory");
 }
 
+// 32 lanes x 32 columns of 32-bit, waited, as 16 column pairs (64-bit registers).
+__device__ __forceinline__ void tmem_ld32_pairs(uint32_t taddr, uint64_t (&r)[16]) {
+    asm volatile(
+        "{\n.reg .b32 a<32>;\n"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {a0,a1,a2,a3,a4,a5,a6,a7,a8,a9,a10,a11,a12,a13,a14,a15,a16,a17,a18,a19,a20,a21,a22,a23,a24,a25,a26,a27,a28,a29,a30,a31}, [%16];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        "mov.b64 %0, {a0, a1};\n"
+        "mov.b64 %1, {a2, a3};\n"
+        "mov.b64 %2, {a4, a5};\n"
+        "mov.b64 %3, {a6, a7};\n"
+        "mov.b64 %4, {a8, a9};\n"
+        "mov.b64 %5, {a10, a11};\n"
+        "mov.b64 %6, {a12, a13};\n"
+        "mov.b64 %7, {a14, a15};\n"
+        "mov.b64 %8, {a16, a17};\n"
+        "mov.b64 %9, {a18, a19};\n"
+        "mov.b64 %10, {a20, a21};\n"
+        "mov.b64 %11, {a22, a23};\n"
+        "mov.b64 %12, {a24, a25};\n"
+        "mov.b64 %13, {a26, a27};\n"
+        "mov.b64 %14, {a28, a29};\n"
+        "mov.b64 %15, {a30, a31};\n"
+        "}\n"
+        : "=l"(r[0]), "=l"(r[1]), "=l"(r[2]), "=l"(r[3]), "=l"(r[4]), "=l"(r[5]), "=l"(r[6]), "=l"(r[7]), "=l"(r[8]), "=l"(r[9]), "=l"(r[10]), "=l"(r[11]), "=l"(r[12]), "=l"(r[13]), "=l"(r[14]), "=l"(r[15])
+        : "r"(taddr) : "memory");
+}
 // 32 lanes x 32 columns of 32-bit: thread t of the warp gets lane (base + t), 32 columns.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
