@@ -78,7 +78,8 @@ typedef struct {
 /*
  * Creates a handle on the current CUDA device and allocates its workspace
  * (rotated q^/k^ buffers of max_tokens * H * 128 fp16 each, the backward's FP32
- * dq^/dk^ rows of max_tokens * H * 128 floats each, softmax row terms,
+ * dq^/dk^ rows of max_tokens * H * 128 floats each, a max_tokens * 256-float
+ * rotary cos/sin table, softmax row terms,
  * weight-gradient partials, a small per-call plan).  The workspace is bounded
  * by the config, never by the inputs.  *out receives the handle.
  * Errors: INVALID_ARG (null pointer, sizes < 1), UNSUPPORTED (head_dim,

@@ -818,12 +818,35 @@ struct RowsParams {
     Plan plan;
     int H;
     float eps;
+    const float* rope_cs;          // [S][cos 128 | sin 128] per token
     const float* dyhat[2];         // scale * dq^, scale * dk^: FP32 [S, H, 128]
     const __nv_bfloat16* x[2];     // raw q, k
     const float* w[2];             // q_norm_w, k_norm_w
     __nv_bfloat16* dx[2];          // dq, dk
     float* dw_part[2];             // [tiles128, H, 128]
 };
+
+// cos / sin of every channel's rotary angle per token, [S][cos 128 | sin 128]:
+// the same FP32 sincosf(p_axis * f_c) as row_angles, computed once per token
+// instead of once per (token, head) row; channels outside the sections get
+// (1, 0).
+__global__ void __launch_bounds__(256)
+rope_table_kernel(const __grid_constant__ RopeTable rt, Seq seq, float* __restrict__ cs) {
+    __shared__ RopeTable srt;
+    rope_to_smem(rt, srt, threadIdx.x, 256);
+    __syncthreads();
+    const long i = (long)blockIdx.x * 256 + threadIdx.x;
+    if (i >= (long)seq.S * kD) return;
+    const int token = (int)(i / kD), ch = (int)(i % kD);
+    const int axis = srt.axis[ch >> 2];
+    float c = 1.f, sn = 0.f;
+    if (axis >= 0) {
+        const int pos = axis == 0 ? seq.pos_t[token] : (axis == 1 ? seq.pos_h[token] : seq.pos_w[token]);
+        sincosf(static_cast<float>(pos) * srt.inv_freq[ch], &sn, &c);
+    }
+    cs[(size_t)token * 2 * kD + ch] = c;
+    cs[(size_t)token * 2 * kD + kD + ch] = sn;
+}
 
 // One CTA per (128-token tile of a sample, head) and per q / k (blockIdx.y):
 // dx = RMSNorm-backward(RoPE^-1(dy)) per row (one warp per row, rows w, w + 8,
@@ -851,7 +874,7 @@ rows_bwd_kernel(const __grid_constant__ RopeTable rt, const RowsParams p) {
     bool nonfinite = false;
     for (int r0 = w8; r0 < nvalid; r0 += 32) {
         float dy[4][4], xr[4][4];
-        int pos[4][3];
+        RowAngles a[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int row = row0 + min(r0 + 8 * u, nvalid - 1);
@@ -859,17 +882,17 @@ rows_bwd_kernel(const __grid_constant__ RopeTable rt, const RowsParams p) {
             const float4 d4 = *reinterpret_cast<const float4*>(dyhat + off);
             dy[u][0] = d4.x; dy[u][1] = d4.y; dy[u][2] = d4.z; dy[u][3] = d4.w;
             load_row4(x + off, xr[u]);
-            pos[u][0] = p.seq.pos_t[row];
-            pos[u][1] = p.seq.pos_h[row];
-            pos[u][2] = p.seq.pos_w[row];
+            const float4 c4 = *reinterpret_cast<const float4*>(p.rope_cs + (size_t)row * 2 * kD + 4 * lane);
+            const float4 s4 = *reinterpret_cast<const float4*>(p.rope_cs + (size_t)row * 2 * kD + kD + 4 * lane);
+            a[u].c[0] = c4.x; a[u].c[1] = c4.y; a[u].c[2] = c4.z; a[u].c[3] = c4.w;
+            a[u].s[0] = s4.x; a[u].s[1] = s4.y; a[u].s[2] = s4.z; a[u].s[3] = s4.w;
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int r = r0 + 8 * u;
             if (r >= nvalid) break;
             float d[4];
-            const RowAngles a = row_angles(lr, pos[u][0], pos[u][1], pos[u][2]);
-            row_norm_rope_bwd(dy[u], xr[u], wl, a, lr, p.eps, d, acc);
+            row_norm_rope_bwd(dy[u], xr[u], wl, a[u], lr, p.eps, d, acc);
             nonfinite |= !(isfinite(d[0]) && isfinite(d[1]) && isfinite(d[2]) && isfinite(d[3]));
             store_row4(dx + ((size_t)(row0 + r) * p.H + h) * kD + 4 * lane, d);
         }
@@ -1023,6 +1046,9 @@ cudaError_t launch_bwd_rows(const Problem& p, const Workspace& ws, const RopeTab
     r.dx[1] = dk;
     r.dw_part[0] = ws.dwq_part;
     r.dw_part[1] = ws.dwk_part;
+    r.rope_cs = ws.rope_cs;
+    const long cells = (long)p.seq.S * kD;
+    rope_table_kernel<<<(unsigned)((cells + 255) / 256), 256, 0, st>>>(*rope, p.seq, ws.rope_cs);
     // an upper bound of the 128-token tiles (every sample adds at most one partial
     // tile); CTAs past the plan's last tile return at once
     const long tiles = (long)(p.seq.S + 127) / 128 + p.seq.n;

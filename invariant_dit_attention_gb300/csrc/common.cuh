@@ -183,6 +183,7 @@ struct Workspace {
     float* delta;            // [H, max_tokens]
     float* dqhat32;          // [max_tokens, H, 128] scale * dq^ (FP32), backward only
     float* dkhat32;          // [max_tokens, H, 128] scale * dk^ (FP32), backward only
+    float* rope_cs;          // [max_tokens, 2, 128] cos / sin of the rotary angles, backward only
     float* dwq_part;         // [max_tiles64, H, 128]
     float* dwk_part;         // [max_tiles64, H, 128]
     float* dwq_sample;       // [max_samples, 128]

@@ -175,7 +175,7 @@ h3attn_status h3attn_create(const h3attn_config* cfg, h3attn_t* out) {
     Workspace& ws = h->ws;
     bool ok = ws_alloc(h, &ws.qhat, T * H * kD * 2) && ws_alloc(h, &ws.khat, T * H * kD * 2) &&
               ws_alloc(h, &ws.delta, T * H * 4) && ws_alloc(h, &ws.dqhat32, T * H * kD * 4) &&
-              ws_alloc(h, &ws.dkhat32, T * H * kD * 4) &&
+              ws_alloc(h, &ws.dkhat32, T * H * kD * 4) && ws_alloc(h, &ws.rope_cs, T * 2 * kD * 4) &&
               ws_alloc(h, &ws.dwq_part, (size_t)h->max_tiles64 * H * kD * 4) &&
               ws_alloc(h, &ws.dwk_part, (size_t)h->max_tiles64 * H * kD * 4) &&
               ws_alloc(h, &ws.dwq_sample, N * kD * 4) && ws_alloc(h, &ws.dwk_sample, N * kD * 4) &&
