@@ -45,9 +45,20 @@ __device__ __forceinline__ bool mbar_try_sleep(uint32_t bar, uint32_t parity, ui
         : "=r"(ok) : "r"(bar), "r"(parity), "r"(ns) : "memory");
     return ok != 0;
 }
+// Non-blocking test of the same condition.  On a phase that has already
+// completed this is far cheaper for the issuing thread than try_wait, which
+// matters on the MMA thread: the tensor pipe only holds about one instruction
+// ahead, so every cycle it spends between MMAs is a cycle the pipe idles.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
 // Waits for the phase of the given parity to complete; false on timeout or abort.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort) {
-    if (mbar_try(bar, parity)) return true;
+    if (mbar_test(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
         if (mbar_try_sleep(bar, parity, 20000u)) return true;
