@@ -115,6 +115,15 @@ __device__ __forceinline__ uint64_t exp2_pair(uint64_t s2, uint64_t c2, uint64_t
         : "=l"(p2) : "l"(s2), "l"(c2), "l"(n2));
     return p2;
 }
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+// the two halves of a pair
+__device__ __forceinline__ float pair_lo(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float pair_hi(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
 // bf16x2 of a pair, low half first (round to nearest even)
 __device__ __forceinline__ uint32_t bf16_pair(uint64_t p2) {
     uint32_t r;

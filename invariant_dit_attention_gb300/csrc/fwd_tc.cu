@@ -300,30 +300,28 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                 if (!ok) { fail(); break; }
                 ++cntS;
                 tc::fence_after_sync();
-                float s[128];
-                {
-                    uint32_t r[4][32];
+                uint64_t s2[64];  // the row's 128 scores as column pairs, then P
+                tc::tmem_ld128_pairs(tS, s2);
+                const int valid = it.L - 128 * j;
+                if (valid < 128) {  // keys past the sample end: -inf, so P = 0 there
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) tc::tmem_ld32(tS + 32 * q4, r[q4]);
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        tc::tmem_wait_ld_dep(r[q4]);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) s[32 * q4 + e] = __uint_as_float(r[q4][e]);
+                    for (int e = 0; e < 64; ++e) {
+                        const float a0 = 2 * e < valid ? pair_lo(s2[e]) : -INFINITY;
+                        const float a1 = 2 * e + 1 < valid ? pair_hi(s2[e]) : -INFINITY;
+                        s2[e] = f2pack(a0, a1);
                     }
                 }
-                const int valid = it.L - 128 * j;
-                if (valid < 128) {
+                float mx0 = pair_lo(s2[0]), mx1 = pair_hi(s2[1]), mx2 = pair_lo(s2[2]), mx3 = pair_hi(s2[3]);
+                mx0 = fmaxf(mx0, pair_hi(s2[0]));
+                mx1 = fmaxf(mx1, pair_lo(s2[1]));
+                mx2 = fmaxf(mx2, pair_hi(s2[2]));
+                mx3 = fmaxf(mx3, pair_lo(s2[3]));
 #pragma unroll
-                    for (int e = 0; e < 128; ++e) s[e] = e < valid ? s[e] : -INFINITY;
-                }
-                float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
-#pragma unroll
-                for (int e = 4; e < 128; e += 4) {
-                    mx0 = fmaxf(mx0, s[e]);
-                    mx1 = fmaxf(mx1, s[e + 1]);
-                    mx2 = fmaxf(mx2, s[e + 2]);
-                    mx3 = fmaxf(mx3, s[e + 3]);
+                for (int e = 4; e < 64; e += 4) {
+                    mx0 = max3f(mx0, pair_lo(s2[e]), pair_hi(s2[e]));
+                    mx1 = max3f(mx1, pair_lo(s2[e + 1]), pair_hi(s2[e + 1]));
+                    mx2 = max3f(mx2, pair_lo(s2[e + 2]), pair_hi(s2[e + 2]));
+                    mx3 = max3f(mx3, pair_lo(s2[e + 3]), pair_hi(s2[e + 3]));
                 }
                 const float m_new = fmaxf(fmaxf(m, fmaxf(mx0, mx1)), fmaxf(mx2, mx3));
                 const bool need = j == 0 || (m_new - m) * c > kMaxStale;
@@ -333,24 +331,21 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                     m = m_new;
                     l *= factor;
                 }
-                const float neg = -m * c;
-                float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
+                const uint64_t c2 = f2pack(c, c), neg2 = f2pack(-m * c, -m * c);
+                uint64_t rs[4] = {0ull, 0ull, 0ull, 0ull};  // pairs of +0.0f
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     uint32_t pk[16];
 #pragma unroll
-                    for (int e = 0; e < 16; e += 2) {
-                        const float p0 = ex2(fmaf(s[32 * q4 + 2 * e], c, neg));
-                        const float p1 = ex2(fmaf(s[32 * q4 + 2 * e + 1], c, neg));
-                        const float p2 = ex2(fmaf(s[32 * q4 + 2 * e + 2], c, neg));
-                        const float p3 = ex2(fmaf(s[32 * q4 + 2 * e + 3], c, neg));
-                        rs0 += p0; rs1 += p1; rs2 += p2; rs3 += p3;
-                        pk[e] = pack_bf16(p0, p1);
-                        pk[e + 1] = pack_bf16(p2, p3);
+                    for (int e = 0; e < 16; ++e) {
+                        const uint64_t p2 = exp2_pair(s2[16 * q4 + e], c2, neg2);
+                        rs[e & 3] = f2add(rs[e & 3], p2);
+                        pk[e] = bf16_pair(p2);
                     }
                     tc::tmem_st16(tS + 16 * q4, pk);
                 }
-                l += (rs0 + rs1) + (rs2 + rs3);
+                l += ((pair_lo(rs[0]) + pair_hi(rs[0])) + (pair_lo(rs[1]) + pair_hi(rs[1]))) +
+                     ((pair_lo(rs[2]) + pair_hi(rs[2])) + (pair_lo(rs[3]) + pair_hi(rs[3])));
                 // O_X was last written by PV_X(j-1), complete before S_X(j) was issued
                 if (j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll

@@ -140,6 +140,87 @@ __device__ __forceinline__ void tmem_ld32_pairs(uint32_t taddr, uint64_t (&r)[16
         : "=l"(r[0]), "=l"(r[1]), "=l"(r[2]), "=l"(r[3]), "=l"(r[4]), "=l"(r[5]), "=l"(r[6]), "=l"(r[7]), "=l"(r[8]), "=l"(r[9]), "=l"(r[10]), "=l"(r[11]), "=l"(r[12]), "=l"(r[13]), "=l"(r[14]), "=l"(r[15])
         : "r"(taddr) : "memory");
 }
+// 32 lanes x 128 columns of 32-bit in one load, waited, as 64 column pairs.
+__device__ __forceinline__ void tmem_ld128_pairs(uint32_t taddr, uint64_t (&r)[64]) {
+    asm volatile(
+        "{\n.reg .b32 a<128>;\n"
+        "tcgen05.ld.sync.aligned.32x32b.x128.b32 {a0,a1,a2,a3,a4,a5,a6,a7,a8,a9,a10,a11,a12,a13,a14,a15,a16,a17,a18,a19,a20,a21,a22,a23,a24,a25,a26,a27,a28,a29,a30,a31,a32,a33,a34,a35,a36,a37,a38,a39,a40,a41,a42,a43,a44,a45,a46,a47,a48,a49,a50,a51,a52,a53,a54,a55,a56,a57,a58,a59,a60,a61,a62,a63,a64,a65,a66,a67,a68,a69,a70,a71,a72,a73,a74,a75,a76,a77,a78,a79,a80,a81,a82,a83,a84,a85,a86,a87,a88,a89,a90,a91,a92,a93,a94,a95,a96,a97,a98,a99,a100,a101,a102,a103,a104,a105,a106,a107,a108,a109,a110,a111,a112,a113,a114,a115,a116,a117,a118,a119,a120,a121,a122,a123,a124,a125,a126,a127}, [%64];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        "mov.b64 %0, {a0, a1};\n"
+        "mov.b64 %1, {a2, a3};\n"
+        "mov.b64 %2, {a4, a5};\n"
+        "mov.b64 %3, {a6, a7};\n"
+        "mov.b64 %4, {a8, a9};\n"
+        "mov.b64 %5, {a10, a11};\n"
+        "mov.b64 %6, {a12, a13};\n"
+        "mov.b64 %7, {a14, a15};\n"
+        "mov.b64 %8, {a16, a17};\n"
+        "mov.b64 %9, {a18, a19};\n"
+        "mov.b64 %10, {a20, a21};\n"
+        "mov.b64 %11, {a22, a23};\n"
+        "mov.b64 %12, {a24, a25};\n"
+        "mov.b64 %13, {a26, a27};\n"
+        "mov.b64 %14, {a28, a29};\n"
+        "mov.b64 %15, {a30, a31};\n"
+        "mov.b64 %16, {a32, a33};\n"
+        "mov.b64 %17, {a34, a35};\n"
+        "mov.b64 %18, {a36, a37};\n"
+        "mov.b64 %19, {a38, a39};\n"
+        "mov.b64 %20, {a40, a41};\n"
+        "mov.b64 %21, {a42, a43};\n"
+        "mov.b64 %22, {a44, a45};\n"
+        "mov.b64 %23, {a46, a47};\n"
+        "mov.b64 %24, {a48, a49};\n"
+        "mov.b64 %25, {a50, a51};\n"
+        "mov.b64 %26, {a52, a53};\n"
+        "mov.b64 %27, {a54, a55};\n"
+        "mov.b64 %28, {a56, a57};\n"
+        "mov.b64 %29, {a58, a59};\n"
+        "mov.b64 %30, {a60, a61};\n"
+        "mov.b64 %31, {a62, a63};\n"
+        "mov.b64 %32, {a64, a65};\n"
+        "mov.b64 %33, {a66, a67};\n"
+        "mov.b64 %34, {a68, a69};\n"
+        "mov.b64 %35, {a70, a71};\n"
+        "mov.b64 %36, {a72, a73};\n"
+        "mov.b64 %37, {a74, a75};\n"
+        "mov.b64 %38, {a76, a77};\n"
+        "mov.b64 %39, {a78, a79};\n"
+        "mov.b64 %40, {a80, a81};\n"
+        "mov.b64 %41, {a82, a83};\n"
+        "mov.b64 %42, {a84, a85};\n"
+        "mov.b64 %43, {a86, a87};\n"
+        "mov.b64 %44, {a88, a89};\n"
+        "mov.b64 %45, {a90, a91};\n"
+        "mov.b64 %46, {a92, a93};\n"
+        "mov.b64 %47, {a94, a95};\n"
+        "mov.b64 %48, {a96, a97};\n"
+        "mov.b64 %49, {a98, a99};\n"
+        "mov.b64 %50, {a100, a101};\n"
+        "mov.b64 %51, {a102, a103};\n"
+        "mov.b64 %52, {a104, a105};\n"
+        "mov.b64 %53, {a106, a107};\n"
+        "mov.b64 %54, {a108, a109};\n"
+        "mov.b64 %55, {a110, a111};\n"
+        "mov.b64 %56, {a112, a113};\n"
+        "mov.b64 %57, {a114, a115};\n"
+        "mov.b64 %58, {a116, a117};\n"
+        "mov.b64 %59, {a118, a119};\n"
+        "mov.b64 %60, {a120, a121};\n"
+        "mov.b64 %61, {a122, a123};\n"
+        "mov.b64 %62, {a124, a125};\n"
+        "mov.b64 %63, {a126, a127};\n"
+        "}\n"
+        : "=l"(r[0]), "=l"(r[1]), "=l"(r[2]), "=l"(r[3]), "=l"(r[4]), "=l"(r[5]), "=l"(r[6]), "=l"(r[7]),
+          "=l"(r[8]), "=l"(r[9]), "=l"(r[10]), "=l"(r[11]), "=l"(r[12]), "=l"(r[13]), "=l"(r[14]), "=l"(r[15]),
+          "=l"(r[16]), "=l"(r[17]), "=l"(r[18]), "=l"(r[19]), "=l"(r[20]), "=l"(r[21]), "=l"(r[22]), "=l"(r[23]),
+          "=l"(r[24]), "=l"(r[25]), "=l"(r[26]), "=l"(r[27]), "=l"(r[28]), "=l"(r[29]), "=l"(r[30]), "=l"(r[31]),
+          "=l"(r[32]), "=l"(r[33]), "=l"(r[34]), "=l"(r[35]), "=l"(r[36]), "=l"(r[37]), "=l"(r[38]), "=l"(r[39]),
+          "=l"(r[40]), "=l"(r[41]), "=l"(r[42]), "=l"(r[43]), "=l"(r[44]), "=l"(r[45]), "=l"(r[46]), "=l"(r[47]),
+          "=l"(r[48]), "=l"(r[49]), "=l"(r[50]), "=l"(r[51]), "=l"(r[52]), "=l"(r[53]), "=l"(r[54]), "=l"(r[55]),
+          "=l"(r[56]), "=l"(r[57]), "=l"(r[58]), "=l"(r[59]), "=l"(r[60]), "=l"(r[61]), "=l"(r[62]), "=l"(r[63])
+        : "r"(taddr) : "memory");
+}
 // 32 lanes x 32 columns of 32-bit: thread t of the warp gets lane (base + t), 32 columns.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
