@@ -88,6 +88,82 @@ __device__ __forceinline__ void zero_rows(uint32_t half, int valid, int rows, in
                      "r"(0) : "memory");
 }
 
+// One ring of 128-row streamed tiles and the warp that fills it.
+struct RingSpec {
+    const CUtensorMap* map;
+    uint32_t base;        // shared address of slot 0 (slots kTile apart)
+    int slots;
+    uint32_t full, empty;  // barrier addresses of slot 0 (8 bytes apart)
+    uint32_t tail;        // barrier of a block that runs past the sample end
+    bool zero_tail;       // zero the rows past the sample end before publishing
+};
+// The item's fixed tile pair, loaded by the first ring's warp once the previous
+// item's last MMA completed.
+struct FixedSpec {
+    const CUtensorMap* map0;
+    const CUtensorMap* map1;
+    uint32_t base, full, acc_done;
+};
+
+// Producer warp of one ring (lane 0 issues): for every streamed 128-row block of
+// every item of this CTA, waits until its slot is released, loads the block's
+// two 64-channel halves with TMA and publishes it.  One warp per ring, so a
+// ring never waits behind a slot of the other.
+__device__ __forceinline__ void ring_producer(const BwdTcParams& p, const RingSpec& r, const FixedSpec* fx,
+                                              volatile int* abort_flag, int lane) {
+    constexpr int kTile = 128 * 128 * 2, kHalf = 128 * 64 * 2;
+    bool failed = false;
+    auto fail = [&]() {
+        failed = true;
+        *abort_flag = 1;
+        atomicOr(p.plan.err, kErrTimeout);
+    };
+    uint32_t blk = 0, items = 0, tails = 0;
+    for (int i = blockIdx.x; !failed; i += gridDim.x) {
+        BwdItem it;
+        if (!bwd_item(p, i, it)) break;
+        const int x0 = it.h * 128;
+        if (fx && lane == 0) {
+            if (items > 0 && !tc::mbar_wait(fx->acc_done, (items - 1) & 1, abort_flag)) fail();
+            if (!failed) {
+                tc::fence_proxy_async();
+                tc::mbar_expect_tx(fx->full, 2 * kTile);
+                for (int hf = 0; hf < 2; ++hf) {
+                    tc::tma_load_2d(fx->base + hf * kHalf, fx->map0, x0 + 64 * hf, it.row0, fx->full);
+                    tc::tma_load_2d(fx->base + kTile + hf * kHalf, fx->map1, x0 + 64 * hf, it.row0, fx->full);
+                }
+            }
+        }
+        failed = __shfl_sync(0xffffffffu, failed, 0);
+        ++items;
+        const int nb = (it.L + 127) / 128;
+        for (int j = 0; j < nb && !failed; ++j) {
+            const uint32_t sl = blk % r.slots, ph = (blk / r.slots) & 1;
+            const uint32_t dst = r.base + sl * kTile;
+            const int y = it.seg0 + 128 * j, valid = it.L - 128 * j;
+            const bool tail = r.zero_tail && valid < 128;
+            if (lane == 0) {
+                if (!tc::mbar_wait(r.empty + 8 * sl, ph ^ 1, abort_flag)) fail();
+                if (!failed) {
+                    const uint32_t b = tail ? r.tail : r.full + 8 * sl;
+                    tc::mbar_expect_tx(b, kTile);
+                    for (int hf = 0; hf < 2; ++hf) tc::tma_load_2d(dst + hf * kHalf, r.map, x0 + 64 * hf, y, b);
+                    if (tail && !tc::mbar_wait(r.tail, tails & 1, abort_flag)) fail();
+                }
+            }
+            failed = __shfl_sync(0xffffffffu, failed, 0);
+            if (tail && !failed) {
+                ++tails;
+                for (int hf = 0; hf < 2; ++hf) zero_rows(dst + hf * kHalf, valid, 128, lane);
+                tc::fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(r.full + 8 * sl);
+            }
+            ++blk;
+        }
+    }
+}
+
 // TMEM column of the A operand for K-step kk of a 128-wide score tile split
 // between two warpgroups: columns 0..63 were packed at [0, 32), 64..127 at [64, 96).
 __device__ __forceinline__ uint32_t a_col(int kk) { return kk < 4 ? 8 * kk : 64 + 8 * (kk - 4); }
@@ -123,7 +199,7 @@ constexpr int kOffLse = kOffO + kOSlots * bwdt::kTile;  // [4 wg][2 buf][lse2 32
 constexpr int kOffBar = kOffLse + 4 * 2 * 64 * 4;
 constexpr int kSmem = kOffBar + 256;                // the dynamic shared memory base is 1024-aligned (checked)
 enum { bFixedFull = 0, bQFull, bQEmpty = bQFull + kQSlots, bOFull = bQEmpty + kQSlots, bOEmpty = bOFull + kOSlots,
-       bSFull = bOEmpty + kOSlots, bPFull, bSUsed, bPtFull, bDsFull, bAccDone, bTail, bDone, bCount };
+       bSFull = bOEmpty + kOSlots, bPFull, bSUsed, bPtFull, bDsFull, bAccDone, bTailQ, bTailO, bDone, bCount };
 constexpr uint32_t cB = 128;
 }  // namespace kvt
 
@@ -169,7 +245,8 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         tc::mbar_init(bar(bPtFull), 16);
         tc::mbar_init(bar(bDsFull), 16);
         tc::mbar_init(bar(bAccDone), 1);
-        tc::mbar_init(bar(bTail), 1);
+        tc::mbar_init(bar(bTailQ), 1);
+        tc::mbar_init(bar(bTailO), 1);
         tc::mbar_init(bar(bDone), 1);
         *abort_flag = 0;
         tc::fence_mbar_init();
@@ -191,74 +268,14 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
     // 640 threads x 96 registers: the MMA issuer and the softmax warps both need about 96,
     // so no setmaxnreg split
 
-    if (warp == 0) {
-        // ------------------------------------------------------ TMA producer
-        // blk counts streamed blocks: q^ slot blk % 3, dO slot blk % 2
-        uint32_t blk = 0, items = 0, tails = 0;
-        for (int i = blockIdx.x; !failed; i += gridDim.x) {
-            BwdItem it;
-            if (!bwd_item(p, i, it)) break;
-            const int x0 = it.h * 128;
-            if (lane == 0) {
-                // the fixed tiles are reloaded once the previous item's last MMA completed
-                if (items > 0 && !tc::mbar_wait(bar(bAccDone), (items - 1) & 1, abort_flag)) fail();
-                if (!failed) {
-                    tc::fence_proxy_async();
-                    tc::mbar_expect_tx(bar(bFixedFull), kPair);
-                    for (int hf = 0; hf < 2; ++hf) {
-                        tc::tma_load_2d(sbase + kOffFixed + hf * kHalf, &mk, x0 + 64 * hf, it.row0, bar(bFixedFull));
-                        tc::tma_load_2d(sbase + kOffFixed + kTile + hf * kHalf, &mv, x0 + 64 * hf, it.row0,
-                                        bar(bFixedFull));
-                    }
-                }
-            }
-            failed = __shfl_sync(0xffffffffu, failed, 0);
-            ++items;
-            const int nq = (it.L + 127) / 128;
-            for (int qj = 0; qj < nq && !failed; ++qj) {
-                const uint32_t qs = blk % kQSlots, os = blk % kOSlots;
-                const uint32_t qdst = sbase + kOffQ + qs * kTile, odst = sbase + kOffO + os * kTile;
-                const int y = it.seg0 + 128 * qj;
-                const int valid = it.L - 128 * qj;
-                const bool tail = valid < 128;
-                if (lane == 0) {
-                    // q^ first: S^T(b) runs a block ahead of dP^T(b)
-                    if (!tc::mbar_wait(bar(bQEmpty + qs), ((blk / kQSlots) & 1) ^ 1, abort_flag)) fail();
-                    if (!failed && !tail) {
-                        tc::mbar_expect_tx(bar(bQFull + qs), kTile);
-                        for (int hf = 0; hf < 2; ++hf)
-                            tc::tma_load_2d(qdst + hf * kHalf, &mq, x0 + 64 * hf, y, bar(bQFull + qs));
-                    }
-                    if (!failed && !tc::mbar_wait(bar(bOEmpty + os), ((blk / kOSlots) & 1) ^ 1, abort_flag)) fail();
-                    if (!failed) {
-                        const uint32_t b = tail ? bar(bTail) : bar(bOFull + os);
-                        tc::mbar_expect_tx(b, tail ? kPair : kTile);
-                        for (int hf = 0; hf < 2; ++hf) {
-                            tc::tma_load_2d(odst + hf * kHalf, &mdo, x0 + 64 * hf, y, b);
-                            if (tail) tc::tma_load_2d(qdst + hf * kHalf, &mq, x0 + 64 * hf, y, b);
-                        }
-                        if (tail && !tc::mbar_wait(bar(bTail), tails & 1, abort_flag)) fail();
-                    }
-                }
-                failed = __shfl_sync(0xffffffffu, failed, 0);
-                if (tail && !failed) {
-                    ++tails;
-                    // query rows past the sample end: zero q^ and dO so no neighbour
-                    // value reaches the dV and dK products
-                    for (int hf = 0; hf < 2; ++hf) {
-                        zero_rows(qdst + hf * kHalf, valid, 128, lane);
-                        zero_rows(odst + hf * kHalf, valid, 128, lane);
-                    }
-                    tc::fence_proxy_async();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tc::mbar_arrive(bar(bQFull + qs));
-                        tc::mbar_arrive(bar(bOFull + os));
-                    }
-                }
-                ++blk;
-            }
-        }
+    if (warp == 0 || warp == 2) {
+        // ------------------------------------- TMA producers: warp 0 the fixed k^ / v
+        // tiles and the q^ ring, warp 2 the dO ring; rows past the sample end are
+        // zeroed in both, so no neighbour value reaches the dV and dK products
+        const FixedSpec fx = {&mk, &mv, sbase + kOffFixed, bar(bFixedFull), bar(bAccDone)};
+        const RingSpec r = warp == 0 ? RingSpec{&mq, sbase + kOffQ, kQSlots, bar(bQFull), bar(bQEmpty), bar(bTailQ), true}
+                                     : RingSpec{&mdo, sbase + kOffO, kOSlots, bar(bOFull), bar(bOEmpty), bar(bTailO), true};
+        ring_producer(p, r, warp == 0 ? &fx : nullptr, abort_flag, lane);
     } else if (warp == 1) {
         // ----------------------------------------------------- MMA issuer
         if (lane == 0) {
@@ -570,64 +587,14 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     };
     // 640 threads x 96 registers for every role (no setmaxnreg split)
 
-    if (warp == 0) {
-        // ------------------------------------------------------ TMA producer
-        uint32_t kr = 0, vr = 0, items = 0, tails = 0;
-        for (int i = blockIdx.x; !failed; i += gridDim.x) {
-            BwdItem it;
-            if (!bwd_item(p, i, it)) break;
-            const int x0 = it.h * 128;
-            if (lane == 0) {
-                // the fixed tiles are reloaded once the previous item's last MMA completed
-                if (items > 0 && !tc::mbar_wait(bar(bAccDone), (items - 1) & 1, abort_flag)) fail();
-                if (!failed) {
-                    tc::fence_proxy_async();
-                    tc::mbar_expect_tx(bar(bFixedFull), kPair);
-                    for (int hf = 0; hf < 2; ++hf) {
-                        tc::tma_load_2d(sbase + kOffFixed + hf * kHalf, &mq, x0 + 64 * hf, it.row0, bar(bFixedFull));
-                        tc::tma_load_2d(sbase + kOffFixed + kTile + hf * kHalf, &mdo, x0 + 64 * hf, it.row0,
-                                        bar(bFixedFull));
-                    }
-                }
-            }
-            failed = __shfl_sync(0xffffffffu, failed, 0);
-            ++items;
-            const int nk = (it.L + 127) / 128;
-            for (int kj = 0; kj < nk && !failed; ++kj) {
-                const int y = it.seg0 + 128 * kj;
-                const int valid = it.L - 128 * kj;
-                const bool tail = valid < 128;
-                const uint32_t ks = kr % kKSlots, vs = vr % kVSlots;
-                const uint32_t kdst = sbase + kOffK + ks * kTile, vdst = sbase + kOffV + vs * kTile;
-                if (lane == 0) {
-                    // v first: its slot frees early, and S(j) waits for both anyway
-                    if (!tc::mbar_wait(bar(bVEmpty + vs), ((vr / kVSlots) & 1) ^ 1, abort_flag)) fail();
-                    if (!failed) {
-                        tc::mbar_expect_tx(bar(bVFull + vs), kTile);
-                        for (int hf = 0; hf < 2; ++hf)
-                            tc::tma_load_2d(vdst + hf * kHalf, &mv, x0 + 64 * hf, y, bar(bVFull + vs));
-                    }
-                    if (!failed && !tc::mbar_wait(bar(bKEmpty + ks), ((kr / kKSlots) & 1) ^ 1, abort_flag)) fail();
-                    if (!failed) {
-                        const uint32_t b = tail ? bar(bTail) : bar(bKFull + ks);
-                        tc::mbar_expect_tx(b, kTile);
-                        for (int hf = 0; hf < 2; ++hf) tc::tma_load_2d(kdst + hf * kHalf, &mk, x0 + 64 * hf, y, b);
-                        if (tail && !tc::mbar_wait(bar(bTail), tails & 1, abort_flag)) fail();
-                    }
-                }
-                failed = __shfl_sync(0xffffffffu, failed, 0);
-                if (tail && !failed) {
-                    ++tails;
-                    // key rows past the sample end: zero k^ (dS is 0 there, k^ may not be finite)
-                    for (int hf = 0; hf < 2; ++hf) zero_rows(kdst + hf * kHalf, valid, 128, lane);
-                    tc::fence_proxy_async();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(bar(bKFull + ks));
-                }
-                ++kr;
-                ++vr;
-            }
-        }
+    if (warp == 0 || warp == 2) {
+        // ------------------------------------- TMA producers: warp 0 the fixed q^ / dO
+        // tiles and the k^ ring (key rows past the sample end zeroed: dS is 0 there,
+        // k^ may not be finite), warp 2 the v ring
+        const FixedSpec fx = {&mq, &mdo, sbase + kOffFixed, bar(bFixedFull), bar(bAccDone)};
+        const RingSpec r = warp == 0 ? RingSpec{&mk, sbase + kOffK, kKSlots, bar(bKFull), bar(bKEmpty), bar(bTail), true}
+                                     : RingSpec{&mv, sbase + kOffV, kVSlots, bar(bVFull), bar(bVEmpty), bar(bTail), false};
+        ring_producer(p, r, warp == 0 ? &fx : nullptr, abort_flag, lane);
     } else if (warp == 1) {
         // ----------------------------------------------------- MMA issuer
         if (lane == 0) {
