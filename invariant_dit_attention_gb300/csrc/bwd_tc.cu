@@ -819,7 +819,7 @@ rope_table_kernel(const __grid_constant__ RopeTable rt, Seq seq, float* __restri
 // dx = RMSNorm-backward(RoPE^-1(dy)) per row (one warp per row, rows w, w + 8,
 // ... with four rows' loads in flight per warp), and the tile's norm-weight
 // partial sum_rows g * n, reduced rows-by-warp then warps in a fixed order.
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 3)
 rows_bwd_kernel(const __grid_constant__ RopeTable rt, const RowsParams p) {
     __shared__ RopeTable srt;
     __shared__ float red[8 * kD];

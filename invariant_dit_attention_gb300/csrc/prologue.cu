@@ -97,7 +97,7 @@ cudaError_t launch_plan(const Problem& p, const Workspace& ws, cudaStream_t st) 
 constexpr int kProWarps = 8;
 constexpr int kProBatch = 4;  // heads loaded ahead per warp
 
-__global__ void __launch_bounds__(kProWarps * 32)
+__global__ void __launch_bounds__(kProWarps * 32, 4)
 prologue_kernel(Problem p, __half* __restrict__ qhat, __half* __restrict__ khat,
                 const __grid_constant__ RopeTable rt, unsigned* err) {
     __shared__ RopeTable srt;
