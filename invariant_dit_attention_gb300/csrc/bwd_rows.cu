@@ -1,0 +1,216 @@
+// bwd_rows.cu -- the backward's row-wise kernels around the tensor-core ones:
+//   delta_kernel      Delta_i = sum_c dO_ic O_ic per (token, head)
+//   rope_table_kernel cos / sin of every channel's rotary angle per token
+//   rows_bwd_kernel   dx = RMSNorm-backward(RoPE^-1(scale * dx^)) per row, for q
+//                     and k, and the norm-weight partial of every 128-token tile
+//   dw_sample_kernel, dw_total_kernel
+//                     the norm-weight gradient per sample, then over samples
+// (the per-leaf gradients of the "ws1_one_h3_block" page of RL-Kernel, PR #539,
+// Results and Tests; the 128-element norm-weight gradient of its Status
+// section).  Every sum runs in one fixed order, with no atomics.
+#include "common.cuh"
+#include "rowops.cuh"
+
+namespace h3 {
+
+// ------------------------------------------------------------------ Delta
+
+__global__ void __launch_bounds__(256) delta_kernel(const __nv_bfloat16* __restrict__ out,
+                                                    const __nv_bfloat16* __restrict__ dout, int S, int H,
+                                                    float* __restrict__ delta) {
+    const int lane = threadIdx.x & 31;
+    const long row = (long)blockIdx.x * 8 + (threadIdx.x >> 5);  // (token, head)
+    if (row >= (long)S * H) return;
+    float o[4], d[4];
+    load_row4(out + row * kD + 4 * lane, o);
+    load_row4(dout + row * kD + 4 * lane, d);
+    float acc = o[0] * d[0] + o[1] * d[1] + o[2] * d[2] + o[3] * d[3];
+    acc = warp_sum(acc);
+    if (lane == 0) delta[(long)(row % H) * S + row / H] = acc;
+}
+
+// ------------------------------------------- RoPE^-1 + RMSNorm backward rows
+
+struct RowsParams {
+    Seq seq;
+    Plan plan;
+    int H;
+    float eps;
+    const float* rope_cs;          // [S][cos 128 | sin 128] per token
+    const float* dyhat[2];         // scale * dq^, scale * dk^: FP32 [S, H, 128]
+    const __nv_bfloat16* x[2];     // raw q, k
+    const float* w[2];             // q_norm_w, k_norm_w
+    __nv_bfloat16* dx[2];          // dq, dk
+    float* dw_part[2];             // [tiles128, H, 128]
+};
+
+// cos / sin of every channel's rotary angle per token, [S][cos 128 | sin 128]:
+// the same FP32 sincosf(p_axis * f_c) as row_angles, computed once per token
+// instead of once per (token, head) row; channels outside the sections get
+// (1, 0).
+__global__ void __launch_bounds__(256)
+rope_table_kernel(const __grid_constant__ RopeTable rt, Seq seq, float* __restrict__ cs) {
+    __shared__ RopeTable srt;
+    rope_to_smem(rt, srt, threadIdx.x, 256);
+    __syncthreads();
+    const long i = (long)blockIdx.x * 256 + threadIdx.x;
+    if (i >= (long)seq.S * kD) return;
+    const int token = (int)(i / kD), ch = (int)(i % kD);
+    const int axis = srt.axis[ch >> 2];
+    float c = 1.f, sn = 0.f;
+    if (axis >= 0) {
+        const int pos = axis == 0 ? seq.pos_t[token] : (axis == 1 ? seq.pos_h[token] : seq.pos_w[token]);
+        sincosf(static_cast<float>(pos) * srt.inv_freq[ch], &sn, &c);
+    }
+    cs[(size_t)token * 2 * kD + ch] = c;
+    cs[(size_t)token * 2 * kD + kD + ch] = sn;
+}
+
+// One CTA per (128-token tile of a sample, head) and per q / k (blockIdx.y):
+// dx = RMSNorm-backward(RoPE^-1(dy)) per row (one warp per row, rows w, w + 8,
+// ... with four rows' loads in flight per warp), and the tile's norm-weight
+// partial sum_rows g * n, reduced rows-by-warp then warps in a fixed order.
+__global__ void __launch_bounds__(256, 3)
+rows_bwd_kernel(const __grid_constant__ RopeTable rt, const RowsParams p) {
+    __shared__ RopeTable srt;
+    __shared__ float red[8 * kD];
+    const int which = blockIdx.y;
+    const int tile = blockIdx.x / p.H, h = blockIdx.x % p.H;
+    const int w8 = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    rope_to_smem(rt, srt, threadIdx.x, 256);
+    __syncthreads();
+    int sample, row0, row_end, local;
+    if (!plan_tile(p.plan.cum128, p.plan.order, p.seq.seg, p.seq.n, 128, tile, sample, row0, row_end, local)) return;
+    const float* dyhat = p.dyhat[which];
+    const __nv_bfloat16* x = p.x[which];
+    __nv_bfloat16* dx = p.dx[which];
+    const LaneRope lr = lane_rope(srt, lane);
+    float wl[4], acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) wl[e] = p.w[which][4 * lane + e];
+    const int nvalid = min(128, row_end - row0);
+    bool nonfinite = false;
+    for (int r0 = w8; r0 < nvalid; r0 += 32) {
+        float dy[4][4], xr[4][4];
+        RowAngles a[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int row = row0 + min(r0 + 8 * u, nvalid - 1);
+            const size_t off = ((size_t)row * p.H + h) * kD + 4 * lane;
+            const float4 d4 = *reinterpret_cast<const float4*>(dyhat + off);
+            dy[u][0] = d4.x; dy[u][1] = d4.y; dy[u][2] = d4.z; dy[u][3] = d4.w;
+            load_row4(x + off, xr[u]);
+            const float4 c4 = *reinterpret_cast<const float4*>(p.rope_cs + (size_t)row * 2 * kD + 4 * lane);
+            const float4 s4 = *reinterpret_cast<const float4*>(p.rope_cs + (size_t)row * 2 * kD + kD + 4 * lane);
+            a[u].c[0] = c4.x; a[u].c[1] = c4.y; a[u].c[2] = c4.z; a[u].c[3] = c4.w;
+            a[u].s[0] = s4.x; a[u].s[1] = s4.y; a[u].s[2] = s4.z; a[u].s[3] = s4.w;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int r = r0 + 8 * u;
+            if (r >= nvalid) break;
+            float d[4];
+            row_norm_rope_bwd(dy[u], xr[u], wl, a[u], lr, p.eps, d, acc);
+            nonfinite |= !(isfinite(d[0]) && isfinite(d[1]) && isfinite(d[2]) && isfinite(d[3]));
+            store_row4(dx + ((size_t)(row0 + r) * p.H + h) * kD + 4 * lane, d);
+        }
+    }
+    // a non-finite gradient row from finite inputs means an fp16 operand (dS) overflowed
+    if (nonfinite) atomicOr(p.plan.err, kErrRange);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) red[w8 * kD + 4 * lane + e] = acc[e];
+    __syncthreads();
+    const int c = threadIdx.x;
+    if (c < kD) {
+        float sum = 0.f;
+#pragma unroll
+        for (int wi = 0; wi < 8; ++wi) sum += red[wi * kD + c];
+        p.dw_part[which][((size_t)tile * p.H + h) * kD + c] = sum;
+    }
+}
+
+// -------------------------------------------------------- weight gradients
+
+// Per-sample weight gradient over the sample's (tile, head) partials, index
+// (tile - first tile) * H + head: eight fixed interleaved groups each sum their
+// indices in ascending order, then the groups are added in ascending order.
+__global__ void __launch_bounds__(1024)
+dw_sample_kernel(const float* __restrict__ part_q, const float* __restrict__ part_k, Seq seq, Plan plan, int H,
+                 float* __restrict__ dwq_s, float* __restrict__ dwk_s) {
+    constexpr int kGroups = 8;
+    const int s = blockIdx.x;
+    const float* part = blockIdx.y == 0 ? part_q : part_k;
+    float* dst = blockIdx.y == 0 ? dwq_s : dwk_s;
+    const int c = threadIdx.x & 127, grp = threadIdx.x >> 7;
+    __shared__ float red[kGroups][kD];
+    const int r = plan.rank_of[s];
+    const int t0 = plan.cum128[r], t1 = plan.cum128[r + 1];
+    const int n = (t1 - t0) * H;
+    const float* base = part + (size_t)t0 * H * kD + c;
+    float acc = 0.f;
+    for (int i = grp; i < n; i += kGroups) acc += base[(size_t)i * kD];
+    red[grp][c] = acc;
+    __syncthreads();
+    if (grp == 0) {
+        float sum = red[0][c];
+#pragma unroll
+        for (int g = 1; g < kGroups; ++g) sum += red[g][c];
+        dst[(size_t)s * kD + c] = sum;
+    }
+}
+
+__global__ void dw_total_kernel(const float* __restrict__ dwq_s, const float* __restrict__ dwk_s, int n,
+                                float* __restrict__ dwq, float* __restrict__ dwk) {
+    const int c = threadIdx.x & 127;
+    const float* src = threadIdx.x < 128 ? dwq_s : dwk_s;
+    float acc = 0.f;
+    for (int s = 0; s < n; ++s) acc += src[(size_t)s * kD + c];
+    (threadIdx.x < 128 ? dwq : dwk)[c] = acc;
+}
+
+// ------------------------------------------------------------------ host
+
+cudaError_t launch_bwd_delta(const Problem& p, const Workspace& ws, const __nv_bfloat16* out,
+                             const __nv_bfloat16* dout, cudaStream_t st) {
+    const long rows = (long)p.seq.S * p.H;
+    delta_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(out, dout, p.seq.S, p.H, ws.delta);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_rows(const Problem& p, const Workspace& ws, const RopeTable* rope, __nv_bfloat16* dq,
+                            __nv_bfloat16* dk, cudaStream_t st) {
+    RowsParams r;
+    r.seq = p.seq;
+    r.plan = ws.plan;
+    r.H = p.H;
+    r.eps = p.eps;
+    r.dyhat[0] = ws.dqhat32;
+    r.dyhat[1] = ws.dkhat32;
+    r.x[0] = p.q;
+    r.x[1] = p.k;
+    r.w[0] = p.wq;
+    r.w[1] = p.wk;
+    r.dx[0] = dq;
+    r.dx[1] = dk;
+    r.dw_part[0] = ws.dwq_part;
+    r.dw_part[1] = ws.dwk_part;
+    r.rope_cs = ws.rope_cs;
+    const long cells = (long)p.seq.S * kD;
+    rope_table_kernel<<<(unsigned)((cells + 255) / 256), 256, 0, st>>>(*rope, p.seq, ws.rope_cs);
+    // an upper bound of the 128-token tiles (every sample adds at most one partial
+    // tile); CTAs past the plan's last tile return at once
+    const long tiles = (long)(p.seq.S + 127) / 128 + p.seq.n;
+    rows_bwd_kernel<<<dim3((unsigned)(tiles * p.H), 2), 256, 0, st>>>(*rope, r);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dw(const Problem& p, const Workspace& ws, float* dwq, float* dwk, float* dwq_s,
+                          float* dwk_s, cudaStream_t st) {
+    float* qs = dwq_s ? dwq_s : ws.dwq_sample;
+    float* ks = dwk_s ? dwk_s : ws.dwk_sample;
+    dw_sample_kernel<<<dim3(p.seq.n, 2), 1024, 0, st>>>(ws.dwq_part, ws.dwk_part, p.seq, ws.plan, p.H, qs, ks);
+    dw_total_kernel<<<1, 256, 0, st>>>(qs, ks, p.seq.n, dwq, dwk);
+    return cudaGetLastError();
+}
+
+}  // namespace h3
