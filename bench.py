@@ -67,7 +67,9 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples during the timed region."""
+    """nvidia-smi clock/throttle samples during the timed region: sampling starts
+    (20 ms interval) before the region, and only the samples taken between
+    mark_start() and mark_end() (host clock) are summarised."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -81,17 +83,26 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            t_end = time.time() + 5.0  # let the sampler start before the timed region
+            while not self.lines and time.time() < t_end:
+                time.sleep(0.01)
         except Exception:
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
 
     def __exit__(self, *a):
         if self.proc:
@@ -104,7 +115,9 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        t0, t1 = getattr(self, "t0", None), getattr(self, "t1", None)
+        inside = [ln for t, ln in self.lines if t0 is not None and t1 is not None and t0 <= t <= t1]
+        for ln in inside:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -213,11 +226,13 @@ def run_ours(args):
     with ClockSampler(local) as clk:
         barrier(ws)
         torch.cuda.synchronize()
+        clk.mark_start()
         e0.record(stream)
         for _ in range(args.steps):
             step()
         e1.record(stream)
         torch.cuda.synchronize()
+        clk.mark_end()
         barrier(ws)
     ms = e0.elapsed_time(e1)
     stages = h.stage_times()
@@ -237,15 +252,23 @@ def run_ours(args):
                       alone["seg_offsets"])
         reps = 10 if L > 1000 else 50
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        h.set_stage_timing(True)
+        h.stage_times()  # reset
         a0.record(stream)
         for _ in range(reps):
             h.forward(alone["q"], alone["k"], alone["v"], alone["q_norm_w"], alone["k_norm_w"], alone["pos"],
                       alone["seg_offsets"])
         a1.record(stream)
         torch.cuda.synchronize()
+        st_alone = h.stage_times()
+        h.set_stage_timing(False)
         t = a0.elapsed_time(a1) / reps
-        per_sample[str(L)] = {"fwd_ms": round(t, 4),
-                              "fwd_tflops": round(4.0 * H * 128 * L * L / (t * 1e-3) / 1e12, 2)}
+        tk = st_alone["fwd"][0] / max(st_alone["fwd"][1], 1)
+        flops = 4.0 * H * 128 * L * L
+        # fwd_*: the whole call (plan, norm/RoPE prologue, attention); fwd_kernel_*: the attention kernel
+        per_sample[str(L)] = {"fwd_ms": round(t, 4), "fwd_tflops": round(flops / (t * 1e-3) / 1e12, 2),
+                              "fwd_kernel_ms": round(tk, 4),
+                              "fwd_kernel_tflops": round(flops / (tk * 1e-3) / 1e12, 2)}
         del alone
 
     # ---- end to end: host (pinned) inputs -> device -> fwd + bwd -> host results
@@ -394,7 +417,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
