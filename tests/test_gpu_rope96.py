@@ -1,0 +1,70 @@
+"""The pages' own rotary width as a tested configuration: 96 of the 128 channels
+rotate ("ws1_one_h3_block" page, Tests), as sections 32/32/32 of the handle's
+config.  Forward and backward parity against the FP64 oracle run with the same
+sections, and the bitwise alone-vs-packed property."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from invariant_dit_attention_gb300 import workloads as W
+from tests.helpers import (BWD_REL_L2, FWD_MAX_ABS, FWD_REL_L2, LSE_MAX_ABS, make_handle, max_abs, max_abs_scaled,
+                           need_gpu, np64, rel_l2)
+
+pytestmark = pytest.mark.gpu
+SECTIONS96 = (32, 32, 32)
+
+
+def _inputs():
+    # positions up to the video grid's extent on all three axes, tails of 1 and 41 tokens
+    return W.make_inputs([W.SampleLayout(n_text=3, grid=(2, 6, 7), n_audio=20), 129, 41], 4, seed=96,
+                         with_grad=True)
+
+
+def _run(inp, sections):
+    from invariant_dit_attention_gb300.h3attn import to_device
+    h = make_handle(inp.num_heads, inp.total_tokens, 8, rope_sections=sections)
+    d = to_device(inp)
+    out, lse = h.forward(d["q"], d["k"], d["v"], d["q_norm_w"], d["k_norm_w"], d["pos"], d["seg_offsets"])
+    g = h.backward(d["q"], d["k"], d["v"], d["q_norm_w"], d["k_norm_w"], d["pos"], d["seg_offsets"], out, lse,
+                   d["dout"])
+    torch.cuda.synchronize()
+    h.check()
+    return out, lse, g
+
+
+def test_rope96_forward_and_backward_match_oracle():
+    need_gpu()
+    inp = _inputs()
+    out, lse, g = _run(inp, SECTIONS96)
+    ref_out, ref_lse = oracle.forward(inp.q, inp.k, inp.v, inp.q_norm_w, inp.k_norm_w, inp.pos, inp.seg_offsets,
+                                      sections=SECTIONS96)
+    o = np64(out)
+    assert rel_l2(o, ref_out) <= FWD_REL_L2 and max_abs_scaled(o, ref_out) <= FWD_MAX_ABS
+    assert max_abs(lse.cpu().numpy().astype(np.float64), ref_lse) <= LSE_MAX_ABS
+    ref = oracle.backward(inp.q, inp.k, inp.v, inp.q_norm_w, inp.k_norm_w, inp.pos, inp.seg_offsets, inp.dout,
+                          sections=SECTIONS96)
+    for name in ("dq", "dk", "dv", "dq_norm_w", "dk_norm_w"):
+        e = rel_l2(np64(g[name]), ref[name])
+        assert e <= BWD_REL_L2, f"{name} rel-L2 {e:.3e}"
+    # the 64-channel default gives a different result on the same inputs (the span is live)
+    out64, _, _ = _run(inp, (16, 24, 24))
+    assert not torch.equal(out64, out)
+
+
+def test_rope96_sample_alone_equals_packed_bitwise():
+    need_gpu()
+    inp = _inputs()
+    out, lse, g = _run(inp, SECTIONS96)
+    seg = inp.seg_offsets.tolist()
+    for s in range(inp.num_samples):
+        alone = W.slice_sample(inp, s)
+        a_out, a_lse, a_g = _run(alone, SECTIONS96)
+        r = slice(seg[s], seg[s + 1])
+        assert torch.equal(a_out, out[r])
+        assert torch.equal(a_lse, lse[:, r])
+        for name in ("dq", "dk", "dv"):
+            assert torch.equal(a_g[name], g[name][r]), name
+        for name in ("dq_norm_w_per_sample", "dk_norm_w_per_sample"):
+            assert torch.equal(a_g[name][0], g[name][s]), name

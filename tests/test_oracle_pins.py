@@ -364,3 +364,28 @@ def test_per_sample_weight_gradients_sum_to_total_and_are_local():
     np.testing.assert_allclose(ga["dq"], g["dq"][5:12], rtol=1e-12, atol=1e-14)
     np.testing.assert_allclose(ga["dv"], g["dv"][5:12], rtol=1e-12, atol=1e-14)
     np.testing.assert_allclose(ga["dk_norm_w"], g["dk_norm_w_per_sample"][1], rtol=1e-12, atol=1e-14)
+
+
+# ------------------------------------------------------ 96-channel rotary span
+
+SECTIONS96 = (32, 32, 32)
+
+
+def test_rope_96_channel_span_matches_complex_rotation_and_keeps_tail():
+    """The pages' own rotary width ("ws1_one_h3_block" page, Tests: 96 of the 128
+    channels rotate), as sections 32/32/32: complex rotation on the first 96
+    channels, the last 32 untouched."""
+    inp = _rand_inputs([10, 7], 3, seed=41)
+    pos = torch.randint(0, 90, inp.pos.shape, generator=torch.Generator().manual_seed(9), dtype=torch.int32)
+    y, n, _ = oracle.norm_rope(inp.q, inp.q_norm_w, pos, sections=SECTIONS96)
+    z = n * inp.q_norm_w.double().numpy()
+    np.testing.assert_allclose(y, _complex_rope(z, pos.numpy(), SECTIONS96), rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(y[..., 96:], z[..., 96:])
+
+
+def test_attention_96_channel_span_matches_torch_sdpa_with_block_mask():
+    inp = _rand_inputs([9, 14], 2, seed=42)
+    inp.pos = torch.randint(0, 40, inp.pos.shape, generator=torch.Generator().manual_seed(10), dtype=torch.int32)
+    out, _ = oracle.forward(inp.q, inp.k, inp.v, inp.q_norm_w, inp.k_norm_w, inp.pos, inp.seg_offsets,
+                            sections=SECTIONS96)
+    np.testing.assert_allclose(out, _library_forward(inp, sections=SECTIONS96), rtol=1e-11, atol=1e-12)
