@@ -199,6 +199,29 @@ h3attn_status h3attn_forward_static(const h3attn_config *cfg,
                                     h3attn_bf16 *out, float *lse, uint32_t *device_error_flags,
                                     void *stream);
 
+/*
+ * The projection either side of the attention core (the block's QKV
+ * projection feeding the q/k norms, and its output projection; "ws1_one_h3_block"
+ * page of RL-Kernel, PR #539, Bindings table and Prior art): y = x W^T (+ b).
+ *   x  bf16 [rows, in_features] row-major;  w bf16 [out_features, in_features]
+ *      row-major (a linear layer's [out, in] weight);  bias FP32 [out_features]
+ *      or NULL;  y bf16 [rows, out_features] row-major.  Caller-owned device
+ *      memory, 16-byte aligned.  The q, k and v of the attention are three calls
+ *      (or one call with the three weights stacked and the outputs split after).
+ *   FP32 accumulation over in_features in ascending order, one rounding to bf16
+ *   after the bias: each output row's bits depend only on that row of x and on
+ *   w and bias (the same whatever the number of rows or the row's position).
+ *   device_error_flags: device uint32, required; the call clears it on `stream`
+ *   and sets bit 2 if an on-device wait timed out (outputs then unspecified).
+ * Needs in_features % 64 == 0 and out_features % 32 == 0 (UNSUPPORTED
+ * otherwise).  rows == 0 is a no-op.  Asynchronous on `stream`; allocates
+ * nothing.  Errors: INVALID_ARG (sizes < 0, null or misaligned pointers),
+ * UNSUPPORTED (shapes, device not sm_103), CAPACITY, CUDA.
+ */
+h3attn_status h3attn_linear(const h3attn_bf16 *x, int rows, int in_features,
+                            const h3attn_bf16 *w, int out_features, const float *bias,
+                            h3attn_bf16 *y, uint32_t *device_error_flags, void *stream);
+
 /* Static, human-readable name of a status code. */
 const char *h3attn_status_string(h3attn_status s);
 

@@ -22,7 +22,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CAPACITY, ERR_CUDA, ERR_TIMEOUT = rang
 # Entry points declared in include/h3attn.h.
 EXPORTS = ("h3attn_create", "h3attn_destroy", "h3attn_forward", "h3attn_backward",
            "h3attn_device_status", "h3attn_set_stage_timing", "h3attn_stage_times", "h3attn_forward_static",
-           "h3attn_status_string")
+           "h3attn_linear", "h3attn_status_string")
 
 # Limits of h3attn_forward_static's built-in scratch (include/h3attn.h).
 STATIC_MAX_TOKEN_HEADS = 131072
@@ -74,6 +74,8 @@ def load_library(path: str = LIB_PATH):
     lib.h3attn_forward_static.argtypes = [ctypes.POINTER(Config), vp, vp, vp, vp, vp, ctypes.POINTER(vp), vp,
                                           i32, i32, vp, vp, vp, vp]
     lib.h3attn_forward_static.restype = i32
+    lib.h3attn_linear.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp, vp]
+    lib.h3attn_linear.restype = i32
     lib.h3attn_status_string.argtypes = [i32]
     lib.h3attn_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -213,6 +215,25 @@ def forward_static(q, k, v, q_norm_w, k_norm_w, pos, seg_offsets, num_heads=None
                                    _ptr(error_flags), _stream(stream))
     _check(st, "h3attn_forward_static")
     return out, lse
+
+
+def linear(x, w, bias=None, out=None, error_flags=None, stream=None):
+    """h3attn_linear: y = x w^T (+ bias) on the tensor cores, row-invariant.
+
+    x bf16 [rows, in], w bf16 [out, in], bias FP32 [out] or None.  ``out`` and
+    ``error_flags`` (int32 [1]) are caller-owned device tensors, created here
+    with torch when not given.  Returns y bf16 [rows, out].
+    """
+    lib = load_library()
+    rows, k = x.shape
+    n = w.shape[0]
+    if out is None:
+        out = torch.empty((rows, n), dtype=torch.bfloat16, device=x.device)
+    if error_flags is None:
+        error_flags = torch.zeros(1, dtype=torch.int32, device=x.device)
+    st = lib.h3attn_linear(_ptr(x), rows, k, _ptr(w), n, _ptr(bias), _ptr(out), _ptr(error_flags), _stream(stream))
+    _check(st, "h3attn_linear")
+    return out
 
 
 def to_device(inp, device="cuda"):

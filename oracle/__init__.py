@@ -223,3 +223,18 @@ def backward(q, k, v, q_norm_w, k_norm_w, pos, seg_offsets, dout, sections=(16, 
 
 if __name__ == "__main__":  # `python -m oracle` compiles the library
     print(build(force="--force" in sys.argv))
+
+
+def linear(x, w, bias=None, rows=None):
+    """y = x w^T (+ bias) in float64: the block's QKV / output projection either
+    side of the attention core ("ws1_one_h3_block" page of RL-Kernel, PR #539,
+    Bindings table).  x [rows, in] and w [out, in] as fed to the GPU (bf16,
+    widened exactly), bias FP32 [out] or None; ``rows`` selects output rows.
+    The product is the library matmul (numpy, float64): the definition itself."""
+    xs = _f32(x).astype(np.float64)
+    if rows is not None:
+        xs = xs[np.asarray(rows)]
+    y = xs @ _f32(w).astype(np.float64).T
+    if bias is not None:
+        y = y + _f32(bias).astype(np.float64)[None, :]
+    return y
