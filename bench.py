@@ -135,6 +135,37 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def projection_rate(S, D, stream, pk):
+    """QKV (D -> 3D) and output (D -> D) projections of S tokens with h3attn_linear
+    (synthetic bf16 activations and weights, FP32 bias), CUDA-event timed."""
+    from invariant_dit_attention_gb300.h3attn import linear
+    g = torch.Generator(device="cuda").manual_seed(7)
+    x = torch.randn(S, D, device="cuda", generator=g).to(torch.bfloat16)
+    flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+    res = {}
+    for name, n in (("qkv", 3 * D), ("out", D)):
+        w = (torch.randn(n, D, device="cuda", generator=g) / D ** 0.5).to(torch.bfloat16)
+        b = torch.randn(n, device="cuda", generator=g)
+        y = torch.empty(S, n, dtype=torch.bfloat16, device="cuda")
+        for _ in range(3):
+            linear(x, w, b, out=y, error_flags=flags)
+        reps = 5
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            linear(x, w, b, out=y, error_flags=flags)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if int(flags.item()) != 0:
+            raise RuntimeError("h3attn_linear reported a device error")
+        ms = e0.elapsed_time(e1) / reps
+        tf = 2.0 * S * D * n / (ms * 1e-3) / 1e12
+        res[name] = {"shape": [S, D, n], "ms": round(ms, 4), "tflops": round(tf, 1),
+                     "frac": round(tf / pk["bf16_tflops"], 4)}
+        del w, b, y
+    return res
+
+
 def measured_traffic(kernel_key):
     """DRAM bytes (read + write) of one launch from the committed ncu summary, or
     None if the kernel's source changed since the counters were taken."""
@@ -328,7 +359,11 @@ def run_ours(args):
     prologue = {"bound": "hbm", "achieved": round(pro_bytes / (pro_ms * 1e-3) / 1e9, 1), "peak": pk["hbm_gbs"],
                 "unit": "GB/s", "frac": round(pro_bytes / (pro_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
                 "traffic": measured_traffic("prologue"), "ms": round(pro_ms, 4)}
-    launches_per_step = 3 + 7
+    launches_per_step = 3 + 9  # forward: plan, prologue, attention; backward: plan, prologue, delta, dK/dV, dQ,
+    #                             rotary table, row backward, dw per sample, dw total
+
+    # ---- the projections either side of the path (h3attn_linear), same tokens, D = H * 128
+    projection = projection_rate(S, H * 128, stream, pk)
 
     # ---- CPU baseline: the oracle as it stands, bounded sample, rank 0 only
     cpu = None
@@ -346,7 +381,7 @@ def run_ours(args):
         "fwd_tflops_batch": round(fwd_flops / (fwd_ms / args.steps * 1e-3) / 1e12, 2) if fwd_ms else None,
         "fwd_per_sample": per_sample,
         "stages_ms_per_step": {k: round(v[0] / args.steps, 4) for k, v in stages.items()},
-        "roofline": roof, "fwd_roofline": fwd_roof, "prologue_roofline": prologue,
+        "roofline": roof, "fwd_roofline": fwd_roof, "prologue_roofline": prologue, "projection": projection,
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / args.steps, 4)},
         "gpu_launches": launches_per_step * args.steps,
