@@ -162,6 +162,8 @@ def projection_rate(S, D, stream, pk):
         tf = 2.0 * S * D * n / (ms * 1e-3) / 1e12
         res[name] = {"shape": [S, D, n], "ms": round(ms, 4), "tflops": round(tf, 1),
                      "frac": round(tf / pk["bf16_tflops"], 4)}
+        if name == "qkv":
+            res[name]["traffic"] = measured_traffic("linear_qkv")
         del w, b, y
     return res
 
@@ -246,8 +248,18 @@ def run_ours(args):
             step()
         torch.cuda.synchronize()
         h.check()
+        # then one QKV and one output projection of the same tokens (h3attn_linear)
+        from invariant_dit_attention_gb300.h3attn import linear
+        D = H * 128
+        x = torch.randn(S, D, device="cuda").to(torch.bfloat16)
+        flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+        for n in (3 * D, D):
+            w = (torch.randn(n, D, device="cuda") / D ** 0.5).to(torch.bfloat16)
+            linear(x, w, torch.randn(n, device="cuda"), error_flags=flags)
+        torch.cuda.synchronize()
         if rank == 0:
-            print(json.dumps({"profile_run": WORKLOAD, "steps": args.steps, "warmup": args.warmup}))
+            print(json.dumps({"profile_run": WORKLOAD, "steps": args.steps, "warmup": args.warmup,
+                              "then": "projections qkv, out"}))
         return
 
     # ---- device-resident timed region
