@@ -205,3 +205,19 @@ def pack(parts: list) -> Inputs:
                   torch.cat([p.v for p in parts]), parts[0].q_norm_w.clone(),
                   parts[0].k_norm_w.clone(), torch.cat([p.pos for p in parts], dim=1).contiguous(),
                   seg, dout, meta={"lengths": lengths})
+
+
+def permute_within_samples(inp: Inputs, seed: int) -> tuple:
+    """The same batch with each sample's tokens in a seeded random order: every
+    per-token input (q, k, v, positions, dout) moves with its token.  Returns
+    (permuted Inputs, sigma) with row r of the result = row sigma[r] of ``inp``."""
+    rng = np.random.default_rng(seed)
+    seg = [int(x) for x in inp.seg_offsets]
+    sigma = np.concatenate([a + rng.permutation(b - a) for a, b in zip(seg[:-1], seg[1:])]
+                           ) if len(seg) > 1 else np.zeros(0, np.int64)
+    idx = torch.from_numpy(sigma.astype(np.int64))
+    out = Inputs(inp.q[idx].contiguous(), inp.k[idx].contiguous(), inp.v[idx].contiguous(),
+                 inp.q_norm_w.clone(), inp.k_norm_w.clone(), inp.pos[:, idx].contiguous(),
+                 inp.seg_offsets.clone(), None if inp.dout is None else inp.dout[idx].contiguous(),
+                 meta=dict(inp.meta, permuted_seed=seed))
+    return out, sigma

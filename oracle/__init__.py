@@ -221,10 +221,6 @@ def backward(q, k, v, q_norm_w, k_norm_w, pos, seg_offsets, dout, sections=(16, 
             "dq_norm_w_per_sample": dwq_s[:nseg], "dk_norm_w_per_sample": dwk_s[:nseg]}
 
 
-if __name__ == "__main__":  # `python -m oracle` compiles the library
-    print(build(force="--force" in sys.argv))
-
-
 def linear(x, w, bias=None, rows=None):
     """y = x w^T (+ bias) in float64: the block's QKV / output projection either
     side of the attention core ("ws1_one_h3_block" page of RL-Kernel, PR #539,
@@ -238,3 +234,66 @@ def linear(x, w, bias=None, rows=None):
     if bias is not None:
         y = y + _f32(bias).astype(np.float64)[None, :]
     return y
+
+
+def _bf16_bits(x) -> np.ndarray:
+    """Bit patterns of a bf16 tensor (torch bfloat16, or numpy uint16 already) as
+    uint16, one row per token: [S, everything else flattened in memory order]."""
+    if hasattr(x, "detach"):
+        import torch
+        x = x.detach().cpu().contiguous()
+        if x.dtype != torch.bfloat16:
+            raise TypeError("canonical_order: bf16 tensors expected")
+        x = x.view(torch.int16).numpy().view(np.uint16)
+    x = np.ascontiguousarray(np.asarray(x))
+    if x.dtype != np.uint16:
+        raise TypeError("canonical_order: bf16 bit patterns (uint16) expected")
+    return x.reshape(x.shape[0], -1)
+
+
+def canonical_order(pos, seg_offsets, k, v, q, dout=None):
+    """Canonical order of each sample's tokens, the order in which a
+    packing-permutation-invariant attention sums keys (and queries, in the
+    backward).  The "ws1_one_h3_block" page of RL-Kernel (PR #539), Results,
+    control H-C3, reports that permuting the packed rows of a sample
+    together with their positions changes output rows because attention sums
+    keys in packed order; an order fixed by the tokens themselves settles it.
+
+    Within each sample the tokens are sorted by
+      1. their position (t, h, w), as signed integers, t first;
+      2. then their k row, v row, q row and (when given) dout row, each taken
+         over all heads in memory order and compared as a sequence of bf16 bit
+         patterns read as unsigned 16-bit integers (a total order on bits, not
+         the numeric order of the values);
+      3. then their packed index (the tokens compared equal here are identical
+         in every input, so which comes first changes no result).
+    Returns perm (int64 [S]): perm[c] is the packed index of the token in
+    canonical slot c; the slots of sample s are seg[s] .. seg[s+1]-1.
+    The content comparison only runs inside groups of equal position."""
+    pos = _i32(pos)
+    seg = [int(x) for x in _i32(seg_offsets)]
+    rows = [_bf16_bits(t) for t in (k, v, q) + ((dout,) if dout is not None else ())]
+    S = pos.shape[1]
+    perm = np.empty(S, dtype=np.int64)
+    for s in range(len(seg) - 1):
+        a, b = seg[s], seg[s + 1]
+        by_pos = sorted(range(a, b), key=lambda i: (int(pos[0, i]), int(pos[1, i]), int(pos[2, i]), i))
+        out = []
+        g = 0
+        while g < len(by_pos):
+            e = g
+            p0 = tuple(int(pos[ax, by_pos[g]]) for ax in range(3))
+            while e < len(by_pos) and tuple(int(pos[ax, by_pos[e]]) for ax in range(3)) == p0:
+                e += 1
+            group = by_pos[g:e]
+            if len(group) > 1:
+                # big-endian bytes of uint16 words compare like the words themselves
+                group = sorted(group, key=lambda i: tuple(r[i].astype(">u2").tobytes() for r in rows) + (i,))
+            out.extend(group)
+            g = e
+        perm[a:b] = out
+    return perm
+
+
+if __name__ == "__main__":  # `python -m oracle` compiles the library
+    print(build(force="--force" in sys.argv))
