@@ -168,6 +168,40 @@ def projection_rate(S, D, stream, pk):
     return res
 
 
+def canonical_rate(H, S, d, grads, step_flops, packed_ms, stream, steps=10):
+    """The same forward + backward step with the canonical key order (sums over a
+    sample's tokens in an order fixed by the tokens, not by their packing),
+    CUDA-event timed outside the headline's timed region."""
+    from invariant_dit_attention_gb300.h3attn import H3Attn
+    h = H3Attn(H, S, 8, key_order="canonical")
+
+    def step():
+        out, lse = h.forward(d["q"], d["k"], d["v"], d["q_norm_w"], d["k_norm_w"], d["pos"], d["seg_offsets"])
+        h.backward(d["q"], d["k"], d["v"], d["q_norm_w"], d["k_norm_w"], d["pos"], d["seg_offsets"],
+                   out, lse, d["dout"], grads=grads)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    h.check()
+    h.set_stage_timing(True)
+    h.stage_times()  # reset
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    st = h.stage_times()
+    h.check()
+    h.close()
+    ms = e0.elapsed_time(e1) / steps
+    return {"ms_per_step": round(ms, 4), "tflops": round(step_flops / (ms * 1e-3) / 1e12, 2),
+            "overhead_vs_packed": round(ms / packed_ms - 1.0, 4),
+            "order_ms": round(st["order"][0] / steps, 4), "permute_ms": round(st["permute"][0] / steps, 4),
+            "steps": steps}
+
+
 def measured_traffic(kernel_key):
     """DRAM bytes (read + write) of one launch from the committed ncu summary, or
     None if the kernel's source changed since the counters were taken."""
@@ -377,6 +411,9 @@ def run_ours(args):
     # ---- the projections either side of the path (h3attn_linear), same tokens, D = H * 128
     projection = projection_rate(S, H * 128, stream, pk)
 
+    # ---- the canonical key order (packing-permutation-invariant sums), same step
+    canonical = canonical_rate(H, S, d, grads, step_flops, ms_max / args.steps, stream)
+
     # ---- CPU baseline: the oracle as it stands, bounded sample, rank 0 only
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -394,6 +431,7 @@ def run_ours(args):
         "fwd_per_sample": per_sample,
         "stages_ms_per_step": {k: round(v[0] / args.steps, 4) for k, v in stages.items()},
         "roofline": roof, "fwd_roofline": fwd_roof, "prologue_roofline": prologue, "projection": projection,
+        "canonical_order": canonical,
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / args.steps, 4)},
         "gpu_launches": launches_per_step * args.steps,

@@ -73,7 +73,33 @@ typedef struct {
     float softmax_scale;   /* 0 -> 1/sqrt(128)                                          */
     int max_tokens;        /* capacity: largest total_tokens of any call                */
     int max_samples;       /* capacity: largest num_samples of any call                 */
+    int key_order;         /* H3ATTN_KEY_ORDER_PACKED (0) or H3ATTN_KEY_ORDER_CANONICAL */
 } h3attn_config;
+
+/*
+ * Order in which a call sums over a sample's tokens.
+ *
+ * PACKED: keys (forward, dq) and queries (dk, dv, weight gradients) are summed
+ * in the order the tokens sit in memory.  Results are bitwise repeatable and
+ * identical alone vs packed, but permuting a sample's rows (with their
+ * positions) changes output bits: control H-C3 in the Results of the
+ * "ws1_one_h3_block" page of RL-Kernel (PR #539).
+ *
+ * CANONICAL: every call first sorts each sample's tokens by
+ *   1. position (t, h, w) as signed integers, t first;
+ *   2. the k row, then the v row, then the q row (and in the backward the dout
+ *      row), each over all heads in memory order, as sequences of bf16 bit
+ *      patterns compared as unsigned 16-bit integers;
+ *   3. packed index (tokens equal up to here are identical in every input);
+ * gathers its per-token inputs into that order, runs the same kernels and
+ * scatters the outputs back.  Every output bit is then also independent of how
+ * each sample's tokens are permuted in memory.  Cost: an O(L^2) rank count per
+ * sample of L tokens and HBM-bound row copies (forward: q, k, v in, out back;
+ * backward: q, k, v, out, dout in, dq, dk, dv back), and eight more
+ * [max_tokens, H, 128] bf16 buffers in the workspace.
+ */
+#define H3ATTN_KEY_ORDER_PACKED 0
+#define H3ATTN_KEY_ORDER_CANONICAL 1
 
 /*
  * Creates a handle on the current CUDA device and allocates its workspace
@@ -82,8 +108,12 @@ typedef struct {
  * rotary cos/sin table, softmax row terms,
  * weight-gradient partials, a small per-call plan).  The workspace is bounded
  * by the config, never by the inputs.  *out receives the handle.
- * Errors: INVALID_ARG (null pointer, sizes < 1), UNSUPPORTED (head_dim,
- * pairing, sections, device not sm_103), CUDA (allocation failed).
+ * With key_order CANONICAL it also allocates the order's buffers: a
+ * permutation and positions (4 * max_tokens int32), row terms (H * max_tokens
+ * floats) and eight max_tokens * H * 128 bf16 row copies.
+ * Errors: INVALID_ARG (null pointer, sizes < 1, key_order not 0 or 1),
+ * UNSUPPORTED (head_dim, pairing, sections, device not sm_103), CUDA
+ * (allocation failed).
  */
 h3attn_status h3attn_create(const h3attn_config *cfg, h3attn_t *out);
 
@@ -113,6 +143,8 @@ h3attn_status h3attn_forward(h3attn_t h,
  * order); dq_norm_w_per_sample, dk_norm_w_per_sample float32 [num_samples, 128]
  * or NULL (per-sample sums; these, like dq/dk/dv, are identical whether a sample
  * runs alone or packed).  All reductions run in a fixed order, no atomics.
+ * With key_order CANONICAL the order of every sum is the canonical one (see
+ * H3ATTN_KEY_ORDER_CANONICAL), including the dout rows in the sort.
  * Errors: INVALID_ARG, CAPACITY, CUDA.
  */
 h3attn_status h3attn_backward(h3attn_t h,
@@ -138,6 +170,25 @@ h3attn_status h3attn_backward(h3attn_t h,
 h3attn_status h3attn_device_status(h3attn_t h, void *stream);
 
 /*
+ * The canonical order itself (see H3ATTN_KEY_ORDER_CANONICAL), for callers
+ * that want to store or check it; usable with a handle of either key order.
+ * Inputs as in h3attn_forward; dout (bf16 [S, H, 128]) may be NULL, and when
+ * given joins the sort after q, as in the backward.  perm: device int32
+ * [total_tokens], caller-owned, receives for every canonical slot c the packed
+ * index of the token placed there; the slots of sample s are seg_offsets[s] ..
+ * seg_offsets[s + 1] - 1, so perm only moves tokens within their sample.
+ * Integer work only: perm is exact.  total_tokens == 0 is a no-op.
+ * Errors: INVALID_ARG, CAPACITY, CUDA (host); an invalid seg_offsets array is
+ * reported by h3attn_device_status and leaves perm unspecified.
+ */
+h3attn_status h3attn_canonical_order(h3attn_t h,
+                                     const h3attn_bf16 *q, const h3attn_bf16 *k, const h3attn_bf16 *v,
+                                     const h3attn_bf16 *dout,
+                                     const int32_t *const pos_ids[3], const int32_t *seg_offsets,
+                                     int num_samples, int total_tokens,
+                                     int32_t *perm, void *stream);
+
+/*
  * Per-stage GPU time, for profiling (instrumentation; not part of the method).
  * When enabled, every launch of a stage is bracketed by CUDA events on the call's
  * stream (about 2 x 7 events per forward + backward; up to 4096 per handle,
@@ -155,7 +206,9 @@ enum {
     H3ATTN_STAGE_BWD_DQ = 5,    /* dQ (through RoPE/RMSNorm)                   */
     H3ATTN_STAGE_BWD_DW = 6,    /* fixed-order norm-weight gradient reduction  */
     H3ATTN_STAGE_BWD_ROWS = 7,  /* RoPE^-1 + RMSNorm backward of dq^, dk^ rows */
-    H3ATTN_NUM_STAGES = 8
+    H3ATTN_STAGE_ORDER = 8,     /* canonical order: rank count per sample      */
+    H3ATTN_STAGE_PERMUTE = 9,   /* canonical order: row gathers and scatters   */
+    H3ATTN_NUM_STAGES = 10
 };
 h3attn_status h3attn_set_stage_timing(h3attn_t h, int enable);
 h3attn_status h3attn_stage_times(h3attn_t h, float *total_ms, int *launches, int n_stages);
@@ -186,7 +239,9 @@ h3attn_status h3attn_stage_times(h3attn_t h, float *total_ms, int *launches, int
  * contents behind; the call clears what must start at zero.  Two calls whose
  * work overlaps on the GPU (different streams, or different host threads)
  * race on the array: serialise them.  Results are bitwise those of
- * h3attn_forward for the same inputs.
+ * h3attn_forward for the same inputs.  Only the packed key order is offered
+ * (the canonical order's row copies do not fit the static scratch):
+ * cfg->key_order != H3ATTN_KEY_ORDER_PACKED returns UNSUPPORTED.
  * Errors: INVALID_ARG, UNSUPPORTED, CAPACITY, CUDA.
  */
 #define H3ATTN_STATIC_MAX_TOKEN_HEADS 131072

@@ -1,0 +1,249 @@
+// canonical.cu -- the canonical token order and the row permutations around it.
+//
+// The attention core sums keys (forward, dQ) and queries (dK, dV, the weight
+// gradients) in the order the tokens sit in memory, so permuting a sample's
+// packed rows together with their positions changes output bits: control H-C3
+// in the Results of the "ws1_one_h3_block" page of RL-Kernel (PR #539).  With
+// the canonical key order a call first sorts each sample's tokens by
+//   1. position (t, h, w) as signed integers, t first,
+//   2. the k, v, q (and, in the backward, dout) rows, all heads in memory
+//      order, compared as sequences of bf16 bit patterns read as unsigned
+//      16-bit integers,
+//   3. packed index (tokens equal up to here are identical in every input),
+// gathers every per-token input into that order, runs the unchanged kernels
+// on the gathered copies and scatters the per-token outputs back.  The
+// gathered copies depend only on each sample's multiset of tokens, and the
+// kernels are deterministic with tiles anchored at the sample start, so every
+// output bit is independent of the packed order.
+//
+// The sort is a rank count: the rank of token i is the number of tokens of its
+// sample that come before it.  A sample of L tokens costs L^2 comparisons of a
+// 16-byte key (position plus the first two bf16 of the k row) held in shared
+// memory; equal keys fall back to comparing the rows in global memory.  The
+// permutations are plain row copies, bound by HBM bandwidth.
+#include "common.cuh"
+
+namespace h3 {
+
+namespace {
+
+constexpr int kOrdThreads = 256;
+constexpr int kOrdLanes = 8;  // threads sharing one token's comparisons
+constexpr int kOrdTokens = kOrdThreads / kOrdLanes;
+
+struct OrderArgs {
+    const int32_t* seg;
+    int n, S;
+    const int32_t* pos[3];
+    const uint4* rows[4];  // k, v, q, dout (dout may be absent)
+    int nrows;
+    int row_vecs;  // 16-byte vectors per token row: H * 128 * 2 / 16
+    int32_t* perm;
+    unsigned* err;
+};
+
+// Order-preserving map of int32 onto uint32.
+__device__ __forceinline__ uint32_t ukey(int32_t x) { return static_cast<uint32_t>(x) ^ 0x80000000u; }
+
+// Sort key of token j: position, then the first two bf16 of the k row (element
+// 0 is the low half of the first 32-bit word, so rotate it to the high half).
+__device__ __forceinline__ uint4 token_key(const OrderArgs& A, int j) {
+    const uint32_t w = reinterpret_cast<const uint32_t*>(A.rows[0] + (size_t)j * A.row_vecs)[0];
+    return make_uint4(ukey(A.pos[0][j]), ukey(A.pos[1][j]), ukey(A.pos[2][j]), (w << 16) | (w >> 16));
+}
+
+__device__ __forceinline__ int cmp_u32(uint32_t a, uint32_t b) { return a == b ? 0 : (a < b ? -1 : 1); }
+
+__device__ __forceinline__ int cmp_key(const uint4& a, const uint4& b) {
+    int c = cmp_u32(a.x, b.x);
+    if (!c) c = cmp_u32(a.y, b.y);
+    if (!c) c = cmp_u32(a.z, b.z);
+    if (!c) c = cmp_u32(a.w, b.w);
+    return c;
+}
+
+// Two bf16 in memory order: element 0 in the low half.
+__device__ __forceinline__ int cmp_pair(uint32_t a, uint32_t b) {
+    if (a == b) return 0;
+    const uint32_t al = a & 0xffffu, bl = b & 0xffffu;
+    if (al != bl) return al < bl ? -1 : 1;
+    return (a >> 16) < (b >> 16) ? -1 : 1;
+}
+
+// Rows of tokens j and i, lexicographically over k, v, q (, dout).
+__device__ int cmp_rows(const OrderArgs& A, int j, int i) {
+    for (int r = 0; r < A.nrows; ++r) {
+        const uint4* __restrict__ x = A.rows[r] + (size_t)j * A.row_vecs;
+        const uint4* __restrict__ y = A.rows[r] + (size_t)i * A.row_vecs;
+        for (int e = 0; e < A.row_vecs; ++e) {
+            const uint4 a = x[e], b = y[e];
+            int c = cmp_pair(a.x, b.x);
+            if (!c) c = cmp_pair(a.y, b.y);
+            if (!c) c = cmp_pair(a.z, b.z);
+            if (!c) c = cmp_pair(a.w, b.w);
+            if (c) return c;
+        }
+    }
+    return 0;
+}
+
+// One block ranks kOrdTokens tokens; the kOrdLanes threads of a token split
+// each chunk of keys between them and add their counts at the end.
+__global__ void __launch_bounds__(kOrdThreads) order_kernel(const __grid_constant__ OrderArgs A) {
+    __shared__ uint4 skey[kOrdThreads];
+    __shared__ int range_lo, range_hi;
+    const int tid = threadIdx.x;
+    const int lane8 = tid % kOrdLanes;
+    const int i = blockIdx.x * kOrdTokens + tid / kOrdLanes;
+    const bool act = i < A.S;
+    int a = 0, b = 0;
+    if (act) {  // sample of token i: the last s with seg[s] <= i
+        int lo = 0, hi = A.n;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (A.seg[mid] <= i) lo = mid; else hi = mid;
+        }
+        a = max(A.seg[lo], 0);
+        b = min(A.seg[lo + 1], A.S);
+    }
+    const bool ok = act && a <= i && i < b;
+    if (tid == 0) { range_lo = A.S; range_hi = 0; }
+    __syncthreads();
+    if (ok && lane8 == 0) { atomicMin(&range_lo, a); atomicMax(&range_hi, b); }
+    __syncthreads();
+    const int J0 = range_lo, J1 = range_hi;
+    const uint4 mine = ok ? token_key(A, i) : make_uint4(0, 0, 0, 0);
+    int rank = 0;
+    for (int j0 = J0; j0 < J1; j0 += kOrdThreads) {
+        if (j0 + tid < J1) skey[tid] = token_key(A, j0 + tid);
+        __syncthreads();
+        if (ok) {
+            const int e0 = max(a - j0, 0), e1 = min(b - j0, min(kOrdThreads, J1 - j0));
+            for (int e = e0 + ((lane8 - e0) % kOrdLanes + kOrdLanes) % kOrdLanes; e < e1; e += kOrdLanes) {
+                int c = cmp_key(skey[e], mine);
+                const int j = j0 + e;
+                if (c == 0 && j != i) {
+                    c = cmp_rows(A, j, i);
+                    if (c == 0) c = j < i ? -1 : 1;
+                }
+                rank += c < 0;
+            }
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int o = kOrdLanes / 2; o; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+    if (act && lane8 == 0) {
+        if (!ok) {
+            atomicOr(A.err, kErrBadOffsets);
+        } else if (a + rank < b) {
+            A.perm[a + rank] = i;
+        } else {
+            atomicOr(A.err, kErrBadOffsets);
+        }
+    }
+}
+
+constexpr int kPermWarps = 8;
+constexpr int kMaxPermTensors = 6;
+
+struct PermArgs {
+    const uint4* src[kMaxPermTensors];
+    uint4* dst[kMaxPermTensors];
+};
+
+// Row c of the canonical copy <-> row perm[c] of the packed tensor; one warp
+// per (row, tensor).  A perm value outside [0, S) (only after bad offsets)
+// is reported and skipped.
+__global__ void __launch_bounds__(kPermWarps * 32)
+permute_rows_kernel(const __grid_constant__ PermArgs P, const int32_t* __restrict__ perm, int S, int row_vecs, int scatter, unsigned* err) {
+    const int lane = threadIdx.x & 31;
+    const int c = blockIdx.x * kPermWarps + (threadIdx.x >> 5);
+    if (c >= S) return;
+    const int t = perm[c];
+    if (t < 0 || t >= S) {
+        if (lane == 0) atomicOr(err, kErrBadOffsets);
+        return;
+    }
+    const size_t from = (size_t)(scatter ? c : t) * row_vecs, to = (size_t)(scatter ? t : c) * row_vecs;
+    const uint4* __restrict__ s = P.src[blockIdx.y] + from;
+    uint4* __restrict__ d = P.dst[blockIdx.y] + to;
+#pragma unroll 4
+    for (int e = lane; e < row_vecs; e += 32) d[e] = __ldcs(s + e);
+}
+
+// The [H, S] softmax row terms (gather or scatter) and, when gathering, the
+// three position rows.
+__global__ void __launch_bounds__(256)
+permute_small_kernel(const int32_t* __restrict__ perm, int S, int H, const float* __restrict__ lse_src,
+                     float* __restrict__ lse_dst, const int32_t* p0, const int32_t* p1, const int32_t* p2,
+                     int32_t* d0, int32_t* d1, int32_t* d2, int scatter) {
+    const long total = (long)(H + 1) * S;
+    for (long x = blockIdx.x * (long)blockDim.x + threadIdx.x; x < total; x += (long)gridDim.x * blockDim.x) {
+        const int r = (int)(x / S), c = (int)(x % S);
+        const int t = perm[c];
+        if (t < 0 || t >= S) continue;  // reported by permute_rows_kernel
+        if (r < H) {
+            if (lse_src) {
+                if (scatter) lse_dst[(size_t)r * S + t] = lse_src[(size_t)r * S + c];
+                else lse_dst[(size_t)r * S + c] = lse_src[(size_t)r * S + t];
+            }
+        } else if (d0) {
+            d0[c] = p0[t];
+            d1[c] = p1[t];
+            d2[c] = p2[t];
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_order(const Problem& p, const __nv_bfloat16* dout, int32_t* perm, unsigned* err, cudaStream_t st) {
+    if (p.seq.S == 0) return cudaSuccess;
+    OrderArgs A;
+    A.seg = p.seq.seg;
+    A.n = p.seq.n;
+    A.S = p.seq.S;
+    A.pos[0] = p.seq.pos_t;
+    A.pos[1] = p.seq.pos_h;
+    A.pos[2] = p.seq.pos_w;
+    A.rows[0] = reinterpret_cast<const uint4*>(p.k);
+    A.rows[1] = reinterpret_cast<const uint4*>(p.v);
+    A.rows[2] = reinterpret_cast<const uint4*>(p.q);
+    A.rows[3] = reinterpret_cast<const uint4*>(dout);
+    A.nrows = dout ? 4 : 3;
+    A.row_vecs = p.H * kD * 2 / 16;
+    A.perm = perm;
+    A.err = err;
+    order_kernel<<<(p.seq.S + kOrdTokens - 1) / kOrdTokens, kOrdThreads, 0, st>>>(A);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_permute(const int32_t* perm, int S, int H, int ntensors, const void* const* src, void* const* dst,
+                           const float* lse_src, float* lse_dst, const int32_t* const pos_src[3], int32_t* pos_dst[3],
+                           bool scatter, unsigned* err, cudaStream_t st) {
+    if (S == 0) return cudaSuccess;
+    if (ntensors < 0 || ntensors > kMaxPermTensors) return cudaErrorInvalidValue;
+    if (ntensors > 0) {
+        PermArgs P;
+        for (int t = 0; t < kMaxPermTensors; ++t) {
+            P.src[t] = t < ntensors ? static_cast<const uint4*>(src[t]) : nullptr;
+            P.dst[t] = t < ntensors ? static_cast<uint4*>(dst[t]) : nullptr;
+        }
+        dim3 grid((S + kPermWarps - 1) / kPermWarps, ntensors);
+        permute_rows_kernel<<<grid, kPermWarps * 32, 0, st>>>(P, perm, S, H * kD * 2 / 16, scatter ? 1 : 0, err);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    const bool pos = pos_src && pos_dst && !scatter;
+    if (!lse_src && !pos) return cudaSuccess;
+    const long total = (long)(H + 1) * S;
+    const int blocks = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
+    permute_small_kernel<<<blocks, 256, 0, st>>>(perm, S, H, lse_src, lse_dst, pos ? pos_src[0] : nullptr,
+                                                 pos ? pos_src[1] : nullptr, pos ? pos_src[2] : nullptr,
+                                                 pos ? pos_dst[0] : nullptr, pos ? pos_dst[1] : nullptr,
+                                                 pos ? pos_dst[2] : nullptr, scatter ? 1 : 0);
+    return cudaGetLastError();
+}
+
+}  // namespace h3

@@ -198,6 +198,11 @@ struct Workspace {
     float* dwq_sample;       // [max_samples, 128]
     float* dwk_sample;       // [max_samples, 128]
     Plan plan;
+    // canonical key order only (null otherwise)
+    int32_t* perm;           // [max_tokens] packed index of canonical slot c
+    int32_t* pos_c;          // [3, max_tokens] positions in canonical order
+    float* lse_c;            // [H, max_tokens] softmax row terms in canonical order
+    __nv_bfloat16* rows_c[8];  // [max_tokens, H, 128] each: q, k, v, out, dout, dq, dk, dv in canonical order
 };
 
 struct Problem {
@@ -214,7 +219,8 @@ struct Problem {
 
 // Stages of one call, in launch order (timed separately when stage timing is on).
 // Values match the h3attn_stage enum of the C ABI.
-enum Stage { kStagePlan = 0, kStagePrologue, kStageFwd, kStageDelta, kStageDkdv, kStageDq, kStageDw, kStageRows, kStages };
+enum Stage { kStagePlan = 0, kStagePrologue, kStageFwd, kStageDelta, kStageDkdv, kStageDq, kStageDw, kStageRows,
+             kStageOrder, kStagePermute, kStages };
 
 cudaError_t init_fwd_tc();
 cudaError_t init_bwd_attributes();
@@ -229,6 +235,13 @@ cudaError_t launch_bwd_dq(const Problem& p, const Workspace& ws, const float* ls
                           const __nv_bfloat16* dout, __nv_bfloat16* dq, cudaStream_t st);
 cudaError_t launch_bwd_rows(const Problem& p, const Workspace& ws, const RopeTable* rope, __nv_bfloat16* dq,
                             __nv_bfloat16* dk, cudaStream_t st);
+cudaError_t launch_order(const Problem& p, const __nv_bfloat16* dout, int32_t* perm, unsigned* err, cudaStream_t st);
+// Gather (canonical copy row c <- packed row perm[c]) or scatter (the reverse) of
+// up to six [S, H, 128] bf16 tensors, the [H, S] row terms (either may be
+// absent) and, gathering only, the three position rows.
+cudaError_t launch_permute(const int32_t* perm, int S, int H, int ntensors, const void* const* src, void* const* dst,
+                           const float* lse_src, float* lse_dst, const int32_t* const pos_src[3], int32_t* pos_dst[3],
+                           bool scatter, unsigned* err, cudaStream_t st);
 cudaError_t launch_bwd_dw(const Problem& p, const Workspace& ws, float* dwq, float* dwk, float* dwq_s,
                           float* dwk_s, cudaStream_t st);
 

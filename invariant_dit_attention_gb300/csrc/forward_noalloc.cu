@@ -90,7 +90,8 @@ extern "C" h3attn_status h3attn_forward_static(const h3attn_config* cfg, const h
     if (!cfg) return H3ATTN_ERR_INVALID_ARG;
     if (cfg->num_heads < 1 || !(cfg->eps >= 0.f) || !(cfg->rope_theta > 0.f) || !(cfg->softmax_scale >= 0.f))
         return H3ATTN_ERR_INVALID_ARG;
-    if (cfg->head_dim != kD || cfg->rope_pairing != 0) return H3ATTN_ERR_UNSUPPORTED;
+    if (cfg->head_dim != kD || cfg->rope_pairing != 0 || cfg->key_order != H3ATTN_KEY_ORDER_PACKED)
+        return H3ATTN_ERR_UNSUPPORTED;
     RopeTable rt;
     if (!build_rope_table(*cfg, rt)) return H3ATTN_ERR_UNSUPPORTED;
     if (total_tokens < 0 || num_samples < 0) return H3ATTN_ERR_INVALID_ARG;

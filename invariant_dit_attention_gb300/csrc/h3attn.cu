@@ -21,7 +21,7 @@ struct h3attn_ctx {
     Workspace ws;
     int max_tiles64;
     unsigned* host_err;  // pinned
-    void* allocs[24];
+    void* allocs[40];
     int nalloc;
     // stage timing (instrumentation)
     int timing;
@@ -63,6 +63,7 @@ h3attn_status build_rope(const h3attn_config& c, RopeTable& rt) {
 template <class T>
 bool ws_alloc(h3attn_ctx* h, T** p, size_t bytes) {
     void* d = nullptr;
+    if (h->nalloc >= (int)(sizeof h->allocs / sizeof h->allocs[0])) return false;
     if (cudaMalloc(&d, bytes < 256 ? 256 : bytes) != cudaSuccess) return false;
     h->allocs[h->nalloc++] = d;
     *p = reinterpret_cast<T*>(d);
@@ -118,6 +119,19 @@ Problem make_problem(h3attn_t h, const void* q, const void* k, const void* v, co
     return p;
 }
 
+// The problem on the canonical copies: same samples, gathered rows and positions.
+Problem canonical_problem(h3attn_t h, const Problem& p) {
+    Problem c = p;
+    const Workspace& ws = h->ws;
+    c.q = ws.rows_c[0];
+    c.k = ws.rows_c[1];
+    c.v = ws.rows_c[2];
+    c.seq.pos_t = ws.pos_c;
+    c.seq.pos_h = ws.pos_c + h->cfg.max_tokens;
+    c.seq.pos_w = ws.pos_c + 2 * (size_t)h->cfg.max_tokens;
+    return c;
+}
+
 // Runs one stage's launches, bracketed by events when stage timing is on.
 template <class F>
 cudaError_t stage(h3attn_ctx* h, int which, cudaStream_t s, F&& launch) {
@@ -154,6 +168,8 @@ h3attn_status h3attn_create(const h3attn_config* cfg, h3attn_t* out) {
     *out = nullptr;
     if (cfg->num_heads < 1 || cfg->max_tokens < 1 || cfg->max_samples < 1) return H3ATTN_ERR_INVALID_ARG;
     if (!(cfg->eps >= 0.f) || !(cfg->rope_theta > 0.f) || !(cfg->softmax_scale >= 0.f)) return H3ATTN_ERR_INVALID_ARG;
+    if (cfg->key_order != H3ATTN_KEY_ORDER_PACKED && cfg->key_order != H3ATTN_KEY_ORDER_CANONICAL)
+        return H3ATTN_ERR_INVALID_ARG;
     if (cfg->head_dim != kD || cfg->rope_pairing != 0) return H3ATTN_ERR_UNSUPPORTED;
     if ((long)cfg->max_tokens * cfg->num_heads * kD >= (1L << 40)) return H3ATTN_ERR_CAPACITY;
     RopeTable rt;
@@ -183,6 +199,10 @@ h3attn_status h3attn_create(const h3attn_config* cfg, h3attn_t* out) {
               ws_alloc(h, &ws.plan.cum64, (N + 1) * 4) && ws_alloc(h, &ws.plan.cum128, (N + 1) * 4) &&
               ws_alloc(h, &ws.plan.cum256, (N + 1) * 4) &&
               ws_alloc(h, &ws.plan.err, 4);
+    if (ok && cfg->key_order == H3ATTN_KEY_ORDER_CANONICAL) {
+        ok = ws_alloc(h, &ws.perm, T * 4) && ws_alloc(h, &ws.pos_c, 3 * T * 4) && ws_alloc(h, &ws.lse_c, T * H * 4);
+        for (int t = 0; ok && t < 8; ++t) ok = ws_alloc(h, &ws.rows_c[t], T * H * kD * 2);
+    }
     if (ok) ok = cudaMemset(ws.plan.err, 0, 4) == cudaSuccess;
     if (ok) ok = cudaMallocHost(&h->host_err, 4) == cudaSuccess;
     if (ok) ok = init_fwd_tc() == cudaSuccess && init_bwd_attributes() == cudaSuccess;
@@ -213,6 +233,30 @@ h3attn_status h3attn_forward(h3attn_t h, const h3attn_bf16* q, const h3attn_bf16
     Problem p = make_problem(h, q, k, v, q_norm_w, k_norm_w, pos_ids, seg_offsets, num_samples, total_tokens);
     Workspace& ws = h->ws;
     __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out);
+    if (h->cfg.key_order == H3ATTN_KEY_ORDER_CANONICAL) {
+        const Problem c = canonical_problem(h, p);
+        const int S = total_tokens, H = p.H;
+        const void* gsrc[3] = {q, k, v};
+        void* gdst[3] = {ws.rows_c[0], ws.rows_c[1], ws.rows_c[2]};
+        const int32_t* psrc[3] = {p.seq.pos_t, p.seq.pos_h, p.seq.pos_w};
+        int32_t* pdst[3] = {const_cast<int32_t*>(c.seq.pos_t), const_cast<int32_t*>(c.seq.pos_h),
+                            const_cast<int32_t*>(c.seq.pos_w)};
+        const void* ssrc[1] = {ws.rows_c[3]};
+        void* sdst[1] = {out};
+        float* lc = lse ? ws.lse_c : nullptr;
+        if (stage(h, kStagePlan, s, [&] { return launch_plan(p, ws, s); }) != cudaSuccess ||
+            stage(h, kStageOrder, s, [&] { return launch_order(p, nullptr, ws.perm, ws.plan.err, s); }) != cudaSuccess ||
+            stage(h, kStagePermute, s, [&] {
+                return launch_permute(ws.perm, S, H, 3, gsrc, gdst, nullptr, nullptr, psrc, pdst, false, ws.plan.err, s);
+            }) != cudaSuccess ||
+            stage(h, kStagePrologue, s, [&] { return launch_prologue(c, ws, &h->rope, s); }) != cudaSuccess ||
+            stage(h, kStageFwd, s, [&] { return launch_fwd(c, ws, ws.rows_c[3], lc, s); }) != cudaSuccess ||
+            stage(h, kStagePermute, s, [&] {
+                return launch_permute(ws.perm, S, H, 1, ssrc, sdst, lc, lse, nullptr, nullptr, true, ws.plan.err, s);
+            }) != cudaSuccess)
+            return H3ATTN_ERR_CUDA;
+        return H3ATTN_OK;
+    }
     if (stage(h, kStagePlan, s, [&] { return launch_plan(p, ws, s); }) != cudaSuccess ||
         stage(h, kStagePrologue, s, [&] { return launch_prologue(p, ws, &h->rope, s); }) != cudaSuccess ||
         stage(h, kStageFwd, s, [&] { return launch_fwd(p, ws, o, lse, s); }) != cudaSuccess)
@@ -248,6 +292,38 @@ h3attn_status h3attn_backward(h3attn_t h, const h3attn_bf16* q, const h3attn_bf1
     __nv_bfloat16* gq = reinterpret_cast<__nv_bfloat16*>(dq);
     __nv_bfloat16* gk = reinterpret_cast<__nv_bfloat16*>(dk);
     __nv_bfloat16* gv = reinterpret_cast<__nv_bfloat16*>(dv);
+    if (h->cfg.key_order == H3ATTN_KEY_ORDER_CANONICAL) {
+        const Problem c = canonical_problem(h, p);
+        const int S = total_tokens, H = p.H;
+        const void* gsrc[5] = {q, k, v, out, dout};
+        void* gdst[5] = {ws.rows_c[0], ws.rows_c[1], ws.rows_c[2], ws.rows_c[3], ws.rows_c[4]};
+        const int32_t* psrc[3] = {p.seq.pos_t, p.seq.pos_h, p.seq.pos_w};
+        int32_t* pdst[3] = {const_cast<int32_t*>(c.seq.pos_t), const_cast<int32_t*>(c.seq.pos_h),
+                            const_cast<int32_t*>(c.seq.pos_w)};
+        const void* ssrc[3] = {ws.rows_c[5], ws.rows_c[6], ws.rows_c[7]};
+        void* sdst[3] = {dq, dk, dv};
+        __nv_bfloat16 *oc = ws.rows_c[3], *doc = ws.rows_c[4];
+        __nv_bfloat16 *dqc = ws.rows_c[5], *dkc = ws.rows_c[6], *dvc = ws.rows_c[7];
+        if (stage(h, kStagePlan, s, [&] { return launch_plan(p, ws, s); }) != cudaSuccess ||
+            stage(h, kStageOrder, s, [&] { return launch_order(p, dO, ws.perm, ws.plan.err, s); }) != cudaSuccess ||
+            stage(h, kStagePermute, s, [&] {
+                return launch_permute(ws.perm, S, H, 5, gsrc, gdst, lse, ws.lse_c, psrc, pdst, false, ws.plan.err, s);
+            }) != cudaSuccess ||
+            stage(h, kStagePrologue, s, [&] { return launch_prologue(c, ws, &h->rope, s); }) != cudaSuccess ||
+            stage(h, kStageDelta, s, [&] { return launch_bwd_delta(c, ws, oc, doc, s); }) != cudaSuccess ||
+            stage(h, kStageDkdv, s, [&] { return launch_bwd_dkdv(c, ws, ws.lse_c, doc, dkc, dvc, s); }) != cudaSuccess ||
+            stage(h, kStageDq, s, [&] { return launch_bwd_dq(c, ws, ws.lse_c, doc, dqc, s); }) != cudaSuccess ||
+            stage(h, kStageRows, s, [&] { return launch_bwd_rows(c, ws, &h->rope, dqc, dkc, s); }) != cudaSuccess ||
+            stage(h, kStageDw, s, [&] {
+                return launch_bwd_dw(c, ws, dq_norm_w, dk_norm_w, dq_norm_w_per_sample, dk_norm_w_per_sample, s);
+            }) != cudaSuccess ||
+            stage(h, kStagePermute, s, [&] {
+                return launch_permute(ws.perm, S, H, 3, ssrc, sdst, nullptr, nullptr, nullptr, nullptr, true,
+                                      ws.plan.err, s);
+            }) != cudaSuccess)
+            return H3ATTN_ERR_CUDA;
+        return H3ATTN_OK;
+    }
     if (stage(h, kStagePlan, s, [&] { return launch_plan(p, ws, s); }) != cudaSuccess ||
         stage(h, kStagePrologue, s, [&] { return launch_prologue(p, ws, &h->rope, s); }) != cudaSuccess ||
         stage(h, kStageDelta, s, [&] { return launch_bwd_delta(p, ws, o, dO, s); }) != cudaSuccess ||
@@ -257,6 +333,30 @@ h3attn_status h3attn_backward(h3attn_t h, const h3attn_bf16* q, const h3attn_bf1
         stage(h, kStageDw, s, [&] {
             return launch_bwd_dw(p, ws, dq_norm_w, dk_norm_w, dq_norm_w_per_sample, dk_norm_w_per_sample, s);
         }) != cudaSuccess)
+        return H3ATTN_ERR_CUDA;
+    return H3ATTN_OK;
+}
+
+h3attn_status h3attn_canonical_order(h3attn_t h, const h3attn_bf16* q, const h3attn_bf16* k, const h3attn_bf16* v,
+                                     const h3attn_bf16* dout, const int32_t* const pos_ids[3],
+                                     const int32_t* seg_offsets, int num_samples, int total_tokens, int32_t* perm,
+                                     void* stream) {
+    if (!h) return H3ATTN_ERR_INVALID_ARG;
+    if (total_tokens < 0 || num_samples < 0) return H3ATTN_ERR_INVALID_ARG;
+    if (total_tokens == 0) return H3ATTN_OK;
+    if (num_samples < 1 || num_samples > total_tokens) return H3ATTN_ERR_INVALID_ARG;
+    if (total_tokens > h->cfg.max_tokens || num_samples > h->cfg.max_samples) return H3ATTN_ERR_CAPACITY;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || (dout && !aligned16(dout)) || !aligned4(perm))
+        return H3ATTN_ERR_INVALID_ARG;
+    if (!pos_ids || !aligned4(pos_ids[0]) || !aligned4(pos_ids[1]) || !aligned4(pos_ids[2]) || !aligned4(seg_offsets))
+        return H3ATTN_ERR_INVALID_ARG;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return H3ATTN_ERR_CUDA;
+    if (dev != h->device) return H3ATTN_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const Problem p = make_problem(h, q, k, v, nullptr, nullptr, pos_ids, seg_offsets, num_samples, total_tokens);
+    if (launch_plan(p, h->ws, s) != cudaSuccess ||
+        launch_order(p, reinterpret_cast<const __nv_bfloat16*>(dout), perm, h->ws.plan.err, s) != cudaSuccess)
         return H3ATTN_ERR_CUDA;
     return H3ATTN_OK;
 }

@@ -22,13 +22,16 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CAPACITY, ERR_CUDA, ERR_TIMEOUT = rang
 # Entry points declared in include/h3attn.h.
 EXPORTS = ("h3attn_create", "h3attn_destroy", "h3attn_forward", "h3attn_backward",
            "h3attn_device_status", "h3attn_set_stage_timing", "h3attn_stage_times", "h3attn_forward_static",
-           "h3attn_linear", "h3attn_status_string")
+           "h3attn_linear", "h3attn_canonical_order", "h3attn_status_string")
 
 # Limits of h3attn_forward_static's built-in scratch (include/h3attn.h).
 STATIC_MAX_TOKEN_HEADS = 131072
 STATIC_MAX_SAMPLES = 2048
 
-STAGES = ("plan", "prologue", "fwd", "bwd_delta", "bwd_dkdv", "bwd_dq", "bwd_dw", "bwd_rows")
+STAGES = ("plan", "prologue", "fwd", "bwd_delta", "bwd_dkdv", "bwd_dq", "bwd_dw", "bwd_rows", "order", "permute")
+
+# Key orders (include/h3attn.h, H3ATTN_KEY_ORDER_*).
+KEY_ORDERS = {"packed": 0, "canonical": 1}
 
 
 class H3AttnError(RuntimeError):
@@ -41,7 +44,7 @@ class Config(ctypes.Structure):
     _fields_ = [("num_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("eps", ctypes.c_float),
                 ("rope_theta", ctypes.c_float), ("rope_sections", ctypes.c_int * 3),
                 ("rope_pairing", ctypes.c_int), ("softmax_scale", ctypes.c_float),
-                ("max_tokens", ctypes.c_int), ("max_samples", ctypes.c_int)]
+                ("max_tokens", ctypes.c_int), ("max_samples", ctypes.c_int), ("key_order", ctypes.c_int)]
 
 
 _lib = None
@@ -76,6 +79,8 @@ def load_library(path: str = LIB_PATH):
     lib.h3attn_forward_static.restype = i32
     lib.h3attn_linear.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp, vp]
     lib.h3attn_linear.restype = i32
+    lib.h3attn_canonical_order.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(vp), vp, i32, i32, vp, vp]
+    lib.h3attn_canonical_order.restype = i32
     lib.h3attn_status_string.argtypes = [i32]
     lib.h3attn_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -111,19 +116,27 @@ class H3Attn:
     """A handle of the library: configuration plus its bounded device workspace."""
 
     def __init__(self, num_heads: int, max_tokens: int, max_samples: int = 64, eps: float = 1e-6,
-                 rope_theta: float = 10000.0, rope_sections=(16, 24, 24), softmax_scale: float = 0.0):
+                 rope_theta: float = 10000.0, rope_sections=(16, 24, 24), softmax_scale: float = 0.0,
+                 key_order: str = "packed"):
+        """``key_order``: "packed" sums over a sample's tokens in memory order,
+        "canonical" in an order fixed by the tokens themselves, so that results
+        do not depend on how each sample's tokens are permuted."""
         lib = load_library()
+        if key_order not in KEY_ORDERS:
+            raise ValueError(f"key_order must be one of {sorted(KEY_ORDERS)}")
         cfg = Config()
         cfg.num_heads, cfg.head_dim, cfg.eps, cfg.rope_theta = num_heads, 128, eps, rope_theta
         cfg.rope_sections[:] = list(rope_sections)
         cfg.rope_pairing, cfg.softmax_scale = 0, softmax_scale
         cfg.max_tokens, cfg.max_samples = max_tokens, max_samples
+        cfg.key_order = KEY_ORDERS[key_order]
         h = ctypes.c_void_p()
         _check(lib.h3attn_create(ctypes.byref(cfg), ctypes.byref(h)), "h3attn_create")
         self._h = h
         self._lib = lib
         self.num_heads = num_heads
         self.scale = softmax_scale if softmax_scale else 1.0 / math.sqrt(128)
+        self.key_order = key_order
 
     def close(self):
         if getattr(self, "_h", None) is not None and self._h.value:
@@ -173,6 +186,18 @@ class H3Attn:
         _check(st, "h3attn_backward")
         return grads
 
+    def canonical_order(self, q, k, v, pos, seg_offsets, dout=None, num_samples=None, perm=None, stream=None):
+        """h3attn_canonical_order: int32 [S] device tensor, perm[c] = packed index
+        of the token in canonical slot c (dout joins the sort when given)."""
+        S = q.shape[0]
+        n = int(seg_offsets.numel() - 1) if num_samples is None else num_samples
+        if perm is None:
+            perm = torch.empty(S, dtype=torch.int32, device=q.device)
+        st = self._lib.h3attn_canonical_order(self._h, _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _pos_array(pos),
+                                              _ptr(seg_offsets), n, S, _ptr(perm), _stream(stream))
+        _check(st, "h3attn_canonical_order")
+        return perm
+
     def set_stage_timing(self, enable: bool):
         _check(self._lib.h3attn_set_stage_timing(self._h, 1 if enable else 0), "h3attn_set_stage_timing")
 
@@ -207,6 +232,7 @@ def forward_static(q, k, v, q_norm_w, k_norm_w, pos, seg_offsets, num_heads=None
     cfg.num_heads, cfg.head_dim, cfg.eps, cfg.rope_theta = H, 128, eps, rope_theta
     cfg.rope_sections[:] = list(rope_sections)
     cfg.rope_pairing, cfg.softmax_scale, cfg.max_tokens, cfg.max_samples = 0, softmax_scale, 0, 0
+    cfg.key_order = KEY_ORDERS["packed"]
     n = int(seg_offsets.numel() - 1) if num_samples is None else num_samples
     if out is None:
         out = torch.empty_like(q)
