@@ -94,9 +94,10 @@ typedef struct {
  * gathers its per-token inputs into that order, runs the same kernels and
  * scatters the outputs back.  Every output bit is then also independent of how
  * each sample's tokens are permuted in memory.  Cost: an O(L^2) rank count per
- * sample of L tokens and HBM-bound row copies (forward: q, k, v in, out back;
- * backward: q, k, v, out, dout in, dq, dk, dv back), and eight more
- * [max_tokens, H, 128] bf16 buffers in the workspace.
+ * sample of L tokens and HBM-bound row copies (forward: v in, out back;
+ * backward: v, dout in, dv back; q, k, out, dq and dk are read or written in
+ * place through the order), and four more [max_tokens, H, 128] bf16 buffers in
+ * the workspace.
  */
 #define H3ATTN_KEY_ORDER_PACKED 0
 #define H3ATTN_KEY_ORDER_CANONICAL 1
@@ -106,11 +107,12 @@ typedef struct {
  * (rotated q^/k^ buffers of max_tokens * H * 128 fp16 each, the backward's FP32
  * dq^/dk^ rows of max_tokens * H * 128 floats each, a max_tokens * 256-float
  * rotary cos/sin table, softmax row terms,
- * weight-gradient partials, a small per-call plan).  The workspace is bounded
- * by the config, never by the inputs.  *out receives the handle.
- * With key_order CANONICAL it also allocates the order's buffers: a
- * permutation and positions (4 * max_tokens int32), row terms (H * max_tokens
- * floats) and eight max_tokens * H * 128 bf16 row copies.
+ * weight-gradient partials, a small per-call plan, 16 bytes of sort key per
+ * token for the canonical order).  The workspace is bounded by the config,
+ * never by the inputs.  *out receives the handle.  With
+ * key_order CANONICAL it also allocates the order's buffers: a permutation and
+ * positions (4 * max_tokens int32), row terms (H * max_tokens floats) and four
+ * max_tokens * H * 128 bf16 row copies.
  * Errors: INVALID_ARG (null pointer, sizes < 1, key_order not 0 or 1),
  * UNSUPPORTED (head_dim, pairing, sections, device not sm_103), CUDA
  * (allocation failed).

@@ -17,12 +17,14 @@ namespace h3 {
 
 __global__ void __launch_bounds__(256) delta_kernel(const __nv_bfloat16* __restrict__ out,
                                                     const __nv_bfloat16* __restrict__ dout, int S, int H,
-                                                    float* __restrict__ delta) {
+                                                    const int32_t* __restrict__ out_map, float* __restrict__ delta) {
     const int lane = threadIdx.x & 31;
     const long row = (long)blockIdx.x * 8 + (threadIdx.x >> 5);  // (token, head)
     if (row >= (long)S * H) return;
+    // out is read through the canonical order's map (its packed row), dout is not
+    const long orow = out_map ? (long)out_map[row / H] * H + row % H : row;
     float o[4], d[4];
-    load_row4(out + row * kD + 4 * lane, o);
+    load_row4(out + orow * kD + 4 * lane, o);
     load_row4(dout + row * kD + 4 * lane, d);
     float acc = o[0] * d[0] + o[1] * d[1] + o[2] * d[2] + o[3] * d[3];
     acc = warp_sum(acc);
@@ -37,6 +39,7 @@ struct RowsParams {
     int H;
     float eps;
     const float* rope_cs;          // [S][cos 128 | sin 128] per token
+    const int32_t* rowmap;         // canonical order: packed row of x and dx (null = identity)
     const float* dyhat[2];         // scale * dq^, scale * dk^: FP32 [S, H, 128]
     const __nv_bfloat16* x[2];     // raw q, k
     const float* w[2];             // q_norm_w, k_norm_w
@@ -99,7 +102,8 @@ rows_bwd_kernel(const __grid_constant__ RopeTable rt, const RowsParams p) {
             const size_t off = ((size_t)row * p.H + h) * kD + 4 * lane;
             const float4 d4 = *reinterpret_cast<const float4*>(dyhat + off);
             dy[u][0] = d4.x; dy[u][1] = d4.y; dy[u][2] = d4.z; dy[u][3] = d4.w;
-            load_row4(x + off, xr[u]);
+            const size_t xoff = p.rowmap ? ((size_t)p.rowmap[row] * p.H + h) * kD + 4 * lane : off;
+            load_row4(x + xoff, xr[u]);
             const float4 c4 = *reinterpret_cast<const float4*>(p.rope_cs + (size_t)row * 2 * kD + 4 * lane);
             const float4 s4 = *reinterpret_cast<const float4*>(p.rope_cs + (size_t)row * 2 * kD + kD + 4 * lane);
             a[u].c[0] = c4.x; a[u].c[1] = c4.y; a[u].c[2] = c4.z; a[u].c[3] = c4.w;
@@ -112,7 +116,8 @@ rows_bwd_kernel(const __grid_constant__ RopeTable rt, const RowsParams p) {
             float d[4];
             row_norm_rope_bwd(dy[u], xr[u], wl, a[u], lr, p.eps, d, acc);
             nonfinite |= !(isfinite(d[0]) && isfinite(d[1]) && isfinite(d[2]) && isfinite(d[3]));
-            store_row4(dx + ((size_t)(row0 + r) * p.H + h) * kD + 4 * lane, d);
+            const size_t orow = p.rowmap ? (size_t)p.rowmap[row0 + r] : (size_t)(row0 + r);
+            store_row4(dx + (orow * p.H + h) * kD + 4 * lane, d);
         }
     }
     // a non-finite gradient row from finite inputs means an fp16 operand (dS) overflowed
@@ -173,7 +178,7 @@ __global__ void dw_total_kernel(const float* __restrict__ dwq_s, const float* __
 cudaError_t launch_bwd_delta(const Problem& p, const Workspace& ws, const __nv_bfloat16* out,
                              const __nv_bfloat16* dout, cudaStream_t st) {
     const long rows = (long)p.seq.S * p.H;
-    delta_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(out, dout, p.seq.S, p.H, ws.delta);
+    delta_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(out, dout, p.seq.S, p.H, p.rowmap, ws.delta);
     return cudaGetLastError();
 }
 
@@ -195,6 +200,7 @@ cudaError_t launch_bwd_rows(const Problem& p, const Workspace& ws, const RopeTab
     r.dw_part[0] = ws.dwq_part;
     r.dw_part[1] = ws.dwk_part;
     r.rope_cs = ws.rope_cs;
+    r.rowmap = p.rowmap;
     const long cells = (long)p.seq.S * kD;
     rope_table_kernel<<<(unsigned)((cells + 255) / 256), 256, 0, st>>>(*rope, p.seq, ws.rope_cs);
     // an upper bound of the 128-token tiles (every sample adds at most one partial

@@ -10,17 +10,20 @@
 //      order, compared as sequences of bf16 bit patterns read as unsigned
 //      16-bit integers,
 //   3. packed index (tokens equal up to here are identical in every input),
-// gathers every per-token input into that order, runs the unchanged kernels
-// on the gathered copies and scatters the per-token outputs back.  The
-// gathered copies depend only on each sample's multiset of tokens, and the
-// kernels are deterministic with tiles anchored at the sample start, so every
-// output bit is independent of the packed order.
+// runs the same kernels on the tokens in that order (gathering or mapping each
+// per-token input) and scatters the per-token outputs back.  What the kernels
+// see then depends only on each sample's multiset of tokens, and they are
+// deterministic with tiles anchored at the sample start, so every output bit
+// is independent of the packed order.
 //
 // The sort is a rank count: the rank of token i is the number of tokens of its
 // sample that come before it.  A sample of L tokens costs L^2 comparisons of a
-// 16-byte key (position plus the first two bf16 of the k row) held in shared
-// memory; equal keys fall back to comparing the rows in global memory.  The
-// permutations are plain row copies, bound by HBM bandwidth.
+// 16-byte key (position plus the first two bf16 of the k row) streamed through
+// shared memory; equal keys fall back to comparing the rows in global memory.
+// The permutations are plain row copies, bound by HBM bandwidth; the kernels
+// that address q, k and out one row at a time read and write them through the
+// order instead (Problem::rowmap), so only the rows that other kernels move by
+// TMA or store as tiles are copied: v and dout in, out and dv back.
 #include "common.cuh"
 
 namespace h3 {
@@ -38,28 +41,26 @@ struct OrderArgs {
     const uint4* rows[4];  // k, v, q, dout (dout may be absent)
     int nrows;
     int row_vecs;  // 16-byte vectors per token row: H * 128 * 2 / 16
+    ulonglong2* keys;  // [S] sort keys
     int32_t* perm;
     unsigned* err;
 };
 
 // Order-preserving map of int32 onto uint32.
-__device__ __forceinline__ uint32_t ukey(int32_t x) { return static_cast<uint32_t>(x) ^ 0x80000000u; }
+__device__ __forceinline__ uint64_t ukey(int32_t x) { return static_cast<uint32_t>(x) ^ 0x80000000u; }
 
-// Sort key of token j: position, then the first two bf16 of the k row (element
-// 0 is the low half of the first 32-bit word, so rotate it to the high half).
-__device__ __forceinline__ uint4 token_key(const OrderArgs& A, int j) {
+// Sort key of every token as two 64-bit words compared in turn: (t, h) and
+// (w, first two bf16 of the k row; element 0 is the low half of the first
+// 32-bit word, so it is rotated to the high half).  Also starts perm as the
+// identity, so that slots an invalid seg_offsets array leaves unranked still
+// name a token of the batch.
+__global__ void __launch_bounds__(256) key_kernel(const __grid_constant__ OrderArgs A) {
+    const int j = blockIdx.x * 256 + threadIdx.x;
+    if (j >= A.S) return;
     const uint32_t w = reinterpret_cast<const uint32_t*>(A.rows[0] + (size_t)j * A.row_vecs)[0];
-    return make_uint4(ukey(A.pos[0][j]), ukey(A.pos[1][j]), ukey(A.pos[2][j]), (w << 16) | (w >> 16));
-}
-
-__device__ __forceinline__ int cmp_u32(uint32_t a, uint32_t b) { return a == b ? 0 : (a < b ? -1 : 1); }
-
-__device__ __forceinline__ int cmp_key(const uint4& a, const uint4& b) {
-    int c = cmp_u32(a.x, b.x);
-    if (!c) c = cmp_u32(a.y, b.y);
-    if (!c) c = cmp_u32(a.z, b.z);
-    if (!c) c = cmp_u32(a.w, b.w);
-    return c;
+    A.keys[j] = make_ulonglong2((ukey(A.pos[0][j]) << 32) | ukey(A.pos[1][j]),
+                                (ukey(A.pos[2][j]) << 32) | ((w << 16) | (w >> 16)));
+    A.perm[j] = j;
 }
 
 // Two bf16 in memory order: element 0 in the low half.
@@ -88,9 +89,11 @@ __device__ int cmp_rows(const OrderArgs& A, int j, int i) {
 }
 
 // One block ranks kOrdTokens tokens; the kOrdLanes threads of a token split
-// each chunk of keys between them and add their counts at the end.
+// each chunk of keys between them and add their counts at the end.  Chunks of
+// keys are double-buffered in shared memory, the next one loaded into
+// registers while the current one is compared.
 __global__ void __launch_bounds__(kOrdThreads) order_kernel(const __grid_constant__ OrderArgs A) {
-    __shared__ uint4 skey[kOrdThreads];
+    __shared__ ulonglong2 skey[2][kOrdThreads];
     __shared__ int range_lo, range_hi;
     const int tid = threadIdx.x;
     const int lane8 = tid % kOrdLanes;
@@ -112,35 +115,34 @@ __global__ void __launch_bounds__(kOrdThreads) order_kernel(const __grid_constan
     if (ok && lane8 == 0) { atomicMin(&range_lo, a); atomicMax(&range_hi, b); }
     __syncthreads();
     const int J0 = range_lo, J1 = range_hi;
-    const uint4 mine = ok ? token_key(A, i) : make_uint4(0, 0, 0, 0);
-    int rank = 0;
-    for (int j0 = J0; j0 < J1; j0 += kOrdThreads) {
-        if (j0 + tid < J1) skey[tid] = token_key(A, j0 + tid);
+    const ulonglong2* __restrict__ K = A.keys;
+    const ulonglong2 mine = ok ? K[i] : make_ulonglong2(0, 0);
+    ulonglong2 next = J0 + tid < J1 ? K[J0 + tid] : make_ulonglong2(0, 0);
+    int rank = 0, buf = 0;
+    for (int j0 = J0; j0 < J1; j0 += kOrdThreads, buf ^= 1) {
+        skey[buf][tid] = next;
         __syncthreads();
+        if (j0 + kOrdThreads + tid < J1) next = K[j0 + kOrdThreads + tid];
         if (ok) {
             const int e0 = max(a - j0, 0), e1 = min(b - j0, min(kOrdThreads, J1 - j0));
             for (int e = e0 + ((lane8 - e0) % kOrdLanes + kOrdLanes) % kOrdLanes; e < e1; e += kOrdLanes) {
-                int c = cmp_key(skey[e], mine);
-                const int j = j0 + e;
-                if (c == 0 && j != i) {
-                    c = cmp_rows(A, j, i);
-                    if (c == 0) c = j < i ? -1 : 1;
+                const ulonglong2 kj = skey[buf][e];
+                rank += (kj.x < mine.x) | ((kj.x == mine.x) & (kj.y < mine.y));
+                if (kj.x == mine.x && kj.y == mine.y && j0 + e != i) {
+                    const int j = j0 + e;
+                    const int c = cmp_rows(A, j, i);
+                    rank += c < 0 || (c == 0 && j < i);
                 }
-                rank += c < 0;
             }
         }
-        __syncthreads();
+        // the buffer written next iteration was last read two iterations ago,
+        // before every thread passed this iteration's barrier
     }
 #pragma unroll
     for (int o = kOrdLanes / 2; o; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
     if (act && lane8 == 0) {
-        if (!ok) {
-            atomicOr(A.err, kErrBadOffsets);
-        } else if (a + rank < b) {
-            A.perm[a + rank] = i;
-        } else {
-            atomicOr(A.err, kErrBadOffsets);
-        }
+        if (ok && a + rank < b) A.perm[a + rank] = i;
+        else atomicOr(A.err, kErrBadOffsets);
     }
 }
 
@@ -198,7 +200,8 @@ permute_small_kernel(const int32_t* __restrict__ perm, int S, int H, const float
 
 }  // namespace
 
-cudaError_t launch_order(const Problem& p, const __nv_bfloat16* dout, int32_t* perm, unsigned* err, cudaStream_t st) {
+cudaError_t launch_order(const Problem& p, const __nv_bfloat16* dout, uint4* keys, int32_t* perm, unsigned* err,
+                         cudaStream_t st) {
     if (p.seq.S == 0) return cudaSuccess;
     OrderArgs A;
     A.seg = p.seq.seg;
@@ -213,8 +216,10 @@ cudaError_t launch_order(const Problem& p, const __nv_bfloat16* dout, int32_t* p
     A.rows[3] = reinterpret_cast<const uint4*>(dout);
     A.nrows = dout ? 4 : 3;
     A.row_vecs = p.H * kD * 2 / 16;
+    A.keys = reinterpret_cast<ulonglong2*>(keys);
     A.perm = perm;
     A.err = err;
+    key_kernel<<<(p.seq.S + 255) / 256, 256, 0, st>>>(A);
     order_kernel<<<(p.seq.S + kOrdTokens - 1) / kOrdTokens, kOrdThreads, 0, st>>>(A);
     return cudaGetLastError();
 }

@@ -202,7 +202,8 @@ struct Workspace {
     int32_t* perm;           // [max_tokens] packed index of canonical slot c
     int32_t* pos_c;          // [3, max_tokens] positions in canonical order
     float* lse_c;            // [H, max_tokens] softmax row terms in canonical order
-    __nv_bfloat16* rows_c[8];  // [max_tokens, H, 128] each: q, k, v, out, dout, dq, dk, dv in canonical order
+    __nv_bfloat16* rows_c[4];  // [max_tokens, H, 128] each, canonical order: v, out, dout, dv
+    uint4* keys;             // [max_tokens] sort keys of the canonical order
 };
 
 struct Problem {
@@ -215,6 +216,10 @@ struct Problem {
     int H;
     float eps;
     float scale;
+    // Canonical key order: packed row of the token in canonical slot i (null =
+    // identity).  Kernels that address the caller's q, k or out rows one token
+    // at a time (prologue, Delta, row backward) read and write them through it.
+    const int32_t* rowmap = nullptr;
 };
 
 // Stages of one call, in launch order (timed separately when stage timing is on).
@@ -235,7 +240,8 @@ cudaError_t launch_bwd_dq(const Problem& p, const Workspace& ws, const float* ls
                           const __nv_bfloat16* dout, __nv_bfloat16* dq, cudaStream_t st);
 cudaError_t launch_bwd_rows(const Problem& p, const Workspace& ws, const RopeTable* rope, __nv_bfloat16* dq,
                             __nv_bfloat16* dk, cudaStream_t st);
-cudaError_t launch_order(const Problem& p, const __nv_bfloat16* dout, int32_t* perm, unsigned* err, cudaStream_t st);
+cudaError_t launch_order(const Problem& p, const __nv_bfloat16* dout, uint4* keys, int32_t* perm, unsigned* err,
+                         cudaStream_t st);
 // Gather (canonical copy row c <- packed row perm[c]) or scatter (the reverse) of
 // up to six [S, H, 128] bf16 tensors, the [H, S] row terms (either may be
 // absent) and, gathering only, the three position rows.

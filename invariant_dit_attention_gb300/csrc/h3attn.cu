@@ -119,13 +119,13 @@ Problem make_problem(h3attn_t h, const void* q, const void* k, const void* v, co
     return p;
 }
 
-// The problem on the canonical copies: same samples, gathered rows and positions.
+// The problem in canonical order: same samples; q and k read through the order's
+// map, v and the positions gathered.
 Problem canonical_problem(h3attn_t h, const Problem& p) {
     Problem c = p;
     const Workspace& ws = h->ws;
-    c.q = ws.rows_c[0];
-    c.k = ws.rows_c[1];
-    c.v = ws.rows_c[2];
+    c.v = ws.rows_c[0];
+    c.rowmap = ws.perm;
     c.seq.pos_t = ws.pos_c;
     c.seq.pos_h = ws.pos_c + h->cfg.max_tokens;
     c.seq.pos_w = ws.pos_c + 2 * (size_t)h->cfg.max_tokens;
@@ -199,9 +199,10 @@ h3attn_status h3attn_create(const h3attn_config* cfg, h3attn_t* out) {
               ws_alloc(h, &ws.plan.cum64, (N + 1) * 4) && ws_alloc(h, &ws.plan.cum128, (N + 1) * 4) &&
               ws_alloc(h, &ws.plan.cum256, (N + 1) * 4) &&
               ws_alloc(h, &ws.plan.err, 4);
+    if (ok) ok = ws_alloc(h, &ws.keys, T * 16);
     if (ok && cfg->key_order == H3ATTN_KEY_ORDER_CANONICAL) {
         ok = ws_alloc(h, &ws.perm, T * 4) && ws_alloc(h, &ws.pos_c, 3 * T * 4) && ws_alloc(h, &ws.lse_c, T * H * 4);
-        for (int t = 0; ok && t < 8; ++t) ok = ws_alloc(h, &ws.rows_c[t], T * H * kD * 2);
+        for (int t = 0; ok && t < 4; ++t) ok = ws_alloc(h, &ws.rows_c[t], T * H * kD * 2);
     }
     if (ok) ok = cudaMemset(ws.plan.err, 0, 4) == cudaSuccess;
     if (ok) ok = cudaMallocHost(&h->host_err, 4) == cudaSuccess;
@@ -236,21 +237,23 @@ h3attn_status h3attn_forward(h3attn_t h, const h3attn_bf16* q, const h3attn_bf16
     if (h->cfg.key_order == H3ATTN_KEY_ORDER_CANONICAL) {
         const Problem c = canonical_problem(h, p);
         const int S = total_tokens, H = p.H;
-        const void* gsrc[3] = {q, k, v};
-        void* gdst[3] = {ws.rows_c[0], ws.rows_c[1], ws.rows_c[2]};
+        const void* gsrc[1] = {v};
+        void* gdst[1] = {ws.rows_c[0]};
         const int32_t* psrc[3] = {p.seq.pos_t, p.seq.pos_h, p.seq.pos_w};
         int32_t* pdst[3] = {const_cast<int32_t*>(c.seq.pos_t), const_cast<int32_t*>(c.seq.pos_h),
                             const_cast<int32_t*>(c.seq.pos_w)};
-        const void* ssrc[1] = {ws.rows_c[3]};
+        const void* ssrc[1] = {ws.rows_c[1]};
         void* sdst[1] = {out};
         float* lc = lse ? ws.lse_c : nullptr;
         if (stage(h, kStagePlan, s, [&] { return launch_plan(p, ws, s); }) != cudaSuccess ||
-            stage(h, kStageOrder, s, [&] { return launch_order(p, nullptr, ws.perm, ws.plan.err, s); }) != cudaSuccess ||
+            stage(h, kStageOrder, s, [&] {
+                return launch_order(p, nullptr, ws.keys, ws.perm, ws.plan.err, s);
+            }) != cudaSuccess ||
             stage(h, kStagePermute, s, [&] {
-                return launch_permute(ws.perm, S, H, 3, gsrc, gdst, nullptr, nullptr, psrc, pdst, false, ws.plan.err, s);
+                return launch_permute(ws.perm, S, H, 1, gsrc, gdst, nullptr, nullptr, psrc, pdst, false, ws.plan.err, s);
             }) != cudaSuccess ||
             stage(h, kStagePrologue, s, [&] { return launch_prologue(c, ws, &h->rope, s); }) != cudaSuccess ||
-            stage(h, kStageFwd, s, [&] { return launch_fwd(c, ws, ws.rows_c[3], lc, s); }) != cudaSuccess ||
+            stage(h, kStageFwd, s, [&] { return launch_fwd(c, ws, ws.rows_c[1], lc, s); }) != cudaSuccess ||
             stage(h, kStagePermute, s, [&] {
                 return launch_permute(ws.perm, S, H, 1, ssrc, sdst, lc, lse, nullptr, nullptr, true, ws.plan.err, s);
             }) != cudaSuccess)
@@ -295,30 +298,30 @@ h3attn_status h3attn_backward(h3attn_t h, const h3attn_bf16* q, const h3attn_bf1
     if (h->cfg.key_order == H3ATTN_KEY_ORDER_CANONICAL) {
         const Problem c = canonical_problem(h, p);
         const int S = total_tokens, H = p.H;
-        const void* gsrc[5] = {q, k, v, out, dout};
-        void* gdst[5] = {ws.rows_c[0], ws.rows_c[1], ws.rows_c[2], ws.rows_c[3], ws.rows_c[4]};
+        const void* gsrc[2] = {v, dout};
+        void* gdst[2] = {ws.rows_c[0], ws.rows_c[2]};
         const int32_t* psrc[3] = {p.seq.pos_t, p.seq.pos_h, p.seq.pos_w};
         int32_t* pdst[3] = {const_cast<int32_t*>(c.seq.pos_t), const_cast<int32_t*>(c.seq.pos_h),
                             const_cast<int32_t*>(c.seq.pos_w)};
-        const void* ssrc[3] = {ws.rows_c[5], ws.rows_c[6], ws.rows_c[7]};
-        void* sdst[3] = {dq, dk, dv};
-        __nv_bfloat16 *oc = ws.rows_c[3], *doc = ws.rows_c[4];
-        __nv_bfloat16 *dqc = ws.rows_c[5], *dkc = ws.rows_c[6], *dvc = ws.rows_c[7];
+        const void* ssrc[1] = {ws.rows_c[3]};
+        void* sdst[1] = {dv};
+        __nv_bfloat16 *doc = ws.rows_c[2], *dvc = ws.rows_c[3];
+        // dq, dk and out are addressed through the order's map by the row kernels
         if (stage(h, kStagePlan, s, [&] { return launch_plan(p, ws, s); }) != cudaSuccess ||
-            stage(h, kStageOrder, s, [&] { return launch_order(p, dO, ws.perm, ws.plan.err, s); }) != cudaSuccess ||
+            stage(h, kStageOrder, s, [&] { return launch_order(p, dO, ws.keys, ws.perm, ws.plan.err, s); }) != cudaSuccess ||
             stage(h, kStagePermute, s, [&] {
-                return launch_permute(ws.perm, S, H, 5, gsrc, gdst, lse, ws.lse_c, psrc, pdst, false, ws.plan.err, s);
+                return launch_permute(ws.perm, S, H, 2, gsrc, gdst, lse, ws.lse_c, psrc, pdst, false, ws.plan.err, s);
             }) != cudaSuccess ||
             stage(h, kStagePrologue, s, [&] { return launch_prologue(c, ws, &h->rope, s); }) != cudaSuccess ||
-            stage(h, kStageDelta, s, [&] { return launch_bwd_delta(c, ws, oc, doc, s); }) != cudaSuccess ||
-            stage(h, kStageDkdv, s, [&] { return launch_bwd_dkdv(c, ws, ws.lse_c, doc, dkc, dvc, s); }) != cudaSuccess ||
-            stage(h, kStageDq, s, [&] { return launch_bwd_dq(c, ws, ws.lse_c, doc, dqc, s); }) != cudaSuccess ||
-            stage(h, kStageRows, s, [&] { return launch_bwd_rows(c, ws, &h->rope, dqc, dkc, s); }) != cudaSuccess ||
+            stage(h, kStageDelta, s, [&] { return launch_bwd_delta(c, ws, o, doc, s); }) != cudaSuccess ||
+            stage(h, kStageDkdv, s, [&] { return launch_bwd_dkdv(c, ws, ws.lse_c, doc, gk, dvc, s); }) != cudaSuccess ||
+            stage(h, kStageDq, s, [&] { return launch_bwd_dq(c, ws, ws.lse_c, doc, gq, s); }) != cudaSuccess ||
+            stage(h, kStageRows, s, [&] { return launch_bwd_rows(c, ws, &h->rope, gq, gk, s); }) != cudaSuccess ||
             stage(h, kStageDw, s, [&] {
                 return launch_bwd_dw(c, ws, dq_norm_w, dk_norm_w, dq_norm_w_per_sample, dk_norm_w_per_sample, s);
             }) != cudaSuccess ||
             stage(h, kStagePermute, s, [&] {
-                return launch_permute(ws.perm, S, H, 3, ssrc, sdst, nullptr, nullptr, nullptr, nullptr, true,
+                return launch_permute(ws.perm, S, H, 1, ssrc, sdst, nullptr, nullptr, nullptr, nullptr, true,
                                       ws.plan.err, s);
             }) != cudaSuccess)
             return H3ATTN_ERR_CUDA;
@@ -356,7 +359,8 @@ h3attn_status h3attn_canonical_order(h3attn_t h, const h3attn_bf16* q, const h3a
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const Problem p = make_problem(h, q, k, v, nullptr, nullptr, pos_ids, seg_offsets, num_samples, total_tokens);
     if (launch_plan(p, h->ws, s) != cudaSuccess ||
-        launch_order(p, reinterpret_cast<const __nv_bfloat16*>(dout), perm, h->ws.plan.err, s) != cudaSuccess)
+        launch_order(p, reinterpret_cast<const __nv_bfloat16*>(dout), h->ws.keys, perm, h->ws.plan.err, s) !=
+            cudaSuccess)
         return H3ATTN_ERR_CUDA;
     return H3ATTN_OK;
 }

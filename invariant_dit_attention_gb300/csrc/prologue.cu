@@ -114,14 +114,15 @@ prologue_kernel(Problem p, __half* __restrict__ qhat, __half* __restrict__ khat,
     const __nv_bfloat16* __restrict__ q = p.q;
     const __nv_bfloat16* __restrict__ k = p.k;
     const size_t base = (size_t)tok * p.H * kD + 4 * lane;
+    const size_t src = p.rowmap ? (size_t)p.rowmap[tok] * p.H * kD + 4 * lane : base;
     bool ok = true;
     for (int h0 = 0; h0 < p.H; h0 += kProBatch) {
         float xq[kProBatch][4], xk[kProBatch][4];
 #pragma unroll
         for (int b = 0; b < kProBatch; ++b)
             if (h0 + b < p.H) {
-                load_row4(q + base + (size_t)(h0 + b) * kD, xq[b]);
-                load_row4(k + base + (size_t)(h0 + b) * kD, xk[b]);
+                load_row4(q + src + (size_t)(h0 + b) * kD, xq[b]);
+                load_row4(k + src + (size_t)(h0 + b) * kD, xk[b]);
             }
 #pragma unroll
         for (int b = 0; b < kProBatch; ++b)
