@@ -18,8 +18,8 @@
 //
 // The sort is a rank count: the rank of token i is the number of tokens of its
 // sample that come before it.  A sample of L tokens costs L^2 comparisons of a
-// 16-byte key (position plus the first two bf16 of the k row) streamed through
-// shared memory; equal keys fall back to comparing the rows in global memory.
+// 16-byte key (position plus the first two bf16 of the k row); equal keys fall
+// back to comparing the rows in global memory.
 // The permutations are plain row copies, bound by HBM bandwidth; the kernels
 // that address q, k and out one row at a time read and write them through the
 // order instead (Problem::rowmap), so only the rows that other kernels move by
@@ -31,8 +31,7 @@ namespace h3 {
 namespace {
 
 constexpr int kOrdThreads = 256;
-constexpr int kOrdLanes = 8;  // threads sharing one token's comparisons
-constexpr int kOrdTokens = kOrdThreads / kOrdLanes;
+constexpr int kOrdTokens = kOrdThreads / 32;  // one warp per token
 
 struct OrderArgs {
     const int32_t* seg;
@@ -88,60 +87,39 @@ __device__ int cmp_rows(const OrderArgs& A, int j, int i) {
     return 0;
 }
 
-// One block ranks kOrdTokens tokens; the kOrdLanes threads of a token split
-// each chunk of keys between them and add their counts at the end.  Chunks of
-// keys are double-buffered in shared memory, the next one loaded into
-// registers while the current one is compared.
+// One warp per token: its lanes stride over the token's sample comparing keys
+// (read through L1: the warps of a block share a sample's keys) and add their
+// counts at the end.
 __global__ void __launch_bounds__(kOrdThreads) order_kernel(const __grid_constant__ OrderArgs A) {
-    __shared__ ulonglong2 skey[2][kOrdThreads];
-    __shared__ int range_lo, range_hi;
-    const int tid = threadIdx.x;
-    const int lane8 = tid % kOrdLanes;
-    const int i = blockIdx.x * kOrdTokens + tid / kOrdLanes;
-    const bool act = i < A.S;
-    int a = 0, b = 0;
-    if (act) {  // sample of token i: the last s with seg[s] <= i
-        int lo = 0, hi = A.n;
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (A.seg[mid] <= i) lo = mid; else hi = mid;
-        }
-        a = max(A.seg[lo], 0);
-        b = min(A.seg[lo + 1], A.S);
+    const int lane = threadIdx.x & 31;
+    const int i = blockIdx.x * kOrdTokens + (threadIdx.x >> 5);
+    if (i >= A.S) return;  // whole warps leave together
+    int lo = 0, hi = A.n;  // sample of token i: the last s with seg[s] <= i
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (A.seg[mid] <= i) lo = mid; else hi = mid;
     }
-    const bool ok = act && a <= i && i < b;
-    if (tid == 0) { range_lo = A.S; range_hi = 0; }
-    __syncthreads();
-    if (ok && lane8 == 0) { atomicMin(&range_lo, a); atomicMax(&range_hi, b); }
-    __syncthreads();
-    const int J0 = range_lo, J1 = range_hi;
+    const int a = max(A.seg[lo], 0), b = min(A.seg[lo + 1], A.S);
+    if (!(a <= i && i < b)) {
+        if (lane == 0) atomicOr(A.err, kErrBadOffsets);
+        return;
+    }
     const ulonglong2* __restrict__ K = A.keys;
-    const ulonglong2 mine = ok ? K[i] : make_ulonglong2(0, 0);
-    ulonglong2 next = J0 + tid < J1 ? K[J0 + tid] : make_ulonglong2(0, 0);
-    int rank = 0, buf = 0;
-    for (int j0 = J0; j0 < J1; j0 += kOrdThreads, buf ^= 1) {
-        skey[buf][tid] = next;
-        __syncthreads();
-        if (j0 + kOrdThreads + tid < J1) next = K[j0 + kOrdThreads + tid];
-        if (ok) {
-            const int e0 = max(a - j0, 0), e1 = min(b - j0, min(kOrdThreads, J1 - j0));
-            for (int e = e0 + ((lane8 - e0) % kOrdLanes + kOrdLanes) % kOrdLanes; e < e1; e += kOrdLanes) {
-                const ulonglong2 kj = skey[buf][e];
-                rank += (kj.x < mine.x) | ((kj.x == mine.x) & (kj.y < mine.y));
-                if (kj.x == mine.x && kj.y == mine.y && j0 + e != i) {
-                    const int j = j0 + e;
-                    const int c = cmp_rows(A, j, i);
-                    rank += c < 0 || (c == 0 && j < i);
-                }
-            }
+    const ulonglong2 mine = K[i];
+    int rank = 0;
+#pragma unroll 4
+    for (int j = a + lane; j < b; j += 32) {
+        const ulonglong2 kj = __ldg(K + j);
+        rank += (kj.x < mine.x) | ((kj.x == mine.x) & (kj.y < mine.y));
+        if (kj.x == mine.x && kj.y == mine.y && j != i) {
+            const int c = cmp_rows(A, j, i);
+            rank += c < 0 || (c == 0 && j < i);
         }
-        // the buffer written next iteration was last read two iterations ago,
-        // before every thread passed this iteration's barrier
     }
 #pragma unroll
-    for (int o = kOrdLanes / 2; o; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
-    if (act && lane8 == 0) {
-        if (ok && a + rank < b) A.perm[a + rank] = i;
+    for (int o = 16; o; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+    if (lane == 0) {
+        if (a + rank < b) A.perm[a + rank] = i;
         else atomicOr(A.err, kErrBadOffsets);
     }
 }
