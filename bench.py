@@ -168,6 +168,53 @@ def projection_rate(S, D, stream, pk):
     return res
 
 
+def qkv_rate(H, S, d, stream, reps=5):
+    """QKV projection (D = H * 128 -> 3D) plus the attention forward of the same
+    tokens: fused (h3attn_qkv_forward: the q/k norm and RoPE in the projection's
+    epilogue) against the separate calls (h3attn_linear, then h3attn_forward on
+    its q, k, v), CUDA-event timed."""
+    from invariant_dit_attention_gb300.h3attn import H3Attn, linear
+    D = H * 128
+    g = torch.Generator(device="cuda").manual_seed(11)
+    x = torch.randn(S, D, device="cuda", generator=g).to(torch.bfloat16)
+    w = (torch.randn(3 * D, D, device="cuda", generator=g) / D ** 0.5).to(torch.bfloat16)
+    b = 0.1 * torch.randn(3 * D, device="cuda", generator=g)
+    h = H3Attn(H, S, 8)
+    flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+    qkv = [torch.empty(S, H, 128, dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    out = torch.empty_like(qkv[0])
+    lse = torch.empty(H, S, device="cuda")
+
+    def fused():
+        h.qkv_forward(x, w, b, d["q_norm_w"], d["k_norm_w"], d["pos"], d["seg_offsets"], q=qkv[0], k=qkv[1],
+                      v=qkv[2], out=out, lse=lse)
+
+    def separate():
+        for i in range(3):  # one projection per q, k, v slice of W, straight into its tensor
+            linear(x, w[i * D:(i + 1) * D], b[i * D:(i + 1) * D], out=qkv[i].view(S, D), error_flags=flags)
+        h.forward(qkv[0], qkv[1], qkv[2], d["q_norm_w"], d["k_norm_w"], d["pos"], d["seg_offsets"], out=out,
+                  lse=lse)
+
+    res = {}
+    for name, fn in (("fused_ms", fused), ("separate_ms", separate)):
+        for _ in range(2):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        res[name] = round(e0.elapsed_time(e1) / reps, 4)
+    h.check()
+    h.close()
+    if int(flags.item()) != 0:
+        raise RuntimeError("h3attn_linear reported a device error")
+    res["shape"] = [S, D, 3 * D]
+    res["separate_includes"] = "three projections (the q, k, v slices of W), forward (prologue + attention)"
+    return res
+
+
 def canonical_rate(H, S, d, grads, step_flops, packed_ms, stream, steps=10):
     """The same forward + backward step with the canonical key order (sums over a
     sample's tokens in an order fixed by the tokens, not by their packing),
@@ -435,6 +482,9 @@ def run_ours(args):
     # ---- the projections either side of the path (h3attn_linear), same tokens, D = H * 128
     projection = projection_rate(S, H * 128, stream, pk)
 
+    # ---- the QKV projection with the norm/RoPE fused in, then the forward
+    qkv = qkv_rate(H, S, d, stream)
+
     # ---- the canonical key order (packing-permutation-invariant sums), same step
     canonical = canonical_rate(H, S, d, grads, step_flops, ms_max / args.steps, stream)
 
@@ -456,6 +506,7 @@ def run_ours(args):
         "stages_ms_per_step": {k: round(v[0] / args.steps, 4) for k, v in stages.items()},
         "roofline": roof, "fwd_roofline": fwd_roof, "prologue_roofline": prologue, "projection": projection,
         "canonical_order": canonical,
+        "qkv_forward": qkv,
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / args.steps, 4),
                 "pipelining": "inputs up and results down on two copy streams beside the kernels, "

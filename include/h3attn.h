@@ -183,6 +183,32 @@ h3attn_status h3attn_device_status(h3attn_t h, void *stream);
  * Errors: INVALID_ARG, CAPACITY, CUDA (host); an invalid seg_offsets array is
  * reported by h3attn_device_status and leaves perm unspecified.
  */
+/*
+ * The QKV projection and the attention forward in one call:
+ *   [q | k | v] = x w_qkv^T (+ b_qkv), rounded once to bf16,
+ *   then out, lse = h3attn_forward(q, k, v, ...).
+ * The projection is the block's QKV node ("ws1_one_h3_block" page of
+ * RL-Kernel, PR #539, Bindings table) and its epilogue also performs the q/k
+ * RMSNorm + RoPE while each row is on chip (the separate prologue pass of
+ * h3attn_forward is skipped).  x: bf16 [total_tokens, in_features];
+ * w_qkv: bf16 [3 * H * 128, in_features], rows = the q heads, then the k
+ * heads, then the v heads (each 128 rows, head-major); b_qkv: float32
+ * [3 * H * 128] or NULL.  q, k, v: bf16 [total_tokens, H, 128], written (the
+ * backward takes them); out, lse as in h3attn_forward.  Other inputs as in
+ * h3attn_forward.  Results are bitwise those of h3attn_linear on the same x,
+ * w_qkv, b_qkv, split into q, k, v, followed by h3attn_forward.
+ * Requires in_features % 64 == 0 and a handle with the packed key order,
+ * else UNSUPPORTED.  total_tokens == 0 is a no-op.
+ * Errors: INVALID_ARG, UNSUPPORTED, CAPACITY, CUDA.
+ */
+h3attn_status h3attn_qkv_forward(h3attn_t h, const h3attn_bf16 *x, int in_features,
+                                 const h3attn_bf16 *w_qkv, const float *b_qkv,
+                                 const float *q_norm_w, const float *k_norm_w,
+                                 const int32_t *const pos_ids[3], const int32_t *seg_offsets,
+                                 int num_samples, int total_tokens,
+                                 h3attn_bf16 *q, h3attn_bf16 *k, h3attn_bf16 *v,
+                                 h3attn_bf16 *out, float *lse, void *stream);
+
 h3attn_status h3attn_canonical_order(h3attn_t h,
                                      const h3attn_bf16 *q, const h3attn_bf16 *k, const h3attn_bf16 *v,
                                      const h3attn_bf16 *dout,
@@ -210,7 +236,8 @@ enum {
     H3ATTN_STAGE_BWD_ROWS = 7,  /* RoPE^-1 + RMSNorm backward of dq^, dk^ rows */
     H3ATTN_STAGE_ORDER = 8,     /* canonical order: rank count per sample      */
     H3ATTN_STAGE_PERMUTE = 9,   /* canonical order: row gathers and scatters   */
-    H3ATTN_NUM_STAGES = 10
+    H3ATTN_STAGE_QKV = 10,      /* fused QKV projection + q/k norm and RoPE    */
+    H3ATTN_NUM_STAGES = 11
 };
 h3attn_status h3attn_set_stage_timing(h3attn_t h, int enable);
 h3attn_status h3attn_stage_times(h3attn_t h, float *total_ms, int *launches, int n_stages);

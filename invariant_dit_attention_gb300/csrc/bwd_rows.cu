@@ -63,7 +63,7 @@ rope_table_kernel(const __grid_constant__ RopeTable rt, Seq seq, float* __restri
     float c = 1.f, sn = 0.f;
     if (axis >= 0) {
         const int pos = axis == 0 ? seq.pos_t[token] : (axis == 1 ? seq.pos_h[token] : seq.pos_w[token]);
-        sincosf(static_cast<float>(pos) * srt.inv_freq[ch], &sn, &c);
+        sincosf(__fmul_rn(static_cast<float>(pos), srt.inv_freq[ch]), &sn, &c);
     }
     cs[(size_t)token * 2 * kD + ch] = c;
     cs[(size_t)token * 2 * kD + kD + ch] = sn;
@@ -182,6 +182,13 @@ cudaError_t launch_bwd_delta(const Problem& p, const Workspace& ws, const __nv_b
     return cudaGetLastError();
 }
 
+cudaError_t launch_rope_table(const Problem& p, const Workspace& ws, const RopeTable* rope, cudaStream_t st) {
+    const long cells = (long)p.seq.S * kD;
+    if (cells == 0) return cudaSuccess;
+    rope_table_kernel<<<(unsigned)((cells + 255) / 256), 256, 0, st>>>(*rope, p.seq, ws.rope_cs);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_bwd_rows(const Problem& p, const Workspace& ws, const RopeTable* rope, __nv_bfloat16* dq,
                             __nv_bfloat16* dk, cudaStream_t st) {
     RowsParams r;
@@ -201,8 +208,8 @@ cudaError_t launch_bwd_rows(const Problem& p, const Workspace& ws, const RopeTab
     r.dw_part[1] = ws.dwk_part;
     r.rope_cs = ws.rope_cs;
     r.rowmap = p.rowmap;
-    const long cells = (long)p.seq.S * kD;
-    rope_table_kernel<<<(unsigned)((cells + 255) / 256), 256, 0, st>>>(*rope, p.seq, ws.rope_cs);
+    cudaError_t e = launch_rope_table(p, ws, rope, st);
+    if (e != cudaSuccess) return e;
     // an upper bound of the 128-token tiles (every sample adds at most one partial
     // tile); CTAs past the plan's last tile return at once
     const long tiles = (long)(p.seq.S + 127) / 128 + p.seq.n;

@@ -225,7 +225,7 @@ struct Problem {
 // Stages of one call, in launch order (timed separately when stage timing is on).
 // Values match the h3attn_stage enum of the C ABI.
 enum Stage { kStagePlan = 0, kStagePrologue, kStageFwd, kStageDelta, kStageDkdv, kStageDq, kStageDw, kStageRows,
-             kStageOrder, kStagePermute, kStages };
+             kStageOrder, kStagePermute, kStageQkv, kStages };
 
 cudaError_t init_fwd_tc();
 cudaError_t init_bwd_attributes();
@@ -248,6 +248,13 @@ cudaError_t launch_order(const Problem& p, const __nv_bfloat16* dout, uint4* key
 cudaError_t launch_permute(const int32_t* perm, int S, int H, int ntensors, const void* const* src, void* const* dst,
                            const float* lse_src, float* lse_dst, const int32_t* const pos_src[3], int32_t* pos_dst[3],
                            bool scatter, unsigned* err, cudaStream_t st);
+// cos / sin of every channel's rotary angle per token into ws.rope_cs (bwd_rows.cu).
+cudaError_t launch_rope_table(const Problem& p, const Workspace& ws, const RopeTable* rope, cudaStream_t st);
+// The fused QKV projection (linear_tc.cu): q, k, v rows and the workspace's q^, k^
+// (reads the rotary table launch_rope_table wrote).
+cudaError_t launch_qkv(const Problem& p, const Workspace& ws, const RopeTable* rope, const __nv_bfloat16* x,
+                       int in_features, const __nv_bfloat16* w, const float* bias, __nv_bfloat16* q, __nv_bfloat16* k,
+                       __nv_bfloat16* v, cudaStream_t st);
 cudaError_t launch_bwd_dw(const Problem& p, const Workspace& ws, float* dwq, float* dwk, float* dwq_s,
                           float* dwk_s, cudaStream_t st);
 

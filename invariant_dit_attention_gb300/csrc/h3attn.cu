@@ -340,6 +340,41 @@ h3attn_status h3attn_backward(h3attn_t h, const h3attn_bf16* q, const h3attn_bf1
     return H3ATTN_OK;
 }
 
+h3attn_status h3attn_qkv_forward(h3attn_t h, const h3attn_bf16* x, int in_features, const h3attn_bf16* w_qkv,
+                                 const float* b_qkv, const float* q_norm_w, const float* k_norm_w,
+                                 const int32_t* const pos_ids[3], const int32_t* seg_offsets, int num_samples,
+                                 int total_tokens, h3attn_bf16* q, h3attn_bf16* k, h3attn_bf16* v, h3attn_bf16* out,
+                                 float* lse, void* stream) {
+    h3attn_status st = check_common(h, q, k, v, q_norm_w, k_norm_w, pos_ids, seg_offsets, num_samples, total_tokens);
+    if (st != H3ATTN_OK) return st;
+    if (in_features < 1) return H3ATTN_ERR_INVALID_ARG;
+    if (in_features % 64 != 0 || h->cfg.key_order != H3ATTN_KEY_ORDER_PACKED) return H3ATTN_ERR_UNSUPPORTED;
+    if (total_tokens == 0) return H3ATTN_OK;
+    if (!aligned16(x) || !aligned16(w_qkv) || (b_qkv && !aligned16(b_qkv)) || !aligned16(out) ||
+        (lse && !aligned4(lse)))
+        return H3ATTN_ERR_INVALID_ARG;
+    if ((long long)total_tokens * in_features >= (1LL << 40) ||
+        (long long)3 * h->cfg.num_heads * kD * in_features >= (1LL << 40))
+        return H3ATTN_ERR_CAPACITY;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Problem p = make_problem(h, q, k, v, q_norm_w, k_norm_w, pos_ids, seg_offsets, num_samples, total_tokens);
+    Workspace& ws = h->ws;
+    const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
+    const __nv_bfloat16* wb = reinterpret_cast<const __nv_bfloat16*>(w_qkv);
+    __nv_bfloat16* qb = reinterpret_cast<__nv_bfloat16*>(q);
+    __nv_bfloat16* kb = reinterpret_cast<__nv_bfloat16*>(k);
+    __nv_bfloat16* vb = reinterpret_cast<__nv_bfloat16*>(v);
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out);
+    if (stage(h, kStagePlan, s, [&] { return launch_plan(p, ws, s); }) != cudaSuccess ||
+        stage(h, kStageQkv, s, [&] {
+            cudaError_t e = launch_rope_table(p, ws, &h->rope, s);
+            return e != cudaSuccess ? e : launch_qkv(p, ws, &h->rope, xb, in_features, wb, b_qkv, qb, kb, vb, s);
+        }) != cudaSuccess ||
+        stage(h, kStageFwd, s, [&] { return launch_fwd(p, ws, o, lse, s); }) != cudaSuccess)
+        return H3ATTN_ERR_CUDA;
+    return H3ATTN_OK;
+}
+
 h3attn_status h3attn_canonical_order(h3attn_t h, const h3attn_bf16* q, const h3attn_bf16* k, const h3attn_bf16* v,
                                      const h3attn_bf16* dout, const int32_t* const pos_ids[3],
                                      const int32_t* seg_offsets, int num_samples, int total_tokens, int32_t* perm,

@@ -19,10 +19,24 @@
 // accumulator while the other one fills.  Tiles are visited in groups of 16
 // row tiles with the column tiles inside, so the operands a wave of CTAs works
 // on stay in L2.
+//
+// The QKV form (h3attn_qkv_forward) runs the same kernel with a wider
+// epilogue: W's rows are the q, k and v heads in that order, and each
+// 128-column half of a tile is one head of one of them.  The epilogue writes
+// the bf16 q, k, v rows and, for q and k, also the normalised and rotated
+// fp16 rows q^ / k^ that the attention kernels read - the prologue's work done
+// while the row is still on chip.  It computes them from the rounded bf16 row
+// with the prologue's operations in the prologue's order (its lane partial
+// sums of squares, the warp butterfly seen from one lane, then the same
+// per-channel products and rotations, with the angles' cos / sin taken from
+// the per-token table, which holds the prologue's own sincosf values), so the
+// results are bitwise those of the projection followed by the separate
+// prologue.
 #include <cudaTypedefs.h>
 
 #include "../../include/h3attn.h"
 #include "common.cuh"
+#include "rowops.cuh"
 #include "tc.cuh"
 
 namespace h3 {
@@ -36,10 +50,31 @@ constexpr int kBBytes = kBN * kBK * 2;          // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;  // 48 KB
 constexpr int kOffBar = kRing * kStageBytes;
 constexpr int kSmem = kOffBar + 256;            // the dynamic shared memory base is 1024-aligned (checked)
+// QKV form: one head of the thread's row as bf16 pairs (65 words per row: the
+// odd stride keeps the rows' words in different banks), then the rotary table
+constexpr int kRowWords = 65;
+constexpr int kOffRows = kSmem;
+constexpr int kOffRope = kOffRows + kBM * kRowWords * 4;
+constexpr int kOffWn = kOffRope + (int)sizeof(RopeTable);  // q_norm_w, k_norm_w
+constexpr int kSmemQkv = kOffWn + 2 * kD * 4;
+static_assert(kThreads == 2 * kD, "one thread per norm weight when staging them");
+static_assert(kSmemQkv <= 232448, "shared memory of the QKV form");
+static_assert(sizeof(RopeTable) % 16 == 0, "norm weights stay 16-byte aligned");
 constexpr int kGroupM = 16;                     // row tiles per raster group
 enum { bFull = 0, bEmpty = bFull + kRing, bAccFull = bEmpty + kRing, bAccEmpty = bAccFull + 2, bDone = bAccEmpty + 2,
        bCount };
 }  // namespace lint
+
+struct QkvParams {
+    int H, D;                    // heads, D = H * 128 (q, k and v each D columns of y)
+    float eps;
+    const float* wn[2];          // q_norm_w, k_norm_w
+    const int32_t* pos[3];       // t, h, w positions of each row
+    __nv_bfloat16* out[3];       // q, k, v rows [rows, H, 128]
+    __half* hat[2];              // q^, k^ rows [rows, H, 128]
+    const float* rope_cs;        // [rows][cos 128 | sin 128]: the angles' cos / sin per token
+    RopeTable rope;
+};
 
 struct LinearParams {
     int rows, N, K;
@@ -47,6 +82,7 @@ struct LinearParams {
     const float* bias;
     __nv_bfloat16* y;
     unsigned* err;
+    QkvParams qkv;  // QKV form only
 };
 
 // Tile t of the raster: groups of kGroupM row tiles, column tiles inside a group.
@@ -59,8 +95,121 @@ __device__ __forceinline__ void linear_tile(const LinearParams& p, int t, int& t
     tn = r / gsize;
 }
 
+// Channel c of the staged bf16 row (two per 32-bit word, element 0 low).
+__device__ __forceinline__ float staged(const uint32_t* row, int c) {
+    const uint32_t w = row[c >> 1];
+    return (c & 1) ? bf16_hi(w) : bf16_lo(w);
+}
+
+// The QKV epilogue of one tile for one thread (row): both 128-column heads of
+// the tile, from the TMEM accumulator columns at acc.  A q or k head is staged
+// in shared memory as bf16, normalised and rotated pair by pair (each rotated
+// pair once, both outputs from one cos / sin), written back into the staging
+// row as fp16 in place (a pair's inputs are not needed by any other pair) and
+// then copied out.  Returns false if a q^ / k^ value left the fp16 range.
+__device__ __forceinline__ bool qkv_epilogue(const LinearParams& p, uint8_t* smem, uint32_t acc, int row_in, int row,
+                                             bool row_ok, int tn) {
+    using namespace lint;
+    const QkvParams& q = p.qkv;
+    uint32_t* srow = reinterpret_cast<uint32_t*>(smem + kOffRows) + row_in * kRowWords;
+    __half* srow16 = reinterpret_cast<__half*>(srow);
+    const RopeTable& rt = *reinterpret_cast<const RopeTable*>(smem + kOffRope);
+    bool in_range = true;
+    for (int hh = 0; hh < 2; ++hh) {
+        const int col0 = tn * kBN + 128 * hh;
+        if (col0 >= p.N) break;
+        const int which = col0 / q.D, head = (col0 - which * q.D) >> 7;
+        __syncwarp();  // the TMEM loads below are warp-collective
+        float part[32];  // the lanes' sums of squares in the prologue's layout (lane l: channels 4l..4l+3)
+#pragma unroll
+        for (int c32 = 0; c32 < 4; ++c32) {
+            uint32_t r[32];
+            tc::tmem_ld32(acc + 128 * hh + 32 * c32, r);
+            tc::tmem_wait_ld_dep(r);
+            float v[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
+            if (p.bias) {
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    const float4 b4 = *reinterpret_cast<const float4*>(p.bias + col0 + 32 * c32 + e);
+                    v[e] += b4.x; v[e + 1] += b4.y; v[e + 2] += b4.z; v[e + 3] += b4.w;
+                }
+            }
+            uint32_t u[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) u[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
+            if (row_ok) {
+                uint4* dst = reinterpret_cast<uint4*>(q.out[which] + ((size_t)row * q.H + head) * kD + 32 * c32);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) dst[e] = make_uint4(u[4 * e], u[4 * e + 1], u[4 * e + 2], u[4 * e + 3]);
+            }
+            if (which < 2) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) srow[16 * c32 + e] = u[e];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    part[8 * c32 + j] =
+                        sq4(bf16_lo(u[2 * j]), bf16_hi(u[2 * j]), bf16_lo(u[2 * j + 1]), bf16_hi(u[2 * j + 1]));
+            }
+        }
+        if (which == 2 || !row_ok) continue;
+        // warp_sum's butterfly (offsets 16, 8, 4, 2, 1) as lane 0 sees it
+        float a16[16], a8[8], a4[4];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) a16[j] = part[j] + part[j + 16];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a8[j] = a16[j] + a16[j + 8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) a4[j] = a8[j] + a8[j + 4];
+        const float rs = rstd_of((a4[0] + a4[2]) + (a4[1] + a4[3]), q.eps);
+        const float* wn = reinterpret_cast<const float*>(smem + kOffWn) + kD * which;
+        const float* csr = q.rope_cs + (size_t)row * 2 * kD;  // the prologue's sincosf values, per token
+        uint32_t notfit = 0, nonfinite = 0;  // per group of four channels (a prologue lane), as its check
+        auto note = [&](float y, int g) {
+            notfit |= (uint32_t)!(fabsf(y) <= 65504.f) << g;
+            nonfinite |= (uint32_t)!isfinite(y) << g;
+        };
+        for (int g = 0; g < 32; ++g) {
+            if (rt.axis[g] < 0) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int c = 4 * g + e;
+                    const float y = norm_w(staged(srow, c), rs, wn[c]);
+                    note(y, g);
+                    srow16[c] = __float2half_rn(y);
+                }
+            } else if (!rt.second[g]) {  // the pair (4g + e, 4pg + e); the second half's groups are done here
+                const int pg = rt.partner[g];
+                const float4 c4 = *reinterpret_cast<const float4*>(csr + 4 * g);
+                const float4 s4 = *reinterpret_cast<const float4*>(csr + kD + 4 * g);
+                const float cs[4] = {c4.x, c4.y, c4.z, c4.w}, sn[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int cu = 4 * g + e, cv = 4 * pg + e;
+                    const float zu = norm_w(staged(srow, cu), rs, wn[cu]);
+                    const float zv = norm_w(staged(srow, cv), rs, wn[cv]);
+                    const float yu = rope_u(zu, zv, cs[e], sn[e]), yv = rope_v(zu, zv, cs[e], sn[e]);
+                    note(yu, g);
+                    note(yv, pg);
+                    srow16[cu] = __float2half_rn(yu);
+                    srow16[cv] = __float2half_rn(yv);
+                }
+            }
+        }
+        in_range &= (notfit & ~nonfinite) == 0;
+        uint4* hat = reinterpret_cast<uint4*>(q.hat[which] + ((size_t)row * q.H + head) * kD);
+#pragma unroll 4
+        for (int w16 = 0; w16 < 16; ++w16)
+            hat[w16] = make_uint4(srow[4 * w16], srow[4 * w16 + 1], srow[4 * w16 + 2], srow[4 * w16 + 3]);
+    }
+    return in_range;
+}
+
+template <bool kQkv>
 __global__ void __launch_bounds__(lint::kThreads, 1)
-linear_tc_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mb, const LinearParams p) {
+linear_tc_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mb,
+                 const __grid_constant__ LinearParams p) {
     using namespace lint;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if (smem_u32(smem_raw) & 1023u) {  // the layout below needs a 1024-byte aligned base
@@ -89,6 +238,10 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__
         tc::fence_mbar_init();
         tc::prefetch_map(&ma);
         tc::prefetch_map(&mb);
+    }
+    if constexpr (kQkv) {
+        rope_to_smem(p.qkv.rope, *reinterpret_cast<RopeTable*>(smem + kOffRope), tid, kThreads);
+        reinterpret_cast<float*>(smem + kOffWn)[tid] = p.qkv.wn[tid / kD][tid % kD];  // kThreads == 2 * kD
     }
     if (warp == 1) {
         tc::tmem_alloc(smem_u32(tmem_slot), 512);
@@ -169,6 +322,13 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__
             tc::fence_after_sync();
             const int row = tm * kBM + row_in;
             const bool row_ok = row < p.rows;
+            if constexpr (kQkv) {
+                if (!qkv_epilogue(p, smem, tmem + lane_base + kBN * b, row_in, row, row_ok, tn)) atomicOr(p.err, kErrRange);
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(bar(bAccEmpty + b));
+                continue;
+            }
             __nv_bfloat16* dst = p.y + (size_t)row * p.N + tn * kBN;
             for (int c32 = 0; c32 < kBN / 32; ++c32) {
                 uint32_t r[32];
@@ -245,8 +405,10 @@ h3attn_status init_linear(int dev) {
         cudaDeviceProp prop;
         if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return H3ATTN_ERR_CUDA;
         if (!(prop.major == 10 && prop.minor == 3)) return H3ATTN_ERR_UNSUPPORTED;
-        if (cudaFuncSetAttribute(linear_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lint::kSmem) !=
-            cudaSuccess)
+        if (cudaFuncSetAttribute(linear_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, lint::kSmem) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(linear_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, lint::kSmemQkv) !=
+                cudaSuccess)
             return H3ATTN_ERR_CUDA;
         g_sms_l = prop.multiProcessorCount;
         g_dev_l = dev;
@@ -291,6 +453,52 @@ extern "C" h3attn_status h3attn_linear(const h3attn_bf16* x, int rows, int in_fe
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(device_error_flags, 0, 4, s) != cudaSuccess) return H3ATTN_ERR_CUDA;
     const int tiles = p.tiles_m * p.tiles_n;
-    linear_tc_kernel<<<tiles < g_sms_l ? tiles : g_sms_l, lint::kThreads, lint::kSmem, s>>>(ma, mb, p);
+    linear_tc_kernel<false><<<tiles < g_sms_l ? tiles : g_sms_l, lint::kThreads, lint::kSmem, s>>>(ma, mb, p);
     return cudaGetLastError() == cudaSuccess ? H3ATTN_OK : H3ATTN_ERR_CUDA;
 }
+
+namespace h3 {
+
+// The QKV form: y = x W^T + b with W [3 H 128, in_features] (q, k, v heads),
+// written as the q, k, v rows plus q^ / k^ into the workspace.
+cudaError_t launch_qkv(const Problem& p, const Workspace& ws, const RopeTable* rope, const __nv_bfloat16* x,
+                       int in_features, const __nv_bfloat16* w, const float* bias, __nv_bfloat16* q, __nv_bfloat16* k,
+                       __nv_bfloat16* v, cudaStream_t st) {
+    if (p.seq.S == 0) return cudaSuccess;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return cudaErrorInvalidDevice;
+    if (init_linear(dev) != H3ATTN_OK) return cudaErrorNotSupported;
+    const int D = p.H * kD, N = 3 * D;
+    CUtensorMap ma, mb;
+    if (!encode_2d(&ma, x, in_features, p.seq.S, lint::kBM) || !encode_2d(&mb, w, in_features, N, lint::kBN))
+        return cudaErrorInvalidValue;
+    LinearParams lp;
+    lp.rows = p.seq.S;
+    lp.N = N;
+    lp.K = in_features;
+    lp.tiles_m = (lp.rows + lint::kBM - 1) / lint::kBM;
+    lp.tiles_n = (N + lint::kBN - 1) / lint::kBN;
+    lp.bias = bias;
+    lp.y = nullptr;
+    lp.err = ws.plan.err;
+    lp.qkv.H = p.H;
+    lp.qkv.D = D;
+    lp.qkv.eps = p.eps;
+    lp.qkv.wn[0] = p.wq;
+    lp.qkv.wn[1] = p.wk;
+    lp.qkv.pos[0] = p.seq.pos_t;
+    lp.qkv.pos[1] = p.seq.pos_h;
+    lp.qkv.pos[2] = p.seq.pos_w;
+    lp.qkv.out[0] = q;
+    lp.qkv.out[1] = k;
+    lp.qkv.out[2] = v;
+    lp.qkv.hat[0] = ws.qhat;
+    lp.qkv.hat[1] = ws.khat;
+    lp.qkv.rope_cs = ws.rope_cs;
+    lp.qkv.rope = *rope;
+    const int tiles = lp.tiles_m * lp.tiles_n;
+    linear_tc_kernel<true><<<tiles < g_sms_l ? tiles : g_sms_l, lint::kThreads, lint::kSmemQkv, st>>>(ma, mb, lp);
+    return cudaGetLastError();
+}
+
+}  // namespace h3

@@ -61,15 +61,29 @@ __device__ __forceinline__ RowAngles row_angles(const LaneRope& lr, int pt, int 
     }
     const float p = static_cast<float>(lr.axis == 0 ? pt : (lr.axis == 1 ? ph : pw));
 #pragma unroll
-    for (int e = 0; e < 4; ++e) sincosf(p * lr.f[e], &a.s[e], &a.c[e]);
+    for (int e = 0; e < 4; ++e) sincosf(__fmul_rn(p, lr.f[e]), &a.s[e], &a.c[e]);
     return a;
 }
 
+// The forward's roundings, spelled out operation by operation (no contraction
+// left to the compiler), so that every kernel computing q^ / k^ - the prologue
+// here, one warp per row, and the QKV projection's epilogue, one thread per
+// row - gets the same bits from the same bf16 row.
+//   sum of squares of four channels (a lane's share of the row)
+__device__ __forceinline__ float sq4(float x0, float x1, float x2, float x3) {
+    return __fmaf_rn(x3, x3, __fmaf_rn(x2, x2, __fmaf_rn(x1, x1, __fmul_rn(x0, x0))));
+}
+//   1 / sqrt(mean of squares + eps) from the row's sum of squares
+__device__ __forceinline__ float rstd_of(float ss, float eps) { return 1.0f / sqrtf(__fmaf_rn(ss, 1.0f / kD, eps)); }
+//   z = (x r) w
+__device__ __forceinline__ float norm_w(float x, float r, float w) { return __fmul_rn(__fmul_rn(x, r), w); }
+//   the rotated pair (u, v) -> (u cos - v sin, u sin + v cos)
+__device__ __forceinline__ float rope_u(float u, float v, float c, float s) { return __fmaf_rn(u, c, -__fmul_rn(v, s)); }
+__device__ __forceinline__ float rope_v(float u, float v, float c, float s) { return __fmaf_rn(u, s, __fmul_rn(v, c)); }
+
 // 1/sqrt(mean of squares + eps) of the row held 4 channels per lane.
 __device__ __forceinline__ float row_rstd(const float (&x)[4], float eps) {
-    float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
-    ss = warp_sum(ss);
-    return 1.0f / sqrtf(ss * (1.0f / kD) + eps);
+    return rstd_of(warp_sum(sq4(x[0], x[1], x[2], x[3])), eps);
 }
 
 // y = RoPE(RMSNorm(x) * w) for one row.
@@ -78,7 +92,7 @@ __device__ __forceinline__ void row_norm_rope(const float (&x)[4], const float (
     float r = row_rstd(x, eps);
     float z[4], zp[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) z[e] = (x[e] * r) * w[e];
+    for (int e = 0; e < 4; ++e) z[e] = norm_w(x[e], r, w[e]);
 #pragma unroll
     for (int e = 0; e < 4; ++e) zp[e] = __shfl_sync(0xffffffffu, z[e], lr.partner);
     if (lr.axis < 0) {
@@ -86,10 +100,10 @@ __device__ __forceinline__ void row_norm_rope(const float (&x)[4], const float (
         for (int e = 0; e < 4; ++e) y[e] = z[e];
     } else if (!lr.second) {  // (u, v) = (own, partner): u cos - v sin
 #pragma unroll
-        for (int e = 0; e < 4; ++e) y[e] = z[e] * a.c[e] - zp[e] * a.s[e];
+        for (int e = 0; e < 4; ++e) y[e] = rope_u(z[e], zp[e], a.c[e], a.s[e]);
     } else {                         // (u, v) = (partner, own): u sin + v cos
 #pragma unroll
-        for (int e = 0; e < 4; ++e) y[e] = zp[e] * a.s[e] + z[e] * a.c[e];
+        for (int e = 0; e < 4; ++e) y[e] = rope_v(zp[e], z[e], a.c[e], a.s[e]);
     }
 }
 

@@ -22,13 +22,14 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CAPACITY, ERR_CUDA, ERR_TIMEOUT = rang
 # Entry points declared in include/h3attn.h.
 EXPORTS = ("h3attn_create", "h3attn_destroy", "h3attn_forward", "h3attn_backward",
            "h3attn_device_status", "h3attn_set_stage_timing", "h3attn_stage_times", "h3attn_forward_static",
-           "h3attn_linear", "h3attn_canonical_order", "h3attn_status_string")
+           "h3attn_linear", "h3attn_canonical_order", "h3attn_qkv_forward", "h3attn_status_string")
 
 # Limits of h3attn_forward_static's built-in scratch (include/h3attn.h).
 STATIC_MAX_TOKEN_HEADS = 131072
 STATIC_MAX_SAMPLES = 2048
 
-STAGES = ("plan", "prologue", "fwd", "bwd_delta", "bwd_dkdv", "bwd_dq", "bwd_dw", "bwd_rows", "order", "permute")
+STAGES = ("plan", "prologue", "fwd", "bwd_delta", "bwd_dkdv", "bwd_dq", "bwd_dw", "bwd_rows", "order", "permute",
+          "qkv")
 
 # Key orders (include/h3attn.h, H3ATTN_KEY_ORDER_*).
 KEY_ORDERS = {"packed": 0, "canonical": 1}
@@ -81,6 +82,9 @@ def load_library(path: str = LIB_PATH):
     lib.h3attn_linear.restype = i32
     lib.h3attn_canonical_order.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(vp), vp, i32, i32, vp, vp]
     lib.h3attn_canonical_order.restype = i32
+    lib.h3attn_qkv_forward.argtypes = [vp, vp, i32, vp, vp, vp, vp, ctypes.POINTER(vp), vp, i32, i32, vp, vp, vp, vp,
+                                       vp, vp]
+    lib.h3attn_qkv_forward.restype = i32
     lib.h3attn_status_string.argtypes = [i32]
     lib.h3attn_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -185,6 +189,27 @@ class H3Attn:
                                        _ptr(grads.get("dk_norm_w_per_sample")), _stream(stream))
         _check(st, "h3attn_backward")
         return grads
+
+    def qkv_forward(self, x, w_qkv, b_qkv, q_norm_w, k_norm_w, pos, seg_offsets, num_samples=None, q=None, k=None,
+                    v=None, out=None, lse=None, want_lse=True, stream=None):
+        """h3attn_qkv_forward: [q | k | v] = x w_qkv^T (+ b_qkv) with the q/k norm and
+        RoPE fused into the projection, then the attention forward.  x bf16 [S, in],
+        w_qkv bf16 [3 H 128, in] (q, k, v heads).  Returns (q, k, v, out, lse)."""
+        S = x.shape[0]
+        H = self.num_heads
+        n = int(seg_offsets.numel() - 1) if num_samples is None else num_samples
+        dev = x.device
+        q = torch.empty((S, H, 128), dtype=torch.bfloat16, device=dev) if q is None else q
+        k = torch.empty((S, H, 128), dtype=torch.bfloat16, device=dev) if k is None else k
+        v = torch.empty((S, H, 128), dtype=torch.bfloat16, device=dev) if v is None else v
+        out = torch.empty((S, H, 128), dtype=torch.bfloat16, device=dev) if out is None else out
+        if lse is None and want_lse:
+            lse = torch.empty((H, S), dtype=torch.float32, device=dev)
+        st = self._lib.h3attn_qkv_forward(self._h, _ptr(x), x.shape[1], _ptr(w_qkv), _ptr(b_qkv), _ptr(q_norm_w),
+                                          _ptr(k_norm_w), _pos_array(pos), _ptr(seg_offsets), n, S, _ptr(q), _ptr(k),
+                                          _ptr(v), _ptr(out), _ptr(lse), _stream(stream))
+        _check(st, "h3attn_qkv_forward")
+        return q, k, v, out, lse
 
     def canonical_order(self, q, k, v, pos, seg_offsets, dout=None, num_samples=None, perm=None, stream=None):
         """h3attn_canonical_order: int32 [S] device tensor, perm[c] = packed index
