@@ -337,10 +337,15 @@ def run_ours(args):
         for n in (3 * D, D):
             w = (torch.randn(n, D, device="cuda") / D ** 0.5).to(torch.bfloat16)
             linear(x, w, torch.randn(n, device="cuda"), error_flags=flags)
+        # and one fused QKV projection + forward (h3attn_qkv_forward) of the same tokens
+        w = (torch.randn(3 * D, D, device="cuda") / D ** 0.5).to(torch.bfloat16)
+        h.qkv_forward(x, w, 0.1 * torch.randn(3 * D, device="cuda"), d["q_norm_w"], d["k_norm_w"], d["pos"],
+                      d["seg_offsets"])
         torch.cuda.synchronize()
+        h.check()
         if rank == 0:
             print(json.dumps({"profile_run": WORKLOAD, "steps": args.steps, "warmup": args.warmup,
-                              "then": "projections qkv, out"}))
+                              "then": "projections qkv, out; fused qkv forward"}))
         return
 
     # ---- device-resident timed region
