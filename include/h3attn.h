@@ -74,6 +74,10 @@ typedef struct {
     int max_tokens;        /* capacity: largest total_tokens of any call                */
     int max_samples;       /* capacity: largest num_samples of any call                 */
     int key_order;         /* H3ATTN_KEY_ORDER_PACKED (0) or H3ATTN_KEY_ORDER_CANONICAL */
+    int store_ds;          /* 1: the dK/dV kernel also writes dS to the workspace and dQ
+                              is one product per block (faster; workspace H * ceil(T/128)
+                              * (ceil(T/128) + max_samples) * 32 KB, T = max_tokens);
+                              0: the dQ kernel recomputes S and dP                     */
 } h3attn_config;
 
 /*
@@ -113,8 +117,10 @@ typedef struct {
  * key_order CANONICAL it also allocates the order's buffers: a permutation and
  * positions (4 * max_tokens int32), row terms (H * max_tokens floats) and four
  * max_tokens * H * 128 bf16 row copies.
- * Errors: INVALID_ARG (null pointer, sizes < 1, key_order not 0 or 1),
- * UNSUPPORTED (head_dim, pairing, sections, device not sm_103), CUDA
+ * With store_ds = 1 it also allocates the stored dS blocks (see store_ds).
+ * Errors: INVALID_ARG (null pointer, sizes < 1, key_order or store_ds not 0
+ * or 1), UNSUPPORTED (head_dim, pairing, sections, device not sm_103),
+ * CAPACITY (the stored dS would exceed 2^31 rows of 128 values), CUDA
  * (allocation failed).
  */
 h3attn_status h3attn_create(const h3attn_config *cfg, h3attn_t *out);

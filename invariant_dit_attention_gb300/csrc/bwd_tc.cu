@@ -46,11 +46,19 @@ struct BwdTcParams {
     const float* delta;
     __nv_bfloat16* dv;  // dkdv kernel only
     float* dyhat;       // scale * dk^ (dkdv) or scale * dq^ (dq): FP32 [S, H, 128]
+    __half* ds;         // stored dS^T blocks (dkdv writes, dq_ds reads), or null
+    long long ds_blocks;
 };
 
 struct BwdItem {
-    int h, seg0, L, tile, row0, n_other, tile_global;
+    int h, seg0, L, tile, row0, n_other, tile_global, rank;
 };
+
+// First stored block of (sample of plan rank r, head h): the blocks of one head
+// of a sample with nq tiles are (key tile j, query tile i) at + j nq + i.
+__device__ __forceinline__ long long ds_base(const BwdTcParams& p, const BwdItem& it) {
+    return (long long)p.H * p.plan.cumsq[it.rank] + (long long)it.h * it.n_other * it.n_other;
+}
 
 // Item i over (rank, head, 128-token tile), samples longest first.
 __device__ __forceinline__ bool bwd_item(const BwdTcParams& p, int i, BwdItem& it) {
@@ -72,6 +80,7 @@ __device__ __forceinline__ bool bwd_item(const BwdTcParams& p, int i, BwdItem& i
     it.row0 = it.seg0 + 128 * it.tile;
     it.n_other = nb;
     it.tile_global = cum[lo] + it.tile;
+    it.rank = lo;
     return true;
 }
 
@@ -427,16 +436,37 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(bar(bPtFull));
                 // ---- dS = P (dP - Delta_col), fp16, over B's other 16 columns (zero where P is)
-                {
-                    uint32_t dk[16];
+                uint32_t dk[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) dk[e] = ds_f16_pair(p2[e], d2[e], lb2[16 + e]);
-                    tc::tmem_st16(tB + 16, dk);
-                }
+                for (int e = 0; e < 16; ++e) dk[e] = ds_f16_pair(p2[e], d2[e], lb2[16 + e]);
+                tc::tmem_st16(tB + 16, dk);
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(bar(bDsFull));
+                if (p.ds) {  // the block for the dQ kernel (key row t, this quarter's 32 queries), off the
+                             // tensor cores' path; rows past the sample end hold zeros
+                    const long long blk = ds_base(p, it) + (long long)it.tile * nq + qj;
+                    if (blk < p.ds_blocks) {
+                        // block layout [16-query chunk c][key][16 queries]: one warp's store of chunk c
+                        // is 1 KB contiguous; streamed once, so evict-first in L2
+                        const uint64_t pol = tc::policy_evict_first();
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const uint32_t m = key_ok ? 0xffffffffu : 0u;
+                            uint32_t* dst = reinterpret_cast<uint32_t*>(p.ds + (size_t)blk * (128 * 128) +
+                                                                       ((size_t)(2 * wg + e) * 128 + t) * 16);
+                            asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;"
+                                         ::"l"(dst), "r"(dk[8 * e] & m), "r"(dk[8 * e + 1] & m),
+                                         "r"(dk[8 * e + 2] & m), "r"(dk[8 * e + 3] & m), "r"(dk[8 * e + 4] & m),
+                                         "r"(dk[8 * e + 5] & m), "r"(dk[8 * e + 6] & m), "r"(dk[8 * e + 7] & m),
+                                         "l"(pol)
+                                         : "memory");
+                        }
+                    } else if (lane == 0) {
+                        atomicOr(p.plan.err, kErrRange);
+                    }
+                }
             }
             if (failed) break;
             // ---- drain: each warpgroup its 32 channels of dV (bf16 output rows) and of
@@ -752,6 +782,201 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
     }
 }
 
+// ------------------------------------------------------------- dQ from stored dS
+//
+// When the dK/dV kernel has written every dS^T block (fp16, [key][query], keys
+// past the sample end zero), dq^_i = scale sum_j dS_ij k^_j needs no
+// recomputation of S and dP: it is one product per block.  Item = (sample,
+// head, 128-query tile).  Warp 0 loads, per key block j, dS^T(j, i) and k^(j)
+// (key rows past the sample end zeroed: k^ may not be finite there) into one
+// of three 64 KB stages; warp 1 issues dQ += dS k^ (A = the dS^T tile read
+// MN-major, B = k^ MN-major) into one of two TMEM accumulators; warps 4-7
+// drain the finished one as scale * dq^ FP32 rows while the next item
+// accumulates.  The sum over j runs in ascending order from the sample start.
+// Bound by HBM: every stored block is read once.
+namespace dqs {
+constexpr int kThreads = 256;
+constexpr int kRingStages = 3;
+constexpr int kStage = bwdt::kPair;  // dS^T + k^ tiles: 64 KB
+constexpr int kOffBar = kRingStages * kStage;
+constexpr int kSmem = kOffBar + 256;  // the dynamic shared memory base is 1024-aligned (checked)
+enum { bFull = 0, bEmpty = bFull + kRingStages, bAccFull = bEmpty + kRingStages, bAccEmpty = bAccFull + 2, bTail = bAccEmpty + 2,
+       bDone, bCount };
+}  // namespace dqs
+
+__global__ void __launch_bounds__(dqs::kThreads, 1)
+dq_ds_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constant__ CUtensorMap mk, const BwdTcParams p) {
+    using namespace dqs;
+    using bwdt::kHalf;
+    using bwdt::kTile;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if (smem_u32(smem_raw) & 1023u) {  // the layout below needs a 1024-byte aligned base
+        if (threadIdx.x == 0) atomicOr(p.plan.err, kErrTimeout);
+        return;
+    }
+    uint8_t* smem = smem_raw;
+    const uint32_t sbase = smem_u32(smem);
+    auto bar = [&](int i) { return sbase + kOffBar + 8u * i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * bCount);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 8 * bCount + 4);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid == 0) {
+        for (int i = 0; i < kRingStages; ++i) {
+            tc::mbar_init(bar(bFull + i), 1);
+            tc::mbar_init(bar(bEmpty + i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(bar(bAccFull + i), 1);
+            tc::mbar_init(bar(bAccEmpty + i), 4);
+        }
+        tc::mbar_init(bar(bTail), 1);
+        tc::mbar_init(bar(bDone), 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+        tc::prefetch_map(&mds);
+        tc::prefetch_map(&mk);
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(smem_u32(tmem_slot), 256);
+        tc::tmem_relinquish();
+        tc::fence_before_sync();
+    }
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    bool failed = false;
+    auto fail = [&]() {
+        failed = true;
+        *abort_flag = 1;
+        atomicOr(p.plan.err, kErrTimeout);
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        const uint64_t pol = tc::policy_evict_first();
+        uint32_t blk = 0, tails = 0;
+        for (int i = blockIdx.x; !failed; i += gridDim.x) {
+            BwdItem it;
+            if (!bwd_item(p, i, it)) break;
+            const int nk = it.n_other;
+            const long long base = ds_base(p, it);
+            for (int j = 0; j < nk && !failed; ++j, ++blk) {
+                const uint32_t s = blk % kRingStages, ph = (blk / kRingStages) & 1;
+                const uint32_t dst = sbase + s * kStage;
+                const int valid = it.L - 128 * j;
+                const bool tail = valid < 128;
+                if (lane == 0) {
+                    if (!tc::mbar_wait(bar(bEmpty + s), ph ^ 1, abort_flag)) fail();
+                    if (!failed) {
+                        const uint32_t b = tail ? bar(bTail) : bar(bFull + s);
+                        const int bds = (int)(base + (long long)j * nk + it.tile);
+                        tc::mbar_expect_tx(b, 2 * kTile);
+                        for (int hf = 0; hf < 2; ++hf) {
+                            // chunks 4 hf .. 4 hf + 3 (queries 64 hf .. 64 hf + 63), read once
+                            tc::tma_load_4d_hint(dst + hf * kHalf, &mds, 0, 0, 4 * hf, bds, b, pol);
+                            tc::tma_load_2d(dst + kTile + hf * kHalf, &mk, it.h * 128 + 64 * hf, it.seg0 + 128 * j, b);
+                        }
+                        if (tail && !tc::mbar_wait(bar(bTail), tails & 1, abort_flag)) fail();
+                    }
+                }
+                failed = __shfl_sync(0xffffffffu, failed, 0);
+                if (tail && !failed) {
+                    ++tails;
+                    for (int hf = 0; hf < 2; ++hf) zero_rows(dst + kTile + hf * kHalf, valid, 128, lane);
+                    tc::fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(bar(bFull + s));
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ----------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t id = tc::idesc_f16_amn(false, true, 128, 128);  // fp16, A and B MN-major
+            // A: the dS^T tile as [16-query chunk][key][16 queries], 32-byte swizzled: atoms of
+            // 8 keys x 16 queries (256 bytes), 4 KB from one chunk to the next
+            const uint64_t dA = tc::smem_desc_sw32(sbase, 128 * 32, 256);
+            const uint64_t dB = tc::smem_desc_sw128(sbase + kTile, kHalf, 1024);
+            uint32_t blk = 0, items = 0;
+            for (int i = blockIdx.x; !failed; i += gridDim.x, ++items) {
+                BwdItem it;
+                if (!bwd_item(p, i, it)) break;
+                const uint32_t b = items & 1;
+                // the epilogue has drained this accumulator (two items ago)
+                if (items >= 2 && !tc::mbar_wait(bar(bAccEmpty + b), ((items >> 1) - 1) & 1, abort_flag)) {
+                    fail();
+                    break;
+                }
+                tc::fence_after_sync();
+                for (int j = 0; j < it.n_other; ++j, ++blk) {
+                    const uint32_t s = blk % kRingStages;
+                    if (!tc::mbar_wait(bar(bFull + s), (blk / kRingStages) & 1, abort_flag)) { fail(); break; }
+                    tc::fence_after_sync();
+                    const uint32_t so = (s * kStage) >> 4;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)  // 16 keys per step: 512 bytes of A, 2 KB of B
+                        tc::mma_ss(tmem + 128 * b, dA + so + ((kk * 512) >> 4), dB + so + ((kk * 2048) >> 4), id,
+                                   (j > 0) || (kk > 0));
+                    tc::mma_commit(bar(bEmpty + s));
+                }
+                if (failed) break;
+                tc::mma_commit(bar(bAccFull + b));
+            }
+            tc::mma_commit(bar(bDone));
+            if (!tc::mbar_wait(bar(bDone), 0, abort_flag) && !failed) fail();
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------------- drain
+        const int t = tid - 128;  // TMEM lane == query row of the tile
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        uint32_t items = 0;
+        for (int i = blockIdx.x; !failed; i += gridDim.x, ++items) {
+            BwdItem it;
+            if (!bwd_item(p, i, it)) break;
+            const uint32_t b = items & 1;
+            bool ok = true;
+            if (lane == 0) ok = tc::mbar_wait(bar(bAccFull + b), (items >> 1) & 1, abort_flag);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) { fail(); break; }
+            tc::fence_after_sync();
+            const bool row_ok = 128 * it.tile + t < it.L;
+            float* dst = p.dyhat + ((size_t)(it.row0 + t) * p.H + it.h) * kD;
+#pragma unroll
+            for (int c32 = 0; c32 < 4; ++c32) {
+                uint32_t r[32];
+                tc::tmem_ld32(tmem + lane_base + 128 * b + 32 * c32, r);
+                tc::tmem_wait_ld_dep(r);
+                if (row_ok) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4*>(dst + 32 * c32 + e) =
+                            make_float4(__uint_as_float(r[e]) * p.scale, __uint_as_float(r[e + 1]) * p.scale,
+                                        __uint_as_float(r[e + 2]) * p.scale, __uint_as_float(r[e + 3]) * p.scale);
+                }
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(bar(bAccEmpty + b));
+        }
+    }
+
+    __syncthreads();
+    if (warp == 0 && lane == 0 && *abort_flag) {
+        // let any TMA still in flight land before the CTA's shared memory goes away
+        const long long t0 = clock64();
+        while (clock64() - t0 < 20000000LL) {
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 256);
+    }
+}
+
 // ------------------------------------------------------------------ host
 
 namespace {
@@ -796,6 +1021,8 @@ cudaError_t init_bwd_attributes() {
         e = cudaFuncSetAttribute(dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kvt::kSmem);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dqt::kSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(dq_ds_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dqs::kSmem);
     return e;
 }
 
@@ -807,6 +1034,8 @@ static BwdTcParams bwd_params(const Problem& p, const Workspace& ws, const float
     b.scale = p.scale;
     b.lse = lse;
     b.delta = ws.delta;
+    b.ds = ws.ds;
+    b.ds_blocks = ws.ds_blocks;
     return b;
 }
 
@@ -828,6 +1057,21 @@ cudaError_t launch_bwd_dq(const Problem& p, const Workspace& ws, const float* ls
     BwdTcParams b = bwd_params(p, ws, lse);
     b.dv = nullptr;
     b.dyhat = ws.dqhat32;
+    if (ws.ds) {  // dS was stored by the dK/dV kernel: dQ is one product per block
+        // a block is [16-query chunk][key][16 queries] (query in chunk, key, chunk, block);
+        // a box of 4 chunks lands in shared memory in the same order, 32-byte swizzled
+        CUtensorMap mds;
+        const cuuint64_t dims[4] = {16, 128, 8, (cuuint64_t)ws.ds_blocks};
+        const cuuint64_t strides[3] = {16 * 2, 128 * 16 * 2, 128 * 128 * 2};
+        const cuuint32_t box[4] = {16, 128, 4, 1};
+        const cuuint32_t es[4] = {1, 1, 1, 1};
+        if (g_encode_b(&mds, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, ws.ds, dims, strides, box, es,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        dq_ds_kernel<<<g_sms_b, dqs::kThreads, dqs::kSmem, st>>>(mds, m.k, b);
+        return cudaGetLastError();
+    }
     dq_tc_kernel<<<g_sms_b, dqt::kThreads, dqt::kSmem, st>>>(m.q, m.k, m.v, m.dout, b);
     return cudaGetLastError();
 }

@@ -40,6 +40,8 @@ struct Plan {
     int* cum128;     // [max_samples + 1] tiles of 128 tokens before rank r
     int* cum256;     // [max_samples + 1] blocks of 256 tokens before rank r
     int* rank_of;    // [max_samples] rank of sample s
+    int* cumsq;      // [max_samples + 1] sum of (tiles of 128 tokens)^2 before rank r: the
+                     //   128 x 128 score blocks of one head of the samples before it
     unsigned* err;   // device error word
 };
 
@@ -204,6 +206,12 @@ struct Workspace {
     float* lse_c;            // [H, max_tokens] softmax row terms in canonical order
     __nv_bfloat16* rows_c[4];  // [max_tokens, H, 128] each, canonical order: v, out, dout, dv
     uint4* keys;             // [max_tokens] sort keys of the canonical order
+    // stored dS (null if the handle recomputes it in the dQ kernel): fp16 128 x 128
+    // blocks of dS^T laid out [16-query chunk][key][16 queries], block (sample of rank
+    // r, head h, key tile j, query tile i) at H cumsq[r] + h nq^2 + j nq + i, nq = the
+    // sample's 128-token tiles
+    __half* ds;
+    long long ds_blocks;     // capacity in blocks
 };
 
 struct Problem {

@@ -23,10 +23,10 @@ using namespace h3;
 
 namespace {
 
-constexpr size_t kPlanBytes = 64u << 10;  // order, rank, three cumulative tables, error word
+constexpr size_t kPlanBytes = 64u << 10;  // order, rank, four cumulative tables, error word
 constexpr size_t kRowBytes = (size_t)H3ATTN_STATIC_MAX_TOKEN_HEADS * kD * 2;  // one fp16 [S, H, 128] buffer
 constexpr size_t kScratchBytes = kPlanBytes + 2 * kRowBytes;
-static_assert((H3ATTN_STATIC_MAX_SAMPLES + 1) * 4 * 5 + 16 <= kPlanBytes, "plan region too small");
+static_assert((H3ATTN_STATIC_MAX_SAMPLES + 1) * 4 * 6 + 16 <= kPlanBytes, "plan region too small");
 
 // The shared scratch.  Host code must not use this name as an address: it is
 // resolved per device with cudaGetSymbolAddress below.
@@ -121,7 +121,8 @@ extern "C" h3attn_status h3attn_forward_static(const h3attn_config* cfg, const h
     ws.plan.cum64 = ints + 2 * n1;
     ws.plan.cum128 = ints + 3 * n1;
     ws.plan.cum256 = ints + 4 * n1;
-    ws.plan.err = reinterpret_cast<unsigned*>(ints + 5 * n1);
+    ws.plan.cumsq = ints + 5 * n1;
+    ws.plan.err = reinterpret_cast<unsigned*>(ints + 6 * n1);
     ws.qhat = reinterpret_cast<__half*>(base + kPlanBytes);
     ws.khat = reinterpret_cast<__half*>(base + kPlanBytes + kRowBytes);
 

@@ -170,6 +170,12 @@ h3attn_status h3attn_create(const h3attn_config* cfg, h3attn_t* out) {
     if (!(cfg->eps >= 0.f) || !(cfg->rope_theta > 0.f) || !(cfg->softmax_scale >= 0.f)) return H3ATTN_ERR_INVALID_ARG;
     if (cfg->key_order != H3ATTN_KEY_ORDER_PACKED && cfg->key_order != H3ATTN_KEY_ORDER_CANONICAL)
         return H3ATTN_ERR_INVALID_ARG;
+    if (cfg->store_ds != 0 && cfg->store_ds != 1) return H3ATTN_ERR_INVALID_ARG;
+    {
+        const long long t128 = ((long long)cfg->max_tokens + 127) / 128;
+        if (cfg->store_ds && (long long)cfg->num_heads * t128 * (t128 + cfg->max_samples) * 128 >= (1LL << 31))
+            return H3ATTN_ERR_CAPACITY;  // TMA row coordinates of the stored blocks are 32-bit
+    }
     if (cfg->head_dim != kD || cfg->rope_pairing != 0) return H3ATTN_ERR_UNSUPPORTED;
     if ((long)cfg->max_tokens * cfg->num_heads * kD >= (1L << 40)) return H3ATTN_ERR_CAPACITY;
     RopeTable rt;
@@ -197,9 +203,15 @@ h3attn_status h3attn_create(const h3attn_config* cfg, h3attn_t* out) {
               ws_alloc(h, &ws.dwq_sample, N * kD * 4) && ws_alloc(h, &ws.dwk_sample, N * kD * 4) &&
               ws_alloc(h, &ws.plan.order, N * 4) && ws_alloc(h, &ws.plan.rank_of, N * 4) &&
               ws_alloc(h, &ws.plan.cum64, (N + 1) * 4) && ws_alloc(h, &ws.plan.cum128, (N + 1) * 4) &&
-              ws_alloc(h, &ws.plan.cum256, (N + 1) * 4) &&
+              ws_alloc(h, &ws.plan.cum256, (N + 1) * 4) && ws_alloc(h, &ws.plan.cumsq, (N + 1) * 4) &&
               ws_alloc(h, &ws.plan.err, 4);
     if (ok) ok = ws_alloc(h, &ws.keys, T * 16);
+    if (ok && cfg->store_ds) {
+        // sum over samples of tiles^2 <= (largest tiles) * (sum of tiles) <= ceil(T/128) (ceil(T/128) + N)
+        const long long t128 = ((long long)T + 127) / 128;
+        ws.ds_blocks = (long long)H * t128 * (t128 + (long long)N);
+        ok = ws_alloc(h, &ws.ds, (size_t)ws.ds_blocks * 128 * kD * 2);
+    }
     if (ok && cfg->key_order == H3ATTN_KEY_ORDER_CANONICAL) {
         ok = ws_alloc(h, &ws.perm, T * 4) && ws_alloc(h, &ws.pos_c, 3 * T * 4) && ws_alloc(h, &ws.lse_c, T * H * 4);
         for (int t = 0; ok && t < 4; ++t) ok = ws_alloc(h, &ws.rows_c[t], T * H * kD * 2);

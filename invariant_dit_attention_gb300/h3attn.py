@@ -45,7 +45,18 @@ class Config(ctypes.Structure):
     _fields_ = [("num_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("eps", ctypes.c_float),
                 ("rope_theta", ctypes.c_float), ("rope_sections", ctypes.c_int * 3),
                 ("rope_pairing", ctypes.c_int), ("softmax_scale", ctypes.c_float),
-                ("max_tokens", ctypes.c_int), ("max_samples", ctypes.c_int), ("key_order", ctypes.c_int)]
+                ("max_tokens", ctypes.c_int), ("max_samples", ctypes.c_int), ("key_order", ctypes.c_int),
+                ("store_ds", ctypes.c_int)]
+
+
+def stored_ds_bytes(num_heads: int, max_tokens: int, max_samples: int) -> int:
+    """Workspace of the stored dS blocks (include/h3attn.h, store_ds)."""
+    t128 = (max_tokens + 127) // 128
+    return num_heads * t128 * (t128 + max_samples) * 128 * 128 * 2
+
+
+# store_ds="auto" turns the stored dS on while its workspace stays below this.
+STORED_DS_AUTO_LIMIT = 32 << 30
 
 
 _lib = None
@@ -121,10 +132,13 @@ class H3Attn:
 
     def __init__(self, num_heads: int, max_tokens: int, max_samples: int = 64, eps: float = 1e-6,
                  rope_theta: float = 10000.0, rope_sections=(16, 24, 24), softmax_scale: float = 0.0,
-                 key_order: str = "packed"):
+                 key_order: str = "packed", store_ds="auto"):
         """``key_order``: "packed" sums over a sample's tokens in memory order,
         "canonical" in an order fixed by the tokens themselves, so that results
-        do not depend on how each sample's tokens are permuted."""
+        do not depend on how each sample's tokens are permuted.
+        ``store_ds``: True keeps dS from the dK/dV kernel for the dQ kernel (see
+        ``stored_ds_bytes`` for its workspace), False recomputes it, "auto"
+        stores it while the workspace stays under STORED_DS_AUTO_LIMIT."""
         lib = load_library()
         if key_order not in KEY_ORDERS:
             raise ValueError(f"key_order must be one of {sorted(KEY_ORDERS)}")
@@ -134,6 +148,10 @@ class H3Attn:
         cfg.rope_pairing, cfg.softmax_scale = 0, softmax_scale
         cfg.max_tokens, cfg.max_samples = max_tokens, max_samples
         cfg.key_order = KEY_ORDERS[key_order]
+        if store_ds == "auto":
+            store_ds = stored_ds_bytes(num_heads, max_tokens, max_samples) <= STORED_DS_AUTO_LIMIT
+        cfg.store_ds = 1 if store_ds else 0
+        self.store_ds = bool(store_ds)
         h = ctypes.c_void_p()
         _check(lib.h3attn_create(ctypes.byref(cfg), ctypes.byref(h)), "h3attn_create")
         self._h = h

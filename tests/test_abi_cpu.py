@@ -59,6 +59,7 @@ def _cfg(**kw):
     (dict(head_dim=64), 2), (dict(rope_pairing=1), 2), (dict(rope_sections=[12, 24, 24]), 2),
     (dict(rope_sections=[64, 64, 8]), 2), (dict(num_heads=0), 1), (dict(max_tokens=0), 1),
     (dict(max_samples=0), 1), (dict(eps=-1.0), 1), (dict(key_order=2), 1), (dict(key_order=-1), 1),
+    (dict(store_ds=2), 1), (dict(store_ds=1, num_heads=48, max_tokens=1 << 22), 3),
 ])
 def test_create_rejects_bad_config_on_host(kw, status):
     from invariant_dit_attention_gb300.h3attn import load_library

@@ -10,9 +10,9 @@ from tests.helpers import BWD_REL_L2, make_handle, need_gpu, np64, oracle_backwa
 pytestmark = pytest.mark.gpu
 
 
-def run_fwd_bwd(inp, max_samples=64):
+def run_fwd_bwd(inp, max_samples=64, store_ds="auto"):
     from invariant_dit_attention_gb300.h3attn import to_device
-    h = make_handle(inp.num_heads, max(inp.total_tokens, 1), max_samples)
+    h = make_handle(inp.num_heads, max(inp.total_tokens, 1), max_samples, store_ds=store_ds)
     d = to_device(inp)
     out, lse = h.forward(d["q"], d["k"], d["v"], d["q_norm_w"], d["k_norm_w"], d["pos"], d["seg_offsets"])
     g = h.backward(d["q"], d["k"], d["v"], d["q_norm_w"], d["k_norm_w"], d["pos"], d["seg_offsets"], out, lse,
@@ -49,6 +49,15 @@ def test_backward_ragged(lengths):
     inp = W.make_inputs(lengths, 6, seed=7 + sum(lengths), with_grad=True)
     _, _, g = run_fwd_bwd(inp)
     check_grads(g, oracle_backward(("ragged_bwd", tuple(lengths)), inp), inp.num_samples)
+
+
+@pytest.mark.parametrize("store_ds", [False, True])
+def test_backward_both_dq_paths(store_ds):
+    """dQ from the dS the dK/dV kernel stored, and dQ recomputing S and dP."""
+    need_gpu()
+    inp = W.make_inputs([1, 64, 65, 300], 6, seed=321, with_grad=True)
+    _, _, g = run_fwd_bwd(inp, store_ds=store_ds)
+    check_grads(g, oracle_backward("both_dq_paths", inp), inp.num_samples)
 
 
 def test_backward_single_925():
