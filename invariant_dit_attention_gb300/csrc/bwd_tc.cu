@@ -784,25 +784,54 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 
 // ------------------------------------------------------------- dQ from stored dS
 //
-// When the dK/dV kernel has written every dS^T block (fp16, [key][query], keys
-// past the sample end zero), dq^_i = scale sum_j dS_ij k^_j needs no
-// recomputation of S and dP: it is one product per block.  Item = (sample,
-// head, 128-query tile).  Warp 0 loads, per key block j, dS^T(j, i) and k^(j)
-// (key rows past the sample end zeroed: k^ may not be finite there) into one
-// of three 64 KB stages; warp 1 issues dQ += dS k^ (A = the dS^T tile read
-// MN-major, B = k^ MN-major) into one of two TMEM accumulators; warps 4-7
-// drain the finished one as scale * dq^ FP32 rows while the next item
-// accumulates.  The sum over j runs in ascending order from the sample start.
-// Bound by HBM: every stored block is read once.
+// When the dK/dV kernel has written every dS^T block (fp16, keys past the
+// sample end zero), dq^_i = scale sum_j dS_ij k^_j needs no recomputation of S
+// and dP: it is one product per block.  Item = (sample, head, pair of 128-query
+// tiles), so each k^ tile is loaded once for two tiles' products.  Warp 0
+// loads, per key block j, dS^T(j, i0), dS^T(j, i1) and k^(j) (key rows past the
+// sample end zeroed: k^ may not be finite there) into one of two 96 KB stages;
+// warp 1 issues dQ0 += dS0 k^ and dQ1 += dS1 k^ (A = a dS^T tile read MN-major
+// from its 32-byte swizzled chunks, B = k^ MN-major) into one of two pairs of
+// TMEM accumulators; warps 4-7 drain the finished pair as scale * dq^ FP32 rows
+// while the next item accumulates.  The sum over j runs in ascending order
+// from the sample start.  Bound by HBM: every stored block is read once.
 namespace dqs {
 constexpr int kThreads = 256;
-constexpr int kRingStages = 3;
-constexpr int kStage = bwdt::kPair;  // dS^T + k^ tiles: 64 KB
+constexpr int kRingStages = 2;
+constexpr int kStage = 3 * bwdt::kTile;  // dS^T of two query tiles + k^: 96 KB
 constexpr int kOffBar = kRingStages * kStage;
 constexpr int kSmem = kOffBar + 256;  // the dynamic shared memory base is 1024-aligned (checked)
-enum { bFull = 0, bEmpty = bFull + kRingStages, bAccFull = bEmpty + kRingStages, bAccEmpty = bAccFull + 2, bTail = bAccEmpty + 2,
-       bDone, bCount };
+enum { bFull = 0, bEmpty = bFull + kRingStages, bAccFull = bEmpty + kRingStages, bAccEmpty = bAccFull + 2,
+       bTail = bAccEmpty + 2, bDone, bCount };
 }  // namespace dqs
+
+struct DqsItem {
+    int h, seg0, L, pair, nq, rank;
+    bool has1;  // the pair's second query tile exists
+};
+
+// Item i over (rank, head, 256-token query pair), samples longest first.
+__device__ __forceinline__ bool dqs_item(const BwdTcParams& p, int i, DqsItem& it) {
+    const int n = p.seq.n;
+    const int* cum = p.plan.cum256;
+    if (i >= p.H * cum[n]) return false;
+    int lo = 0, hi = n;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (p.H * cum[mid] <= i) lo = mid; else hi = mid;
+    }
+    const int np = cum[lo + 1] - cum[lo];
+    const int local = i - p.H * cum[lo];
+    const int s = p.plan.order[lo];
+    it.h = local / np;
+    it.pair = local % np;
+    it.seg0 = p.seq.seg[s];
+    it.L = p.seq.seg[s + 1] - it.seg0;
+    it.nq = (it.L + 127) / 128;
+    it.rank = lo;
+    it.has1 = 2 * it.pair + 1 < it.nq;
+    return true;
+}
 
 __global__ void __launch_bounds__(dqs::kThreads, 1)
 dq_ds_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constant__ CUtensorMap mk, const BwdTcParams p) {
@@ -838,7 +867,7 @@ dq_ds_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constant__ CU
         tc::prefetch_map(&mk);
     }
     if (warp == 1) {
-        tc::tmem_alloc(smem_u32(tmem_slot), 256);
+        tc::tmem_alloc(smem_u32(tmem_slot), 512);
         tc::tmem_relinquish();
         tc::fence_before_sync();
     }
@@ -857,11 +886,10 @@ dq_ds_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constant__ CU
         const uint64_t pol = tc::policy_evict_first();
         uint32_t blk = 0, tails = 0;
         for (int i = blockIdx.x; !failed; i += gridDim.x) {
-            BwdItem it;
-            if (!bwd_item(p, i, it)) break;
-            const int nk = it.n_other;
-            const long long base = ds_base(p, it);
-            for (int j = 0; j < nk && !failed; ++j, ++blk) {
+            DqsItem it;
+            if (!dqs_item(p, i, it)) break;
+            const long long base = (long long)p.H * p.plan.cumsq[it.rank] + (long long)it.h * it.nq * it.nq;
+            for (int j = 0; j < it.nq && !failed; ++j, ++blk) {
                 const uint32_t s = blk % kRingStages, ph = (blk / kRingStages) & 1;
                 const uint32_t dst = sbase + s * kStage;
                 const int valid = it.L - 128 * j;
@@ -870,12 +898,13 @@ dq_ds_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constant__ CU
                     if (!tc::mbar_wait(bar(bEmpty + s), ph ^ 1, abort_flag)) fail();
                     if (!failed) {
                         const uint32_t b = tail ? bar(bTail) : bar(bFull + s);
-                        const int bds = (int)(base + (long long)j * nk + it.tile);
-                        tc::mbar_expect_tx(b, 2 * kTile);
+                        const int b0 = (int)(base + (long long)j * it.nq + 2 * it.pair);
+                        tc::mbar_expect_tx(b, (it.has1 ? 3 : 2) * kTile);
                         for (int hf = 0; hf < 2; ++hf) {
                             // chunks 4 hf .. 4 hf + 3 (queries 64 hf .. 64 hf + 63), read once
-                            tc::tma_load_4d_hint(dst + hf * kHalf, &mds, 0, 0, 4 * hf, bds, b, pol);
-                            tc::tma_load_2d(dst + kTile + hf * kHalf, &mk, it.h * 128 + 64 * hf, it.seg0 + 128 * j, b);
+                            tc::tma_load_4d_hint(dst + hf * kHalf, &mds, 0, 0, 4 * hf, b0, b, pol);
+                            if (it.has1) tc::tma_load_4d_hint(dst + kTile + hf * kHalf, &mds, 0, 0, 4 * hf, b0 + 1, b, pol);
+                            tc::tma_load_2d(dst + 2 * kTile + hf * kHalf, &mk, it.h * 128 + 64 * hf, it.seg0 + 128 * j, b);
                         }
                         if (tail && !tc::mbar_wait(bar(bTail), tails & 1, abort_flag)) fail();
                     }
@@ -883,7 +912,7 @@ dq_ds_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constant__ CU
                 failed = __shfl_sync(0xffffffffu, failed, 0);
                 if (tail && !failed) {
                     ++tails;
-                    for (int hf = 0; hf < 2; ++hf) zero_rows(dst + kTile + hf * kHalf, valid, 128, lane);
+                    for (int hf = 0; hf < 2; ++hf) zero_rows(dst + 2 * kTile + hf * kHalf, valid, 128, lane);
                     tc::fence_proxy_async();
                     __syncwarp();
                     if (lane == 0) tc::mbar_arrive(bar(bFull + s));
@@ -895,30 +924,36 @@ dq_ds_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constant__ CU
         // ----------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t id = tc::idesc_f16_amn(false, true, 128, 128);  // fp16, A and B MN-major
-            // A: the dS^T tile as [16-query chunk][key][16 queries], 32-byte swizzled: atoms of
+            // A: a dS^T tile as [16-query chunk][key][16 queries], 32-byte swizzled: atoms of
             // 8 keys x 16 queries (256 bytes), 4 KB from one chunk to the next
             const uint64_t dA = tc::smem_desc_sw32(sbase, 128 * 32, 256);
-            const uint64_t dB = tc::smem_desc_sw128(sbase + kTile, kHalf, 1024);
+            const uint64_t dB = tc::smem_desc_sw128(sbase + 2 * kTile, kHalf, 1024);
             uint32_t blk = 0, items = 0;
             for (int i = blockIdx.x; !failed; i += gridDim.x, ++items) {
-                BwdItem it;
-                if (!bwd_item(p, i, it)) break;
+                DqsItem it;
+                if (!dqs_item(p, i, it)) break;
                 const uint32_t b = items & 1;
-                // the epilogue has drained this accumulator (two items ago)
+                // the epilogue has drained this accumulator pair (two items ago)
                 if (items >= 2 && !tc::mbar_wait(bar(bAccEmpty + b), ((items >> 1) - 1) & 1, abort_flag)) {
                     fail();
                     break;
                 }
                 tc::fence_after_sync();
-                for (int j = 0; j < it.n_other; ++j, ++blk) {
+                for (int j = 0; j < it.nq; ++j, ++blk) {
                     const uint32_t s = blk % kRingStages;
                     if (!tc::mbar_wait(bar(bFull + s), (blk / kRingStages) & 1, abort_flag)) { fail(); break; }
                     tc::fence_after_sync();
                     const uint32_t so = (s * kStage) >> 4;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)  // 16 keys per step: 512 bytes of A, 2 KB of B
-                        tc::mma_ss(tmem + 128 * b, dA + so + ((kk * 512) >> 4), dB + so + ((kk * 2048) >> 4), id,
+                        tc::mma_ss(tmem + 256 * b, dA + so + ((kk * 512) >> 4), dB + so + ((kk * 2048) >> 4), id,
                                    (j > 0) || (kk > 0));
+                    if (it.has1) {
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            tc::mma_ss(tmem + 256 * b + 128, dA + so + ((kTile + kk * 512) >> 4),
+                                       dB + so + ((kk * 2048) >> 4), id, (j > 0) || (kk > 0));
+                    }
                     tc::mma_commit(bar(bEmpty + s));
                 }
                 if (failed) break;
@@ -930,31 +965,34 @@ dq_ds_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constant__ CU
         __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------------------------- drain
-        const int t = tid - 128;  // TMEM lane == query row of the tile
+        const int t = tid - 128;  // TMEM lane == query row of each tile
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         uint32_t items = 0;
         for (int i = blockIdx.x; !failed; i += gridDim.x, ++items) {
-            BwdItem it;
-            if (!bwd_item(p, i, it)) break;
+            DqsItem it;
+            if (!dqs_item(p, i, it)) break;
             const uint32_t b = items & 1;
             bool ok = true;
             if (lane == 0) ok = tc::mbar_wait(bar(bAccFull + b), (items >> 1) & 1, abort_flag);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) { fail(); break; }
             tc::fence_after_sync();
-            const bool row_ok = 128 * it.tile + t < it.L;
-            float* dst = p.dyhat + ((size_t)(it.row0 + t) * p.H + it.h) * kD;
+            for (int u = 0; u < (it.has1 ? 2 : 1); ++u) {
+                const int r_in = 256 * it.pair + 128 * u + t;  // query row within the sample
+                const bool row_ok = r_in < it.L;
+                float* dst = p.dyhat + ((size_t)(it.seg0 + r_in) * p.H + it.h) * kD;
 #pragma unroll
-            for (int c32 = 0; c32 < 4; ++c32) {
-                uint32_t r[32];
-                tc::tmem_ld32(tmem + lane_base + 128 * b + 32 * c32, r);
-                tc::tmem_wait_ld_dep(r);
-                if (row_ok) {
+                for (int c32 = 0; c32 < 4; ++c32) {
+                    uint32_t r[32];
+                    tc::tmem_ld32(tmem + lane_base + 256 * b + 128 * u + 32 * c32, r);
+                    tc::tmem_wait_ld_dep(r);
+                    if (row_ok) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        *reinterpret_cast<float4*>(dst + 32 * c32 + e) =
-                            make_float4(__uint_as_float(r[e]) * p.scale, __uint_as_float(r[e + 1]) * p.scale,
-                                        __uint_as_float(r[e + 2]) * p.scale, __uint_as_float(r[e + 3]) * p.scale);
+                        for (int e = 0; e < 32; e += 4)
+                            *reinterpret_cast<float4*>(dst + 32 * c32 + e) =
+                                make_float4(__uint_as_float(r[e]) * p.scale, __uint_as_float(r[e + 1]) * p.scale,
+                                            __uint_as_float(r[e + 2]) * p.scale, __uint_as_float(r[e + 3]) * p.scale);
+                    }
                 }
             }
             tc::fence_before_sync();
@@ -973,7 +1011,7 @@ dq_ds_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constant__ CU
     __syncthreads();
     if (warp == 1) {
         tc::fence_after_sync();
-        tc::tmem_dealloc(tmem, 256);
+        tc::tmem_dealloc(tmem, 512);
     }
 }
 
