@@ -73,8 +73,9 @@ __device__ __forceinline__ RowAngles row_angles(const LaneRope& lr, int pt, int 
 __device__ __forceinline__ float sq4(float x0, float x1, float x2, float x3) {
     return __fmaf_rn(x3, x3, __fmaf_rn(x2, x2, __fmaf_rn(x1, x1, __fmul_rn(x0, x0))));
 }
-//   1 / sqrt(mean of squares + eps) from the row's sum of squares
-__device__ __forceinline__ float rstd_of(float ss, float eps) { return 1.0f / sqrtf(__fmaf_rn(ss, 1.0f / kD, eps)); }
+//   1 / sqrt(mean of squares + eps) from the row's sum of squares, correctly
+//   rounded (one rounding)
+__device__ __forceinline__ float rstd_of(float ss, float eps) { return __frsqrt_rn(__fmaf_rn(ss, 1.0f / kD, eps)); }
 //   z = (x r) w
 __device__ __forceinline__ float norm_w(float x, float r, float w) { return __fmul_rn(__fmul_rn(x, r), w); }
 //   the rotated pair (u, v) -> (u cos - v sin, u sin + v cos)
@@ -147,15 +148,17 @@ __device__ __forceinline__ void load_row4(const __nv_bfloat16* p, float (&x)[4])
     x[0] = bf16_lo(u.x); x[1] = bf16_hi(u.x); x[2] = bf16_lo(u.y); x[3] = bf16_hi(u.y);
 }
 
-// Rounds the row to fp16 and stores it; returns false if a value overflowed.
+// Rounds the row to fp16 and stores it; returns false if the four values are
+// finite and one of them is beyond the fp16 range (non-finite inputs are not
+// range errors).  y - y is 0 for a finite y and NaN otherwise.
 __device__ __forceinline__ bool store_row4_f16(__half* p, const float (&y)[4]) {
     uint2 u;
     u.x = pack_f16(y[0], y[1]);
     u.y = pack_f16(y[2], y[3]);
     *reinterpret_cast<uint2*>(p) = u;
-    const bool ok = fabsf(y[0]) <= 65504.f && fabsf(y[1]) <= 65504.f && fabsf(y[2]) <= 65504.f &&
-                    fabsf(y[3]) <= 65504.f;
-    return ok || !(isfinite(y[0]) && isfinite(y[1]) && isfinite(y[2]) && isfinite(y[3]));
+    const float m = fmaxf(fmaxf(fabsf(y[0]), fabsf(y[1])), fmaxf(fabsf(y[2]), fabsf(y[3])));
+    const float t = ((y[0] - y[0]) + (y[1] - y[1])) + ((y[2] - y[2]) + (y[3] - y[3]));
+    return m <= 65504.f || t != 0.f;
 }
 
 __device__ __forceinline__ void store_row4(__nv_bfloat16* p, const float (&y)[4]) {
