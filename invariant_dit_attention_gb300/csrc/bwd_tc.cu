@@ -6,16 +6,17 @@
 //   Delta_i = sum_c dO_ic O_ic                                         (delta_kernel, bwd_rows.cu)
 //   P_ij = exp(scale q^_i.k^_j - lse_i),  dP_ij = dO_i . v_j,  dS_ij = P_ij (dP_ij - Delta_i)
 //   dV_j = sum_i P_ij dO_i,  dk^_j = scale sum_i dS_ij q^_i              (dkdv_tc_kernel)
-//   dq^_i = scale sum_j dS_ij k^_j                                       (dq_tc_kernel)
-// Both leave scale * dk^ and scale * dq^ as FP32 rows for rows_bwd_kernel
+//   dq^_i = scale sum_j dS_ij k^_j                        (dq_ds_kernel or dq_tc_kernel)
+// They leave scale * dk^ and scale * dq^ as FP32 rows for rows_bwd_kernel
 // (bwd_rows.cu), which applies RoPE^-1 and the RMSNorm backward.
 //
-// No atomics anywhere: dkdv and dq each recompute S and P (7 tile products for
-// the 5 of the algorithm) and every sum runs over tiles anchored at the sample
-// start in ascending order, so a sample's gradients are the same bits alone or
-// packed.
+// No atomics anywhere: dQ is a second pass, either over the dS blocks that
+// dkdv stored (dq_ds_kernel) or recomputing S and P (dq_tc_kernel: 7 tile
+// products for the 5 of the algorithm), and every sum runs over tiles anchored
+// at the sample start in ascending order, so a sample's gradients are the same
+// bits alone or packed.
 //
-// Both kernels are persistent (one CTA per SM, 640 threads): warps 0 and 2 TMA
+// dkdv and dq_tc are persistent (one CTA per SM, 640 threads): warps 0 and 2 TMA
 // producers (one per streamed ring), warp 1 the single-thread tcgen05 issuer,
 // warps 4-19 four warpgroups that split each 128 x 128 score block by columns
 // (thread = TMEM lane = one row of the CTA's 128-row tile) and compute on
