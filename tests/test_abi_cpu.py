@@ -79,3 +79,18 @@ def test_null_handle_and_pointers_rejected():
     assert lib.h3attn_forward(None, None, None, None, None, None, pos, None, 1, 4, None, None, None) == 1
     assert lib.h3attn_device_status(None, None) == 1
     assert lib.h3attn_destroy(None) == 0
+
+
+def test_static_forward_and_new_entry_points_reject_on_host():
+    """Checks that need no device: the static forward offers only the packed key
+    order; the fused QKV forward and the canonical-order call reject a null
+    handle."""
+    from invariant_dit_attention_gb300.h3attn import load_library
+    lib_built()
+    lib = load_library()
+    pos = (ctypes.c_void_p * 3)()
+    assert lib.h3attn_forward_static(ctypes.byref(_cfg(key_order=1)), None, None, None, None, None, pos, None,
+                                     1, 4, None, None, None, None) == 2
+    assert lib.h3attn_qkv_forward(None, None, 64, None, None, None, None, pos, None, 1, 4, None, None, None, None,
+                                  None, None) == 1
+    assert lib.h3attn_canonical_order(None, None, None, None, None, pos, None, 1, 4, None, None) == 1
