@@ -136,7 +136,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     };
 
     // Register split: the producer/issuer warpgroup gives registers to the two
-    // softmax warpgroups (launch: 384 x 168 = 128 x 56 + 256 x 224).
+    // softmax warpgroups (launch: 384 x 168 = 128 x 152 + 256 x 176).
     if (warp < 4) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 152;");
     } else {
