@@ -449,14 +449,14 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                              // tensor cores' path; rows past the sample end hold zeros
                     const long long blk = ds_base(p, it) + (long long)it.tile * nq + qj;
                     if (blk < p.ds_blocks) {
-                        // block layout [16-query chunk c][key][16 queries]: one warp's store of chunk c
-                        // is 1 KB contiguous; streamed once, so evict-first in L2
+                        // block layout [32-query chunk wg][key][32 queries]: a warp's 32 key rows of its
+                        // chunk are 2 KB contiguous; streamed once, so evict-first in L2
                         const uint64_t pol = tc::policy_evict_first();
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
                             const uint32_t m = key_ok ? 0xffffffffu : 0u;
                             uint32_t* dst = reinterpret_cast<uint32_t*>(p.ds + (size_t)blk * (128 * 128) +
-                                                                       ((size_t)(2 * wg + e) * 128 + t) * 16);
+                                                                       ((size_t)wg * 128 + t) * 32 + 16 * e);
                             asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;"
                                          ::"l"(dst), "r"(dk[8 * e] & m), "r"(dk[8 * e + 1] & m),
                                          "r"(dk[8 * e + 2] & m), "r"(dk[8 * e + 3] & m), "r"(dk[8 * e + 4] & m),
@@ -902,9 +902,9 @@ dq_ds_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constant__ CU
                         const int b0 = (int)(base + (long long)j * it.nq + 2 * it.pair);
                         tc::mbar_expect_tx(b, (it.has1 ? 3 : 2) * kTile);
                         for (int hf = 0; hf < 2; ++hf) {
-                            // chunks 4 hf .. 4 hf + 3 (queries 64 hf .. 64 hf + 63), read once
-                            tc::tma_load_4d_hint(dst + hf * kHalf, &mds, 0, 0, 4 * hf, b0, b, pol);
-                            if (it.has1) tc::tma_load_4d_hint(dst + kTile + hf * kHalf, &mds, 0, 0, 4 * hf, b0 + 1, b, pol);
+                            // chunks 2 hf, 2 hf + 1 (queries 64 hf .. 64 hf + 63), read once
+                            tc::tma_load_4d_hint(dst + hf * kHalf, &mds, 0, 0, 2 * hf, b0, b, pol);
+                            if (it.has1) tc::tma_load_4d_hint(dst + kTile + hf * kHalf, &mds, 0, 0, 2 * hf, b0 + 1, b, pol);
                             tc::tma_load_2d(dst + 2 * kTile + hf * kHalf, &mk, it.h * 128 + 64 * hf, it.seg0 + 128 * j, b);
                         }
                         if (tail && !tc::mbar_wait(bar(bTail), tails & 1, abort_flag)) fail();
@@ -925,9 +925,9 @@ dq_ds_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constant__ CU
         // ----------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t id = tc::idesc_f16_amn(false, true, 128, 128);  // fp16, A and B MN-major
-            // A: a dS^T tile as [16-query chunk][key][16 queries], 32-byte swizzled: atoms of
-            // 8 keys x 16 queries (256 bytes), 4 KB from one chunk to the next
-            const uint64_t dA = tc::smem_desc_sw32(sbase, 128 * 32, 256);
+            // A: a dS^T tile as [32-query chunk][key][32 queries], 64-byte swizzled: atoms of
+            // 8 keys x 32 queries (512 bytes), 8 KB from one chunk to the next
+            const uint64_t dA = tc::smem_desc_sw64(sbase, 128 * 64, 512);
             const uint64_t dB = tc::smem_desc_sw128(sbase + 2 * kTile, kHalf, 1024);
             uint32_t blk = 0, items = 0;
             for (int i = blockIdx.x; !failed; i += gridDim.x, ++items) {
@@ -946,13 +946,13 @@ dq_ds_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constant__ CU
                     tc::fence_after_sync();
                     const uint32_t so = (s * kStage) >> 4;
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)  // 16 keys per step: 512 bytes of A, 2 KB of B
-                        tc::mma_ss(tmem + 256 * b, dA + so + ((kk * 512) >> 4), dB + so + ((kk * 2048) >> 4), id,
+                    for (int kk = 0; kk < 8; ++kk)  // 16 keys per step: 1 KB of A, 2 KB of B
+                        tc::mma_ss(tmem + 256 * b, dA + so + ((kk * 1024) >> 4), dB + so + ((kk * 2048) >> 4), id,
                                    (j > 0) || (kk > 0));
                     if (it.has1) {
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
-                            tc::mma_ss(tmem + 256 * b + 128, dA + so + ((kTile + kk * 512) >> 4),
+                            tc::mma_ss(tmem + 256 * b + 128, dA + so + ((kTile + kk * 1024) >> 4),
                                        dB + so + ((kk * 2048) >> 4), id, (j > 0) || (kk > 0));
                     }
                     tc::mma_commit(bar(bEmpty + s));
@@ -1097,15 +1097,15 @@ cudaError_t launch_bwd_dq(const Problem& p, const Workspace& ws, const float* ls
     b.dv = nullptr;
     b.dyhat = ws.dqhat32;
     if (ws.ds) {  // dS was stored by the dK/dV kernel: dQ is one product per block
-        // a block is [16-query chunk][key][16 queries] (query in chunk, key, chunk, block);
-        // a box of 4 chunks lands in shared memory in the same order, 32-byte swizzled
+        // a block is [32-query chunk][key][32 queries] (query in chunk, key, chunk, block);
+        // a box of 2 chunks lands in shared memory in the same order, 64-byte swizzled
         CUtensorMap mds;
-        const cuuint64_t dims[4] = {16, 128, 8, (cuuint64_t)ws.ds_blocks};
-        const cuuint64_t strides[3] = {16 * 2, 128 * 16 * 2, 128 * 128 * 2};
-        const cuuint32_t box[4] = {16, 128, 4, 1};
+        const cuuint64_t dims[4] = {32, 128, 4, (cuuint64_t)ws.ds_blocks};
+        const cuuint64_t strides[3] = {32 * 2, 128 * 32 * 2, 128 * 128 * 2};
+        const cuuint32_t box[4] = {32, 128, 2, 1};
         const cuuint32_t es[4] = {1, 1, 1, 1};
         if (g_encode_b(&mds, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, ws.ds, dims, strides, box, es,
-                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
         dq_ds_kernel<<<g_sms_b, dqs::kThreads, dqs::kSmem, st>>>(mds, m.k, b);
