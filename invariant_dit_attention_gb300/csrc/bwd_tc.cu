@@ -792,7 +792,7 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 // loads, per key block j, dS^T(j, i0), dS^T(j, i1) and k^(j) (key rows past the
 // sample end zeroed: k^ may not be finite there) into one of two 96 KB stages;
 // warp 1 issues dQ0 += dS0 k^ and dQ1 += dS1 k^ (A = a dS^T tile read MN-major
-// from its 32-byte swizzled chunks, B = k^ MN-major) into one of two pairs of
+// from its 64-byte swizzled chunks, B = k^ MN-major) into one of two pairs of
 // TMEM accumulators; warps 4-7 drain the finished pair as scale * dq^ FP32 rows
 // while the next item accumulates.  The sum over j runs in ascending order
 // from the sample start.  Bound by HBM: every stored block is read once.

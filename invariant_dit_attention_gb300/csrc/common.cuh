@@ -207,7 +207,7 @@ struct Workspace {
     __nv_bfloat16* rows_c[4];  // [max_tokens, H, 128] each, canonical order: v, out, dout, dv
     uint4* keys;             // [max_tokens] sort keys of the canonical order
     // stored dS (null if the handle recomputes it in the dQ kernel): fp16 128 x 128
-    // blocks of dS^T laid out [16-query chunk][key][16 queries], block (sample of rank
+    // blocks of dS^T laid out [32-query chunk][key][32 queries], block (sample of rank
     // r, head h, key tile j, query tile i) at H cumsq[r] + h nq^2 + j nq + i, nq = the
     // sample's 128-token tiles
     __half* ds;

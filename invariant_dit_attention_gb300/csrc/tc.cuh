@@ -295,16 +295,6 @@ __device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr, uint32_t lbo_
     d |= 4ull << 61;
     return d;
 }
-// The same for a 32-byte swizzled operand (atoms of 8 rows x 32 bytes).
-__device__ __forceinline__ uint64_t smem_desc_sw32(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
-    d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
-    d |= 1ull << 46;
-    d |= 6ull << 61;
-    return d;
-}
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
     uint64_t d = 0;
     d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
