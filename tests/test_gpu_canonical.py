@@ -27,9 +27,9 @@ GRADS = ("dq", "dk", "dv")
 WGRADS = ("dq_norm_w", "dk_norm_w", "dq_norm_w_per_sample", "dk_norm_w_per_sample")
 
 
-def _run(inp, key_order="canonical", backward=True, max_samples=64):
+def _run(inp, key_order="canonical", backward=True, max_samples=64, store_ds="auto"):
     from invariant_dit_attention_gb300.h3attn import to_device
-    h = make_handle(inp.num_heads, max(inp.total_tokens, 1), max_samples, key_order=key_order)
+    h = make_handle(inp.num_heads, max(inp.total_tokens, 1), max_samples, key_order=key_order, store_ds=store_ds)
     d = to_device(inp)
     out, lse = h.forward(d["q"], d["k"], d["v"], d["q_norm_w"], d["k_norm_w"], d["pos"], d["seg_offsets"])
     g = None
@@ -139,10 +139,10 @@ def _case_inputs(case):
     return W.make_inputs(w.samples, w.num_heads, w.seed, w.std, w.outlier_frac, w.outlier_scale, with_grad=True)
 
 
-def _check_invariant(base, inp, seeds):
+def _check_invariant(base, inp, seeds, store_ds="auto"):
     for seed in seeds:
         pin, sigma = W.permute_within_samples(inp, seed)
-        r = _run(pin)
+        r = _run(pin, store_ds=store_ds)
         idx = torch.from_numpy(sigma)
         assert _same_bits(r["out"], base["out"][idx]), f"out, permutation {seed}"
         assert _same_bits(r["lse"], base["lse"][:, idx]), f"lse, permutation {seed}"
@@ -157,6 +157,13 @@ def test_canonical_results_do_not_depend_on_the_packed_order(case):
     need_gpu()
     inp = _case_inputs(case)
     _check_invariant(_run(inp), inp, (1, 2))
+
+
+def test_canonical_invariance_with_dq_recomputing_s_and_dp():
+    """The same property on the dQ path that recomputes S and dP (store_ds off)."""
+    need_gpu()
+    inp = _case_inputs("ragged")
+    _check_invariant(_run(inp, store_ds=False), inp, (1,), store_ds=False)
 
 
 def test_packed_order_does_depend_on_it():

@@ -40,6 +40,38 @@ def _sha(t):
     return hashlib.sha256(t.contiguous().view(torch.uint8).cpu().numpy().tobytes()).hexdigest()
 
 
+@pytest.mark.parametrize("store_ds", [False, True])
+def test_backward_alone_vs_packed_both_dq_paths(store_ds):
+    """dq, dk, dv and the per-sample weight gradients of each sample, alone and
+    packed with others, on both dQ paths (stored dS, recomputed S and dP)."""
+    need_gpu()
+    from invariant_dit_attention_gb300.h3attn import to_device
+    parts = [W.make_inputs([W.SampleLayout(n_text=5, grid=(2, 6, 11), n_audio=4)], 6, seed=41, with_grad=True),
+             W.make_inputs([130, 1], 6, seed=42, with_grad=True)]
+    packed = W.pack(parts)
+
+    def run(inp):
+        h = make_handle(6, inp.total_tokens, 8, store_ds=store_ds)
+        d = to_device(inp)
+        out, lse = h.forward(d["q"], d["k"], d["v"], d["q_norm_w"], d["k_norm_w"], d["pos"], d["seg_offsets"])
+        g = h.backward(d["q"], d["k"], d["v"], d["q_norm_w"], d["k_norm_w"], d["pos"], d["seg_offsets"], out, lse,
+                       d["dout"])
+        torch.cuda.synchronize()
+        h.check()
+        h.close()
+        return {k: v.cpu() for k, v in g.items()}
+
+    gp = run(packed)
+    seg = packed.seg_offsets.tolist()
+    for s in range(packed.num_samples):
+        ga = run(W.slice_sample(packed, s))
+        a, b = seg[s], seg[s + 1]
+        for name in ("dq", "dk", "dv"):
+            assert _sha(ga[name]) == _sha(gp[name][a:b]), f"sample {s} {name}"
+        for name in ("dq_norm_w_per_sample", "dk_norm_w_per_sample"):
+            assert _sha(ga[name][0]) == _sha(gp[name][s]), f"sample {s} {name}"
+
+
 def test_forward_repeat_bitwise_925():
     need_gpu()
     w, inp = workload("single_925")
