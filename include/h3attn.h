@@ -262,7 +262,7 @@ h3attn_status h3attn_stage_times(h3attn_t h, float *total_ms, int *launches, int
  * process exits.
  *
  * Arguments are those of h3attn_forward with the configuration passed directly
- * (cfg->max_tokens and cfg->max_samples are ignored), plus device_error_flags:
+ * (cfg->max_tokens, cfg->max_samples and cfg->store_ds are ignored), plus device_error_flags:
  * a device uint32 (may be NULL) that receives this call's device-side error
  * bits (0 = none; 1 = invalid seg_offsets, 2 = a bounded wait timed out, 4 = a
  * value beyond the fp16 operand range), written on `stream` after the kernels.
