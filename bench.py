@@ -281,12 +281,21 @@ def dist_env():
 
 
 def barrier_max(x: float, ws: int) -> float:
+    """The largest of the ranks' values (the slowest rank's time sets the job's)."""
     if ws == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_tflops(flops_per_step: float, steps: int, ws: int, ms_max: float) -> float:
+    """Whole-job rate: every rank runs the same steps on its own replica of the
+    workload (weak scaling), so the job's work is ws times one rank's, done in
+    the slowest rank's time."""
+    return flops_per_step * steps * ws / (ms_max * 1e-3) / 1e12
 
 
 def barrier(ws):
@@ -378,7 +387,7 @@ def run_ours(args):
     h.set_stage_timing(False)
     h.check()
     ms_max = barrier_max(ms, ws)
-    value = step_flops * args.steps * ws / (ms_max * 1e-3) / 1e12
+    value = whole_job_tflops(step_flops, args.steps, ws, ms_max)
 
     # ---- forward-only rates: whole batch and every sample alone (same kernels)
     fwd_ms = stages["fwd"][0] + 0.5 * (stages["prologue"][0] + stages["plan"][0])
@@ -467,7 +476,7 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = barrier_max(e0.elapsed_time(e1), ws)
-    e2e_value = step_flops * args.steps * ws / (e2e_ms * 1e-3) / 1e12
+    e2e_value = whole_job_tflops(step_flops, args.steps, ws, e2e_ms)
     h.check()
 
     # ---- roofline of the dominant kernel (stage timing over the timed region)
