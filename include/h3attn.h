@@ -77,7 +77,10 @@ typedef struct {
     int store_ds;          /* 1: the dK/dV kernel also writes dS to the workspace and dQ
                               is one product per block (faster; workspace H * ceil(T/128)
                               * (ceil(T/128) + max_samples) * 32 KB, T = max_tokens);
-                              0: the dQ kernel recomputes S and dP                     */
+                              0: the dQ kernel recomputes S and dP.  Both are
+                              deterministic and identical alone vs packed; dq may
+                              differ between them in the last bits (dS comes from the
+                              transposed product in the first)                        */
 } h3attn_config;
 
 /*
