@@ -94,3 +94,15 @@ def test_static_forward_and_new_entry_points_reject_on_host():
     assert lib.h3attn_qkv_forward(None, None, 64, None, None, None, None, pos, None, 1, 4, None, None, None, None,
                                   None, None) == 1
     assert lib.h3attn_canonical_order(None, None, None, None, None, pos, None, 1, 4, None, None) == 1
+
+
+def test_binding_checks_and_stored_ds_workspace_size():
+    """Python-side checks before the library is asked for a handle, and the
+    stored-dS workspace size the "auto" setting compares with its limit."""
+    from invariant_dit_attention_gb300.h3attn import STORED_DS_AUTO_LIMIT, H3Attn, stored_ds_bytes
+    lib_built()
+    with pytest.raises(ValueError):
+        H3Attn(4, 64, 4, key_order="sorted")
+    # H ceil(T/128) (ceil(T/128) + N) blocks of 128 x 128 fp16
+    assert stored_ds_bytes(48, 13539, 8) == 48 * 106 * 114 * 32768
+    assert stored_ds_bytes(48, 13539, 8) < STORED_DS_AUTO_LIMIT < stored_ds_bytes(48, 32768, 8)
