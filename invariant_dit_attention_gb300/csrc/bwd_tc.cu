@@ -27,6 +27,7 @@
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
+#include "host.cuh"
 #include "tc.cuh"
 
 namespace h3 {
@@ -1019,17 +1020,14 @@ dq_ds_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constant__ CU
 // ------------------------------------------------------------------ host
 
 namespace {
-PFN_cuTensorMapEncodeTiled_v12000 g_encode_b = nullptr;
-int g_sms_b = 0;
-
 bool encode_rows_b(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int H, int S, int rows) {
     const cuuint64_t dims[2] = {(cuuint64_t)H * kD, (cuuint64_t)S};
     const cuuint64_t strides[1] = {(cuuint64_t)H * kD * 2};
     const cuuint32_t box[2] = {64, (cuuint32_t)rows};
     const cuuint32_t es[2] = {1, 1};
-    return g_encode_b(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return tensor_map_encoder()(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 struct BwdMaps {
@@ -1046,18 +1044,8 @@ bool encode_all(BwdMaps& m, const Problem& p, const Workspace& ws, const __nv_bf
 }
 }  // namespace
 
-cudaError_t init_bwd_attributes() {
-    if (!g_encode_b) {
-        cudaDriverEntryPointQueryResult q;
-        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", reinterpret_cast<void**>(&g_encode_b),
-                                                         12000, cudaEnableDefault, &q);
-        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !g_encode_b) return cudaErrorNotSupported;
-    }
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_sms_b, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kvt::kSmem);
+cudaError_t set_bwd_attributes() {
+    cudaError_t e = cudaFuncSetAttribute(dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kvt::kSmem);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dqt::kSmem);
     if (e == cudaSuccess)
@@ -1085,7 +1073,9 @@ cudaError_t launch_bwd_dkdv(const Problem& p, const Workspace& ws, const float* 
     BwdTcParams b = bwd_params(p, ws, lse);
     b.dv = dv;
     b.dyhat = ws.dkhat32;
-    dkdv_tc_kernel<<<g_sms_b, kvt::kThreads, kvt::kSmem, st>>>(m.q, m.k, m.v, m.dout, b);
+    const int sms = device_sms();
+    if (sms < 1) return cudaErrorNotSupported;
+    dkdv_tc_kernel<<<sms, kvt::kThreads, kvt::kSmem, st>>>(m.q, m.k, m.v, m.dout, b);
     return cudaGetLastError();
 }
 
@@ -1094,6 +1084,8 @@ cudaError_t launch_bwd_dq(const Problem& p, const Workspace& ws, const float* ls
     BwdMaps m;
     if (!encode_all(m, p, ws, dout, 128, 128)) return cudaErrorInvalidValue;
     BwdTcParams b = bwd_params(p, ws, lse);
+    const int sms = device_sms();
+    if (sms < 1) return cudaErrorNotSupported;
     b.dv = nullptr;
     b.dyhat = ws.dqhat32;
     if (ws.ds) {  // dS was stored by the dK/dV kernel: dQ is one product per block
@@ -1104,14 +1096,14 @@ cudaError_t launch_bwd_dq(const Problem& p, const Workspace& ws, const float* ls
         const cuuint64_t strides[3] = {32 * 2, 128 * 32 * 2, 128 * 128 * 2};
         const cuuint32_t box[4] = {32, 128, 2, 1};
         const cuuint32_t es[4] = {1, 1, 1, 1};
-        if (g_encode_b(&mds, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, ws.ds, dims, strides, box, es,
+        if (tensor_map_encoder()(&mds, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, ws.ds, dims, strides, box, es,
                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
-        dq_ds_kernel<<<g_sms_b, dqs::kThreads, dqs::kSmem, st>>>(mds, m.k, b);
+        dq_ds_kernel<<<sms, dqs::kThreads, dqs::kSmem, st>>>(mds, m.k, b);
         return cudaGetLastError();
     }
-    dq_tc_kernel<<<g_sms_b, dqt::kThreads, dqt::kSmem, st>>>(m.q, m.k, m.v, m.dout, b);
+    dq_tc_kernel<<<sms, dqt::kThreads, dqt::kSmem, st>>>(m.q, m.k, m.v, m.dout, b);
     return cudaGetLastError();
 }
 

@@ -235,8 +235,6 @@ struct Problem {
 enum Stage { kStagePlan = 0, kStagePrologue, kStageFwd, kStageDelta, kStageDkdv, kStageDq, kStageDw, kStageRows,
              kStageOrder, kStagePermute, kStageQkv, kStages };
 
-cudaError_t init_fwd_tc();
-cudaError_t init_bwd_attributes();
 cudaError_t launch_plan(const Problem& p, const Workspace& ws, cudaStream_t st);
 cudaError_t launch_prologue(const Problem& p, const Workspace& ws, const RopeTable* rope, cudaStream_t st);
 cudaError_t launch_fwd(const Problem& p, const Workspace& ws, __nv_bfloat16* out, float* lse, cudaStream_t st);

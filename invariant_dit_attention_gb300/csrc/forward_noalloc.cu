@@ -12,12 +12,12 @@
 //
 // The arithmetic is exactly h3attn_forward's (same plan, prologue and
 // attention kernels), only the scratch pointers differ.
-#include <math.h>
 #include <mutex>
 #include <string.h>
 
 #include "../../include/h3attn.h"
 #include "common.cuh"
+#include "host.cuh"
 
 using namespace h3;
 
@@ -36,45 +36,20 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
 uint8_t* g_scratch_ptr[kMaxDevices];  // device address of g_static_scratch, per device
 
-// Once per device, with that device current: resolve the scratch address and
-// prepare the kernels.  Allocates nothing.
+// Once per device, with that device current: prepare the device (kernel
+// attributes, SM count) and resolve the scratch's device address.  Allocates
+// nothing.
 h3attn_status setup_device(int dev, uint8_t** out) {
     std::lock_guard<std::mutex> lock(g_mutex);
     if (!g_scratch_ptr[dev]) {
-        cudaDeviceProp prop;
-        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return H3ATTN_ERR_CUDA;
-        if (!(prop.major == 10 && prop.minor == 3)) return H3ATTN_ERR_UNSUPPORTED;
+        const cudaError_t pe = prepare_device();
+        if (pe != cudaSuccess) return pe == cudaErrorNotSupported ? H3ATTN_ERR_UNSUPPORTED : H3ATTN_ERR_CUDA;
         void* ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) return H3ATTN_ERR_CUDA;
-        if (init_fwd_tc() != cudaSuccess) return H3ATTN_ERR_CUDA;
         g_scratch_ptr[dev] = static_cast<uint8_t*>(ptr);
     }
     *out = g_scratch_ptr[dev];
     return H3ATTN_OK;
-}
-
-bool build_rope_table(const h3attn_config& c, RopeTable& rt) {
-    memset(&rt, 0, sizeof rt);
-    for (int g = 0; g < 32; ++g) { rt.axis[g] = -1; rt.partner[g] = (int8_t)g; }
-    int off = 0;
-    for (int a = 0; a < 3; ++a) {
-        const int n = c.rope_sections[a];
-        if (n < 0 || n % 8 != 0 || off + n > kD) return false;
-        const int half = n / 2;
-        for (int j = 0; j < half; ++j) {
-            const float f = (float)pow((double)c.rope_theta, -2.0 * j / (double)n);
-            rt.inv_freq[off + j] = f;
-            rt.inv_freq[off + j + half] = f;
-        }
-        for (int grp = off / 4; grp < (off + n) / 4; ++grp) {
-            const bool second = grp * 4 - off >= half;
-            rt.axis[grp] = (int8_t)a;
-            rt.second[grp] = second ? 1 : 0;
-            rt.partner[grp] = (int8_t)(second ? grp - half / 4 : grp + half / 4);
-        }
-        off += n;
-    }
-    return true;
 }
 
 bool al16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -93,7 +68,7 @@ extern "C" h3attn_status h3attn_forward_static(const h3attn_config* cfg, const h
     if (cfg->head_dim != kD || cfg->rope_pairing != 0 || cfg->key_order != H3ATTN_KEY_ORDER_PACKED)
         return H3ATTN_ERR_UNSUPPORTED;
     RopeTable rt;
-    if (!build_rope_table(*cfg, rt)) return H3ATTN_ERR_UNSUPPORTED;
+    if (!build_rope_table(cfg->rope_sections, cfg->rope_theta, rt)) return H3ATTN_ERR_UNSUPPORTED;
     if (total_tokens < 0 || num_samples < 0) return H3ATTN_ERR_INVALID_ARG;
     if (total_tokens == 0) return H3ATTN_OK;
     if (num_samples < 1 || num_samples > total_tokens) return H3ATTN_ERR_INVALID_ARG;

@@ -26,6 +26,7 @@
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
+#include "host.cuh"
 #include "tc.cuh"
 
 namespace h3 {
@@ -417,33 +418,19 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 // ------------------------------------------------------------------ host
 
 namespace {
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-int g_num_sms = 0;
-
 bool encode_rows(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int H, int S) {
     const cuuint64_t dims[2] = {(cuuint64_t)H * kD, (cuuint64_t)S};
     const cuuint64_t strides[1] = {(cuuint64_t)H * kD * 2};
     const cuuint32_t box[2] = {64, 128};
     const cuuint32_t es[2] = {1, 1};
-    return g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return tensor_map_encoder()(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 }  // namespace
 
-cudaError_t init_fwd_tc() {
-    if (!g_encode) {
-        cudaDriverEntryPointQueryResult q;
-        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", reinterpret_cast<void**>(&g_encode),
-                                                         12000, cudaEnableDefault, &q);
-        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !g_encode) return cudaErrorNotSupported;
-    }
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, fwdt::kSmem);
-    return e;
+cudaError_t set_fwd_attributes() {
+    return cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, fwdt::kSmem);
 }
 
 cudaError_t launch_fwd(const Problem& p, const Workspace& ws, __nv_bfloat16* out, float* lse, cudaStream_t st) {
@@ -459,7 +446,9 @@ cudaError_t launch_fwd(const Problem& p, const Workspace& ws, __nv_bfloat16* out
     prm.scale_log2 = p.scale * 1.4426950408889634f;
     prm.out = out;
     prm.lse = lse;
-    fwd_tc_kernel<<<g_num_sms, fwdt::kThreads, fwdt::kSmem, st>>>(mq, mk, mv, prm);
+    const int sms = device_sms();
+    if (sms < 1) return cudaErrorNotSupported;
+    fwd_tc_kernel<<<sms, fwdt::kThreads, fwdt::kSmem, st>>>(mq, mk, mv, prm);
     return cudaGetLastError();
 }
 

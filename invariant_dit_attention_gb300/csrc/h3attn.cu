@@ -9,6 +9,7 @@
 
 #include "../../include/h3attn.h"
 #include "common.cuh"
+#include "host.cuh"
 
 using namespace h3;
 
@@ -34,31 +35,6 @@ namespace {
 
 bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
-
-h3attn_status build_rope(const h3attn_config& c, RopeTable& rt) {
-    memset(&rt, 0, sizeof rt);
-    for (int g = 0; g < 32; ++g) { rt.axis[g] = -1; rt.partner[g] = (int8_t)g; rt.second[g] = 0; }
-    int off = 0;
-    for (int a = 0; a < 3; ++a) {
-        const int n = c.rope_sections[a];
-        if (n < 0 || n % 8 != 0 || off + n > kD) return H3ATTN_ERR_UNSUPPORTED;
-        const int half = n / 2;
-        for (int j = 0; j < half; ++j) {
-            // frequency of pair j of an n-channel axis: theta^(-2j/n)
-            const float f = (float)pow((double)c.rope_theta, -2.0 * j / (double)n);
-            rt.inv_freq[off + j] = f;
-            rt.inv_freq[off + j + half] = f;
-        }
-        for (int grp = off / 4; grp < (off + n) / 4; ++grp) {
-            const bool second = grp * 4 - off >= half;
-            rt.axis[grp] = (int8_t)a;
-            rt.second[grp] = second ? 1 : 0;
-            rt.partner[grp] = (int8_t)(second ? grp - half / 4 : grp + half / 4);
-        }
-        off += n;
-    }
-    return H3ATTN_OK;
-}
 
 template <class T>
 bool ws_alloc(h3attn_ctx* h, T** p, size_t bytes) {
@@ -179,12 +155,13 @@ h3attn_status h3attn_create(const h3attn_config* cfg, h3attn_t* out) {
     if (cfg->head_dim != kD || cfg->rope_pairing != 0) return H3ATTN_ERR_UNSUPPORTED;
     if ((long)cfg->max_tokens * cfg->num_heads * kD >= (1L << 40)) return H3ATTN_ERR_CAPACITY;
     RopeTable rt;
-    if (build_rope(*cfg, rt) != H3ATTN_OK) return H3ATTN_ERR_UNSUPPORTED;
+    if (!build_rope_table(cfg->rope_sections, cfg->rope_theta, rt)) return H3ATTN_ERR_UNSUPPORTED;
     int dev = 0;
-    cudaDeviceProp prop;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaGetDeviceProperties(&prop, dev) != cudaSuccess)
-        return H3ATTN_ERR_CUDA;
-    if (!(prop.major == 10 && prop.minor == 3)) return H3ATTN_ERR_UNSUPPORTED;
+    if (cudaGetDevice(&dev) != cudaSuccess) return H3ATTN_ERR_CUDA;
+    {
+        const cudaError_t pe = prepare_device();
+        if (pe != cudaSuccess) return pe == cudaErrorNotSupported ? H3ATTN_ERR_UNSUPPORTED : H3ATTN_ERR_CUDA;
+    }
 
     h3attn_ctx* h = static_cast<h3attn_ctx*>(calloc(1, sizeof(h3attn_ctx)));
     if (!h) return H3ATTN_ERR_CUDA;
@@ -218,7 +195,6 @@ h3attn_status h3attn_create(const h3attn_config* cfg, h3attn_t* out) {
     }
     if (ok) ok = cudaMemset(ws.plan.err, 0, 4) == cudaSuccess;
     if (ok) ok = cudaMallocHost(&h->host_err, 4) == cudaSuccess;
-    if (ok) ok = init_fwd_tc() == cudaSuccess && init_bwd_attributes() == cudaSuccess;
     if (ok) ok = cudaDeviceSynchronize() == cudaSuccess;
     if (!ok) {
         free_ctx(h);

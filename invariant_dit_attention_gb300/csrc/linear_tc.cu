@@ -36,6 +36,7 @@
 
 #include "../../include/h3attn.h"
 #include "common.cuh"
+#include "host.cuh"
 #include "rowops.cuh"
 #include "tc.cuh"
 
@@ -380,44 +381,26 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__
 // ------------------------------------------------------------------ host
 
 namespace {
-PFN_cuTensorMapEncodeTiled_v12000 g_encode_l = nullptr;
-int g_sms_l = 0;
-int g_dev_l = -1;
-
 bool encode_2d(CUtensorMap* m, const void* base, int inner, int outer, int box_outer) {
     const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
     const cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
     const cuuint32_t box[2] = {(cuuint32_t)lint::kBK, (cuuint32_t)box_outer};
     const cuuint32_t es[2] = {1, 1};
-    return g_encode_l(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-h3attn_status init_linear(int dev) {
-    if (!g_encode_l) {
-        cudaDriverEntryPointQueryResult q;
-        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", reinterpret_cast<void**>(&g_encode_l),
-                                                         12000, cudaEnableDefault, &q);
-        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !g_encode_l) return H3ATTN_ERR_CUDA;
-    }
-    if (g_dev_l != dev) {
-        cudaDeviceProp prop;
-        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return H3ATTN_ERR_CUDA;
-        if (!(prop.major == 10 && prop.minor == 3)) return H3ATTN_ERR_UNSUPPORTED;
-        if (cudaFuncSetAttribute(linear_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, lint::kSmem) !=
-                cudaSuccess ||
-            cudaFuncSetAttribute(linear_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, lint::kSmemQkv) !=
-                cudaSuccess)
-            return H3ATTN_ERR_CUDA;
-        g_sms_l = prop.multiProcessorCount;
-        g_dev_l = dev;
-    }
-    return H3ATTN_OK;
+    return tensor_map_encoder()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool al16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 }  // namespace
+
+cudaError_t set_linear_attributes() {
+    cudaError_t e = cudaFuncSetAttribute(linear_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         lint::kSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(linear_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, lint::kSmemQkv);
+    return e;
+}
 
 }  // namespace h3
 
@@ -434,10 +417,9 @@ extern "C" h3attn_status h3attn_linear(const h3attn_bf16* x, int rows, int in_fe
         return H3ATTN_ERR_INVALID_ARG;
     if ((long long)rows * in_features >= (1LL << 40) || (long long)out_features * in_features >= (1LL << 40))
         return H3ATTN_ERR_CAPACITY;
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return H3ATTN_ERR_CUDA;
-    const h3attn_status st = init_linear(dev);
-    if (st != H3ATTN_OK) return st;
+    const cudaError_t pe = prepare_device();
+    if (pe != cudaSuccess) return pe == cudaErrorNotSupported ? H3ATTN_ERR_UNSUPPORTED : H3ATTN_ERR_CUDA;
+    const int sms = device_sms();
     CUtensorMap ma, mb;
     if (!encode_2d(&ma, x, in_features, rows, lint::kBM) || !encode_2d(&mb, w, in_features, out_features, lint::kBN))
         return H3ATTN_ERR_INVALID_ARG;
@@ -453,7 +435,7 @@ extern "C" h3attn_status h3attn_linear(const h3attn_bf16* x, int rows, int in_fe
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(device_error_flags, 0, 4, s) != cudaSuccess) return H3ATTN_ERR_CUDA;
     const int tiles = p.tiles_m * p.tiles_n;
-    linear_tc_kernel<false><<<tiles < g_sms_l ? tiles : g_sms_l, lint::kThreads, lint::kSmem, s>>>(ma, mb, p);
+    linear_tc_kernel<false><<<tiles < sms ? tiles : sms, lint::kThreads, lint::kSmem, s>>>(ma, mb, p);
     return cudaGetLastError() == cudaSuccess ? H3ATTN_OK : H3ATTN_ERR_CUDA;
 }
 
@@ -465,9 +447,8 @@ cudaError_t launch_qkv(const Problem& p, const Workspace& ws, const RopeTable* r
                        int in_features, const __nv_bfloat16* w, const float* bias, __nv_bfloat16* q, __nv_bfloat16* k,
                        __nv_bfloat16* v, cudaStream_t st) {
     if (p.seq.S == 0) return cudaSuccess;
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return cudaErrorInvalidDevice;
-    if (init_linear(dev) != H3ATTN_OK) return cudaErrorNotSupported;
+    const int sms = device_sms();
+    if (sms < 1) return cudaErrorNotSupported;
     const int D = p.H * kD, N = 3 * D;
     CUtensorMap ma, mb;
     if (!encode_2d(&ma, x, in_features, p.seq.S, lint::kBM) || !encode_2d(&mb, w, in_features, N, lint::kBN))
@@ -497,7 +478,7 @@ cudaError_t launch_qkv(const Problem& p, const Workspace& ws, const RopeTable* r
     lp.qkv.rope_cs = ws.rope_cs;
     lp.qkv.rope = *rope;
     const int tiles = lp.tiles_m * lp.tiles_n;
-    linear_tc_kernel<true><<<tiles < g_sms_l ? tiles : g_sms_l, lint::kThreads, lint::kSmemQkv, st>>>(ma, mb, lp);
+    linear_tc_kernel<true><<<tiles < sms ? tiles : sms, lint::kThreads, lint::kSmemQkv, st>>>(ma, mb, lp);
     return cudaGetLastError();
 }
 

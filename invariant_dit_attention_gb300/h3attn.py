@@ -260,14 +260,33 @@ class H3Attn:
         _check(self.device_status(stream), "device")
 
 
+# Bits of the device error word (the static forward's error_flags, h3attn_linear's).
+_DEVICE_ERROR_STATUS = ((2, ERR_TIMEOUT), (1, ERR_INVALID_ARG), (4, ERR_INVALID_ARG))
+
+
+def _raise_device_flags(flags, stream, where):
+    """Waits for the stream and raises on a nonzero device error word."""
+    (torch.cuda.current_stream() if stream is None else stream).synchronize()
+    bits = int(flags.item())
+    for bit, status in _DEVICE_ERROR_STATUS:
+        if bits & bit:
+            raise H3AttnError(status, f"{where} (device error bits {bits:#x})")
+
+
 def forward_static(q, k, v, q_norm_w, k_norm_w, pos, seg_offsets, num_heads=None, eps=1e-6,
                    rope_theta=10000.0, rope_sections=(16, 24, 24), softmax_scale=0.0, num_samples=None,
-                   out=None, lse=None, error_flags=None, stream=None):
+                   out=None, lse=None, want_lse=True, error_flags=None, stream=None):
     """h3attn_forward_static: the forward with no handle and no device allocation
     inside the library (for hosts that forbid cudaMalloc while serving).
 
-    ``out``/``lse``/``error_flags`` are caller-owned device tensors; they are
-    created here with torch when not given.  Returns (out, lse).
+    ``out`` and ``lse`` are caller-owned device tensors; when not given they are
+    created here with torch (``lse`` only if ``want_lse``).  ``error_flags``
+    (int32 [1] on the device): when given, the call's device-side error bits
+    are written there on the stream and checking them is the caller's job; when
+    omitted, a zeroed word is created here and the binding waits for the stream
+    and raises H3AttnError if the device reported an error (invalid
+    seg_offsets, a wait that timed out, an fp16 range overflow).
+    Returns (out, lse).
     """
     lib = load_library()
     S, H = q.shape[0], q.shape[1] if num_heads is None else num_heads
@@ -279,10 +298,17 @@ def forward_static(q, k, v, q_norm_w, k_norm_w, pos, seg_offsets, num_heads=None
     n = int(seg_offsets.numel() - 1) if num_samples is None else num_samples
     if out is None:
         out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((H, S), dtype=torch.float32, device=q.device)
+    own_flags = error_flags is None
+    if own_flags:
+        error_flags = torch.zeros(1, dtype=torch.int32, device=q.device)
     st = lib.h3attn_forward_static(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(q_norm_w), _ptr(k_norm_w),
                                    _pos_array(pos), _ptr(seg_offsets), n, S, _ptr(out), _ptr(lse),
                                    _ptr(error_flags), _stream(stream))
     _check(st, "h3attn_forward_static")
+    if own_flags and S > 0:
+        _raise_device_flags(error_flags, stream, "h3attn_forward_static")
     return out, lse
 
 

@@ -12,9 +12,10 @@ from invariant_dit_attention_gb300 import workloads as W
 
 # Tolerances against the FP64 oracle: forward rel-L2 <= 5e-3 and max-abs <= 2e-2
 # on the bf16 outputs, backward rel-L2 <= 1e-2.  The lse bound follows from
-# rounding q^ and k^ to bf16 (2^-9 relative per element): a score moves by at
-# most about 2^-8 |q^||k^| scale, a few 1e-3 for unit-RMS heads, and lse moves
-# by no more than the largest score shift.
+# rounding q^ and k^ to fp16 (2^-11 relative per element): a score moves by at
+# most about 2^-10 |q^||k^| scale, about 1e-3 for unit-RMS heads, and lse moves
+# by no more than the largest score shift; 1e-2 leaves room for the outlier
+# workloads' larger rows.
 FWD_REL_L2 = 5e-3
 FWD_MAX_ABS = 2e-2
 BWD_REL_L2 = 1e-2

@@ -4,6 +4,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from invariant_dit_attention_gb300 import workloads as W
 from tests.helpers import BWD_REL_L2, make_handle, need_gpu, np64, oracle_backward, rel_l2, workload
 
@@ -74,3 +75,50 @@ def test_backward_full_4253_outliers():
     w, inp = workload("fwd_bwd_4253")
     _, _, g = run_fwd_bwd(inp)
     check_grads(g, oracle_backward("fwd_bwd_4253", inp), 1)
+
+
+# ---- the backward as the bench times it: the packed batch of 12 + 925 + 4253 + 8349
+# tokens with the stored dS.  The dS blocks of one head of this pack number
+# 1 + 64 + 1156 + 4356 = 5577 (32 KB each): at 24 heads they take 4.39 GB, past
+# 2^32 bytes of workspace; at 48 heads 8.77 GB, with block indices up to 267,696.
+
+def _bench_pack_inputs(num_heads):
+    w = W.WORKLOADS["packed_13539"]
+    return W.make_inputs(w.samples, num_heads, w.seed, w.std, w.outlier_frac, w.outlier_scale, with_grad=True)
+
+
+def _ds_bytes(inp):
+    blocks = sum(((L + 127) // 128) ** 2 for L in inp.meta["lengths"]) * inp.num_heads
+    return blocks * 128 * 128 * 2
+
+
+@pytest.mark.slow
+def test_backward_bench_pack_24_heads_full_oracle():
+    """Every gradient of the 13539-token pack at 24 heads (4.39 GB of stored dS)
+    against the full FP64 backward: dq, dk, dv, the total and per-sample weight
+    gradients."""
+    need_gpu()
+    inp = _bench_pack_inputs(24)
+    assert _ds_bytes(inp) > (1 << 32)
+    _, _, g = run_fwd_bwd(inp, max_samples=8, store_ds=True)
+    check_grads(g, oracle_backward("bench_pack_24", inp), inp.num_samples)
+
+
+@pytest.mark.slow
+def test_backward_bench_pack_48_heads_first_and_last_heads():
+    """The bench's own inputs (48 heads, seed as the bench draws them, stored dS
+    of 8.77 GB): dq, dk, dv of heads 0-1 and 46-47 against the oracle restricted
+    to those heads.  Heads 46-47 of the later-ranked samples own the highest
+    block indices and byte offsets of the stored dS."""
+    need_gpu()
+    inp = _bench_pack_inputs(48)
+    assert _ds_bytes(inp) > 8 * (1 << 30)
+    _, _, g = run_fwd_bwd(inp, max_samples=8, store_ds=True)
+    for lo, hi in ((0, 2), (46, 48)):
+        ref = oracle.backward(inp.q, inp.k, inp.v, inp.q_norm_w, inp.k_norm_w, inp.pos, inp.seg_offsets,
+                              inp.dout, heads=(lo, hi))
+        for name in ("dq", "dk", "dv"):
+            x = np64(g[name][:, lo:hi])
+            assert np.isfinite(x).all(), (name, lo, hi)
+            e = rel_l2(x, ref[name][:, lo:hi])
+            assert e <= BWD_REL_L2, f"{name} heads [{lo}, {hi}) rel-L2 {e:.3e}"

@@ -12,7 +12,8 @@ import pytest
 import torch
 
 from invariant_dit_attention_gb300 import workloads as W
-from tests.helpers import FWD_MAX_ABS, FWD_REL_L2, lib_built, make_handle, max_abs_scaled, need_gpu, np64, rel_l2
+from tests.helpers import (FWD_MAX_ABS, FWD_REL_L2, LSE_MAX_ABS, lib_built, make_handle, max_abs, max_abs_scaled,
+                           need_gpu, np64, oracle_forward, rel_l2)
 
 pytestmark = pytest.mark.gpu
 
@@ -41,6 +42,29 @@ def test_static_scratch_forward_matches_handle_forward_twice():
         # same kernels on the same inputs: the results are in fact bitwise equal
         assert torch.equal(out, ref_out), f"call {call}: out differs from h3attn_forward"
         assert torch.equal(lse, ref_lse), f"call {call}: lse differs from h3attn_forward"
+    # and against the FP64 oracle, independently of h3attn_forward
+    o_ref, lse_ref = oracle_forward("static_scratch_4242", inp)
+    o = np64(out)
+    assert rel_l2(o, o_ref) <= FWD_REL_L2 and max_abs_scaled(o, o_ref) <= FWD_MAX_ABS
+    assert max_abs(np64(lse), lse_ref) <= LSE_MAX_ABS
+
+
+def test_static_scratch_forward_raises_on_device_errors_without_flags():
+    """With error_flags omitted the binding checks the device word itself: an
+    invalid seg_offsets array (not increasing) must raise, not pass silently."""
+    need_gpu()
+    lib_built()
+    from invariant_dit_attention_gb300.h3attn import ERR_INVALID_ARG, H3AttnError, forward_static, to_device
+    inp = W.make_inputs([200, 100], 4, seed=77)
+    d = to_device(inp)
+    bad = torch.tensor([0, 200, 100, 300], dtype=torch.int32, device="cuda")
+    with pytest.raises(H3AttnError) as e:
+        forward_static(d["q"], d["k"], d["v"], d["q_norm_w"], d["k_norm_w"], d["pos"], bad)
+    assert e.value.status == ERR_INVALID_ARG
+    # a valid call right after is clean
+    out, _ = forward_static(d["q"], d["k"], d["v"], d["q_norm_w"], d["k_norm_w"], d["pos"], d["seg_offsets"])
+    torch.cuda.synchronize()
+    assert np.isfinite(np64(out)).all()
 
 
 def test_static_scratch_forward_rejects_sizes_beyond_its_limit():
