@@ -81,6 +81,15 @@ typedef struct {
                               deterministic and identical alone vs packed; dq may
                               differ between them in the last bits (dS comes from the
                               transposed product in the first)                        */
+    int reuse_qk_hat;      /* 1: h3attn_backward skips the q/k norm + RoPE pass when the
+                              handle's last forward (h3attn_forward or
+                              h3attn_qkv_forward, packed key order) computed the
+                              rotated rows from the same q, k, norm-weight, position
+                              and offset pointers and sizes: the workspace still
+                              holds them.  The caller promises that the contents of
+                              those tensors did not change in between (as a training
+                              step's saved tensors do not); results are bitwise those
+                              of the recomputation.  0: always recompute.           */
 } h3attn_config;
 
 /*
@@ -121,8 +130,8 @@ typedef struct {
  * positions (4 * max_tokens int32), row terms (H * max_tokens floats) and four
  * max_tokens * H * 128 bf16 row copies.
  * With store_ds = 1 it also allocates the stored dS blocks (see store_ds).
- * Errors: INVALID_ARG (null pointer, sizes < 1, key_order or store_ds not 0
- * or 1), UNSUPPORTED (head_dim, pairing, sections, device not sm_103),
+ * Errors: INVALID_ARG (null pointer, sizes < 1, key_order, store_ds or
+ * reuse_qk_hat not 0 or 1), UNSUPPORTED (head_dim, pairing, sections, device not sm_103),
  * CAPACITY (the stored dS would exceed 2^31 rows of 128 values), CUDA
  * (allocation failed).
  */
@@ -153,7 +162,10 @@ h3attn_status h3attn_forward(h3attn_t h,
  * (overwritten with the sum over all tokens and heads, samples added in index
  * order); dq_norm_w_per_sample, dk_norm_w_per_sample float32 [num_samples, 128]
  * or NULL (per-sample sums; these, like dq/dk/dv, are identical whether a sample
- * runs alone or packed).  All reductions run in a fixed order, no atomics.
+ * runs alone or packed).  All reductions run in a fixed order, no atomics: the
+ * weight gradients per (sample, head) over 128-token tiles, then per sample over
+ * heads, then over samples, each in ascending order (see the head-sharded runs
+ * below).
  * With key_order CANONICAL the order of every sum is the canonical one (see
  * H3ATTN_KEY_ORDER_CANONICAL), including the dout rows in the sort.
  * Errors: INVALID_ARG, CAPACITY, CUDA.
@@ -314,6 +326,88 @@ h3attn_status h3attn_forward_static(const h3attn_config *cfg,
 h3attn_status h3attn_linear(const h3attn_bf16 *x, int rows, int in_features,
                             const h3attn_bf16 *w, int out_features, const float *bias,
                             h3attn_bf16 *y, uint32_t *device_error_flags, void *stream);
+
+/*
+ * Head-sharded runs.  The path has no exchange step between heads: a layer's
+ * heads can be split across GPUs, each GPU running its own heads (q, k, v,
+ * dout as contiguous [S, H_g, 128] tensors) through a handle of H_g heads, and
+ * its out, lse, dq, dk and dv are bitwise those of a one-GPU run of all heads.
+ * The norm weights are shared by all heads, so their gradient needs the other
+ * GPUs' heads; it is reduced in a fixed order that does not depend on how the
+ * heads are split: per (sample, head) over the sample's 128-token tiles in
+ * ascending order, then per sample over heads in ascending order, then over
+ * samples in ascending order (h3attn_backward itself reduces this way).  A
+ * head-sharded run gathers every GPU's (sample, head) partials in head order
+ * and reduces them with h3attn_combine_norm_weight_grads: the result is
+ * bitwise the one-GPU result for every split.  (The pages' precedent is the
+ * WS2 parallel layer, ws2_comm.py in the changed-file list of the
+ * "ws1_full_h3_transformer" page, PR #571.)
+ *
+ * h3attn_norm_weight_grad_partials: copies the per-(sample, head) partials of
+ * the handle's last h3attn_backward call, float32 [num_samples, H, 128] each
+ * for q_norm_w and k_norm_w, into caller-owned device memory, on `stream`
+ * (call it on the backward's stream, before the next backward on the handle).
+ * Nothing is copied before the first backward or after an empty one.
+ * Errors: INVALID_ARG (null handle or pointer, other device), CUDA.
+ *
+ * h3attn_combine_norm_weight_grads: partials float32 [num_samples,
+ * num_heads, 128] (device, heads in global order) -> per_sample float32
+ * [num_samples, 128] (device, required: the total is summed from it) and
+ * total float32 [128] (device).  Allocates nothing; asynchronous on `stream`.
+ * num_samples == 0 zeroes total.  Errors: INVALID_ARG (sizes, null or
+ * misaligned pointers), UNSUPPORTED (device not sm_103), CUDA.
+ */
+h3attn_status h3attn_norm_weight_grad_partials(h3attn_t h, float *dq_norm_w_partials, float *dk_norm_w_partials,
+                                               void *stream);
+h3attn_status h3attn_combine_norm_weight_grads(const float *partials, int num_samples, int num_heads,
+                                               float *per_sample, float *total, void *stream);
+
+/*
+ * A 64-bit fingerprint of `bytes` bytes of device memory at `data`, computed on
+ * the GPU and written to the device uint64 *fingerprint on `stream`, so that
+ * runs can be compared without copying their outputs to the host (the
+ * "ws1_full_h3_transformer" page, PR #571, Status: GPU-side checksum
+ * fingerprints of the provider and candidate runs).  Definition: the bytes as
+ * little-endian 64-bit words w_0 .. w_{m-1} (the last zero-padded), mix() the
+ * splitmix64 finaliser (shifts 30, 27, 31; multipliers 0xbf58476d1ce4e5b9 and
+ * 0x94d049bb133111eb), G = 0x9e3779b97f4a7c15:
+ *   fingerprint = mix( sum_i mix(w_i + (i + 1) G) + bytes )   (mod 2^64).
+ * The sum is an integer sum, so the value is a pure function of the bytes
+ * (no dependence on the GPU's thread order).  data must be 8-byte aligned (may
+ * be NULL when bytes == 0), fingerprint 8-byte aligned.  Allocates nothing.
+ * Errors: INVALID_ARG, UNSUPPORTED (device not sm_103), CUDA.
+ */
+h3attn_status h3attn_fingerprint(const void *data, uint64_t bytes, uint64_t *fingerprint, void *stream);
+
+/*
+ * Test hook for the bounded waits (instrumentation; no counterpart on the
+ * pages, which ask that a failure close rather than fall back: the strict mode
+ * of the "ws1_full_h3_transformer" page, PR #571, Scope / Known limitations).
+ * The next h3attn_forward, h3attn_backward or h3attn_qkv_forward call on this
+ * handle makes one role of one kernel wait once, early in its first work item,
+ * on an on-device barrier that nothing completes.  That wait gives up after
+ * budget_cycles SM clock cycles, as every wait of the library does after its
+ * own budget: the kernel records TIMEOUT, its other warps leave their loops,
+ * it waits for the bulk copies and tensor-core products it already issued,
+ * releases its tensor memory and returns.  h3attn_device_status() then
+ * returns H3ATTN_ERR_TIMEOUT (outputs of that call are unspecified) and the
+ * following call is an ordinary one.  The request is cleared by the call that
+ * reads it, whether or not that call launches the named kernel.
+ * kernel: H3ATTN_STALL_FWD (attention forward), H3ATTN_STALL_DKDV,
+ * H3ATTN_STALL_DQ (whichever dQ kernel the handle runs), H3ATTN_STALL_QKV (the
+ * fused QKV projection of h3attn_qkv_forward), or 0 to cancel a request;
+ * role: H3ATTN_STALL_PRODUCER (the TMA producer warp), H3ATTN_STALL_MMA (the
+ * tensor-core issuer), H3ATTN_STALL_CONSUMER (a softmax or epilogue warp).
+ * Errors: INVALID_ARG (null handle, unknown kernel or role, budget_cycles < 1).
+ */
+#define H3ATTN_STALL_FWD 1
+#define H3ATTN_STALL_DKDV 2
+#define H3ATTN_STALL_DQ 3
+#define H3ATTN_STALL_QKV 4
+#define H3ATTN_STALL_PRODUCER 1
+#define H3ATTN_STALL_MMA 2
+#define H3ATTN_STALL_CONSUMER 3
+h3attn_status h3attn_debug_stall(h3attn_t h, int kernel, int role, long long budget_cycles);
 
 /* Static, human-readable name of a status code. */
 const char *h3attn_status_string(h3attn_status s);

@@ -3,8 +3,9 @@
 //   rope_table_kernel cos / sin of every channel's rotary angle per token
 //   rows_bwd_kernel   dx = RMSNorm-backward(RoPE^-1(scale * dx^)) per row, for q
 //                     and k, and the norm-weight partial of every 128-token tile
-//   dw_sample_kernel, dw_total_kernel
-//                     the norm-weight gradient per sample, then over samples
+//   dw_head_kernel, dw_sample_kernel, dw_total_kernel
+//                     the norm-weight gradient per (sample, head), then per
+//                     sample over heads, then over samples
 // (the per-leaf gradients of the "ws1_one_h3_block" page of RL-Kernel, PR #539,
 // Results and Tests; the 128-element norm-weight gradient of its Status
 // section).  Every sum runs in one fixed order, with no atomics.
@@ -136,41 +137,55 @@ rows_bwd_kernel(const __grid_constant__ RopeTable rt, const RowsParams p) {
 
 // -------------------------------------------------------- weight gradients
 
-// Per-sample weight gradient over the sample's (tile, head) partials, index
-// (tile - first tile) * H + head: eight fixed interleaved groups each sum their
-// indices in ascending order, then the groups are added in ascending order.
+// The norm-weight gradient is reduced in three fixed orders:
+//   per (sample, head): the sample's 128-token tile partials in ascending order;
+//   per sample: those (sample, head) partials over heads in ascending order;
+//   in total: the per-sample sums in ascending sample order.
+// A (sample, head) partial depends only on that head's rows of that sample, so
+// when the heads are split across GPUs (each GPU running its heads as a handle
+// of its own) and the partials are gathered in head order, the same two last
+// reductions give the same bits whatever the number of GPUs.
+
+// Per (sample, head) partial: dst[s][h][c] = sum over the sample's tiles t, in
+// ascending order, of part[t][h][c].  One CTA per (sample, q / k).
 __global__ void __launch_bounds__(1024)
-dw_sample_kernel(const float* __restrict__ part_q, const float* __restrict__ part_k, Seq seq, Plan plan, int H,
-                 float* __restrict__ dwq_s, float* __restrict__ dwk_s) {
-    constexpr int kGroups = 8;
+dw_head_kernel(const float* __restrict__ part_q, const float* __restrict__ part_k, Plan plan, int n, int H,
+               float* __restrict__ dst_q, float* __restrict__ dst_k) {
     const int s = blockIdx.x;
     const float* part = blockIdx.y == 0 ? part_q : part_k;
-    float* dst = blockIdx.y == 0 ? dwq_s : dwk_s;
-    const int c = threadIdx.x & 127, grp = threadIdx.x >> 7;
-    __shared__ float red[kGroups][kD];
+    float* dst = blockIdx.y == 0 ? dst_q : dst_k;
     const int r = plan.rank_of[s];
     const int t0 = plan.cum128[r], t1 = plan.cum128[r + 1];
-    const int n = (t1 - t0) * H;
-    const float* base = part + (size_t)t0 * H * kD + c;
-    float acc = 0.f;
-    for (int i = grp; i < n; i += kGroups) acc += base[(size_t)i * kD];
-    red[grp][c] = acc;
-    __syncthreads();
-    if (grp == 0) {
-        float sum = red[0][c];
-#pragma unroll
-        for (int g = 1; g < kGroups; ++g) sum += red[g][c];
-        dst[(size_t)s * kD + c] = sum;
+    for (int hc = threadIdx.x; hc < H * kD; hc += blockDim.x) {
+        float acc = 0.f;
+        for (int t = t0; t < t1; ++t) acc += part[(size_t)t * H * kD + hc];
+        dst[(size_t)s * H * kD + hc] = acc;
     }
 }
 
-__global__ void dw_total_kernel(const float* __restrict__ dwq_s, const float* __restrict__ dwk_s, int n,
-                                float* __restrict__ dwq, float* __restrict__ dwk) {
-    const int c = threadIdx.x & 127;
-    const float* src = threadIdx.x < 128 ? dwq_s : dwk_s;
+// Up to two reductions side by side (blockIdx.y): q_norm_w's and k_norm_w's.
+struct DwCombine {
+    const float* part[2];  // [n][H][128] per (sample, head) partials
+    float* per_sample[2];  // [n][128]
+    float* total[2];       // [128]
+};
+
+// Per sample over heads: per_sample[s][c] = sum over h ascending of part[s][h][c].
+// One CTA of 128 threads per sample.
+__global__ void __launch_bounds__(128) dw_sample_kernel(const __grid_constant__ DwCombine d, int H) {
+    const int s = blockIdx.x, c = threadIdx.x, y = blockIdx.y;
+    const float* p = d.part[y] + (size_t)s * H * kD + c;
     float acc = 0.f;
-    for (int s = 0; s < n; ++s) acc += src[(size_t)s * kD + c];
-    (threadIdx.x < 128 ? dwq : dwk)[c] = acc;
+    for (int h = 0; h < H; ++h) acc += p[(size_t)h * kD];
+    d.per_sample[y][(size_t)s * kD + c] = acc;
+}
+
+// Over samples in ascending order.
+__global__ void __launch_bounds__(128) dw_total_kernel(const __grid_constant__ DwCombine d, int n) {
+    const int c = threadIdx.x, y = blockIdx.y;
+    float acc = 0.f;
+    for (int s = 0; s < n; ++s) acc += d.per_sample[y][(size_t)s * kD + c];
+    d.total[y][c] = acc;
 }
 
 // ------------------------------------------------------------------ host
@@ -217,13 +232,29 @@ cudaError_t launch_bwd_rows(const Problem& p, const Workspace& ws, const RopeTab
     return cudaGetLastError();
 }
 
+namespace {
+cudaError_t combine(const DwCombine& d, int pairs, int n, int H, cudaStream_t st) {
+    dw_sample_kernel<<<dim3(n, pairs), kD, 0, st>>>(d, H);
+    dw_total_kernel<<<dim3(1, pairs), kD, 0, st>>>(d, n);
+    return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_dw_combine(const float* partials, int n, int H, float* per_sample, float* total,
+                              cudaStream_t st) {
+    DwCombine d = {{partials, partials}, {per_sample, per_sample}, {total, total}};
+    return combine(d, 1, n, H, st);
+}
+
 cudaError_t launch_bwd_dw(const Problem& p, const Workspace& ws, float* dwq, float* dwk, float* dwq_s,
                           float* dwk_s, cudaStream_t st) {
-    float* qs = dwq_s ? dwq_s : ws.dwq_sample;
-    float* ks = dwk_s ? dwk_s : ws.dwk_sample;
-    dw_sample_kernel<<<dim3(p.seq.n, 2), 1024, 0, st>>>(ws.dwq_part, ws.dwk_part, p.seq, ws.plan, p.H, qs, ks);
-    dw_total_kernel<<<1, 256, 0, st>>>(qs, ks, p.seq.n, dwq, dwk);
-    return cudaGetLastError();
+    const int n = p.seq.n, H = p.H;
+    dw_head_kernel<<<dim3(n, 2), 1024, 0, st>>>(ws.dwq_part, ws.dwk_part, ws.plan, n, H, ws.dwq_head, ws.dwk_head);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    DwCombine d = {{ws.dwq_head, ws.dwk_head}, {dwq_s ? dwq_s : ws.dwq_sample, dwk_s ? dwk_s : ws.dwk_sample},
+                   {dwq, dwk}};
+    return combine(d, 2, n, H, st);
 }
 
 }  // namespace h3

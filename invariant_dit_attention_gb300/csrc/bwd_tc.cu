@@ -50,6 +50,8 @@ struct BwdTcParams {
     float* dyhat;       // scale * dk^ (dkdv) or scale * dq^ (dq): FP32 [S, H, 128]
     __half* ds;         // stored dS^T blocks (dkdv writes, dq_ds reads), or null
     long long ds_blocks;
+    int stall;               // tc::StallRole stalled once on the CTA's first item (tests), else 0
+    long long stall_budget;  // clock cycles of that stall's bounded wait
 };
 
 struct BwdItem {
@@ -86,10 +88,6 @@ __device__ __forceinline__ bool bwd_item(const BwdTcParams& p, int i, BwdItem& i
     return true;
 }
 
-__device__ __forceinline__ void named_bar(int id, int count) {
-    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
-}
-
 // Zeroes rows [valid, rows) of a 64-channel-half tile (whole 128-byte rows).
 __device__ __forceinline__ void zero_rows(uint32_t half, int valid, int rows, int lane) {
     for (int r = valid + (lane >> 3); r < rows; r += 4)
@@ -117,9 +115,12 @@ struct FixedSpec {
 // Producer warp of one ring (lane 0 issues): for every streamed 128-row block of
 // every item of this CTA, waits until its slot is released, loads the block's
 // two 64-channel halves with TMA and publishes it.  One warp per ring, so a
-// ring never waits behind a slot of the other.
+// ring never waits behind a slot of the other.  Before returning it waits for
+// every copy it issued (an aborted kernel's consumers may have left some
+// unread), so no copy lands after the CTA's shared memory is released.
+// `never`: a barrier nothing completes, the target of a test's stall (`stall`).
 __device__ __forceinline__ void ring_producer(const BwdTcParams& p, const RingSpec& r, const FixedSpec* fx,
-                                              volatile int* abort_flag, int lane) {
+                                              volatile int* abort_flag, int lane, uint32_t never, bool stall) {
     constexpr int kTile = 128 * 128 * 2, kHalf = 128 * 64 * 2;
     bool failed = false;
     auto fail = [&]() {
@@ -128,6 +129,10 @@ __device__ __forceinline__ void ring_producer(const BwdTcParams& p, const RingSp
         atomicOr(p.plan.err, kErrTimeout);
     };
     uint32_t blk = 0, items = 0, tails = 0;
+    // copies issued (lane 0): fixed tile pairs, ring blocks whose full barrier was
+    // armed, and a tail block whose own wait gave up with its copy possibly in flight
+    uint32_t fixed_armed = 0, armed = 0;
+    bool tail_pending = false;
     for (int i = blockIdx.x; !failed; i += gridDim.x) {
         BwdItem it;
         if (!bwd_item(p, i, it)) break;
@@ -141,6 +146,7 @@ __device__ __forceinline__ void ring_producer(const BwdTcParams& p, const RingSp
                     tc::tma_load_2d(fx->base + hf * kHalf, fx->map0, x0 + 64 * hf, it.row0, fx->full);
                     tc::tma_load_2d(fx->base + kTile + hf * kHalf, fx->map1, x0 + 64 * hf, it.row0, fx->full);
                 }
+                ++fixed_armed;
             }
         }
         failed = __shfl_sync(0xffffffffu, failed, 0);
@@ -152,12 +158,17 @@ __device__ __forceinline__ void ring_producer(const BwdTcParams& p, const RingSp
             const int y = it.seg0 + 128 * j, valid = it.L - 128 * j;
             const bool tail = r.zero_tail && valid < 128;
             if (lane == 0) {
-                if (!tc::mbar_wait(r.empty + 8 * sl, ph ^ 1, abort_flag)) fail();
+                if (stall && items == 1 && j == 0 && !tc::mbar_wait(never, 0, abort_flag, p.stall_budget)) fail();
+                if (!failed && !tc::mbar_wait(r.empty + 8 * sl, ph ^ 1, abort_flag)) fail();
                 if (!failed) {
                     const uint32_t b = tail ? r.tail : r.full + 8 * sl;
                     tc::mbar_expect_tx(b, kTile);
                     for (int hf = 0; hf < 2; ++hf) tc::tma_load_2d(dst + hf * kHalf, r.map, x0 + 64 * hf, y, b);
-                    if (tail && !tc::mbar_wait(r.tail, tails & 1, abort_flag)) fail();
+                    if (!tail) ++armed;
+                    if (tail && !tc::mbar_wait(r.tail, tails & 1, abort_flag)) {
+                        tail_pending = true;
+                        fail();
+                    }
                 }
             }
             failed = __shfl_sync(0xffffffffu, failed, 0);
@@ -166,11 +177,21 @@ __device__ __forceinline__ void ring_producer(const BwdTcParams& p, const RingSp
                 for (int hf = 0; hf < 2; ++hf) zero_rows(dst + hf * kHalf, valid, 128, lane);
                 tc::fence_proxy_async();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(r.full + 8 * sl);
+                if (lane == 0) {
+                    tc::mbar_arrive(r.full + 8 * sl);
+                    ++armed;
+                }
             }
             ++blk;
         }
     }
+    if (lane == 0) {
+        bool ok = !fx || fixed_armed == 0 || tc::mbar_drain(fx->full, (fixed_armed - 1) & 1);
+        ok &= tc::drain_ring(r.full, r.slots, armed);
+        if (tail_pending) ok &= tc::mbar_drain(r.tail, tails & 1);
+        if (!ok) atomicOr(p.plan.err, kErrTimeout);
+    }
+    __syncwarp();
 }
 
 // ------------------------------------------------------------------ dK, dV
@@ -200,7 +221,8 @@ constexpr int kOffLse = kOffO + kOSlots * bwdt::kTile;  // [4 wg][2 buf][lse2 32
 constexpr int kOffBar = kOffLse + 4 * 2 * 64 * 4;
 constexpr int kSmem = kOffBar + 256;                // the dynamic shared memory base is 1024-aligned (checked)
 enum { bFixedFull = 0, bQFull, bQEmpty = bQFull + kQSlots, bOFull = bQEmpty + kQSlots, bOEmpty = bOFull + kOSlots,
-       bSFull = bOEmpty + kOSlots, bPFull, bSUsed, bPtFull, bDsFull, bAccDone, bTailQ, bTailO, bDone, bCount };
+       bSFull = bOEmpty + kOSlots, bPFull, bSUsed, bPtFull, bDsFull, bAccDone, bTailQ, bTailO, bDone, bNever,
+       bCount };
 constexpr uint32_t cB = 128;
 }  // namespace kvt
 
@@ -249,6 +271,7 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         tc::mbar_init(bar(bTailQ), 1);
         tc::mbar_init(bar(bTailO), 1);
         tc::mbar_init(bar(bDone), 1);
+        tc::mbar_init(bar(bNever), 1);  // nothing arrives: the target of a test's stall
         *abort_flag = 0;
         tc::fence_mbar_init();
     }
@@ -276,7 +299,8 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         const FixedSpec fx = {&mk, &mv, sbase + kOffFixed, bar(bFixedFull), bar(bAccDone)};
         const RingSpec r = warp == 0 ? RingSpec{&mq, sbase + kOffQ, kQSlots, bar(bQFull), bar(bQEmpty), bar(bTailQ), true}
                                      : RingSpec{&mdo, sbase + kOffO, kOSlots, bar(bOFull), bar(bOEmpty), bar(bTailO), true};
-        ring_producer(p, r, warp == 0 ? &fx : nullptr, abort_flag, lane);
+        ring_producer(p, r, warp == 0 ? &fx : nullptr, abort_flag, lane, bar(bNever),
+                      warp == 0 && p.stall == tc::kStallProducer);
     } else if (warp == 1) {
         // ----------------------------------------------------- MMA issuer
         if (lane == 0) {
@@ -328,6 +352,11 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 const int nq = (it.L + 127) / 128;
                 const uint32_t b0 = blk;
                 if (!issue_st(b0) || !issue_dpt(b0)) { fail(); break; }
+                if (p.stall == tc::kStallMma && items == 1 &&
+                    !tc::mbar_wait(bar(bNever), 0, abort_flag, p.stall_budget)) {
+                    fail();
+                    break;
+                }
                 for (int qj = 0; qj < nq && !failed; ++qj) {
                     const uint32_t b = b0 + qj;
                     const bool more = qj + 1 < nq;
@@ -360,8 +389,9 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 blk = b0 + nq;
                 tc::mma_commit(bar(bAccDone));
             }
+            // every issued MMA has completed before TMEM is released (also on an abort)
             tc::mma_commit(bar(bDone));
-            if (!tc::mbar_wait(bar(bDone), 0, abort_flag) && !failed) fail();
+            if (!tc::mbar_drain(bar(bDone), 0)) fail();
         }
         __syncwarp();
     } else if (warp >= 4) {
@@ -391,6 +421,11 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 }
             };
             fetch(0);
+            // The four warps of a warpgroup meet at a named barrier once per block and once
+            // after the last one, and must all leave the loops at the same barrier: a warp
+            // whose wait failed skips to the next barrier, where the barrier's OR tells the
+            // others and the warpgroup leaves together.
+            bool left = false;
             for (int qj = 0; qj < nq; ++qj) {
                 float* lb = lsebuf + (qj & 1) * 64;
                 if (t < 32) {
@@ -398,13 +433,21 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                     lb[32 + t] = nd;
                 }
                 fetch(qj + 1);
-                named_bar(1 + wg, 128);
+                if (tc::bar_sync_or(1 + wg, 128, failed)) {
+                    failed = true;
+                    left = true;
+                    break;
+                }
                 const uint64_t* lb2 = reinterpret_cast<const uint64_t*>(lb);  // (-lse2, -lse2') pairs, then -Delta pairs
                 const int validq = it.L - 128 * qj - 32 * wg;  // columns of this quarter inside the sample
                 bool ok = true;
-                if (lane == 0) ok = tc::mbar_wait(bar(bSFull), cntS & 1, abort_flag);
+                if (lane == 0) {
+                    if (p.stall == tc::kStallConsumer && warp == 4 && cntS == 0)
+                        ok = tc::mbar_wait(bar(bNever), 0, abort_flag, p.stall_budget);
+                    if (ok) ok = tc::mbar_wait(bar(bSFull), cntS & 1, abort_flag);
+                }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) { fail(); break; }
+                if (!ok) { fail(); continue; }
                 tc::fence_after_sync();
                 uint64_t p2[16];  // S^T column pairs, then P in FP32
                 tc::tmem_ld32_pairs(tS, p2);
@@ -422,7 +465,7 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 // ---- dP^T(b) from B, then P^T (bf16) over B's first 16 columns of this quarter
                 if (lane == 0) ok = tc::mbar_wait(bar(bPFull), cntS & 1, abort_flag);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) { fail(); break; }
+                if (!ok) { fail(); continue; }
                 ++cntS;
                 tc::fence_after_sync();
                 uint64_t d2[16];
@@ -470,13 +513,16 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                     }
                 }
             }
+            if (!left) {  // the last block's failures and the accumulators' wait, agreed by the warpgroup
+                bool ok = !failed;
+                if (ok && lane == 0) ok = tc::mbar_wait(bar(bAccDone), items & 1, abort_flag);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok && !failed) fail();
+                if (tc::bar_sync_or(1 + wg, 128, failed)) failed = true;
+            }
             if (failed) break;
             // ---- drain: each warpgroup its 32 channels of dV (bf16 output rows) and of
             // scale * dk^ (FP32 rows for the RoPE^-1 / RMSNorm backward)
-            bool ok = true;
-            if (lane == 0) ok = tc::mbar_wait(bar(bAccDone), items & 1, abort_flag);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) { fail(); break; }
             ++items;
             tc::fence_after_sync();
             const size_t row_off = ((size_t)(it.row0 + t) * p.H + it.h) * kD + 32 * wg;
@@ -515,12 +561,7 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         }
     }
 
-    __syncthreads();
-    if (warp == 0 && lane == 0 && *abort_flag) {
-        const long long t0 = clock64();
-        while (clock64() - t0 < 20000000LL) {
-        }
-    }
+    // the producers have waited out their copies and the issuer its products
     __syncthreads();
     if (warp == 1) {
         tc::fence_after_sync();
@@ -548,7 +589,7 @@ constexpr int kOffBar = kOffV + kVSlots * bwdt::kTile;
 constexpr int kSmem = kOffBar + 256;               // the dynamic shared memory base is 1024-aligned (checked)
 enum { bFixedFull = 0, bKFull, bKEmpty = bKFull + kKSlots, bVFull = bKEmpty + kKSlots,
        bVEmpty = bVFull + kVSlots, bSFull = bVEmpty + kVSlots, bSUsed, bPFull, bDsFree, bAccDone, bTail, bDone,
-       bCount };
+       bNever, bCount };
 constexpr uint32_t cDs = 384;
 }  // namespace dqt
 
@@ -590,6 +631,7 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         tc::mbar_init(bar(bAccDone), 1);
         tc::mbar_init(bar(bTail), 1);
         tc::mbar_init(bar(bDone), 1);
+        tc::mbar_init(bar(bNever), 1);  // nothing arrives: the target of a test's stall
         *abort_flag = 0;
         tc::fence_mbar_init();
     }
@@ -616,7 +658,8 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         const FixedSpec fx = {&mq, &mdo, sbase + kOffFixed, bar(bFixedFull), bar(bAccDone)};
         const RingSpec r = warp == 0 ? RingSpec{&mk, sbase + kOffK, kKSlots, bar(bKFull), bar(bKEmpty), bar(bTail), true}
                                      : RingSpec{&mv, sbase + kOffV, kVSlots, bar(bVFull), bar(bVEmpty), bar(bTail), false};
-        ring_producer(p, r, warp == 0 ? &fx : nullptr, abort_flag, lane);
+        ring_producer(p, r, warp == 0 ? &fx : nullptr, abort_flag, lane, bar(bNever),
+                      warp == 0 && p.stall == tc::kStallProducer);
     } else if (warp == 1) {
         // ----------------------------------------------------- MMA issuer
         if (lane == 0) {
@@ -661,6 +704,11 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                 uint32_t kcur = kr;  // ring index of the k^ tile of block kj
                 if (!issue_s()) { fail(); break; }
                 ++kr;
+                if (p.stall == tc::kStallMma && items == 1 &&
+                    !tc::mbar_wait(bar(bNever), 0, abort_flag, p.stall_budget)) {
+                    fail();
+                    break;
+                }
                 for (int kj = 0; kj < nk && !failed; ++kj) {
                     // block kj's scores are in registers: refill the buffer with block kj+1
                     if (!tc::mbar_wait(bar(bSUsed), cntS & 1, abort_flag)) { fail(); break; }
@@ -684,8 +732,9 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
                 if (failed) break;
                 tc::mma_commit(bar(bAccDone));
             }
+            // every issued MMA has completed before TMEM is released (also on an abort)
             tc::mma_commit(bar(bDone));
-            if (!tc::mbar_wait(bar(bDone), 0, abort_flag) && !failed) fail();
+            if (!tc::mbar_drain(bar(bDone), 0)) fail();
         }
         __syncwarp();
     } else if (warp >= 4) {
@@ -708,7 +757,11 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
             const uint64_t c2 = f2pack(c, c), nl2 = f2pack(-lse2, -lse2), nd2 = f2pack(-dlt, -dlt);
             for (int kj = 0; kj < nk; ++kj) {
                 bool ok = true;
-                if (lane == 0) ok = tc::mbar_wait(bar(bSFull), cntS & 1, abort_flag);
+                if (lane == 0) {
+                    if (p.stall == tc::kStallConsumer && warp == 4 && cntS == 0)
+                        ok = tc::mbar_wait(bar(bNever), 0, abort_flag, p.stall_budget);
+                    if (ok) ok = tc::mbar_wait(bar(bSFull), cntS & 1, abort_flag);
+                }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) { fail(); break; }
                 ++cntS;
@@ -771,12 +824,7 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
         }
     }
 
-    __syncthreads();
-    if (warp == 0 && lane == 0 && *abort_flag) {
-        const long long t0 = clock64();
-        while (clock64() - t0 < 20000000LL) {
-        }
-    }
+    // the producers have waited out their copies and the issuer its products
     __syncthreads();
     if (warp == 1) {
         tc::fence_after_sync();
@@ -804,7 +852,7 @@ constexpr int kStage = 3 * bwdt::kTile;  // dS^T of two query tiles + k^: 96 KB
 constexpr int kOffBar = kRingStages * kStage;
 constexpr int kSmem = kOffBar + 256;  // the dynamic shared memory base is 1024-aligned (checked)
 enum { bFull = 0, bEmpty = bFull + kRingStages, bAccFull = bEmpty + kRingStages, bAccEmpty = bAccFull + 2,
-       bTail = bAccEmpty + 2, bDone, bCount };
+       bTail = bAccEmpty + 2, bDone, bNever, bCount };
 }  // namespace dqs
 
 struct DqsItem {
@@ -863,6 +911,7 @@ dq_ds_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constant__ CU
         }
         tc::mbar_init(bar(bTail), 1);
         tc::mbar_init(bar(bDone), 1);
+        tc::mbar_init(bar(bNever), 1);  // nothing arrives: the target of a test's stall
         *abort_flag = 0;
         tc::fence_mbar_init();
         tc::prefetch_map(&mds);
@@ -887,7 +936,11 @@ dq_ds_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constant__ CU
         // ------------------------------------------------------ TMA producer
         const uint64_t pol = tc::policy_evict_first();
         uint32_t blk = 0, tails = 0;
-        for (int i = blockIdx.x; !failed; i += gridDim.x) {
+        // copies issued (lane 0): stages whose full barrier was armed, and a tail stage
+        // whose own wait gave up with its copies possibly in flight
+        uint32_t armed = 0;
+        bool tail_pending = false, first = true;
+        for (int i = blockIdx.x; !failed; i += gridDim.x, first = false) {
             DqsItem it;
             if (!dqs_item(p, i, it)) break;
             const long long base = (long long)p.H * p.plan.cumsq[it.rank] + (long long)it.h * it.nq * it.nq;
@@ -897,7 +950,10 @@ dq_ds_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constant__ CU
                 const int valid = it.L - 128 * j;
                 const bool tail = valid < 128;
                 if (lane == 0) {
-                    if (!tc::mbar_wait(bar(bEmpty + s), ph ^ 1, abort_flag)) fail();
+                    if (p.stall == tc::kStallProducer && first && j == 0 &&
+                        !tc::mbar_wait(bar(bNever), 0, abort_flag, p.stall_budget))
+                        fail();
+                    if (!failed && !tc::mbar_wait(bar(bEmpty + s), ph ^ 1, abort_flag)) fail();
                     if (!failed) {
                         const uint32_t b = tail ? bar(bTail) : bar(bFull + s);
                         const int b0 = (int)(base + (long long)j * it.nq + 2 * it.pair);
@@ -908,7 +964,11 @@ dq_ds_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constant__ CU
                             if (it.has1) tc::tma_load_4d_hint(dst + kTile + hf * kHalf, &mds, 0, 0, 2 * hf, b0 + 1, b, pol);
                             tc::tma_load_2d(dst + 2 * kTile + hf * kHalf, &mk, it.h * 128 + 64 * hf, it.seg0 + 128 * j, b);
                         }
-                        if (tail && !tc::mbar_wait(bar(bTail), tails & 1, abort_flag)) fail();
+                        if (!tail) ++armed;
+                        if (tail && !tc::mbar_wait(bar(bTail), tails & 1, abort_flag)) {
+                            tail_pending = true;
+                            fail();
+                        }
                     }
                 }
                 failed = __shfl_sync(0xffffffffu, failed, 0);
@@ -917,9 +977,18 @@ dq_ds_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constant__ CU
                     for (int hf = 0; hf < 2; ++hf) zero_rows(dst + 2 * kTile + hf * kHalf, valid, 128, lane);
                     tc::fence_proxy_async();
                     __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(bar(bFull + s));
+                    if (lane == 0) {
+                        tc::mbar_arrive(bar(bFull + s));
+                        ++armed;
+                    }
                 }
             }
+        }
+        // every copy issued has landed before the CTA's shared memory is released
+        if (lane == 0) {
+            bool ok = tc::drain_ring(bar(bFull), kRingStages, armed);
+            if (tail_pending) ok &= tc::mbar_drain(bar(bTail), tails & 1);
+            if (!ok) atomicOr(p.plan.err, kErrTimeout);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -957,12 +1026,18 @@ dq_ds_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constant__ CU
                                        dB + so + ((kk * 2048) >> 4), id, (j > 0) || (kk > 0));
                     }
                     tc::mma_commit(bar(bEmpty + s));
+                    if (p.stall == tc::kStallMma && items == 0 && j == 0 &&
+                        !tc::mbar_wait(bar(bNever), 0, abort_flag, p.stall_budget)) {
+                        fail();
+                        break;
+                    }
                 }
                 if (failed) break;
                 tc::mma_commit(bar(bAccFull + b));
             }
+            // every issued MMA has completed before TMEM is released (also on an abort)
             tc::mma_commit(bar(bDone));
-            if (!tc::mbar_wait(bar(bDone), 0, abort_flag) && !failed) fail();
+            if (!tc::mbar_drain(bar(bDone), 0)) fail();
         }
         __syncwarp();
     } else if (warp >= 4) {
@@ -975,7 +1050,11 @@ dq_ds_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constant__ CU
             if (!dqs_item(p, i, it)) break;
             const uint32_t b = items & 1;
             bool ok = true;
-            if (lane == 0) ok = tc::mbar_wait(bar(bAccFull + b), (items >> 1) & 1, abort_flag);
+            if (lane == 0) {
+                if (p.stall == tc::kStallConsumer && warp == 4 && items == 0)
+                    ok = tc::mbar_wait(bar(bNever), 0, abort_flag, p.stall_budget);
+                if (ok) ok = tc::mbar_wait(bar(bAccFull + b), (items >> 1) & 1, abort_flag);
+            }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) { fail(); break; }
             tc::fence_after_sync();
@@ -1003,13 +1082,7 @@ dq_ds_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constant__ CU
         }
     }
 
-    __syncthreads();
-    if (warp == 0 && lane == 0 && *abort_flag) {
-        // let any TMA still in flight land before the CTA's shared memory goes away
-        const long long t0 = clock64();
-        while (clock64() - t0 < 20000000LL) {
-        }
-    }
+    // the producer has waited out its copies and the issuer its products
     __syncthreads();
     if (warp == 1) {
         tc::fence_after_sync();
@@ -1063,6 +1136,8 @@ static BwdTcParams bwd_params(const Problem& p, const Workspace& ws, const float
     b.delta = ws.delta;
     b.ds = ws.ds;
     b.ds_blocks = ws.ds_blocks;
+    b.stall = 0;
+    b.stall_budget = p.stall.budget;
     return b;
 }
 
@@ -1073,6 +1148,7 @@ cudaError_t launch_bwd_dkdv(const Problem& p, const Workspace& ws, const float* 
     BwdTcParams b = bwd_params(p, ws, lse);
     b.dv = dv;
     b.dyhat = ws.dkhat32;
+    if (p.stall.kernel == kStallKernelDkdv) b.stall = p.stall.role;
     const int sms = device_sms();
     if (sms < 1) return cudaErrorNotSupported;
     dkdv_tc_kernel<<<sms, kvt::kThreads, kvt::kSmem, st>>>(m.q, m.k, m.v, m.dout, b);
@@ -1088,6 +1164,7 @@ cudaError_t launch_bwd_dq(const Problem& p, const Workspace& ws, const float* ls
     if (sms < 1) return cudaErrorNotSupported;
     b.dv = nullptr;
     b.dyhat = ws.dqhat32;
+    if (p.stall.kernel == kStallKernelDq) b.stall = p.stall.role;
     if (ws.ds) {  // dS was stored by the dK/dV kernel: dQ is one product per block
         // a block is [32-query chunk][key][32 queries] (query in chunk, key, chunk, block);
         // a box of 2 chunks lands in shared memory in the same order, 64-byte swizzled

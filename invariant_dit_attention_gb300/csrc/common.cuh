@@ -199,6 +199,8 @@ struct Workspace {
     float* dwk_part;         // [max_tiles64, H, 128]
     float* dwq_sample;       // [max_samples, 128]
     float* dwk_sample;       // [max_samples, 128]
+    float* dwq_head;         // [max_samples, H, 128] per (sample, head) partials of the last backward
+    float* dwk_head;         // [max_samples, H, 128]
     Plan plan;
     // canonical key order only (null otherwise)
     int32_t* perm;           // [max_tokens] packed index of canonical slot c
@@ -212,6 +214,17 @@ struct Workspace {
     // sample's 128-token tiles
     __half* ds;
     long long ds_blocks;     // capacity in blocks
+};
+
+// A test's request that one kernel of the next call stall one of its roles
+// once, on a bounded wait that nothing completes (see tc::StallRole), to
+// exercise the kernel's unwinding.  kernel 0 = none.
+enum StallKernel { kStallKernelNone = 0, kStallKernelFwd = 1, kStallKernelDkdv = 2, kStallKernelDq = 3,
+                   kStallKernelQkv = 4 };
+struct StallRequest {
+    int kernel = 0;
+    int role = 0;
+    long long budget = 0;  // clock cycles
 };
 
 struct Problem {
@@ -228,6 +241,7 @@ struct Problem {
     // identity).  Kernels that address the caller's q, k or out rows one token
     // at a time (prologue, Delta, row backward) read and write them through it.
     const int32_t* rowmap = nullptr;
+    StallRequest stall;  // tests only
 };
 
 // Stages of one call, in launch order (timed separately when stage timing is on).
@@ -263,5 +277,10 @@ cudaError_t launch_qkv(const Problem& p, const Workspace& ws, const RopeTable* r
                        __nv_bfloat16* v, cudaStream_t st);
 cudaError_t launch_bwd_dw(const Problem& p, const Workspace& ws, float* dwq, float* dwk, float* dwq_s,
                           float* dwk_s, cudaStream_t st);
+// The fixed-order reduction of per-(sample, head) norm-weight partials [n][H][128]:
+// per sample over heads ascending into per_sample [n][128], then over samples
+// ascending into total [128] (bwd_rows.cu).
+cudaError_t launch_dw_combine(const float* partials, int n, int H, float* per_sample, float* total,
+                              cudaStream_t st);
 
 }  // namespace h3

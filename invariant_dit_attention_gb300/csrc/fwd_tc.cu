@@ -46,7 +46,7 @@ constexpr float kMaxStale = 8.0f;            // log2 growth of the max tolerated
 // barrier indices (8 bytes each)
 enum {
     bQFull = 0, bQEmpty, bKVFull, bKVEmpty = bKVFull + kNST, bSFull = bKVEmpty + kNST, bPFull = bSFull + 2,
-    bPVDone = bPFull + 2, bOFree = bPVDone + 2, bTail = bOFree + 2, bDone, bCount
+    bPVDone = bPFull + 2, bOFree = bPVDone + 2, bTail = bOFree + 2, bDone, bNever, bCount
 };
 }  // namespace fwdt
 
@@ -57,6 +57,8 @@ struct FwdTcParams {
     float scale_log2;
     __nv_bfloat16* out;
     float* lse;
+    int stall;               // tc::StallRole stalled once on the CTA's first item (tests), else 0
+    long long stall_budget;  // clock cycles of that stall's bounded wait
 };
 
 struct FwdItem {
@@ -115,6 +117,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         }
         tc::mbar_init(bar(bTail), 1);
         tc::mbar_init(bar(bDone), 1);
+        tc::mbar_init(bar(bNever), 1);  // nothing arrives: the target of a test's stall
         *abort_flag = 0;
         tc::fence_mbar_init();
         tc::prefetch_map(&mq);
@@ -147,6 +150,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         uint32_t kv_it = 0, items = 0, tails = 0;
+        // copies issued (lane 0): Q loads, K/V blocks whose full barrier was armed, and
+        // a tail block whose own wait gave up with its copy possibly in flight
+        uint32_t q_armed = 0, kv_armed = 0;
+        bool tail_pending = false;
         for (int i = blockIdx.x; !failed; i += gridDim.x) {
             FwdItem it;
             if (!fwd_item(p, i, it)) break;
@@ -159,6 +166,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                         for (int hf = 0; hf < 2; ++hf)
                             tc::tma_load_2d(sbase + kOffQ + x * kTile + hf * kHalf, &mq, x0 + 64 * hf,
                                             it.row0 + 128 * x, bar(bQFull));
+                    ++q_armed;
                 }
             }
             failed = __shfl_sync(0xffffffffu, failed, 0);
@@ -172,13 +180,20 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                     const bool tail = kv == 1 && valid < 128;
                     const CUtensorMap* map = kv == 0 ? &mk : &mv;
                     if (lane == 0) {
-                        if (!tc::mbar_wait(bar(bKVEmpty + slot), ph ^ 1, abort_flag)) fail();
+                        if (p.stall == tc::kStallProducer && items == 1 && j == 0 && kv == 0 &&
+                            !tc::mbar_wait(bar(bNever), 0, abort_flag, p.stall_budget))
+                            fail();
+                        if (!failed && !tc::mbar_wait(bar(bKVEmpty + slot), ph ^ 1, abort_flag)) fail();
                         if (!failed) {
                             const uint32_t b = tail ? bar(bTail) : bar(bKVFull + slot);
                             tc::mbar_expect_tx(b, kTile);
                             tc::tma_load_2d(dst, map, x0, y, b);
                             tc::tma_load_2d(dst + kHalf, map, x0 + 64, y, b);
-                            if (tail && !tc::mbar_wait(bar(bTail), tails & 1, abort_flag)) fail();
+                            if (!tail) ++kv_armed;
+                            if (tail && !tc::mbar_wait(bar(bTail), tails & 1, abort_flag)) {
+                                tail_pending = true;
+                                fail();
+                            }
                         }
                     }
                     failed = __shfl_sync(0xffffffffu, failed, 0);
@@ -194,12 +209,24 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                         }
                         tc::fence_proxy_async();
                         __syncwarp();
-                        if (lane == 0) tc::mbar_arrive(bar(bKVFull + slot));
+                        if (lane == 0) {
+                            tc::mbar_arrive(bar(bKVFull + slot));
+                            ++kv_armed;
+                        }
                     }
                     ++kv_it;
                 }
             }
         }
+        // every copy issued has landed before the CTA's shared memory is released (on
+        // an abort, consumers may have left some unread)
+        if (lane == 0) {
+            bool ok = q_armed == 0 || tc::mbar_drain(bar(bQFull), (q_armed - 1) & 1);
+            ok &= tc::drain_ring(bar(bKVFull), kNST, kv_armed);
+            if (tail_pending) ok &= tc::mbar_drain(bar(bTail), tails & 1);
+            if (!ok) atomicOr(p.plan.err, kErrTimeout);
+        }
+        __syncwarp();
     } else if (warp == 1) {
         // ----------------------------------------------------- MMA issuer
         if (lane == 0) {
@@ -237,6 +264,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                 for (int x = 0; x < nX; ++x) issue_s(x, kslot);
                 tc::mma_commit(bar(bKVEmpty + kslot));
                 if (it.nkv == 1) tc::mma_commit(bar(bQEmpty));
+                if (p.stall == tc::kStallMma && items == 1 &&
+                    !tc::mbar_wait(bar(bNever), 0, abort_flag, p.stall_budget)) {
+                    fail();
+                    break;
+                }
                 for (int j = 0; j < it.nkv && !failed; ++j) {
                     const uint32_t vslot = kv_it % kNST;
                     if (!tc::mbar_wait(bar(bKVFull + vslot), (kv_it / kNST) & 1, abort_flag)) { fail(); break; }
@@ -275,9 +307,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                 }
                 for (int x = 0; x < nX; ++x) ++itemsX[x];
             }
-            // every issued MMA has completed before TMEM is released
+            // every issued MMA has completed before TMEM is released (also on an abort)
             tc::mma_commit(bar(bDone));
-            if (!tc::mbar_wait(bar(bDone), 0, abort_flag) && !failed) fail();
+            if (!tc::mbar_drain(bar(bDone), 0)) fail();
         }
         __syncwarp();
     } else if (warp >= 4) {
@@ -296,7 +328,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < it.nkv; ++j) {
                 bool ok = true;
-                if (lane == 0) ok = tc::mbar_wait(bar(bSFull + x), cntS & 1, abort_flag);
+                if (lane == 0) {
+                    if (p.stall == tc::kStallConsumer && warp == 4 && cntS == 0)
+                        ok = tc::mbar_wait(bar(bNever), 0, abort_flag, p.stall_budget);
+                    if (ok) ok = tc::mbar_wait(bar(bSFull + x), cntS & 1, abort_flag);
+                }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) { fail(); break; }
                 ++cntS;
@@ -401,13 +437,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         }
     }
 
-    __syncthreads();
-    if (warp == 0 && lane == 0 && *abort_flag) {
-        // let any TMA still in flight land before the CTA's shared memory goes away
-        const long long t0 = clock64();
-        while (clock64() - t0 < 20000000LL) {
-        }
-    }
+    // the producer has waited out its copies and the issuer its products
     __syncthreads();
     if (warp == 1) {
         tc::fence_after_sync();
@@ -446,6 +476,8 @@ cudaError_t launch_fwd(const Problem& p, const Workspace& ws, __nv_bfloat16* out
     prm.scale_log2 = p.scale * 1.4426950408889634f;
     prm.out = out;
     prm.lse = lse;
+    prm.stall = p.stall.kernel == kStallKernelFwd ? p.stall.role : 0;
+    prm.stall_budget = p.stall.budget;
     const int sms = device_sms();
     if (sms < 1) return cudaErrorNotSupported;
     fwd_tc_kernel<<<sms, fwdt::kThreads, fwdt::kSmem, st>>>(mq, mk, mv, prm);

@@ -15,6 +15,12 @@ using namespace h3;
 
 static constexpr int kMaxEvents = 4096;
 
+// What the rotated rows q^ / k^ in a handle's workspace were computed from.
+struct RowsKey {
+    const void *q, *k, *wq, *wk, *pos[3], *seg;
+    int n, S;
+};
+
 struct h3attn_ctx {
     h3attn_config cfg;
     int device;
@@ -29,9 +35,25 @@ struct h3attn_ctx {
     cudaEvent_t* events;  // kMaxEvents, created on first use
     int ev_used;
     int ev_stage[kMaxEvents / 2];
+    // test hook: a stall requested for the next forward / backward / QKV call
+    StallRequest stall;
+    // samples of the last backward call (its per-(sample, head) weight-gradient
+    // partials stay in the workspace), 0 before the first
+    int last_bwd_samples;
+    // the inputs whose q^ / k^ rows the workspace holds (packed key order), if any
+    RowsKey hat_key;
+    bool hat_valid;
 };
 
 namespace {
+
+bool same_rows(const RowsKey& a, const RowsKey& b) {
+    return a.q == b.q && a.k == b.k && a.wq == b.wq && a.wk == b.wk && a.pos[0] == b.pos[0] &&
+           a.pos[1] == b.pos[1] && a.pos[2] == b.pos[2] && a.seg == b.seg && a.n == b.n && a.S == b.S;
+}
+RowsKey rows_key(const Problem& p) {
+    return RowsKey{p.q, p.k, p.wq, p.wk, {p.seq.pos_t, p.seq.pos_h, p.seq.pos_w}, p.seq.seg, p.seq.n, p.seq.S};
+}
 
 bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -92,6 +114,7 @@ Problem make_problem(h3attn_t h, const void* q, const void* k, const void* v, co
     p.H = h->cfg.num_heads;
     p.eps = h->cfg.eps;
     p.scale = h->cfg.softmax_scale;
+    p.stall = h->stall;
     return p;
 }
 
@@ -107,6 +130,12 @@ Problem canonical_problem(h3attn_t h, const Problem& p) {
     c.seq.pos_w = ws.pos_c + 2 * (size_t)h->cfg.max_tokens;
     return c;
 }
+
+// Clears the handle's stall request when the call that read it returns.
+struct StallClear {
+    h3attn_ctx* h;
+    ~StallClear() { h->stall = StallRequest{}; }
+};
 
 // Runs one stage's launches, bracketed by events when stage timing is on.
 template <class F>
@@ -147,6 +176,7 @@ h3attn_status h3attn_create(const h3attn_config* cfg, h3attn_t* out) {
     if (cfg->key_order != H3ATTN_KEY_ORDER_PACKED && cfg->key_order != H3ATTN_KEY_ORDER_CANONICAL)
         return H3ATTN_ERR_INVALID_ARG;
     if (cfg->store_ds != 0 && cfg->store_ds != 1) return H3ATTN_ERR_INVALID_ARG;
+    if (cfg->reuse_qk_hat != 0 && cfg->reuse_qk_hat != 1) return H3ATTN_ERR_INVALID_ARG;
     {
         const long long t128 = ((long long)cfg->max_tokens + 127) / 128;
         if (cfg->store_ds && (long long)cfg->num_heads * t128 * (t128 + cfg->max_samples) * 128 >= (1LL << 31))
@@ -178,6 +208,7 @@ h3attn_status h3attn_create(const h3attn_config* cfg, h3attn_t* out) {
               ws_alloc(h, &ws.dwq_part, (size_t)h->max_tiles64 * H * kD * 4) &&
               ws_alloc(h, &ws.dwk_part, (size_t)h->max_tiles64 * H * kD * 4) &&
               ws_alloc(h, &ws.dwq_sample, N * kD * 4) && ws_alloc(h, &ws.dwk_sample, N * kD * 4) &&
+              ws_alloc(h, &ws.dwq_head, N * H * kD * 4) && ws_alloc(h, &ws.dwk_head, N * H * kD * 4) &&
               ws_alloc(h, &ws.plan.order, N * 4) && ws_alloc(h, &ws.plan.rank_of, N * 4) &&
               ws_alloc(h, &ws.plan.cum64, (N + 1) * 4) && ws_alloc(h, &ws.plan.cum128, (N + 1) * 4) &&
               ws_alloc(h, &ws.plan.cum256, (N + 1) * 4) && ws_alloc(h, &ws.plan.cumsq, (N + 1) * 4) &&
@@ -217,12 +248,14 @@ h3attn_status h3attn_forward(h3attn_t h, const h3attn_bf16* q, const h3attn_bf16
                              float* lse, void* stream) {
     h3attn_status st = check_common(h, q, k, v, q_norm_w, k_norm_w, pos_ids, seg_offsets, num_samples, total_tokens);
     if (st != H3ATTN_OK || total_tokens == 0) return st;
+    StallClear clear_stall{h};
     if (!aligned16(out) || (lse && !aligned4(lse))) return H3ATTN_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     Problem p = make_problem(h, q, k, v, q_norm_w, k_norm_w, pos_ids, seg_offsets, num_samples, total_tokens);
     Workspace& ws = h->ws;
     __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out);
     if (h->cfg.key_order == H3ATTN_KEY_ORDER_CANONICAL) {
+        h->hat_valid = false;  // q^ / k^ are held in this call's canonical order
         const Problem c = canonical_problem(h, p);
         const int S = total_tokens, H = p.H;
         const void* gsrc[1] = {v};
@@ -248,10 +281,13 @@ h3attn_status h3attn_forward(h3attn_t h, const h3attn_bf16* q, const h3attn_bf16
             return H3ATTN_ERR_CUDA;
         return H3ATTN_OK;
     }
+    h->hat_valid = false;
     if (stage(h, kStagePlan, s, [&] { return launch_plan(p, ws, s); }) != cudaSuccess ||
         stage(h, kStagePrologue, s, [&] { return launch_prologue(p, ws, &h->rope, s); }) != cudaSuccess ||
         stage(h, kStageFwd, s, [&] { return launch_fwd(p, ws, o, lse, s); }) != cudaSuccess)
         return H3ATTN_ERR_CUDA;
+    h->hat_key = rows_key(p);
+    h->hat_valid = true;
     return H3ATTN_OK;
 }
 
@@ -263,6 +299,7 @@ h3attn_status h3attn_backward(h3attn_t h, const h3attn_bf16* q, const h3attn_bf1
                               float* dk_norm_w_per_sample, void* stream) {
     h3attn_status st = check_common(h, q, k, v, q_norm_w, k_norm_w, pos_ids, seg_offsets, num_samples, total_tokens);
     if (st != H3ATTN_OK) return st;
+    StallClear clear_stall{h};
     if (!aligned4(dq_norm_w) || !aligned4(dk_norm_w)) return H3ATTN_ERR_INVALID_ARG;
     if ((dq_norm_w_per_sample && !aligned4(dq_norm_w_per_sample)) ||
         (dk_norm_w_per_sample && !aligned4(dk_norm_w_per_sample)))
@@ -272,6 +309,7 @@ h3attn_status h3attn_backward(h3attn_t h, const h3attn_bf16* q, const h3attn_bf1
         if (cudaMemsetAsync(dq_norm_w, 0, kD * 4, s) != cudaSuccess ||
             cudaMemsetAsync(dk_norm_w, 0, kD * 4, s) != cudaSuccess)
             return H3ATTN_ERR_CUDA;
+        h->last_bwd_samples = 0;
         return H3ATTN_OK;
     }
     if (!aligned16(out) || !aligned4(lse) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
@@ -284,6 +322,7 @@ h3attn_status h3attn_backward(h3attn_t h, const h3attn_bf16* q, const h3attn_bf1
     __nv_bfloat16* gk = reinterpret_cast<__nv_bfloat16*>(dk);
     __nv_bfloat16* gv = reinterpret_cast<__nv_bfloat16*>(dv);
     if (h->cfg.key_order == H3ATTN_KEY_ORDER_CANONICAL) {
+        h->hat_valid = false;
         const Problem c = canonical_problem(h, p);
         const int S = total_tokens, H = p.H;
         const void* gsrc[2] = {v, dout};
@@ -313,10 +352,16 @@ h3attn_status h3attn_backward(h3attn_t h, const h3attn_bf16* q, const h3attn_bf1
                                       ws.plan.err, s);
             }) != cudaSuccess)
             return H3ATTN_ERR_CUDA;
+        h->last_bwd_samples = num_samples;
         return H3ATTN_OK;
     }
+    // q^ / k^ of these inputs are still in the workspace when the handle's last
+    // forward computed them from the same tensors (and the caller allows reuse)
+    const bool reuse = h->cfg.reuse_qk_hat && h->hat_valid && same_rows(h->hat_key, rows_key(p));
+    h->hat_valid = false;
     if (stage(h, kStagePlan, s, [&] { return launch_plan(p, ws, s); }) != cudaSuccess ||
-        stage(h, kStagePrologue, s, [&] { return launch_prologue(p, ws, &h->rope, s); }) != cudaSuccess ||
+        (!reuse &&
+         stage(h, kStagePrologue, s, [&] { return launch_prologue(p, ws, &h->rope, s); }) != cudaSuccess) ||
         stage(h, kStageDelta, s, [&] { return launch_bwd_delta(p, ws, o, dO, s); }) != cudaSuccess ||
         stage(h, kStageDkdv, s, [&] { return launch_bwd_dkdv(p, ws, lse, dO, gk, gv, s); }) != cudaSuccess ||
         stage(h, kStageDq, s, [&] { return launch_bwd_dq(p, ws, lse, dO, gq, s); }) != cudaSuccess ||
@@ -325,6 +370,9 @@ h3attn_status h3attn_backward(h3attn_t h, const h3attn_bf16* q, const h3attn_bf1
             return launch_bwd_dw(p, ws, dq_norm_w, dk_norm_w, dq_norm_w_per_sample, dk_norm_w_per_sample, s);
         }) != cudaSuccess)
         return H3ATTN_ERR_CUDA;
+    h->last_bwd_samples = num_samples;
+    h->hat_key = rows_key(p);
+    h->hat_valid = true;
     return H3ATTN_OK;
 }
 
@@ -335,6 +383,7 @@ h3attn_status h3attn_qkv_forward(h3attn_t h, const h3attn_bf16* x, int in_featur
                                  float* lse, void* stream) {
     h3attn_status st = check_common(h, q, k, v, q_norm_w, k_norm_w, pos_ids, seg_offsets, num_samples, total_tokens);
     if (st != H3ATTN_OK) return st;
+    StallClear clear_stall{h};
     if (in_features < 1) return H3ATTN_ERR_INVALID_ARG;
     if (in_features % 64 != 0 || h->cfg.key_order != H3ATTN_KEY_ORDER_PACKED) return H3ATTN_ERR_UNSUPPORTED;
     if (total_tokens == 0) return H3ATTN_OK;
@@ -353,6 +402,7 @@ h3attn_status h3attn_qkv_forward(h3attn_t h, const h3attn_bf16* x, int in_featur
     __nv_bfloat16* kb = reinterpret_cast<__nv_bfloat16*>(k);
     __nv_bfloat16* vb = reinterpret_cast<__nv_bfloat16*>(v);
     __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out);
+    h->hat_valid = false;
     if (stage(h, kStagePlan, s, [&] { return launch_plan(p, ws, s); }) != cudaSuccess ||
         stage(h, kStageQkv, s, [&] {
             cudaError_t e = launch_rope_table(p, ws, &h->rope, s);
@@ -360,6 +410,8 @@ h3attn_status h3attn_qkv_forward(h3attn_t h, const h3attn_bf16* x, int in_featur
         }) != cudaSuccess ||
         stage(h, kStageFwd, s, [&] { return launch_fwd(p, ws, o, lse, s); }) != cudaSuccess)
         return H3ATTN_ERR_CUDA;
+    h->hat_key = rows_key(p);  // the epilogue wrote q^ / k^ of the q, k it produced
+    h->hat_valid = true;
     return H3ATTN_OK;
 }
 
@@ -411,6 +463,48 @@ h3attn_status h3attn_stage_times(h3attn_t h, float* total_ms, int* launches, int
         if (st < n_stages) { total_ms[st] += ms; launches[st] += 1; }
     }
     h->ev_used = 0;
+    return H3ATTN_OK;
+}
+
+h3attn_status h3attn_norm_weight_grad_partials(h3attn_t h, float* dq_norm_w_partials, float* dk_norm_w_partials,
+                                               void* stream) {
+    if (!h || !aligned4(dq_norm_w_partials) || !aligned4(dk_norm_w_partials)) return H3ATTN_ERR_INVALID_ARG;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return H3ATTN_ERR_CUDA;
+    if (dev != h->device) return H3ATTN_ERR_INVALID_ARG;
+    const size_t bytes = (size_t)h->last_bwd_samples * h->cfg.num_heads * kD * 4;
+    if (bytes == 0) return H3ATTN_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(dq_norm_w_partials, h->ws.dwq_head, bytes, cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(dk_norm_w_partials, h->ws.dwk_head, bytes, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+        return H3ATTN_ERR_CUDA;
+    return H3ATTN_OK;
+}
+
+h3attn_status h3attn_combine_norm_weight_grads(const float* partials, int num_samples, int num_heads,
+                                               float* per_sample, float* total, void* stream) {
+    if (num_samples < 0 || num_heads < 1 || !aligned4(total)) return H3ATTN_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (num_samples == 0) return cudaMemsetAsync(total, 0, kD * 4, s) == cudaSuccess ? H3ATTN_OK : H3ATTN_ERR_CUDA;
+    if (!aligned4(partials) || !aligned4(per_sample)) return H3ATTN_ERR_INVALID_ARG;
+    const cudaError_t pe = prepare_device();
+    if (pe != cudaSuccess) return pe == cudaErrorNotSupported ? H3ATTN_ERR_UNSUPPORTED : H3ATTN_ERR_CUDA;
+    return launch_dw_combine(partials, num_samples, num_heads, per_sample, total, s) == cudaSuccess ? H3ATTN_OK
+                                                                                                      : H3ATTN_ERR_CUDA;
+}
+
+h3attn_status h3attn_debug_stall(h3attn_t h, int kernel, int role, long long budget_cycles) {
+    if (!h) return H3ATTN_ERR_INVALID_ARG;
+    if (kernel == 0) {
+        h->stall = StallRequest{};
+        return H3ATTN_OK;
+    }
+    if (kernel < H3ATTN_STALL_FWD || kernel > H3ATTN_STALL_QKV || role < H3ATTN_STALL_PRODUCER ||
+        role > H3ATTN_STALL_CONSUMER || budget_cycles < 1)
+        return H3ATTN_ERR_INVALID_ARG;
+    h->stall.kernel = kernel;
+    h->stall.role = role;
+    h->stall.budget = budget_cycles;
     return H3ATTN_OK;
 }
 

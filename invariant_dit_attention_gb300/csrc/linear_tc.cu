@@ -63,7 +63,7 @@ static_assert(kSmemQkv <= 232448, "shared memory of the QKV form");
 static_assert(sizeof(RopeTable) % 16 == 0, "norm weights stay 16-byte aligned");
 constexpr int kGroupM = 16;                     // row tiles per raster group
 enum { bFull = 0, bEmpty = bFull + kRing, bAccFull = bEmpty + kRing, bAccEmpty = bAccFull + 2, bDone = bAccEmpty + 2,
-       bCount };
+       bNever, bCount };
 }  // namespace lint
 
 struct QkvParams {
@@ -83,6 +83,8 @@ struct LinearParams {
     const float* bias;
     __nv_bfloat16* y;
     unsigned* err;
+    int stall;               // tc::StallRole stalled once on the CTA's first tile (tests), else 0
+    long long stall_budget;  // clock cycles of that stall's bounded wait
     QkvParams qkv;  // QKV form only
 };
 
@@ -235,6 +237,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__
             tc::mbar_init(bar(bAccEmpty + i), 4);
         }
         tc::mbar_init(bar(bDone), 1);
+        tc::mbar_init(bar(bNever), 1);  // nothing arrives: the target of a test's stall
         *abort_flag = 0;
         tc::fence_mbar_init();
         tc::prefetch_map(&ma);
@@ -262,12 +265,17 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
-            uint32_t it = 0;
+            uint32_t it = 0;  // stages armed (each completed by its two copies)
             for (int t = blockIdx.x; t < n_tiles && !failed; t += gridDim.x) {
                 int tm, tn;
                 linear_tile(p, t, tm, tn);
                 for (int ks = 0; ks < n_k; ++ks, ++it) {
                     const uint32_t s = it % kRing;
+                    if (p.stall == tc::kStallProducer && it == 0 &&
+                        !tc::mbar_wait(bar(bNever), 0, abort_flag, p.stall_budget)) {
+                        fail();
+                        break;
+                    }
                     if (!tc::mbar_wait(bar(bEmpty + s), ((it / kRing) & 1) ^ 1, abort_flag)) { fail(); break; }
                     const uint32_t dst = sbase + s * kStageBytes;
                     tc::mbar_expect_tx(bar(bFull + s), kStageBytes);
@@ -275,6 +283,8 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__
                     tc::tma_load_2d(dst + kABytes, &mb, ks * kBK, tn * kBN, bar(bFull + s));
                 }
             }
+            // every copy issued has landed before the CTA's shared memory is released
+            if (!tc::drain_ring(bar(bFull), kRing, it)) atomicOr(p.err, kErrTimeout);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -299,12 +309,18 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__
                         tc::mma_ss(tmem + kBN * b, da + so + ((kk * 32) >> 4), db + so + ((kk * 32) >> 4), id,
                                    (ks > 0) || (kk > 0));
                     tc::mma_commit(bar(bEmpty + s));
+                    if (p.stall == tc::kStallMma && it == 0 &&
+                        !tc::mbar_wait(bar(bNever), 0, abort_flag, p.stall_budget)) {
+                        fail();
+                        break;
+                    }
                 }
                 if (failed) break;
                 tc::mma_commit(bar(bAccFull + b));
             }
+            // every issued MMA has completed before TMEM is released (also on an abort)
             tc::mma_commit(bar(bDone));
-            if (!tc::mbar_wait(bar(bDone), 0, abort_flag) && !failed) fail();
+            if (!tc::mbar_drain(bar(bDone), 0)) fail();
         }
         __syncwarp();
     } else if (warp >= 4) {
@@ -317,7 +333,11 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__
             linear_tile(p, t, tm, tn);
             const uint32_t b = tc_n & 1;
             bool ok = true;
-            if (lane == 0) ok = tc::mbar_wait(bar(bAccFull + b), (tc_n >> 1) & 1, abort_flag);
+            if (lane == 0) {
+                if (p.stall == tc::kStallConsumer && warp == 4 && tc_n == 0)
+                    ok = tc::mbar_wait(bar(bNever), 0, abort_flag, p.stall_budget);
+                if (ok) ok = tc::mbar_wait(bar(bAccFull + b), (tc_n >> 1) & 1, abort_flag);
+            }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) { fail(); break; }
             tc::fence_after_sync();
@@ -364,13 +384,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__
         }
     }
 
-    __syncthreads();
-    if (warp == 0 && lane == 0 && *abort_flag) {
-        // let any TMA still in flight land before the CTA's shared memory goes away
-        const long long t0 = clock64();
-        while (clock64() - t0 < 20000000LL) {
-        }
-    }
+    // the producer has waited out its copies and the issuer its products
     __syncthreads();
     if (warp == 1) {
         tc::fence_after_sync();
@@ -432,6 +446,8 @@ extern "C" h3attn_status h3attn_linear(const h3attn_bf16* x, int rows, int in_fe
     p.bias = bias;
     p.y = reinterpret_cast<__nv_bfloat16*>(y);
     p.err = device_error_flags;
+    p.stall = 0;
+    p.stall_budget = 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(device_error_flags, 0, 4, s) != cudaSuccess) return H3ATTN_ERR_CUDA;
     const int tiles = p.tiles_m * p.tiles_n;
@@ -462,6 +478,8 @@ cudaError_t launch_qkv(const Problem& p, const Workspace& ws, const RopeTable* r
     lp.bias = bias;
     lp.y = nullptr;
     lp.err = ws.plan.err;
+    lp.stall = p.stall.kernel == kStallKernelQkv ? p.stall.role : 0;
+    lp.stall_budget = p.stall.budget;
     lp.qkv.H = p.H;
     lp.qkv.D = D;
     lp.qkv.eps = p.eps;

@@ -15,6 +15,9 @@ namespace tc {
 
 // ~1 s at 2 GHz: far beyond any legitimate wait inside one kernel.
 constexpr long long kWaitBudget = 2000000000LL;
+// The same bound for the unwinding of an aborted kernel (waits for copies and
+// products already issued, which complete on their own).
+constexpr long long kDrainBudget = 2000000000LL;
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count));
@@ -56,16 +59,60 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
         : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
     return ok != 0;
 }
-// Waits for the phase of the given parity to complete; false on timeout or abort.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort) {
+// Waits for the phase of the given parity to complete; false on timeout (after
+// `budget` clock cycles) or once another thread of the CTA set `abort`.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort,
+                                          long long budget = kWaitBudget) {
     if (mbar_test(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
         if (mbar_try_sleep(bar, parity, 20000u)) return true;
         if (*abort) return false;
-        if (clock64() - t0 > kWaitBudget) return false;
+        if (clock64() - t0 > budget) return false;
     }
 }
+
+// Waits for the phase of the given parity to complete whatever the abort flag
+// says: an aborted kernel uses it to wait out the bulk copies and tensor-core
+// products it already issued (they complete on their own) before its shared
+// and tensor memory are released.  False only past kDrainBudget.
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity) {
+    if (mbar_test(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_try_sleep(bar, parity, 20000u)) return true;
+        if (clock64() - t0 > kDrainBudget) return false;
+    }
+}
+
+// Waits for every copy a ring's producer issued: the full barriers of slots
+// 0 .. slots-1 (8 bytes apart from full0) were armed `armed` times in block
+// order, block b in slot b % slots, each arming completed by its copies (or by
+// the producer's own arrive).  The last armed phase of each slot is waited on.
+__device__ __forceinline__ bool drain_ring(uint32_t full0, int slots, uint32_t armed) {
+    bool ok = true;
+    for (int s = 0; s < slots && (uint32_t)s < armed; ++s) {
+        const uint32_t n = (armed - 1 - (uint32_t)s) / (uint32_t)slots + 1;  // phases armed on slot s
+        ok &= mbar_drain(full0 + 8u * s, (n - 1) & 1);
+    }
+    return ok;
+}
+
+// Named barrier over `count` threads that also ORs a predicate across them:
+// every participating thread gets true if any of them passed true.  Lets the
+// warps of a group leave a loop together when one of them failed a wait.
+__device__ __forceinline__ bool bar_sync_or(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.or.pred q, %2, %3, p;\nselp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r) : "r"((uint32_t)pred), "r"(id), "r"(count) : "memory");
+    return r != 0;
+}
+
+// Roles a test can stall once (a bounded wait on a barrier nothing completes)
+// to exercise a kernel's unwinding: none, the TMA producer, the MMA issuer, a
+// consumer warp (softmax or epilogue).
+enum StallRole { kStallNone = 0, kStallProducer = 1, kStallMma = 2, kStallConsumer = 3 };
 
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 

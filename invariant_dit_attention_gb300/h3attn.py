@@ -22,7 +22,9 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CAPACITY, ERR_CUDA, ERR_TIMEOUT = rang
 # Entry points declared in include/h3attn.h.
 EXPORTS = ("h3attn_create", "h3attn_destroy", "h3attn_forward", "h3attn_backward",
            "h3attn_device_status", "h3attn_set_stage_timing", "h3attn_stage_times", "h3attn_forward_static",
-           "h3attn_linear", "h3attn_canonical_order", "h3attn_qkv_forward", "h3attn_status_string")
+           "h3attn_linear", "h3attn_canonical_order", "h3attn_qkv_forward", "h3attn_debug_stall",
+           "h3attn_norm_weight_grad_partials", "h3attn_combine_norm_weight_grads", "h3attn_fingerprint",
+           "h3attn_status_string")
 
 # Limits of h3attn_forward_static's built-in scratch (include/h3attn.h).
 STATIC_MAX_TOKEN_HEADS = 131072
@@ -33,6 +35,10 @@ STAGES = ("plan", "prologue", "fwd", "bwd_delta", "bwd_dkdv", "bwd_dq", "bwd_dw"
 
 # Key orders (include/h3attn.h, H3ATTN_KEY_ORDER_*).
 KEY_ORDERS = {"packed": 0, "canonical": 1}
+
+# Test hook h3attn_debug_stall (include/h3attn.h, H3ATTN_STALL_*): kernels and roles.
+STALL_KERNELS = {"fwd": 1, "dkdv": 2, "dq": 3, "qkv": 4}
+STALL_ROLES = {"producer": 1, "mma": 2, "consumer": 3}
 
 
 class H3AttnError(RuntimeError):
@@ -46,7 +52,7 @@ class Config(ctypes.Structure):
                 ("rope_theta", ctypes.c_float), ("rope_sections", ctypes.c_int * 3),
                 ("rope_pairing", ctypes.c_int), ("softmax_scale", ctypes.c_float),
                 ("max_tokens", ctypes.c_int), ("max_samples", ctypes.c_int), ("key_order", ctypes.c_int),
-                ("store_ds", ctypes.c_int)]
+                ("store_ds", ctypes.c_int), ("reuse_qk_hat", ctypes.c_int)]
 
 
 def stored_ds_bytes(num_heads: int, max_tokens: int, max_samples: int) -> int:
@@ -96,6 +102,14 @@ def load_library(path: str = LIB_PATH):
     lib.h3attn_qkv_forward.argtypes = [vp, vp, i32, vp, vp, vp, vp, ctypes.POINTER(vp), vp, i32, i32, vp, vp, vp, vp,
                                        vp, vp]
     lib.h3attn_qkv_forward.restype = i32
+    lib.h3attn_norm_weight_grad_partials.argtypes = [vp, vp, vp, vp]
+    lib.h3attn_norm_weight_grad_partials.restype = i32
+    lib.h3attn_combine_norm_weight_grads.argtypes = [vp, i32, i32, vp, vp, vp]
+    lib.h3attn_combine_norm_weight_grads.restype = i32
+    lib.h3attn_fingerprint.argtypes = [vp, ctypes.c_uint64, vp, vp]
+    lib.h3attn_fingerprint.restype = i32
+    lib.h3attn_debug_stall.argtypes = [vp, i32, i32, ctypes.c_longlong]
+    lib.h3attn_debug_stall.restype = i32
     lib.h3attn_status_string.argtypes = [i32]
     lib.h3attn_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -132,13 +146,17 @@ class H3Attn:
 
     def __init__(self, num_heads: int, max_tokens: int, max_samples: int = 64, eps: float = 1e-6,
                  rope_theta: float = 10000.0, rope_sections=(16, 24, 24), softmax_scale: float = 0.0,
-                 key_order: str = "packed", store_ds="auto"):
+                 key_order: str = "packed", store_ds="auto", reuse_qk_hat: bool = True):
         """``key_order``: "packed" sums over a sample's tokens in memory order,
         "canonical" in an order fixed by the tokens themselves, so that results
         do not depend on how each sample's tokens are permuted.
         ``store_ds``: True keeps dS from the dK/dV kernel for the dQ kernel (see
         ``stored_ds_bytes`` for its workspace), False recomputes it, "auto"
-        stores it while the workspace stays under STORED_DS_AUTO_LIMIT."""
+        stores it while the workspace stays under STORED_DS_AUTO_LIMIT.
+        ``reuse_qk_hat``: the backward reuses the rotated q^/k^ rows that the
+        handle's last forward computed from the same tensors (their contents
+        must not change in between, as a training step's saved tensors do not);
+        False recomputes them in every backward."""
         lib = load_library()
         if key_order not in KEY_ORDERS:
             raise ValueError(f"key_order must be one of {sorted(KEY_ORDERS)}")
@@ -151,6 +169,7 @@ class H3Attn:
         if store_ds == "auto":
             store_ds = stored_ds_bytes(num_heads, max_tokens, max_samples) <= STORED_DS_AUTO_LIMIT
         cfg.store_ds = 1 if store_ds else 0
+        cfg.reuse_qk_hat = 1 if reuse_qk_hat else 0
         self.store_ds = bool(store_ds)
         h = ctypes.c_void_p()
         _check(lib.h3attn_create(ctypes.byref(cfg), ctypes.byref(h)), "h3attn_create")
@@ -252,6 +271,26 @@ class H3Attn:
         _check(self._lib.h3attn_stage_times(self._h, ms, cnt, n), "h3attn_stage_times")
         return {STAGES[i]: (float(ms[i]), int(cnt[i])) for i in range(n)}
 
+    def norm_weight_grad_partials(self, num_samples, out_q=None, out_k=None, stream=None):
+        """h3attn_norm_weight_grad_partials: the last backward's per-(sample, head)
+        norm-weight gradient partials, float32 [num_samples, H, 128] each for
+        q_norm_w and k_norm_w (device tensors).  Returns (dq_partials, dk_partials)."""
+        dev = torch.device("cuda", torch.cuda.current_device())
+        shape = (num_samples, self.num_heads, 128)
+        out_q = torch.empty(shape, dtype=torch.float32, device=dev) if out_q is None else out_q
+        out_k = torch.empty(shape, dtype=torch.float32, device=dev) if out_k is None else out_k
+        _check(self._lib.h3attn_norm_weight_grad_partials(self._h, _ptr(out_q), _ptr(out_k), _stream(stream)),
+               "h3attn_norm_weight_grad_partials")
+        return out_q, out_k
+
+    def debug_stall(self, kernel: str | None, role: str = "mma", budget_cycles: int = 2_000_000):
+        """h3attn_debug_stall (test hook): the next forward / backward / QKV call
+        makes ``role`` of ``kernel`` wait once on a barrier nothing completes, for
+        at most ``budget_cycles``; that call then reports ERR_TIMEOUT through
+        device_status().  ``kernel=None`` cancels a request."""
+        k = 0 if kernel is None else STALL_KERNELS[kernel]
+        _check(self._lib.h3attn_debug_stall(self._h, k, STALL_ROLES[role], int(budget_cycles)), "h3attn_debug_stall")
+
     def device_status(self, stream=None) -> int:
         """Waits for the stream; returns (and clears) errors recorded on the device."""
         return int(self._lib.h3attn_device_status(self._h, _stream(stream)))
@@ -310,6 +349,42 @@ def forward_static(q, k, v, q_norm_w, k_norm_w, pos, seg_offsets, num_heads=None
     if own_flags and S > 0:
         _raise_device_flags(error_flags, stream, "h3attn_forward_static")
     return out, lse
+
+
+def combine_norm_weight_grads(partials, per_sample=None, total=None, stream=None):
+    """h3attn_combine_norm_weight_grads: per-(sample, head) norm-weight partials
+    float32 [n, H, 128] (device, heads in global order) reduced in the library's
+    fixed order, per sample over heads, then over samples.  Returns
+    (per_sample [n, 128], total [128])."""
+    lib = load_library()
+    n, H = int(partials.shape[0]), int(partials.shape[1])
+    partials = partials.contiguous()
+    if per_sample is None:
+        per_sample = torch.empty((max(n, 1), 128), dtype=torch.float32, device=partials.device)
+    if total is None:
+        total = torch.empty(128, dtype=torch.float32, device=partials.device)
+    _check(lib.h3attn_combine_norm_weight_grads(_ptr(partials), n, H, _ptr(per_sample), _ptr(total), _stream(stream)),
+           "h3attn_combine_norm_weight_grads")
+    return per_sample[:n], total
+
+
+def fingerprint(t, out=None, stream=None):
+    """h3attn_fingerprint of a contiguous device tensor's bytes.  Returns the
+    device int64 [1] tensor holding it (read it with ``fingerprint_value``);
+    nothing is copied to the host here."""
+    lib = load_library()
+    if not t.is_contiguous():
+        raise ValueError("fingerprint: contiguous tensor expected")
+    if out is None:
+        out = torch.empty(1, dtype=torch.int64, device=t.device)
+    _check(lib.h3attn_fingerprint(_ptr(t), t.numel() * t.element_size(), _ptr(out), _stream(stream)),
+           "h3attn_fingerprint")
+    return out
+
+
+def fingerprint_value(fp) -> int:
+    """The fingerprint as an unsigned 64-bit Python integer."""
+    return int(fp.item()) & 0xFFFFFFFFFFFFFFFF
 
 
 def linear(x, w, bias=None, out=None, error_flags=None, stream=None):

@@ -59,7 +59,7 @@ def _cfg(**kw):
     (dict(head_dim=64), 2), (dict(rope_pairing=1), 2), (dict(rope_sections=[12, 24, 24]), 2),
     (dict(rope_sections=[64, 64, 8]), 2), (dict(num_heads=0), 1), (dict(max_tokens=0), 1),
     (dict(max_samples=0), 1), (dict(eps=-1.0), 1), (dict(key_order=2), 1), (dict(key_order=-1), 1),
-    (dict(store_ds=2), 1), (dict(store_ds=1, num_heads=48, max_tokens=1 << 22), 3),
+    (dict(store_ds=2), 1), (dict(reuse_qk_hat=2), 1), (dict(store_ds=1, num_heads=48, max_tokens=1 << 22), 3),
 ])
 def test_create_rejects_bad_config_on_host(kw, status):
     from invariant_dit_attention_gb300.h3attn import load_library
@@ -106,3 +106,10 @@ def test_binding_checks_and_stored_ds_workspace_size():
     # H ceil(T/128) (ceil(T/128) + N) blocks of 128 x 128 fp16
     assert stored_ds_bytes(48, 13539, 8) == 48 * 106 * 114 * 32768
     assert stored_ds_bytes(48, 13539, 8) < STORED_DS_AUTO_LIMIT < stored_ds_bytes(48, 32768, 8)
+
+
+def test_debug_stall_rejects_bad_arguments_without_a_gpu():
+    from invariant_dit_attention_gb300 import h3attn
+    lib_built()
+    lib = h3attn.load_library()
+    assert lib.h3attn_debug_stall(None, 1, 1, 1000) == h3attn.ERR_INVALID_ARG

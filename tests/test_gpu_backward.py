@@ -122,3 +122,34 @@ def test_backward_bench_pack_48_heads_first_and_last_heads():
             assert np.isfinite(x).all(), (name, lo, hi)
             e = rel_l2(x, ref[name][:, lo:hi])
             assert e <= BWD_REL_L2, f"{name} heads [{lo}, {hi}) rel-L2 {e:.3e}"
+
+
+def test_backward_reuse_of_forward_rows_is_bitwise_the_recomputation():
+    """With reuse_qk_hat the backward skips the norm/RoPE pass when the handle's
+    last forward computed q^/k^ from the same tensors; the gradients must be the
+    recomputing handle's bits, also when another forward ran in between (then
+    the rows are recomputed)."""
+    need_gpu()
+    from invariant_dit_attention_gb300.h3attn import to_device
+    a = W.make_inputs([300, 129, 1], 6, seed=515, with_grad=True)
+    b = W.make_inputs([300, 129, 1], 6, seed=516, with_grad=True)
+    da, db = to_device(a), to_device(b)
+    on = make_handle(6, a.total_tokens, 4, reuse_qk_hat=True)
+    off = make_handle(6, a.total_tokens, 4, reuse_qk_hat=False)
+
+    def fargs(d):
+        return (d["q"], d["k"], d["v"], d["q_norm_w"], d["k_norm_w"], d["pos"], d["seg_offsets"])
+
+    out_a, lse_a = (t.clone() for t in off.forward(*fargs(da)))
+    ref = {k: v.clone() for k, v in off.backward(*fargs(da), out_a, lse_a, da["dout"]).items()}
+    on.forward(*fargs(da))
+    g1 = {k: v.clone() for k, v in on.backward(*fargs(da), out_a, lse_a, da["dout"]).items()}
+    on.forward(*fargs(da))
+    on.forward(*fargs(db))  # the workspace now holds b's rows
+    g2 = on.backward(*fargs(da), out_a, lse_a, da["dout"])
+    torch.cuda.synchronize()
+    on.check()
+    off.check()
+    for k in ref:
+        assert torch.equal(g1[k], ref[k]), f"reused rows: {k}"
+        assert torch.equal(g2[k], ref[k]), f"rows of another forward in between: {k}"

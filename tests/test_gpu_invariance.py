@@ -40,6 +40,12 @@ def _sha(t):
     return hashlib.sha256(t.contiguous().view(torch.uint8).cpu().numpy().tobytes()).hexdigest()
 
 
+def _fp(t):
+    """The library's device-side fingerprint (h3attn_fingerprint) of a tensor."""
+    from invariant_dit_attention_gb300.h3attn import fingerprint, fingerprint_value
+    return fingerprint_value(fingerprint(t.contiguous()))
+
+
 @pytest.mark.parametrize("store_ds", [False, True])
 def test_backward_alone_vs_packed_both_dq_paths(store_ds):
     """dq, dk, dv and the per-sample weight gradients of each sample, alone and
@@ -77,11 +83,13 @@ def test_forward_repeat_bitwise_925():
     w, inp = workload("single_925")
     h = make_handle(w.num_heads, inp.total_tokens)
     digests = set()
+    fps = set()
     for _ in range(3):
         out, lse, _ = _fwd(h, inp)
         digests.add((_sha(out), _sha(lse)))
+        fps.add((_fp(out), _fp(lse)))  # compared on the device, without copying the outputs back
     h.check()
-    assert len(digests) == 1
+    assert len(digests) == 1 and len(fps) == 1
 
 
 def test_forward_alone_vs_packed_13539():
@@ -158,13 +166,15 @@ def test_backward_repeat_and_packed_with_925_bitwise():
     other = W.make_inputs(w2.samples, w.num_heads, seed=77, with_grad=True)
     other.q_norm_w, other.k_norm_w = inp.q_norm_w, inp.k_norm_w
     h = make_handle(w.num_heads, inp.total_tokens + 925, 4)
-    runs = []
+    runs, fps = [], []
     for _ in range(3):
         _, _, g = _fwd_bwd(h, inp)
         runs.append({k: v.clone() for k, v in g.items()})
-    for r in runs[1:]:
+        fps.append({k: _fp(v) for k, v in g.items()})
+    for r, f in zip(runs[1:], fps[1:]):
         for k in r:
             assert torch.equal(r[k], runs[0][k]), f"repeat differs in {k}"
+            assert f[k] == fps[0][k], f"device fingerprint of {k} differs"
     for packing in ([inp, other], [other, inp]):
         packed = W.pack(packing)
         _, _, g = _fwd_bwd(h, packed)
