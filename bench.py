@@ -390,7 +390,9 @@ def run_ours(args):
     value = whole_job_tflops(step_flops, args.steps, ws, ms_max)
 
     # ---- forward-only rates: whole batch and every sample alone (same kernels)
-    fwd_ms = stages["fwd"][0] + 0.5 * (stages["prologue"][0] + stages["plan"][0])
+    # forward's share: the attention kernel, its norm/RoPE prologue (the backward reuses the
+    # rotated rows, so every prologue launch is a forward's) and one of the two plans
+    fwd_ms = stages["fwd"][0] + stages["prologue"][0] + 0.5 * stages["plan"][0]
     per_sample = {}
     for s in range(inp.num_samples):
         alone = to_device(W.slice_sample(inp, s))
@@ -500,8 +502,9 @@ def run_ours(args):
     prologue = {"bound": "hbm", "achieved": round(pro_bytes / (pro_ms * 1e-3) / 1e9, 1), "peak": pk["hbm_gbs"],
                 "unit": "GB/s", "frac": round(pro_bytes / (pro_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
                 "traffic": measured_traffic("prologue"), "ms": round(pro_ms, 4)}
-    launches_per_step = 3 + 9  # forward: plan, prologue, attention; backward: plan, prologue, delta, dK/dV, dQ,
-    #                             rotary table, row backward, dw per sample, dw total
+    launches_per_step = 3 + 9  # forward: plan, prologue, attention; backward: plan, delta, dK/dV, dQ, rotary
+    #                             table, row backward, dw per (sample, head), dw per sample, dw total (the
+    #                             backward reuses the forward's q^/k^, so it runs no prologue)
 
     # ---- the projections either side of the path (h3attn_linear), same tokens, D = H * 128
     projection = projection_rate(S, H * 128, stream, pk)

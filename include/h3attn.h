@@ -409,6 +409,17 @@ h3attn_status h3attn_fingerprint(const void *data, uint64_t bytes, uint64_t *fin
 #define H3ATTN_STALL_CONSUMER 3
 h3attn_status h3attn_debug_stall(h3attn_t h, int kernel, int role, long long budget_cycles);
 
+/*
+ * Test hook (instrumentation; no counterpart on the pages): y[i] = 2^x[i] by
+ * one of the attention kernels' two exponential paths, path 0 = the SFU
+ * instruction (ex2.approx.ftz.f32), path 1 = the FMA-pipe polynomial the
+ * softmax uses for a fixed share of its columns (range reduction to
+ * x = n + f, f in [0, 1), a degree-5 minimax polynomial for 2^f, 2^n through
+ * the exponent field; results below 2^-126 are 0; valid for x <= 127).
+ * x, y: device float32 [n].  Errors: INVALID_ARG, UNSUPPORTED, CUDA.
+ */
+h3attn_status h3attn_debug_exp2(const float *x, float *y, int n, int path, void *stream);
+
 /* Static, human-readable name of a status code. */
 const char *h3attn_status_string(h3attn_status s);
 

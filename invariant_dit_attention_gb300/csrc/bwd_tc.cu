@@ -224,6 +224,11 @@ enum { bFixedFull = 0, bQFull, bQEmpty = bQFull + kQSlots, bOFull = bQEmpty + kQ
        bSFull = bOEmpty + kOSlots, bPFull, bSUsed, bPtFull, bDsFull, bAccDone, bTailQ, bTailO, bDone, bNever,
        bCount };
 constexpr uint32_t cB = 128;
+// Column pairs of a warpgroup's 32 query columns (bit e = columns 2e, 2e + 1)
+// whose 2^x would run on the FMA pipe (exp2_poly_pair) instead of the SFU,
+// fixed by the column's place in the block.  None: measured on the packed
+// 13539-token batch, one pair in four made this kernel 5% slower.
+constexpr uint32_t kPolyPairs = 0x0u;
 }  // namespace kvt
 
 // TMEM column of the A operand for K-step kk (queries 16kk .. 16kk + 15) of P^T
@@ -457,7 +462,9 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 // ---- P = 2^(s c - lse2_col)
                 const uint64_t c2 = f2pack(c, c);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) p2[e] = exp2_pair(p2[e], c2, lb2[e]);
+                for (int e = 0; e < 16; ++e)
+                    p2[e] = ((kvt::kPolyPairs >> e) & 1) ? exp2_poly_pair(p2[e], c2, lb2[e])
+                                                          : exp2_pair(p2[e], c2, lb2[e]);
                 if (validq < 32) {  // tail block: columns past the sample end are exact zeros
 #pragma unroll
                     for (int e = 0; e < 16; ++e) p2[e] = mask_pair(p2[e], 2 * e, validq);

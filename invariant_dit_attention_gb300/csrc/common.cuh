@@ -117,6 +117,52 @@ __device__ __forceinline__ uint64_t exp2_pair(uint64_t s2, uint64_t c2, uint64_t
         : "=l"(p2) : "l"(s2), "l"(c2), "l"(n2));
     return p2;
 }
+//   p2 = 2^(s2 * c2 + n2) per half on the FMA pipe instead of the SFU (the
+//   softmax needs one 2^x per score; a kernel can move a fixed share of its
+//   columns off the SFU with this - measured slower on this GPU, so the
+//   kernels' shares are zero, and h3attn_debug_exp2 keeps it tested):
+//   x = s c + n, clamped to >= -127;  n = floor(x) and f = x - n exactly (a
+//   round-toward-minus-infinity addition of 1.5 * 2^23 leaves floor(x) in the
+//   low mantissa bits);  2^f = p(f) = 1 + c1 f + ... + c5 f^5 by Horner with
+//   fused multiply-adds, the minimax polynomial of relative error with p(0) = 1
+//   (Remez exchange; coefficients from csrc/fit_exp2_poly.py, max relative
+//   error 1.4e-7 evaluated in float32, about the SFU's own);  2^n from the
+//   exponent field ((floor(x) + 127) << 23, which is +0 for x < -126: results
+//   below 2^-126 are 0, as with the flush-to-zero SFU instruction).  Valid for
+//   x <= 127; the softmax passes x <= 8.
+__device__ __forceinline__ uint64_t exp2_poly_pair(uint64_t s2, uint64_t c2, uint64_t n2) {
+    uint64_t r;
+    asm("{\n.reg .b64 x, t, n, f, p, e, k;\n.reg .f32 x0, x1;\n.reg .b32 t0, t1, e0, e1;\n"
+        "fma.rn.f32x2 x, %1, %2, %3;\n"
+        "mov.b64 {x0, x1}, x;\n"
+        "max.f32 x0, x0, 0fC2FE0000;\n"          // -127
+        "max.f32 x1, x1, 0fC2FE0000;\n"
+        "mov.b64 x, {x0, x1};\n"
+        "mov.b64 k, {0f4B400000, 0f4B400000};\n"  // 1.5 * 2^23
+        "add.rm.f32x2 t, x, k;\n"
+        "sub.rn.f32x2 n, t, k;\n"
+        "sub.rn.f32x2 f, x, n;\n"
+        "mov.b64 p, {0f3AF4BA7D, 0f3AF4BA7D};\n"  // c5
+        "mov.b64 k, {0f3C13BC2B, 0f3C13BC2B};\n"  // c4
+        "fma.rn.f32x2 p, p, f, k;\n"
+        "mov.b64 k, {0f3D648E73, 0f3D648E73};\n"  // c3
+        "fma.rn.f32x2 p, p, f, k;\n"
+        "mov.b64 k, {0f3E75EDAB, 0f3E75EDAB};\n"  // c2
+        "fma.rn.f32x2 p, p, f, k;\n"
+        "mov.b64 k, {0f3F31725D, 0f3F31725D};\n"  // c1
+        "fma.rn.f32x2 p, p, f, k;\n"
+        "mov.b64 k, {0f3F800000, 0f3F800000};\n"  // 1
+        "fma.rn.f32x2 p, p, f, k;\n"
+        "mov.b64 {t0, t1}, t;\n"
+        "shl.b32 e0, t0, 23;\n"
+        "shl.b32 e1, t1, 23;\n"
+        "add.u32 e0, e0, 0x3F800000;\n"
+        "add.u32 e1, e1, 0x3F800000;\n"
+        "mov.b64 e, {e0, e1};\n"
+        "mul.rn.f32x2 %0, p, e;\n}"
+        : "=l"(r) : "l"(s2), "l"(c2), "l"(n2));
+    return r;
+}
 // max(a, b, c) in one instruction
 __device__ __forceinline__ float max3f(float a, float b, float c) {
     float d;

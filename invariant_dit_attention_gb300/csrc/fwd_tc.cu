@@ -42,6 +42,13 @@ constexpr int kOffBar = kOffKV + kNST * kTile;
 constexpr int kSmem = kOffBar + 512 + 1024;  // barriers + 1 KB alignment slack
 constexpr uint32_t kColS0 = 0, kColO0 = 256;
 constexpr float kMaxStale = 8.0f;            // log2 growth of the max tolerated before rescaling
+// Column pairs (bit e = columns 2e, 2e + 1 of a 128-key tile) whose 2^x would
+// run on the FMA pipe (exp2_poly_pair) instead of the SFU, fixed by the
+// column's place in its tile so that every row's arithmetic stays the same
+// whatever the packing.  None: measured on the packed 13539-token batch, one
+// pair in eight made the kernel 10% slower and one in four 19% (the softmax is
+// bound by its instruction stream and latency, not by the SFU).
+constexpr uint64_t kPolyPairs = 0x0ull;
 
 // barrier indices (8 bytes each)
 enum {
@@ -375,7 +382,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                     uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
-                        const uint64_t p2 = exp2_pair(s2[16 * q4 + e], c2, neg2);
+                        const uint64_t p2 = ((kPolyPairs >> (16 * q4 + e)) & 1)
+                                                ? exp2_poly_pair(s2[16 * q4 + e], c2, neg2)
+                                                : exp2_pair(s2[16 * q4 + e], c2, neg2);
                         rs[e & 3] = f2add(rs[e & 3], p2);
                         pk[e] = bf16_pair(p2);
                     }

@@ -24,7 +24,7 @@ EXPORTS = ("h3attn_create", "h3attn_destroy", "h3attn_forward", "h3attn_backward
            "h3attn_device_status", "h3attn_set_stage_timing", "h3attn_stage_times", "h3attn_forward_static",
            "h3attn_linear", "h3attn_canonical_order", "h3attn_qkv_forward", "h3attn_debug_stall",
            "h3attn_norm_weight_grad_partials", "h3attn_combine_norm_weight_grads", "h3attn_fingerprint",
-           "h3attn_status_string")
+           "h3attn_debug_exp2", "h3attn_status_string")
 
 # Limits of h3attn_forward_static's built-in scratch (include/h3attn.h).
 STATIC_MAX_TOKEN_HEADS = 131072
@@ -108,6 +108,8 @@ def load_library(path: str = LIB_PATH):
     lib.h3attn_combine_norm_weight_grads.restype = i32
     lib.h3attn_fingerprint.argtypes = [vp, ctypes.c_uint64, vp, vp]
     lib.h3attn_fingerprint.restype = i32
+    lib.h3attn_debug_exp2.argtypes = [vp, vp, i32, i32, vp]
+    lib.h3attn_debug_exp2.restype = i32
     lib.h3attn_debug_stall.argtypes = [vp, i32, i32, ctypes.c_longlong]
     lib.h3attn_debug_stall.restype = i32
     lib.h3attn_status_string.argtypes = [i32]
@@ -366,6 +368,17 @@ def combine_norm_weight_grads(partials, per_sample=None, total=None, stream=None
     _check(lib.h3attn_combine_norm_weight_grads(_ptr(partials), n, H, _ptr(per_sample), _ptr(total), _stream(stream)),
            "h3attn_combine_norm_weight_grads")
     return per_sample[:n], total
+
+
+def debug_exp2(x, path: str, stream=None):
+    """h3attn_debug_exp2 (test hook): 2^x on the device by the SFU path ("sfu")
+    or the FMA-pipe polynomial path ("poly") of the attention kernels."""
+    lib = load_library()
+    x = x.contiguous()
+    y = torch.empty_like(x)
+    _check(lib.h3attn_debug_exp2(_ptr(x), _ptr(y), x.numel(), {"sfu": 0, "poly": 1}[path], _stream(stream)),
+           "h3attn_debug_exp2")
+    return y
 
 
 def fingerprint(t, out=None, stream=None):

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 def declared_symbols():
     text = open(os.path.join(ROOT, "include", "h3attn.h")).read()
-    return sorted(set(re.findall(r"^\S.*?\b(h3attn_[a-z_]+)\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^\S.*?\b(h3attn_[a-z0-9_]+)\(", text, flags=re.M)))
 
 
 def test_header_declares_the_binding_exports():
