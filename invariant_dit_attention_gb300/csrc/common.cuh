@@ -121,9 +121,10 @@ __device__ __forceinline__ uint64_t exp2_pair(uint64_t s2, uint64_t c2, uint64_t
 //   softmax needs one 2^x per score; a kernel can move a fixed share of its
 //   columns off the SFU with this - measured slower on this GPU, so the
 //   kernels' shares are zero, and h3attn_debug_exp2 keeps it tested):
-//   x = s c + n, clamped to >= -127;  n = floor(x) and f = x - n exactly (a
+//   x = s c + n, clamped to >= -127;  n = floor(x) exactly (a
 //   round-toward-minus-infinity addition of 1.5 * 2^23 leaves floor(x) in the
-//   low mantissa bits);  2^f = p(f) = 1 + c1 f + ... + c5 f^5 by Horner with
+//   low mantissa bits) and f = x - n rounded once (exact unless -1 < x < 0 is
+//   small, where the rounding moves 2^f by at most 2^-25 ln 2 relative);  2^f = p(f) = 1 + c1 f + ... + c5 f^5 by Horner with
 //   fused multiply-adds, the minimax polynomial of relative error with p(0) = 1
 //   (Remez exchange; coefficients from csrc/fit_exp2_poly.py, max relative
 //   error 1.4e-7 evaluated in float32, about the SFU's own);  2^n from the

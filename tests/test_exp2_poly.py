@@ -94,7 +94,7 @@ def _exact_poly(x: np.float32) -> np.float32:
     c = [Fraction(float(ck)) for ck in kernel_coefficients()]
     xs = max(float(x), -127.0)
     n = np.floor(xs)
-    f = Fraction(xs) - Fraction(n)  # exact, and a float32
+    f = Fraction(float(_round_f32(Fraction(xs) - Fraction(n))))  # x - n, rounded once as the kernel does
     acc = _round_f32(c[4])
     for ck in (c[3], c[2], c[1], c[0], Fraction(1)):
         acc = _round_f32(Fraction(float(acc)) * f + ck)
