@@ -217,8 +217,7 @@ constexpr int kQSlots = 3, kOSlots = 2;
 constexpr int kOffFixed = 0;                        // k^ + v tiles
 constexpr int kOffQ = bwdt::kPair;                  // q^ ring
 constexpr int kOffO = kOffQ + kQSlots * bwdt::kTile;  // dO ring
-constexpr int kOffLse = kOffO + kOSlots * bwdt::kTile;  // [4 wg][2 buf][lse2 32 | delta 32] floats
-constexpr int kOffBar = kOffLse + 4 * 2 * 64 * 4;
+constexpr int kOffBar = kOffO + kOSlots * bwdt::kTile;
 constexpr int kSmem = kOffBar + 256;                // the dynamic shared memory base is 1024-aligned (checked)
 enum { bFixedFull = 0, bQFull, bQEmpty = bQFull + kQSlots, bOFull = bQEmpty + kQSlots, bOEmpty = bOFull + kOSlots,
        bSFull = bOEmpty + kOSlots, bPFull, bSUsed, bPtFull, bDsFull, bAccDone, bTailQ, bTailO, bDone, bNever,
@@ -406,44 +405,35 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         const uint32_t tS = tmem + lane_base + 32 * wg, tB = tmem + lane_base + cB + 32 * wg;
         const float c = p.scale * kLog2e;
-        float* lsebuf = reinterpret_cast<float*>(smem + kOffLse) + wg * 128;  // [2 buf][lse2 32 | delta 32]
         uint32_t cntS = 0, items = 0;
         for (int i = blockIdx.x; !failed; i += gridDim.x) {
             BwdItem it;
             if (!bwd_item(p, i, it)) break;
             const int nq = (it.L + 127) / 128;
             const bool key_ok = 128 * it.tile + t < it.L;
-            // lse2 / Delta of this warpgroup's 32 queries of the next block, one block ahead
+            // lse2 / Delta of the warpgroup's 32 query columns: lane l holds column l's
+            // (staged negated: the loop adds them), loaded one block ahead; every warp
+            // loads its own copy and hands the column pairs out with shuffles, so the
+            // warps of a warpgroup never wait for one another
             float nl = 0.f, nd = 0.f;
             auto fetch = [&](int qj) {
-                const int q = 128 * qj + 32 * wg + t;
+                const int q = 128 * qj + 32 * wg + lane;
                 nl = 0.f;
                 nd = 0.f;
-                if (t < 32 && qj < nq && q < it.L) {
+                if (qj < nq && q < it.L) {
                     const size_t idx = (size_t)it.h * p.seq.S + it.seg0 + q;
-                    nl = -p.lse[idx] * kLog2e;  // staged negated: the loop adds them
+                    nl = -p.lse[idx] * kLog2e;
                     nd = -p.delta[idx];
                 }
             };
             fetch(0);
-            // The four warps of a warpgroup meet at a named barrier once per block and once
-            // after the last one, and must all leave the loops at the same barrier: a warp
-            // whose wait failed skips to the next barrier, where the barrier's OR tells the
-            // others and the warpgroup leaves together.
-            bool left = false;
             for (int qj = 0; qj < nq; ++qj) {
-                float* lb = lsebuf + (qj & 1) * 64;
-                if (t < 32) {
-                    lb[t] = nl;
-                    lb[32 + t] = nd;
-                }
+                const float bl = nl, bd = nd;  // this block's columns
                 fetch(qj + 1);
-                if (tc::bar_sync_or(1 + wg, 128, failed)) {
-                    failed = true;
-                    left = true;
-                    break;
-                }
-                const uint64_t* lb2 = reinterpret_cast<const uint64_t*>(lb);  // (-lse2, -lse2') pairs, then -Delta pairs
+                // the (column 2e, 2e + 1) pair of a lane-held value
+                auto pair_of = [](float v, int e) {
+                    return f2pack(__shfl_sync(0xffffffffu, v, 2 * e), __shfl_sync(0xffffffffu, v, 2 * e + 1));
+                };
                 const int validq = it.L - 128 * qj - 32 * wg;  // columns of this quarter inside the sample
                 bool ok = true;
                 if (lane == 0) {
@@ -452,7 +442,7 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                     if (ok) ok = tc::mbar_wait(bar(bSFull), cntS & 1, abort_flag);
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) { fail(); continue; }
+                if (!ok) { fail(); break; }
                 tc::fence_after_sync();
                 uint64_t p2[16];  // S^T column pairs, then P in FP32
                 tc::tmem_ld32_pairs(tS, p2);
@@ -463,8 +453,8 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 const uint64_t c2 = f2pack(c, c);
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
-                    p2[e] = ((kvt::kPolyPairs >> e) & 1) ? exp2_poly_pair(p2[e], c2, lb2[e])
-                                                          : exp2_pair(p2[e], c2, lb2[e]);
+                    p2[e] = ((kvt::kPolyPairs >> e) & 1) ? exp2_poly_pair(p2[e], c2, pair_of(bl, e))
+                                                          : exp2_pair(p2[e], c2, pair_of(bl, e));
                 if (validq < 32) {  // tail block: columns past the sample end are exact zeros
 #pragma unroll
                     for (int e = 0; e < 16; ++e) p2[e] = mask_pair(p2[e], 2 * e, validq);
@@ -472,7 +462,7 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 // ---- dP^T(b) from B, then P^T (bf16) over B's first 16 columns of this quarter
                 if (lane == 0) ok = tc::mbar_wait(bar(bPFull), cntS & 1, abort_flag);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) { fail(); continue; }
+                if (!ok) { fail(); break; }
                 ++cntS;
                 tc::fence_after_sync();
                 uint64_t d2[16];
@@ -490,7 +480,7 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 // ---- dS = P (dP - Delta_col), fp16, over B's other 16 columns (zero where P is)
                 uint32_t dk[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) dk[e] = ds_f16_pair(p2[e], d2[e], lb2[16 + e]);
+                for (int e = 0; e < 16; ++e) dk[e] = ds_f16_pair(p2[e], d2[e], pair_of(bd, e));
                 tc::tmem_st16(tB + 16, dk);
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
@@ -520,16 +510,13 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                     }
                 }
             }
-            if (!left) {  // the last block's failures and the accumulators' wait, agreed by the warpgroup
-                bool ok = !failed;
-                if (ok && lane == 0) ok = tc::mbar_wait(bar(bAccDone), items & 1, abort_flag);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok && !failed) fail();
-                if (tc::bar_sync_or(1 + wg, 128, failed)) failed = true;
-            }
             if (failed) break;
             // ---- drain: each warpgroup its 32 channels of dV (bf16 output rows) and of
             // scale * dk^ (FP32 rows for the RoPE^-1 / RMSNorm backward)
+            bool ok = true;
+            if (lane == 0) ok = tc::mbar_wait(bar(bAccDone), items & 1, abort_flag);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) { fail(); break; }
             ++items;
             tc::fence_after_sync();
             const size_t row_off = ((size_t)(it.row0 + t) * p.H + it.h) * kD + 32 * wg;

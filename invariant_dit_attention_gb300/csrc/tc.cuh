@@ -98,17 +98,6 @@ __device__ __forceinline__ bool drain_ring(uint32_t full0, int slots, uint32_t a
     return ok;
 }
 
-// Named barrier over `count` threads that also ORs a predicate across them:
-// every participating thread gets true if any of them passed true.  Lets the
-// warps of a group leave a loop together when one of them failed a wait.
-__device__ __forceinline__ bool bar_sync_or(int id, int count, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.or.pred q, %2, %3, p;\nselp.u32 %0, 1, 0, q;\n}\n"
-        : "=r"(r) : "r"((uint32_t)pred), "r"(id), "r"(count) : "memory");
-    return r != 0;
-}
-
 // Roles a test can stall once (a bounded wait on a barrier nothing completes)
 // to exercise a kernel's unwinding: none, the TMA producer, the MMA issuer, a
 // consumer warp (softmax or epilogue).
