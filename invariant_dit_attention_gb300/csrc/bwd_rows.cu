@@ -147,20 +147,20 @@ rows_bwd_kernel(const __grid_constant__ RopeTable rt, const RowsParams p) {
 // reductions give the same bits whatever the number of GPUs.
 
 // Per (sample, head) partial: dst[s][h][c] = sum over the sample's tiles t, in
-// ascending order, of part[t][h][c].  One CTA per (sample, q / k).
-__global__ void __launch_bounds__(1024)
+// ascending order, of part[t][h][c].  One thread per (sample, head, channel):
+// CTAs of 128 threads over (sample, head, q / k).
+__global__ void __launch_bounds__(128)
 dw_head_kernel(const float* __restrict__ part_q, const float* __restrict__ part_k, Plan plan, int n, int H,
                float* __restrict__ dst_q, float* __restrict__ dst_k) {
-    const int s = blockIdx.x;
-    const float* part = blockIdx.y == 0 ? part_q : part_k;
-    float* dst = blockIdx.y == 0 ? dst_q : dst_k;
+    const int s = blockIdx.x, h = blockIdx.y, c = threadIdx.x;
+    const float* part = blockIdx.z == 0 ? part_q : part_k;
+    float* dst = blockIdx.z == 0 ? dst_q : dst_k;
     const int r = plan.rank_of[s];
     const int t0 = plan.cum128[r], t1 = plan.cum128[r + 1];
-    for (int hc = threadIdx.x; hc < H * kD; hc += blockDim.x) {
-        float acc = 0.f;
-        for (int t = t0; t < t1; ++t) acc += part[(size_t)t * H * kD + hc];
-        dst[(size_t)s * H * kD + hc] = acc;
-    }
+    const size_t hc = (size_t)h * kD + c;
+    float acc = 0.f;
+    for (int t = t0; t < t1; ++t) acc += part[(size_t)t * H * kD + hc];
+    dst[(size_t)s * H * kD + hc] = acc;
 }
 
 // Up to two reductions side by side (blockIdx.y): q_norm_w's and k_norm_w's.
@@ -249,7 +249,7 @@ cudaError_t launch_dw_combine(const float* partials, int n, int H, float* per_sa
 cudaError_t launch_bwd_dw(const Problem& p, const Workspace& ws, float* dwq, float* dwk, float* dwq_s,
                           float* dwk_s, cudaStream_t st) {
     const int n = p.seq.n, H = p.H;
-    dw_head_kernel<<<dim3(n, 2), 1024, 0, st>>>(ws.dwq_part, ws.dwk_part, ws.plan, n, H, ws.dwq_head, ws.dwk_head);
+    dw_head_kernel<<<dim3(n, H, 2), kD, 0, st>>>(ws.dwq_part, ws.dwk_part, ws.plan, n, H, ws.dwq_head, ws.dwk_head);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     DwCombine d = {{ws.dwq_head, ws.dwk_head}, {dwq_s ? dwq_s : ws.dwq_sample, dwk_s ? dwk_s : ws.dwk_sample},

@@ -111,6 +111,24 @@ def test_fused_matches_oracle(case):
     assert max_abs(np64(lse), lse_ref) <= LSE_MAX_ABS
 
 
+@pytest.mark.parametrize("case", ["tiny_packed_H4_in256", "ragged_H6_in384"])
+def test_fused_matches_oracle_end_to_end(case):
+    """x to out through the oracle alone: the FP64 projection of x, rounded to
+    bf16 as the projection's outputs are (nearest even), then the FP64 forward
+    of those rows; compared with the fused call's out and lse."""
+    need_gpu()
+    layouts, H, fin, seed = CASES[case]
+    inp, x, w, b = _inputs(layouts, H, fin, seed)
+    _, _, _, out, lse = _fused(inp, x, w, b)
+    S, D = inp.total_tokens, H * 128
+    y_ref = torch.from_numpy(oracle.linear(x, w, b)).to(torch.bfloat16)  # one rounding of the FP64 result
+    q_r, k_r, v_r = (y_ref[:, i * D:(i + 1) * D].reshape(S, H, 128).contiguous() for i in range(3))
+    out_ref, lse_ref = oracle.forward(q_r, k_r, v_r, inp.q_norm_w, inp.k_norm_w, inp.pos, inp.seg_offsets)
+    assert rel_l2(np64(out), out_ref) <= FWD_REL_L2
+    assert max_abs_scaled(np64(out), out_ref) <= FWD_MAX_ABS
+    assert max_abs(np64(lse), lse_ref) <= LSE_MAX_ABS
+
+
 def test_fused_full_size_pack_bitwise():
     """The 12 + 925 + 4253 + 8349 pack at H = 48 with a 6144-wide input
     (W_qkv 18432 x 6144): fused and separate calls agree bit for bit."""
