@@ -16,20 +16,42 @@ namespace h3 {
 
 // ------------------------------------------------------------------ Delta
 
+// Four (token, head) rows per warp: half a warp per row, each lane's 16-byte
+// loads of out and dout (8 channels) for two rows in flight at once; a lane's
+// eight products are added in channel order, then the 16 lanes of a row in a
+// fixed butterfly.
 __global__ void __launch_bounds__(256) delta_kernel(const __nv_bfloat16* __restrict__ out,
                                                     const __nv_bfloat16* __restrict__ dout, int S, int H,
                                                     const int32_t* __restrict__ out_map, float* __restrict__ delta) {
-    const int lane = threadIdx.x & 31;
-    const long row = (long)blockIdx.x * 8 + (threadIdx.x >> 5);  // (token, head)
-    if (row >= (long)S * H) return;
-    // out is read through the canonical order's map (its packed row), dout is not
-    const long orow = out_map ? (long)out_map[row / H] * H + row % H : row;
-    float o[4], d[4];
-    load_row4(out + orow * kD + 4 * lane, o);
-    load_row4(dout + row * kD + 4 * lane, d);
-    float acc = o[0] * d[0] + o[1] * d[1] + o[2] * d[2] + o[3] * d[3];
-    acc = warp_sum(acc);
-    if (lane == 0) delta[(long)(row % H) * S + row / H] = acc;
+    const int lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
+    const long rows = (long)S * H;
+    const long base = ((long)blockIdx.x * 8 + (threadIdx.x >> 5)) * 4;  // the warp's first row
+    uint4 o[2], d[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const long row = base + 2 * u + half;
+        o[u] = d[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (row < rows) {
+            // out is read through the canonical order's map (its packed row), dout is not
+            const long orow = out_map ? (long)out_map[row / H] * H + row % H : row;
+            o[u] = *reinterpret_cast<const uint4*>(out + orow * kD + 8 * l16);
+            d[u] = *reinterpret_cast<const uint4*>(dout + row * kD + 8 * l16);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const long row = base + 2 * u + half;
+        const uint32_t ow[4] = {o[u].x, o[u].y, o[u].z, o[u].w}, dw[4] = {d[u].x, d[u].y, d[u].z, d[u].w};
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            acc = __fmaf_rn(bf16_lo(ow[e]), bf16_lo(dw[e]), acc);
+            acc = __fmaf_rn(bf16_hi(ow[e]), bf16_hi(dw[e]), acc);
+        }
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (l16 == 0 && row < rows) delta[(row % H) * S + row / H] = acc;
+    }
 }
 
 // ------------------------------------------- RoPE^-1 + RMSNorm backward rows
@@ -193,7 +215,7 @@ __global__ void __launch_bounds__(128) dw_total_kernel(const __grid_constant__ D
 cudaError_t launch_bwd_delta(const Problem& p, const Workspace& ws, const __nv_bfloat16* out,
                              const __nv_bfloat16* dout, cudaStream_t st) {
     const long rows = (long)p.seq.S * p.H;
-    delta_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(out, dout, p.seq.S, p.H, p.rowmap, ws.delta);
+    delta_kernel<<<(unsigned)((rows + 31) / 32), 256, 0, st>>>(out, dout, p.seq.S, p.H, p.rowmap, ws.delta);
     return cudaGetLastError();
 }
 
