@@ -78,6 +78,39 @@ def test_backward_alone_vs_packed_both_dq_paths(store_ds):
             assert _sha(ga[name][0]) == _sha(gp[name][s]), f"sample {s} {name}"
 
 
+def test_many_samples_alone_vs_packed_forward_and_backward():
+    """Twelve samples of 1 to 400 tokens packed together: every sample's out, lse,
+    dq, dk, dv and per-sample weight gradients are the bits it gets alone."""
+    need_gpu()
+    from invariant_dit_attention_gb300.h3attn import to_device
+    lengths = [int(x) for x in np.random.default_rng(12).integers(1, 401, size=12)]
+    packed = W.make_inputs(lengths, 4, seed=12, with_grad=True)
+
+    def run(inp):
+        h = make_handle(4, inp.total_tokens, 16)
+        d = to_device(inp)
+        out, lse = h.forward(d["q"], d["k"], d["v"], d["q_norm_w"], d["k_norm_w"], d["pos"], d["seg_offsets"])
+        g = h.backward(d["q"], d["k"], d["v"], d["q_norm_w"], d["k_norm_w"], d["pos"], d["seg_offsets"], out, lse,
+                       d["dout"])
+        torch.cuda.synchronize()
+        h.check()
+        h.close()
+        r = {k: v.cpu() for k, v in g.items()}
+        r["out"], r["lse"] = out.cpu(), lse.cpu()
+        return r
+
+    rp = run(packed)
+    seg = packed.seg_offsets.tolist()
+    for s in range(packed.num_samples):
+        ra = run(W.slice_sample(packed, s))
+        a, b = seg[s], seg[s + 1]
+        for name in ("out", "dq", "dk", "dv"):
+            assert _sha(ra[name]) == _sha(rp[name][a:b]), f"sample {s} ({lengths[s]} tokens) {name}"
+        assert _sha(ra["lse"]) == _sha(rp["lse"][:, a:b].contiguous()), f"sample {s} lse"
+        for name in ("dq_norm_w_per_sample", "dk_norm_w_per_sample"):
+            assert _sha(ra[name][0]) == _sha(rp[name][s]), f"sample {s} {name}"
+
+
 def test_forward_repeat_bitwise_925():
     need_gpu()
     w, inp = workload("single_925")
