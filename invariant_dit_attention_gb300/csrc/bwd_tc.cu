@@ -411,24 +411,28 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             if (!bwd_item(p, i, it)) break;
             const int nq = (it.L + 127) / 128;
             const bool key_ok = 128 * it.tile + t < it.L;
-            // lse2 / Delta of the warpgroup's 32 query columns: lane l holds column l's
-            // (staged negated: the loop adds them), loaded one block ahead; every warp
-            // loads its own copy and hands the column pairs out with shuffles, so the
-            // warps of a warpgroup never wait for one another
-            float nl = 0.f, nd = 0.f;
+            // lse / Delta of the warpgroup's 32 query columns: lane l holds column l's,
+            // loaded one block ahead; every warp loads its own copy and hands the
+            // column pairs out with shuffles, so the warps of a warpgroup never wait
+            // for one another.  The loaded values are first used a block later (staged
+            // negated, lse in log2 units, when the block starts): a use right after the
+            // load would hold the warp until the load came back, behind the dS stores
+            // that every warp has just queued.
+            float rl = 0.f, rd = 0.f;
             auto fetch = [&](int qj) {
                 const int q = 128 * qj + 32 * wg + lane;
-                nl = 0.f;
-                nd = 0.f;
+                rl = 0.f;
+                rd = 0.f;
                 if (qj < nq && q < it.L) {
                     const size_t idx = (size_t)it.h * p.seq.S + it.seg0 + q;
-                    nl = -p.lse[idx] * kLog2e;
-                    nd = -p.delta[idx];
+                    rl = p.lse[idx];
+                    rd = p.delta[idx];
                 }
             };
             fetch(0);
             for (int qj = 0; qj < nq; ++qj) {
-                const float bl = nl, bd = nd;  // this block's columns
+                // this block's columns (0 - x: a column past the sample end stays +0)
+                const float bl = 0.f - rl * kLog2e, bd = 0.f - rd;
                 fetch(qj + 1);
                 // the (column 2e, 2e + 1) pair of a lane-held value
                 auto pair_of = [](float v, int e) {
