@@ -405,12 +405,18 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         const uint32_t tS = tmem + lane_base + 32 * wg, tB = tmem + lane_base + cB + 32 * wg;
         const float c = p.scale * kLog2e;
+        const uint64_t pol = tc::policy_evict_first();  // the stored dS blocks are streamed once
         uint32_t cntS = 0, items = 0;
         for (int i = blockIdx.x; !failed; i += gridDim.x) {
             BwdItem it;
             if (!bwd_item(p, i, it)) break;
             const int nq = (it.L + 127) / 128;
             const bool key_ok = 128 * it.tile + t < it.L;
+            // the item's stored dS rows of this thread: block qj at dsrow + qj * 8192 words
+            // (layout [32-query chunk wg][key][32 queries] per 128 x 128 block)
+            const long long blk0 = p.ds ? ds_base(p, it) + (long long)it.tile * nq : 0;
+            const bool ds_all_in = blk0 + nq <= p.ds_blocks;
+            const size_t dsrow = (size_t)blk0 * (128 * 128 / 2) + ((size_t)wg * 128 + t) * 16;  // in 32-bit words
             // lse / Delta of the warpgroup's 32 query columns: lane l holds column l's,
             // loaded one block ahead; every warp loads its own copy and hands the
             // column pairs out with shuffles, so the warps of a warpgroup never wait
@@ -419,14 +425,14 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             // load would hold the warp until the load came back, behind the dS stores
             // that every warp has just queued.
             float rl = 0.f, rd = 0.f;
+            const size_t col0 = (size_t)it.h * p.seq.S + it.seg0 + 32 * wg + lane;  // this lane's column of block 0
+            const int col_lim = it.L - 32 * wg - lane;  // block qj's column is inside the sample iff 128 qj < col_lim
             auto fetch = [&](int qj) {
-                const int q = 128 * qj + 32 * wg + lane;
                 rl = 0.f;
                 rd = 0.f;
-                if (qj < nq && q < it.L) {
-                    const size_t idx = (size_t)it.h * p.seq.S + it.seg0 + q;
-                    rl = p.lse[idx];
-                    rd = p.delta[idx];
+                if (qj < nq && 128 * qj < col_lim) {
+                    rl = p.lse[col0 + 128 * qj];
+                    rd = p.delta[col0 + 128 * qj];
                 }
             };
             fetch(0);
@@ -491,23 +497,23 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(bar(bDsFull));
                 if (p.ds) {  // the block for the dQ kernel (key row t, this quarter's 32 queries), off the
-                             // tensor cores' path; rows past the sample end hold zeros
-                    const long long blk = ds_base(p, it) + (long long)it.tile * nq + qj;
-                    if (blk < p.ds_blocks) {
-                        // block layout [32-query chunk wg][key][32 queries]: a warp's 32 key rows of its
-                        // chunk are 2 KB contiguous; streamed once, so evict-first in L2
-                        const uint64_t pol = tc::policy_evict_first();
+                             // tensor cores' path; a warp's 32 key rows of its chunk are 2 KB contiguous,
+                             // and rows past the sample end hold zeros
+                    if (ds_all_in || blk0 + qj < p.ds_blocks) {
+                        uint32_t* const dst = reinterpret_cast<uint32_t*>(p.ds) + dsrow + (size_t)qj * (128 * 128 / 2);
+                        if (key_ok) {
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const uint32_t m = key_ok ? 0xffffffffu : 0u;
-                            uint32_t* dst = reinterpret_cast<uint32_t*>(p.ds + (size_t)blk * (128 * 128) +
-                                                                       ((size_t)wg * 128 + t) * 32 + 16 * e);
-                            asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;"
-                                         ::"l"(dst), "r"(dk[8 * e] & m), "r"(dk[8 * e + 1] & m),
-                                         "r"(dk[8 * e + 2] & m), "r"(dk[8 * e + 3] & m), "r"(dk[8 * e + 4] & m),
-                                         "r"(dk[8 * e + 5] & m), "r"(dk[8 * e + 6] & m), "r"(dk[8 * e + 7] & m),
-                                         "l"(pol)
-                                         : "memory");
+                            for (int e = 0; e < 2; ++e)
+                                asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;"
+                                             ::"l"(dst + 8 * e), "r"(dk[8 * e]), "r"(dk[8 * e + 1]), "r"(dk[8 * e + 2]),
+                                             "r"(dk[8 * e + 3]), "r"(dk[8 * e + 4]), "r"(dk[8 * e + 5]),
+                                             "r"(dk[8 * e + 6]), "r"(dk[8 * e + 7]), "l"(pol)
+                                             : "memory");
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 2; ++e)
+                                asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %1, %1, %1, %1, %1, %1, %1}, %2;"
+                                             ::"l"(dst + 8 * e), "r"(0u), "l"(pol) : "memory");
                         }
                     } else if (lane == 0) {
                         atomicOr(p.plan.err, kErrRange);
