@@ -201,6 +201,17 @@ __device__ __forceinline__ uint64_t mask_pair(uint64_t p2, int col, int valid) {
     return r;
 }
 
+// Item of a persistent CTA's k-th turn: turn k deals items [k G, k G + G) to the
+// G CTAs, in CTA order on even turns and in reverse on odd ones.  The items come
+// longest sample first, so alternating the direction evens out the per-CTA
+// totals that plain round-robin tilts toward the low CTA indices (13539-token
+// pack, H = 48: the largest forward share falls from 3.6% to 2.6% above the
+// mean).  Every role of a CTA walks the same sequence.
+__device__ __forceinline__ int turn_item(int k) {
+    const int c = (k & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x;
+    return k * (int)gridDim.x + c;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
     // fixed butterfly: every lane ends with the same, order-fixed sum
     v += __shfl_xor_sync(0xffffffffu, v, 16);

@@ -161,7 +161,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         // a tail block whose own wait gave up with its copy possibly in flight
         uint32_t q_armed = 0, kv_armed = 0;
         bool tail_pending = false;
-        for (int i = blockIdx.x; !failed; i += gridDim.x) {
+        for (int k = 0, i = turn_item(0); !failed; i = turn_item(++k)) {
             FwdItem it;
             if (!fwd_item(p, i, it)) break;
             const int x0 = it.h * 128;
@@ -257,7 +257,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                 }
                 tc::mma_commit(bar(bSFull + x));
             };
-            for (int i = blockIdx.x; !failed; i += gridDim.x) {
+            for (int k = 0, i = turn_item(0); !failed; i = turn_item(++k)) {
                 FwdItem it;
                 if (!fwd_item(p, i, it)) break;
                 const int nX = it.hasB ? 2 : 1;
@@ -328,7 +328,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         const uint32_t tO = tmem + lane_base + kColO0 + 128 * x;
         const float c = p.scale_log2;
         uint32_t cntS = 0, cntPV = 0;
-        for (int i = blockIdx.x; !failed; i += gridDim.x) {
+        for (int k = 0, i = turn_item(0); !failed; i = turn_item(++k)) {
             FwdItem it;
             if (!fwd_item(p, i, it)) break;
             if (x == 1 && !it.hasB) continue;
