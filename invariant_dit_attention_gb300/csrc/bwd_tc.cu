@@ -47,6 +47,7 @@ struct BwdTcParams {
     const float* lse;
     const float* delta;
     __nv_bfloat16* dv;  // dkdv kernel only
+    int dv_align32;     // dv is 32-byte aligned (else 16: the boundary's promise)
     float* dyhat;       // scale * dk^ (dkdv) or scale * dq^ (dq): FP32 [S, H, 128]
     __half* ds;         // stored dS^T blocks (dkdv writes, dq_ds reads), or null
     long long ds_blocks;
@@ -558,35 +559,74 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             if (!ok) { fail(); break; }
             ++items;
             tc::fence_after_sync();
-            const size_t row_off = ((size_t)(it.row0 + t) * p.H + it.h) * kD + 32 * wg;
+            // A thread holds its key row's 32 channels of this quarter: 64 bytes of dV,
+            // 128 of scale * dk^.  Storing them as is would touch 32 token rows (cache
+            // lines) per instruction; lanes first trade 32-byte pieces (pairs for dV,
+            // quads for dk^: one- and two-bit transposes of (lane, piece) by xor
+            // shuffles), so that each store instruction writes 16 rows' 64 contiguous
+            // bytes of dV, or 8 rows' whole 128-byte lines of dk^.
+            const int m = lane & 3;
+            const int r0 = 32 * (warp & 3);  // the warp's first row of the tile
+            auto row_ptr = [&](int r) {      // row r of the warp's 32, if inside the sample
+                return 128 * it.tile + r0 + r < it.L ? ((size_t)(it.row0 + r0 + r) * p.H + it.h) * kD + 32 * wg
+                                                     : (size_t)-1;
+            };
             {
                 uint32_t r[32];
                 tc::tmem_ld32(tmem + lane_base + 256 + 32 * wg, r);
                 tc::tmem_wait_ld_dep(r);
-                if (key_ok) {
-                    __nv_bfloat16* dst = p.dv + row_off;
+                uint32_t w[16];  // pieces 0, 1: channels 0-15, 16-31 as bf16 pairs
 #pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
-                        uint4 u;
-                        u.x = pack_bf16(__uint_as_float(r[e]), __uint_as_float(r[e + 1]));
-                        u.y = pack_bf16(__uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
-                        u.z = pack_bf16(__uint_as_float(r[e + 4]), __uint_as_float(r[e + 5]));
-                        u.w = pack_bf16(__uint_as_float(r[e + 6]), __uint_as_float(r[e + 7]));
-                        *reinterpret_cast<uint4*>(dst + e) = u;
+                for (int e = 0; e < 16; ++e) w[e] = pack_bf16(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {  // lane 2k + b ends with piece b of rows 2k, 2k + 1
+                    const uint32_t send = (m & 1) ? w[j] : w[8 + j];
+                    const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 1);
+                    if (m & 1) w[j] = recv; else w[8 + j] = recv;
+                }
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const size_t off = row_ptr((lane & ~1) + e);
+                    __nv_bfloat16* const d = p.dv + off + 16 * (m & 1);
+                    if (off == (size_t)-1) continue;
+                    if (p.dv_align32) {
+                        asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                                     ::"l"(d), "r"(w[8 * e]), "r"(w[8 * e + 1]), "r"(w[8 * e + 2]), "r"(w[8 * e + 3]),
+                                     "r"(w[8 * e + 4]), "r"(w[8 * e + 5]), "r"(w[8 * e + 6]), "r"(w[8 * e + 7])
+                                     : "memory");
+                    } else {
+                        *reinterpret_cast<uint4*>(d) = make_uint4(w[8 * e], w[8 * e + 1], w[8 * e + 2], w[8 * e + 3]);
+                        *reinterpret_cast<uint4*>(d + 8) = make_uint4(w[8 * e + 4], w[8 * e + 5], w[8 * e + 6], w[8 * e + 7]);
                     }
                 }
             }
             {
-                uint32_t r[32];
+                uint32_t r[32];  // pieces 0-3: channels 8q .. 8q + 7
                 tc::tmem_ld32(tmem + lane_base + 384 + 32 * wg, r);
                 tc::tmem_wait_ld_dep(r);
-                if (key_ok) {
-                    float* dst = p.dyhat + row_off;
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        *reinterpret_cast<float4*>(dst + e) =
-                            make_float4(__uint_as_float(r[e]) * p.scale, __uint_as_float(r[e + 1]) * p.scale,
-                                        __uint_as_float(r[e + 2]) * p.scale, __uint_as_float(r[e + 3]) * p.scale);
+                for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * p.scale);
+#pragma unroll
+                for (int bit = 1; bit <= 2; bit <<= 1) {  // lane 4k + q ends with piece q of rows 4k .. 4k + 3
+#pragma unroll
+                    for (int q0 = 0; q0 < 4; ++q0) {
+                        if (q0 & bit) continue;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const uint32_t send = (m & bit) ? r[8 * q0 + j] : r[8 * (q0 | bit) + j];
+                            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, bit);
+                            if (m & bit) r[8 * q0 + j] = recv; else r[8 * (q0 | bit) + j] = recv;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const size_t off = row_ptr((lane & ~3) + e);
+                    if (off != (size_t)-1)
+                        asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                                     ::"l"(p.dyhat + off + 8 * m), "r"(r[8 * e]), "r"(r[8 * e + 1]), "r"(r[8 * e + 2]),
+                                     "r"(r[8 * e + 3]), "r"(r[8 * e + 4]), "r"(r[8 * e + 5]), "r"(r[8 * e + 6]),
+                                     "r"(r[8 * e + 7]) : "memory");
                 }
             }
             // the next item's first dV/dK products overwrite the accumulators only after
@@ -1171,6 +1211,7 @@ static BwdTcParams bwd_params(const Problem& p, const Workspace& ws, const float
     b.delta = ws.delta;
     b.ds = ws.ds;
     b.ds_blocks = ws.ds_blocks;
+    b.dv_align32 = 0;
     b.stall = 0;
     b.stall_budget = p.stall.budget;
     return b;
@@ -1182,6 +1223,7 @@ cudaError_t launch_bwd_dkdv(const Problem& p, const Workspace& ws, const float* 
     if (!encode_all(m, p, ws, dout, 128, 128)) return cudaErrorInvalidValue;
     BwdTcParams b = bwd_params(p, ws, lse);
     b.dv = dv;
+    b.dv_align32 = (reinterpret_cast<uintptr_t>(dv) & 31u) == 0;
     b.dyhat = ws.dkhat32;
     if (p.stall.kernel == kStallKernelDkdv) b.stall = p.stall.role;
     const int sms = device_sms();
