@@ -63,6 +63,7 @@ struct FwdTcParams {
     int H;
     float scale_log2;
     __nv_bfloat16* out;
+    int out_align32;  // out is 32-byte aligned (else 16: the boundary's promise)
     float* lse;
     int stall;               // tc::StallRole stalled once on the CTA's first item (tests), else 0
     long long stall_budget;  // clock cycles of that stall's bounded wait
@@ -421,27 +422,54 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             const int row = it.seg0 + r_in;
             const bool store = r_in < it.L;
             const float inv = 1.0f / l;
-            __nv_bfloat16* dst = p.out + ((size_t)row * p.H + it.h) * kD;
+            // The row's 128 channels as bf16 pairs, piece k = words 8k .. 8k + 7 (32 bytes).
+            uint32_t w[64];
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 uint32_t r[32];
                 tc::tmem_ld32(tO + 32 * q4, r);
                 tc::tmem_wait_ld_dep(r);
-                if (store) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
-                        uint4 u;
-                        u.x = pack_bf16(__uint_as_float(r[e]) * inv, __uint_as_float(r[e + 1]) * inv);
-                        u.y = pack_bf16(__uint_as_float(r[e + 2]) * inv, __uint_as_float(r[e + 3]) * inv);
-                        u.z = pack_bf16(__uint_as_float(r[e + 4]) * inv, __uint_as_float(r[e + 5]) * inv);
-                        u.w = pack_bf16(__uint_as_float(r[e + 6]) * inv, __uint_as_float(r[e + 7]) * inv);
-                        *reinterpret_cast<uint4*>(dst + 32 * q4 + e) = u;
-                    }
-                }
+                for (int e = 0; e < 16; ++e)
+                    w[16 * q4 + e] = pack_bf16(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
             }
+            // O_X is in registers: the next item's products may overwrite it
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(bar(bOFree + x));
+            // Storing the row as is would touch 32 token rows per instruction; lanes first
+            // trade pieces (a three-bit transpose of (lane, piece) by xor shuffles within
+            // groups of 8), so lane 8g + k holds piece k of rows 8g .. 8g + 7 and store e
+            // writes 4 whole 256-byte rows.
+            const int m8 = lane & 7;
+#pragma unroll
+            for (int bit = 1; bit <= 4; bit <<= 1) {
+#pragma unroll
+                for (int k0 = 0; k0 < 8; ++k0) {
+                    if (k0 & bit) continue;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t send = (m8 & bit) ? w[8 * k0 + j] : w[8 * (k0 | bit) + j];
+                        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, bit);
+                        if (m8 & bit) w[8 * k0 + j] = recv; else w[8 * (k0 | bit) + j] = recv;
+                    }
+                }
+            }
+            const int tx0 = tx - lane;  // the warp's first row of the subtile
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int rr = 256 * ((it.row0 - it.seg0) / 256) + 128 * x + tx0 + (lane & ~7) + e;
+                if (rr >= it.L) continue;
+                __nv_bfloat16* const d = p.out + ((size_t)(it.seg0 + rr) * p.H + it.h) * kD + 16 * m8;
+                if (p.out_align32) {
+                    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                                 ::"l"(d), "r"(w[8 * e]), "r"(w[8 * e + 1]), "r"(w[8 * e + 2]), "r"(w[8 * e + 3]),
+                                 "r"(w[8 * e + 4]), "r"(w[8 * e + 5]), "r"(w[8 * e + 6]), "r"(w[8 * e + 7]) : "memory");
+                } else {
+                    *reinterpret_cast<uint4*>(d) = make_uint4(w[8 * e], w[8 * e + 1], w[8 * e + 2], w[8 * e + 3]);
+                    *reinterpret_cast<uint4*>(d + 8) = make_uint4(w[8 * e + 4], w[8 * e + 5], w[8 * e + 6], w[8 * e + 7]);
+                }
+            }
             if (store && p.lse) p.lse[(size_t)it.h * p.seq.S + row] = (m * c + log2f(l)) * 0.69314718055994531f;
         }
     }
@@ -484,6 +512,7 @@ cudaError_t launch_fwd(const Problem& p, const Workspace& ws, __nv_bfloat16* out
     prm.H = p.H;
     prm.scale_log2 = p.scale * 1.4426950408889634f;
     prm.out = out;
+    prm.out_align32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
     prm.lse = lse;
     prm.stall = p.stall.kernel == kStallKernelFwd ? p.stall.role : 0;
     prm.stall_budget = p.stall.budget;
