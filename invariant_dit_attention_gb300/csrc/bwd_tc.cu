@@ -1133,21 +1133,41 @@ dq_ds_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constant__ CU
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) { fail(); break; }
             tc::fence_after_sync();
+            // A thread holds its query row; lanes trade 32-byte pieces within quads (a
+            // two-bit transpose of (lane, piece) by xor shuffles), so that each store
+            // instruction writes 8 rows' whole 128-byte lines of a 32-column chunk
+            // instead of 16 bytes of 32 rows.
+            const int m = lane & 3;
             for (int u = 0; u < (it.has1 ? 2 : 1); ++u) {
-                const int r_in = 256 * it.pair + 128 * u + t;  // query row within the sample
-                const bool row_ok = r_in < it.L;
-                float* dst = p.dyhat + ((size_t)(it.seg0 + r_in) * p.H + it.h) * kD;
 #pragma unroll
                 for (int c32 = 0; c32 < 4; ++c32) {
-                    uint32_t r[32];
+                    uint32_t r[32];  // pieces 0-3: columns 8q .. 8q + 7 of the chunk
                     tc::tmem_ld32(tmem + lane_base + 256 * b + 128 * u + 32 * c32, r);
                     tc::tmem_wait_ld_dep(r);
-                    if (row_ok) {
 #pragma unroll
-                        for (int e = 0; e < 32; e += 4)
-                            *reinterpret_cast<float4*>(dst + 32 * c32 + e) =
-                                make_float4(__uint_as_float(r[e]) * p.scale, __uint_as_float(r[e + 1]) * p.scale,
-                                            __uint_as_float(r[e + 2]) * p.scale, __uint_as_float(r[e + 3]) * p.scale);
+                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * p.scale);
+#pragma unroll
+                    for (int bit = 1; bit <= 2; bit <<= 1) {  // lane 4k + q ends with piece q of rows 4k .. 4k + 3
+#pragma unroll
+                        for (int q0 = 0; q0 < 4; ++q0) {
+                            if (q0 & bit) continue;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const uint32_t send = (m & bit) ? r[8 * q0 + j] : r[8 * (q0 | bit) + j];
+                                const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, bit);
+                                if (m & bit) r[8 * q0 + j] = recv; else r[8 * (q0 | bit) + j] = recv;
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int r_in = 256 * it.pair + 128 * u + (t - lane) + (lane & ~3) + e;  // row within the sample
+                        if (r_in >= it.L) continue;
+                        float* const d = p.dyhat + ((size_t)(it.seg0 + r_in) * p.H + it.h) * kD + 32 * c32 + 8 * m;
+                        asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                                     ::"l"(d), "r"(r[8 * e]), "r"(r[8 * e + 1]), "r"(r[8 * e + 2]), "r"(r[8 * e + 3]),
+                                     "r"(r[8 * e + 4]), "r"(r[8 * e + 5]), "r"(r[8 * e + 6]), "r"(r[8 * e + 7])
+                                     : "memory");
                     }
                 }
             }
