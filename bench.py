@@ -515,9 +515,10 @@ def run_ours(args):
     prologue = {"bound": "hbm", "achieved": round(pro_bytes / (pro_ms * 1e-3) / 1e9, 1), "peak": pk["hbm_gbs"],
                 "unit": "GB/s", "frac": round(pro_bytes / (pro_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
                 "traffic": measured_traffic("prologue"), "ms": round(pro_ms, 4)}
-    launches_per_step = 3 + 9  # forward: plan, prologue, attention; backward: plan, delta, dK/dV, dQ, rotary
-    #                             table, row backward, dw per (sample, head), dw per sample, dw total (the
-    #                             backward reuses the forward's q^/k^, so it runs no prologue)
+    launches_per_step = 3 + 8  # forward: plan, prologue, attention; backward: plan, delta, dK/dV, rotary
+    #                             table, dQ (with the row backward beside its products: dS is stored), dw per
+    #                             (sample, head), dw per sample, dw total (the backward reuses the forward's
+    #                             q^/k^, so it runs no prologue)
 
     # ---- the projections either side of the path (h3attn_linear), same tokens, D = H * 128
     projection = projection_rate(S, H * 128, stream, pk)

@@ -28,6 +28,7 @@
 
 #include "common.cuh"
 #include "host.cuh"
+#include "rows_bwd.cuh"
 #include "tc.cuh"
 
 namespace h3 {
@@ -921,11 +922,12 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 // Items are dealt round-robin (item i to CTA i mod G): the alternating order of
 // the other kernels measured 0.5% slower here.
 namespace dqs {
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;  // warps 0-1: producer, MMA issuer; 4-7: drain; 8-15: row backward
 constexpr int kRingStages = 2;
 constexpr int kStage = 3 * bwdt::kTile;  // dS^T of two query tiles + k^: 96 KB
 constexpr int kOffBar = kRingStages * kStage;
-constexpr int kSmem = kOffBar + 256;  // the dynamic shared memory base is 1024-aligned (checked)
+constexpr int kOffRows = kOffBar + 256;  // the rotary table, then 8 x 128 floats for the row units' sums
+constexpr int kSmem = kOffRows + (int)sizeof(RopeTable) + 8 * kD * 4;  // the base is 1024-aligned (checked)
 enum { bFull = 0, bEmpty = bFull + kRingStages, bAccFull = bEmpty + kRingStages, bAccEmpty = bAccFull + 2,
        bTail = bAccEmpty + 2, bDone, bNever, bCount };
 }  // namespace dqs
@@ -959,7 +961,8 @@ __device__ __forceinline__ bool dqs_item(const BwdTcParams& p, int i, DqsItem& i
 }
 
 __global__ void __launch_bounds__(dqs::kThreads, 1)
-dq_ds_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constant__ CUtensorMap mk, const BwdTcParams p) {
+dq_ds_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constant__ CUtensorMap mk, const BwdTcParams p,
+             const __grid_constant__ RopeTable rt, const RowsParams rp) {
     using namespace dqs;
     using bwdt::kHalf;
     using bwdt::kTile;
@@ -973,6 +976,9 @@ dq_ds_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constant__ CU
     auto bar = [&](int i) { return sbase + kOffBar + 8u * i; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * bCount);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 8 * bCount + 4);
+    // the drain warps' count of finished items (4 per item), read by the row warps
+    const uint32_t drained = sbase + kOffBar + 8 * bCount + 8;
+    volatile int* row_ok = reinterpret_cast<volatile int*>(smem + kOffBar + 8 * bCount + 12);  // [2]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
@@ -988,6 +994,7 @@ dq_ds_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constant__ CU
         tc::mbar_init(bar(bDone), 1);
         tc::mbar_init(bar(bNever), 1);  // nothing arrives: the target of a test's stall
         *abort_flag = 0;
+        *reinterpret_cast<volatile uint32_t*>(smem + kOffBar + 8 * bCount + 8) = 0;
         tc::fence_mbar_init();
         tc::prefetch_map(&mds);
         tc::prefetch_map(&mk);
@@ -1115,7 +1122,7 @@ dq_ds_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constant__ CU
             if (!tc::mbar_drain(bar(bDone), 0)) fail();
         }
         __syncwarp();
-    } else if (warp >= 4) {
+    } else if (warp >= 4 && warp < 8) {
         // ------------------------------------------------------- drain
         const int t = tid - 128;  // TMEM lane == query row of each tile
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
@@ -1173,7 +1180,52 @@ dq_ds_kernel(const __grid_constant__ CUtensorMap mds, const __grid_constant__ CU
             }
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(bar(bAccEmpty + b));
+            if (lane == 0) {
+                tc::mbar_arrive(bar(bAccEmpty + b));
+                // this warp's scale * dq^ rows of the item are stored: the row warps may read them
+                asm volatile("red.release.cta.shared::cta.add.u32 [%0], 1;" :: "r"(drained) : "memory");
+            }
+        }
+    } else if (warp >= 8) {
+        // ------------------------------------- row backward (RoPE^-1 + RMSNorm): first
+        // the k tiles (scale * dk^ is complete when the launch starts; CTA c takes
+        // units c, c + G, ...), then the q tiles of this CTA's own items, each once the
+        // drain has stored its rows.  The 8 warps run one unit at a time, joined by
+        // named barrier 1; only warp 8 polls the drain count and the others take its
+        // answer from shared memory, so all 8 leave together when it gives up.
+        RopeTable& srt = *reinterpret_cast<RopeTable*>(smem + kOffRows);
+        float* red = reinterpret_cast<float*>(smem + kOffRows + sizeof(RopeTable));
+        const int w8 = warp - 8;
+        auto sync = [] { asm volatile("bar.sync 1, 256;" ::: "memory"); };
+        rope_to_smem(rt, srt, tid - 256, 256);
+        sync();
+        const int units = p.H * p.plan.cum128[p.seq.n];
+        for (int u = blockIdx.x; u < units; u += gridDim.x) rows_unit(srt, rp, 1, u / p.H, u % p.H, w8, lane, red, sync);
+        uint32_t items = 0;
+        for (int i = blockIdx.x;; i += gridDim.x, ++items) {
+            DqsItem it;
+            if (!dqs_item(p, i, it)) break;
+            if (warp == 8 && lane == 0) {
+                const uint32_t target = 4 * (items + 1);
+                const long long t0 = clock64();
+                int ok = 1;
+                while (true) {
+                    uint32_t v;
+                    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(drained) : "memory");
+                    if (v >= target) break;
+                    if (*abort_flag || clock64() - t0 > tc::kWaitBudget) { ok = 0; break; }
+                    __nanosleep(64);
+                }
+                row_ok[items & 1] = ok;
+            }
+            sync();
+            if (!row_ok[items & 1]) {  // the same answer in every row warp
+                if (warp == 8 && lane == 0) fail();
+                break;
+            }
+            const int t0 = p.plan.cum128[it.rank] + 2 * it.pair;
+            rows_unit(srt, rp, 0, t0, it.h, w8, lane, red, sync);
+            if (it.has1) rows_unit(srt, rp, 0, t0 + 1, it.h, w8, lane, red, sync);
         }
     }
 
@@ -1252,8 +1304,8 @@ cudaError_t launch_bwd_dkdv(const Problem& p, const Workspace& ws, const float* 
     return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_dq(const Problem& p, const Workspace& ws, const float* lse,
-                          const __nv_bfloat16* dout, __nv_bfloat16* dq, cudaStream_t st) {
+cudaError_t launch_bwd_dq(const Problem& p, const Workspace& ws, const float* lse, const __nv_bfloat16* dout,
+                          const RopeTable* rope, __nv_bfloat16* dq, __nv_bfloat16* dk, cudaStream_t st) {
     BwdMaps m;
     if (!encode_all(m, p, ws, dout, 128, 128)) return cudaErrorInvalidValue;
     BwdTcParams b = bwd_params(p, ws, lse);
@@ -1274,7 +1326,10 @@ cudaError_t launch_bwd_dq(const Problem& p, const Workspace& ws, const float* ls
                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
-        dq_ds_kernel<<<sms, dqs::kThreads, dqs::kSmem, st>>>(mds, m.k, b);
+        // the row backward's cos / sin table first: the dQ kernel runs those rows too
+        const cudaError_t e = launch_rope_table(p, ws, rope, st);
+        if (e != cudaSuccess) return e;
+        dq_ds_kernel<<<sms, dqs::kThreads, dqs::kSmem, st>>>(mds, m.k, b, *rope, make_rows_params(p, ws, dq, dk));
         return cudaGetLastError();
     }
     dq_tc_kernel<<<sms, dqt::kThreads, dqt::kSmem, st>>>(m.q, m.k, m.v, m.dout, b);

@@ -314,8 +314,10 @@ cudaError_t launch_bwd_delta(const Problem& p, const Workspace& ws, const __nv_b
                              const __nv_bfloat16* dout, cudaStream_t st);
 cudaError_t launch_bwd_dkdv(const Problem& p, const Workspace& ws, const float* lse,
                             const __nv_bfloat16* dout, __nv_bfloat16* dk, __nv_bfloat16* dv, cudaStream_t st);
-cudaError_t launch_bwd_dq(const Problem& p, const Workspace& ws, const float* lse,
-                          const __nv_bfloat16* dout, __nv_bfloat16* dq, cudaStream_t st);
+// dQ; with the stored dS (ws.ds) also the row backward of q and k (dq, dk), so
+// launch_bwd_rows then has nothing left to do
+cudaError_t launch_bwd_dq(const Problem& p, const Workspace& ws, const float* lse, const __nv_bfloat16* dout,
+                          const RopeTable* rope, __nv_bfloat16* dq, __nv_bfloat16* dk, cudaStream_t st);
 cudaError_t launch_bwd_rows(const Problem& p, const Workspace& ws, const RopeTable* rope, __nv_bfloat16* dq,
                             __nv_bfloat16* dk, cudaStream_t st);
 cudaError_t launch_order(const Problem& p, const __nv_bfloat16* dout, uint4* keys, int32_t* perm, unsigned* err,

@@ -342,7 +342,7 @@ h3attn_status h3attn_backward(h3attn_t h, const h3attn_bf16* q, const h3attn_bf1
             stage(h, kStagePrologue, s, [&] { return launch_prologue(c, ws, &h->rope, s); }) != cudaSuccess ||
             stage(h, kStageDelta, s, [&] { return launch_bwd_delta(c, ws, o, doc, s); }) != cudaSuccess ||
             stage(h, kStageDkdv, s, [&] { return launch_bwd_dkdv(c, ws, ws.lse_c, doc, gk, dvc, s); }) != cudaSuccess ||
-            stage(h, kStageDq, s, [&] { return launch_bwd_dq(c, ws, ws.lse_c, doc, gq, s); }) != cudaSuccess ||
+            stage(h, kStageDq, s, [&] { return launch_bwd_dq(c, ws, ws.lse_c, doc, &h->rope, gq, gk, s); }) != cudaSuccess ||
             stage(h, kStageRows, s, [&] { return launch_bwd_rows(c, ws, &h->rope, gq, gk, s); }) != cudaSuccess ||
             stage(h, kStageDw, s, [&] {
                 return launch_bwd_dw(c, ws, dq_norm_w, dk_norm_w, dq_norm_w_per_sample, dk_norm_w_per_sample, s);
@@ -364,7 +364,7 @@ h3attn_status h3attn_backward(h3attn_t h, const h3attn_bf16* q, const h3attn_bf1
          stage(h, kStagePrologue, s, [&] { return launch_prologue(p, ws, &h->rope, s); }) != cudaSuccess) ||
         stage(h, kStageDelta, s, [&] { return launch_bwd_delta(p, ws, o, dO, s); }) != cudaSuccess ||
         stage(h, kStageDkdv, s, [&] { return launch_bwd_dkdv(p, ws, lse, dO, gk, gv, s); }) != cudaSuccess ||
-        stage(h, kStageDq, s, [&] { return launch_bwd_dq(p, ws, lse, dO, gq, s); }) != cudaSuccess ||
+        stage(h, kStageDq, s, [&] { return launch_bwd_dq(p, ws, lse, dO, &h->rope, gq, gk, s); }) != cudaSuccess ||
         stage(h, kStageRows, s, [&] { return launch_bwd_rows(p, ws, &h->rope, gq, gk, s); }) != cudaSuccess ||
         stage(h, kStageDw, s, [&] {
             return launch_bwd_dw(p, ws, dq_norm_w, dk_norm_w, dq_norm_w_per_sample, dk_norm_w_per_sample, s);
