@@ -3,6 +3,8 @@
 //   rope_table_kernel cos / sin of every channel's rotary angle per token
 //   rows_bwd_kernel   dx = RMSNorm-backward(RoPE^-1(scale * dx^)) per row, for q
 //                     and k, and the norm-weight partial of every 128-token tile
+//                     (the units of rows_bwd.cuh; with stored dS the dQ kernel
+//                     runs them instead)
 //   dw_head_kernel, dw_sample_kernel, dw_total_kernel
 //                     the norm-weight gradient per (sample, head), then per
 //                     sample over heads, then over samples

@@ -7,8 +7,9 @@
 //   P_ij = exp(scale q^_i.k^_j - lse_i),  dP_ij = dO_i . v_j,  dS_ij = P_ij (dP_ij - Delta_i)
 //   dV_j = sum_i P_ij dO_i,  dk^_j = scale sum_i dS_ij q^_i              (dkdv_tc_kernel)
 //   dq^_i = scale sum_j dS_ij k^_j                        (dq_ds_kernel or dq_tc_kernel)
-// They leave scale * dk^ and scale * dq^ as FP32 rows for rows_bwd_kernel
-// (bwd_rows.cu), which applies RoPE^-1 and the RMSNorm backward.
+// They leave scale * dk^ and scale * dq^ as FP32 rows for the row backward
+// (RoPE^-1 and the RMSNorm backward, rows_bwd.cuh): run by 8 warps of
+// dq_ds_kernel, or by rows_bwd_kernel (bwd_rows.cu) after dq_tc_kernel.
 //
 // No atomics anywhere: dQ is a second pass, either over the dS blocks that
 // dkdv stored (dq_ds_kernel) or recomputing S and P (dq_tc_kernel: 7 tile
@@ -919,8 +920,11 @@ dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUt
 // TMEM accumulators; warps 4-7 drain the finished pair as scale * dq^ FP32 rows
 // while the next item accumulates.  The sum over j runs in ascending order
 // from the sample start.  Bound by HBM: every stored block is read once.
-// Items are dealt round-robin (item i to CTA i mod G): the alternating order of
-// the other kernels measured 0.5% slower here.
+// Warps 8-15 run the row backward (RoPE^-1 + RMSNorm backward, rows_bwd.cuh)
+// beside the products: the k tiles first, then the q tiles of this CTA's items
+// once the drain has stored their rows, so its row traffic rides on the same
+// HBM-bound pass.  Items are dealt round-robin (item i to CTA i mod G): the
+// alternating order of the other kernels measured 0.5% slower here.
 namespace dqs {
 constexpr int kThreads = 512;  // warps 0-1: producer, MMA issuer; 4-7: drain; 8-15: row backward
 constexpr int kRingStages = 2;
