@@ -46,10 +46,12 @@ def test_backward_tiny_packed():
 
 # 24 samples of 1 to 200 tokens (a seeded draw)
 MANY_SAMPLES = [int(x) for x in np.random.default_rng(24).integers(1, 201, size=24)]
+# 50 samples of 1 to 60 tokens (a seeded draw): many short items, most of them tails
+FIFTY_SAMPLES = [int(x) for x in np.random.default_rng(50).integers(1, 61, size=50)]
 
 
 @pytest.mark.parametrize("lengths", [[1, 64, 65], [129, 2, 200], [300], [127, 128, 129], [255, 256, 257],
-                                     MANY_SAMPLES])
+                                     MANY_SAMPLES, FIFTY_SAMPLES])
 def test_backward_ragged(lengths):
     need_gpu()
     inp = W.make_inputs(lengths, 6, seed=7 + sum(lengths), with_grad=True)

@@ -65,10 +65,12 @@ def test_forward_full_size_sampled_rows(name):
 
 # 40 samples of 1 to 300 tokens (a seeded draw): many items, many tile tails
 MANY_SAMPLES = [int(x) for x in np.random.default_rng(40).integers(1, 301, size=40)]
+# 50 samples of 1 to 60 tokens (a seeded draw): many short items, most of them tails
+FIFTY_SAMPLES = [int(x) for x in np.random.default_rng(50).integers(1, 61, size=50)]
 
 
 @pytest.mark.parametrize("lengths", [[1], [1, 1, 1], [63, 64, 65], [127, 128, 129], [5, 300, 7, 1, 200],
-                                     [257, 3], [255, 256], MANY_SAMPLES])
+                                     [257, 3], [255, 256], MANY_SAMPLES, FIFTY_SAMPLES])
 def test_forward_ragged_lengths_full(lengths):
     need_gpu()
     inp = W.make_inputs([W.SampleLayout(n_text=2, grid=(1, 1, L - 2)) if L > 2 else L for L in lengths],
