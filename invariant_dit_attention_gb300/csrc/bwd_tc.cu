@@ -423,7 +423,9 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             // the item's stored dS rows of this thread: block qj at dsrow + qj * 8192 words
             // (layout [32-query chunk wg][key][32 queries] per 128 x 128 block)
             const long long blk0 = p.ds ? ds_base(p, it) + (long long)it.tile * nq : 0;
-            const bool ds_all_in = blk0 + nq <= p.ds_blocks;
+            // blocks of the item inside the workspace (all of them unless it was sized too small):
+            // one 32-bit count, as a live 64-bit bound cost the block loop a spill reload
+            const int ds_in = (int)max(0LL, min((long long)nq, p.ds_blocks - blk0));
             const size_t dsrow = (size_t)blk0 * (128 * 128 / 2) + ((size_t)wg * 128 + t) * 16;  // in 32-bit words
             // lse / Delta of the warpgroup's 32 query columns, staged per block in shared
             // memory (negated, lse in log2 units; a column past the sample end holds +0)
@@ -531,7 +533,7 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 if (p.ds) {  // the block for the dQ kernel (key row t, this quarter's 32 queries), off the
                              // tensor cores' path; a warp's 32 key rows of its chunk are 2 KB contiguous,
                              // and rows past the sample end hold zeros
-                    if (ds_all_in || blk0 + qj < p.ds_blocks) {
+                    if (qj < ds_in) {
                         uint32_t* const dst = reinterpret_cast<uint32_t*>(p.ds) + dsrow + (size_t)qj * (128 * 128 / 2);
                         if (key_ok) {
 #pragma unroll
