@@ -439,22 +439,24 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             // loaded one block ahead, so no warp waits on a load right after issuing
             // it behind the dS stores that every warp has just queued.
             float rl = 0.f, rd = 0.f;
-            const bool stager = (lane >> 3) == (warp & 3);
             const size_t col0 = (size_t)it.h * p.seq.S + it.seg0 + 32 * wg + lane;  // this lane's column of block 0
             const int col_lim = it.L - 32 * wg - lane;  // block qj's column is inside the sample iff 128 qj < col_lim
-            float* const colbuf = reinterpret_cast<float*>(smem + kOffCol) + 128 * wg;  // [parity][-lse2 x32, -Delta x32]
+            // column buffers at smem + kOffCol + 512 wg bytes: [parity][-lse2 x32, -Delta x32]; the
+            // staging lanes and that address are recomputed where used: held in registers across
+            // the block loop they cost it spill reloads
             auto fetch = [&](int qj) {
                 rl = 0.f;
                 rd = 0.f;
-                if (stager && qj < nq && 128 * qj < col_lim) {
+                if ((lane >> 3) == (warp & 3) && qj < nq && 128 * qj < col_lim) {
                     rl = p.lse[col0 + 128 * qj];
                     rd = p.delta[col0 + 128 * qj];
                 }
             };
             auto stage = [&](uint32_t n) {
-                if (stager) {
-                    colbuf[64 * (n & 1) + lane] = 0.f - rl * kLog2e;
-                    colbuf[64 * (n & 1) + 32 + lane] = 0.f - rd;
+                if ((lane >> 3) == (warp & 3)) {
+                    float* const cb = reinterpret_cast<float*>(smem + kOffCol) + 128 * wg + 64 * (n & 1);
+                    cb[lane] = 0.f - rl * kLog2e;
+                    cb[32 + lane] = 0.f - rd;
                 }
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(bar(bColReady + 2 * wg + (n & 1)));
@@ -476,7 +478,7 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 if (!ok) { fail(); break; }
                 __syncwarp();  // lane 0's acquire of the staged columns covers the warp
                 tc::fence_after_sync();
-                const float4* const cl = reinterpret_cast<const float4*>(colbuf + 64 * (n & 1));
+                const float4* const cl = reinterpret_cast<const float4*>(smem + kOffCol) + 32 * wg + 16 * (n & 1);
                 const float4* const cd = cl + 8;
                 uint64_t p2[16];  // S^T column pairs, then P in FP32
                 tc::tmem_ld32_pairs(tS, p2);
