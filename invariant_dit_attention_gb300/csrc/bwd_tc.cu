@@ -19,6 +19,7 @@
 //
 // dkdv and dq_tc are persistent (one CTA per SM, 640 threads): warps 0 and 2 TMA
 // producers (one per streamed ring), warp 1 the single-thread tcgen05 issuer,
+// in dkdv warp 3 the stager of each block's lse / Delta columns in shared memory,
 // warps 4-19 four warpgroups that split each 128 x 128 score block by columns
 // (thread = TMEM lane = one row of the CTA's 128-row tile) and compute on
 // register pairs.  Operands: S on fp16 q^/k^, dP on bf16 dO/v, P (bf16) and dS
@@ -215,18 +216,19 @@ __device__ __forceinline__ void ring_producer(const BwdTcParams& p, const RingSp
 // ring (a slot is held from S^T(b), one block ahead, to dK(b)), dO through a
 // 2-slot ring (dP^T(b) to dV(b)).
 namespace kvt {
-constexpr int kThreads = 640;                       // warps 0-3: producer, MMA issuer; 4-19: four warpgroups
+constexpr int kThreads = 640;                       // warps 0-3: producers, MMA issuer, column stager; 4-19: four warpgroups
 constexpr int kQSlots = 3, kOSlots = 2;
 constexpr int kOffFixed = 0;                        // k^ + v tiles
 constexpr int kOffQ = bwdt::kPair;                  // q^ ring
 constexpr int kOffO = kOffQ + kQSlots * bwdt::kTile;  // dO ring
 constexpr int kOffBar = kOffO + kOSlots * bwdt::kTile;
 // per warpgroup and block parity: the block's 32 query columns as -lse2 then -Delta (FP32)
+// (written by warp 3, read by the warpgroup's four softmax warps)
 constexpr int kOffCol = kOffBar + 256;
 constexpr int kSmem = kOffCol + 4 * 2 * 64 * 4;     // the dynamic shared memory base is 1024-aligned (checked)
 enum { bFixedFull = 0, bQFull, bQEmpty = bQFull + kQSlots, bOFull = bQEmpty + kQSlots, bOEmpty = bOFull + kOSlots,
        bSFull = bOEmpty + kOSlots, bPFull, bSUsed, bPtFull, bDsFull, bAccDone, bTailQ, bTailO, bDone, bNever,
-       bColReady, bCount = bColReady + 8 };
+       bColReady, bColFree = bColReady + 2, bCount = bColFree + 2 };
 static_assert(8 * bCount + 8 <= 256, "barrier area");
 static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
 constexpr uint32_t cB = 128;
@@ -283,7 +285,10 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         tc::mbar_init(bar(bTailO), 1);
         tc::mbar_init(bar(bDone), 1);
         tc::mbar_init(bar(bNever), 1);  // nothing arrives: the target of a test's stall
-        for (int i = 0; i < 8; ++i) tc::mbar_init(bar(bColReady + i), 4);  // the 4 warps of a warpgroup
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(bar(bColReady + i), 1);  // warp 3
+            tc::mbar_init(bar(bColFree + i), 16);  // the softmax warps
+        }
         *abort_flag = 0;
         tc::fence_mbar_init();
     }
@@ -406,6 +411,41 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             if (!tc::mbar_drain(bar(bDone), 0)) fail();
         }
         __syncwarp();
+    } else if (warp == 3) {
+        // ------------------------------------- lse / Delta column stager
+        // Block n's 128 query columns, -lse in log2 units and -Delta (+0 past the
+        // sample end), into buffer n & 1: warpgroup g's 32 columns at 128 g + 64 (n & 1)
+        // floats.  The values are loaded before waiting for the buffer (the softmax
+        // warps' release of block n - 2), so the stager runs up to two blocks ahead
+        // and the softmax warps issue no global loads in their block loop.
+        float* const colbase = reinterpret_cast<float*>(smem + kOffCol) + lane;
+        uint32_t n = 0;
+        for (int k = 0, i = turn_item(0); !failed; i = turn_item(++k)) {
+            BwdItem it;
+            if (!bwd_item(p, i, it)) break;
+            const int nq = (it.L + 127) / 128;
+            const size_t col0 = (size_t)it.h * p.seq.S + it.seg0;
+            for (int qj = 0; qj < nq; ++qj, ++n) {
+                float rl[4], rd[4];
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const int c = 128 * qj + 32 * g + lane;
+                    rl[g] = c < it.L ? p.lse[col0 + c] : 0.f;
+                    rd[g] = c < it.L ? p.delta[col0 + c] : 0.f;
+                }
+                bool ok = true;
+                if (lane == 0 && n >= 2) ok = tc::mbar_wait(bar(bColFree + (n & 1)), ((n - 2) >> 1) & 1, abort_flag);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) { fail(); break; }
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    colbase[128 * g + 64 * (n & 1)] = 0.f - rl[g] * kLog2e;
+                    colbase[128 * g + 64 * (n & 1) + 32] = 0.f - rd[g];
+                }
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(bar(bColReady + (n & 1)));
+            }
+        }
     } else if (warp >= 4) {
         // ------------------------------------- softmax gradient + drain
         const int wg = (warp - 4) >> 2;                 // query quarter of the score tile
@@ -427,52 +467,17 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             // one 32-bit count, as a live 64-bit bound cost the block loop a spill reload
             const int ds_in = (int)max(0LL, min((long long)nq, p.ds_blocks - blk0));
             const size_t dsrow = (size_t)blk0 * (128 * 128 / 2) + ((size_t)wg * 128 + t) * 16;  // in 32-bit words
-            // lse / Delta of the warpgroup's 32 query columns, staged per block in shared
-            // memory (negated, lse in log2 units; a column past the sample end holds +0)
-            // and read back as broadcast 16-byte loads: handing them out by shuffles
-            // took 64 shuffles per warp and block, all 16 warps in the same phase.
-            // Warp w of a warpgroup stages columns 8w .. 8w + 7 of block n into buffer
-            // n & 1 and arrives on that buffer's barrier (4 warps per phase).  Block n
-            // is staged by the item's start (its first block) or in block n - 1 after
-            // that block's PFull, i.e. after every warp's DsFull of block n - 2: the
-            // last reads of the buffer's previous block are done.  The values are
-            // loaded one block ahead, so no warp waits on a load right after issuing
-            // it behind the dS stores that every warp has just queued.
-            float rl = 0.f, rd = 0.f;
-            const size_t col0 = (size_t)it.h * p.seq.S + it.seg0 + 32 * wg + lane;  // this lane's column of block 0
-            const int col_lim = it.L - 32 * wg - lane;  // block qj's column is inside the sample iff 128 qj < col_lim
-            // column buffers at smem + kOffCol + 512 wg bytes: [parity][-lse2 x32, -Delta x32]; the
-            // staging lanes and that address are recomputed where used: held in registers across
-            // the block loop they cost it spill reloads
-            auto fetch = [&](int qj) {
-                rl = 0.f;
-                rd = 0.f;
-                if ((lane >> 3) == (warp & 3) && qj < nq && 128 * qj < col_lim) {
-                    rl = p.lse[col0 + 128 * qj];
-                    rd = p.delta[col0 + 128 * qj];
-                }
-            };
-            auto stage = [&](uint32_t n) {
-                if ((lane >> 3) == (warp & 3)) {
-                    float* const cb = reinterpret_cast<float*>(smem + kOffCol) + 128 * wg + 64 * (n & 1);
-                    cb[lane] = 0.f - rl * kLog2e;
-                    cb[32 + lane] = 0.f - rd;
-                }
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(bar(bColReady + 2 * wg + (n & 1)));
-            };
-            fetch(0);
-            stage(cntS);
+            // lse / Delta of the warpgroup's 32 query columns come staged in shared memory
+            // (warp 3, above) and are read as broadcast 16-byte loads
             for (int qj = 0; qj < nq; ++qj) {
                 const uint32_t n = cntS;
-                fetch(qj + 1);
                 const int validq = it.L - 128 * qj - 32 * wg;  // columns of this quarter inside the sample
                 bool ok = true;
                 if (lane == 0) {
                     if (p.stall == tc::kStallConsumer && warp == 4 && cntS == 0)
                         ok = tc::mbar_wait(bar(bNever), 0, abort_flag, p.stall_budget);
                     if (ok) ok = tc::mbar_wait(bar(bSFull), cntS & 1, abort_flag);
-                    if (ok) ok = tc::mbar_wait(bar(bColReady + 2 * wg + (n & 1)), (n >> 1) & 1, abort_flag);
+                    if (ok) ok = tc::mbar_wait(bar(bColReady + (n & 1)), (n >> 1) & 1, abort_flag);
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) { fail(); break; }
@@ -526,12 +531,14 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                     dk[2 * j] = ds_f16_pair(p2[2 * j], d2[2 * j], f2pack(v.x, v.y));
                     dk[2 * j + 1] = ds_f16_pair(p2[2 * j + 1], d2[2 * j + 1], f2pack(v.z, v.w));
                 }
-                if (qj + 1 < nq) stage(n + 1);
                 tc::tmem_st16(tB + 16, dk);
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(bar(bDsFull));
+                if (lane == 0) {
+                    tc::mbar_arrive(bar(bDsFull));
+                    tc::mbar_arrive(bar(bColFree + (n & 1)));  // the warp's reads of the columns are done
+                }
                 if (p.ds) {  // the block for the dQ kernel (key row t, this quarter's 32 queries), off the
                              // tensor cores' path; a warp's 32 key rows of its chunk are 2 KB contiguous,
                              // and rows past the sample end hold zeros
