@@ -489,7 +489,7 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 tc::tmem_ld32_pairs(tS, p2);
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(bar(bSUsed));
+                tc::mbar_arrive_lane0(bar(bSUsed), lane);
                 // ---- P = 2^(s c - lse2_col)
                 const uint64_t c2 = f2pack(c, c);
 #pragma unroll
@@ -522,7 +522,7 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(bar(bPtFull));
+                tc::mbar_arrive_lane0(bar(bPtFull), lane);
                 // ---- dS = P (dP - Delta_col), fp16, over B's other 16 columns (zero where P is)
                 uint32_t dk[16];
 #pragma unroll
@@ -535,10 +535,8 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) {
-                    tc::mbar_arrive(bar(bDsFull));
-                    tc::mbar_arrive(bar(bColFree + (n & 1)));  // the warp's reads of the columns are done
-                }
+                tc::mbar_arrive_lane0(bar(bDsFull), lane);
+                tc::mbar_arrive_lane0(bar(bColFree + (n & 1)), lane);  // the warp's reads of the columns are done
                 if (p.ds) {  // the block for the dQ kernel (key row t, this quarter's 32 queries), off the
                              // tensor cores' path; a warp's 32 key rows of its chunk are 2 KB contiguous,
                              // and rows past the sample end hold zeros
