@@ -1,7 +1,9 @@
 """The pages' own rotary width as a tested configuration: 96 of the 128 channels
 rotate ("ws1_one_h3_block" page, Tests), as sections 32/32/32 of the handle's
 config.  Forward and backward parity against the FP64 oracle run with the same
-sections, and the bitwise alone-vs-packed property."""
+sections, and the bitwise alone-vs-packed property.  Sections whose pairs cross
+channel 64 (the prologue holds channels c and c + 64 in one lane) are checked
+against the oracle too."""
 
 import numpy as np
 import pytest
@@ -14,6 +16,8 @@ from tests.helpers import (BWD_REL_L2, FWD_MAX_ABS, FWD_REL_L2, LSE_MAX_ABS, mak
 
 pytestmark = pytest.mark.gpu
 SECTIONS96 = (32, 32, 32)
+# the h section spans channels 24 .. 71: channels 64 .. 71 pair with 40 .. 47
+SECTIONS_CROSS = (24, 48, 16)
 
 
 def _inputs():
@@ -68,3 +72,20 @@ def test_rope96_sample_alone_equals_packed_bitwise():
             assert torch.equal(a_g[name], g[name][r]), name
         for name in ("dq_norm_w_per_sample", "dk_norm_w_per_sample"):
             assert torch.equal(a_g[name][0], g[name][s]), name
+
+
+@pytest.mark.parametrize("sections", [SECTIONS_CROSS, (8, 56, 64)])
+def test_sections_across_channel_64_match_oracle(sections):
+    need_gpu()
+    inp = _inputs()
+    out, lse, g = _run(inp, sections)
+    ref_out, ref_lse = oracle.forward(inp.q, inp.k, inp.v, inp.q_norm_w, inp.k_norm_w, inp.pos, inp.seg_offsets,
+                                      sections=sections)
+    o = np64(out)
+    assert rel_l2(o, ref_out) <= FWD_REL_L2 and max_abs_scaled(o, ref_out) <= FWD_MAX_ABS
+    assert max_abs(lse.cpu().numpy().astype(np.float64), ref_lse) <= LSE_MAX_ABS
+    ref = oracle.backward(inp.q, inp.k, inp.v, inp.q_norm_w, inp.k_norm_w, inp.pos, inp.seg_offsets, inp.dout,
+                          sections=sections)
+    for name in ("dq", "dk", "dv", "dq_norm_w", "dk_norm_w"):
+        e = rel_l2(np64(g[name]), ref[name])
+        assert e <= BWD_REL_L2, f"{name} rel-L2 {e:.3e}"
