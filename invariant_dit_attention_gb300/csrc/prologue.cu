@@ -22,8 +22,16 @@ namespace h3 {
 // partner exchange when no channel above 64 is rotated (the 16/24/24 sections).
 
 constexpr int kProWarps = 8;
-constexpr int kProCtas = 2;   // resident CTAs per SM (the register budget)
-constexpr int kProBatch = 2;  // head pairs per half-iteration; the next batch's rows load while one is computed
+// resident CTAs per SM (the register budget) and head pairs per half-iteration (the
+// next batch's rows load while one is computed), per rotary layout (kMode below)
+template <int kMode>
+struct ProCfg {
+    static constexpr int ctas = 2, batch = 2;
+};
+template <>
+struct ProCfg<0> {
+    static constexpr int ctas = 3, batch = 1;
+};
 
 namespace {
 // where a group finds its rotary partner: the partner's half-lane and group
@@ -82,7 +90,10 @@ __device__ __forceinline__ bool f16_range_ok(const float (&y)[4]) {
 }
 }  // namespace
 
-__global__ void __launch_bounds__(kProWarps * 32, kProCtas)
+// kMode: 0 = no channel above 64 rotated, 1 = some are, pairs inside each group,
+// 2 = a section crosses channel 64 (a partner may sit in the other group)
+template <int kMode>
+__global__ void __launch_bounds__(kProWarps * 32, ProCfg<kMode>::ctas)
 prologue_kernel(Problem p, __half* __restrict__ qhat, __half* __restrict__ khat,
                 const __grid_constant__ RopeTable rt, unsigned* err) {
     __shared__ RopeTable srt;
@@ -109,16 +120,14 @@ prologue_kernel(Problem p, __half* __restrict__ qhat, __half* __restrict__ khat,
         }
     };
     const int pairs = (H + 1) / 2;
-    uint2 aq[kProBatch][2], ak[kProBatch][2], bq[kProBatch][2], bk[kProBatch][2];
+    uint2 aq[ProCfg<kMode>::batch][2], ak[ProCfg<kMode>::batch][2], bq[ProCfg<kMode>::batch][2], bk[ProCfg<kMode>::batch][2];
 #pragma unroll
-    for (int b = 0; b < kProBatch; ++b) load(b, aq[b], ak[b]);
+    for (int b = 0; b < ProCfg<kMode>::batch; ++b) load(b, aq[b], ak[b]);
     // the lanes' rotary entries, the token's angles and the weights while the first rows load
-    const LaneRope la = lane_rope(srt, j), lb = lane_rope(srt, j + 16);
+    const LaneRope la = lane_rope(srt, j);
+    LaneRope lb = lane_rope(srt, j + 16);
+    if (kMode == 0) lb.axis = -1;
     const PairSrc sa = pair_src(srt, j, half), sb = pair_src(srt, j + 16, half);
-    // partners inside the own group for every lane (no section crosses channel 64),
-    // and whether any channel above 64 is rotated
-    const bool crossed = __any_sync(0xffffffffu, sa.in_b || !sb.in_b);
-    const bool rot_b = __any_sync(0xffffffffu, lb.axis >= 0);
     const int pt = p.seq.pos_t[tok], ph = p.seq.pos_h[tok], pw = p.seq.pos_w[tok];
     const RowAngles ga = row_angles(la, pt, ph, pw), gb = row_angles(lb, pt, ph, pw);
     float wq[2][4], wk[2][4];
@@ -146,10 +155,10 @@ prologue_kernel(Problem p, __half* __restrict__ qhat, __half* __restrict__ khat,
         float za[4], zb[4], pa[4], pb[4], ya[4], yb[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) { za[e] = norm_w(xa[e], rs, w[0][e]); zb[e] = norm_w(xb[e], rs, w[1][e]); }
-        if (!crossed) {
+        if (kMode != 2) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) pa[e] = __shfl_sync(0xffffffffu, za[e], sa.lane);
-            if (rot_b) {
+            if (kMode == 1) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) pb[e] = __shfl_sync(0xffffffffu, zb[e], sb.lane);
             } else {
@@ -179,16 +188,16 @@ prologue_kernel(Problem p, __half* __restrict__ qhat, __half* __restrict__ khat,
         rotate_row(rq, wq, qhat + base + (size_t)h * kD, h < H);
         rotate_row(rk, wk, khat + base + (size_t)h * kD, h < H);
     };
-    // software pipeline: the next kProBatch head pairs' rows load while these are computed
-    for (int i0 = 0; i0 < pairs; i0 += 2 * kProBatch) {
+    // software pipeline: the next batch of head pairs loads while this one is computed
+    for (int i0 = 0; i0 < pairs; i0 += 2 * ProCfg<kMode>::batch) {
 #pragma unroll
-        for (int b = 0; b < kProBatch; ++b) load(i0 + kProBatch + b, bq[b], bk[b]);
+        for (int b = 0; b < ProCfg<kMode>::batch; ++b) load(i0 + ProCfg<kMode>::batch + b, bq[b], bk[b]);
 #pragma unroll
-        for (int b = 0; b < kProBatch; ++b) rotate(i0 + b, aq[b], ak[b]);
+        for (int b = 0; b < ProCfg<kMode>::batch; ++b) rotate(i0 + b, aq[b], ak[b]);
 #pragma unroll
-        for (int b = 0; b < kProBatch; ++b) load(i0 + 2 * kProBatch + b, aq[b], ak[b]);
+        for (int b = 0; b < ProCfg<kMode>::batch; ++b) load(i0 + 2 * ProCfg<kMode>::batch + b, aq[b], ak[b]);
 #pragma unroll
-        for (int b = 0; b < kProBatch; ++b) rotate(i0 + kProBatch + b, bq[b], bk[b]);
+        for (int b = 0; b < ProCfg<kMode>::batch; ++b) rotate(i0 + ProCfg<kMode>::batch + b, bq[b], bk[b]);
     }
     if (!ok) atomicOr(err, kErrRange);
 }
@@ -196,7 +205,19 @@ prologue_kernel(Problem p, __half* __restrict__ qhat, __half* __restrict__ khat,
 cudaError_t launch_prologue(const Problem& p, const Workspace& ws, const RopeTable* rope, cudaStream_t st) {
     if (p.seq.S == 0) return cudaSuccess;
     const int blocks = (p.seq.S + kProWarps - 1) / kProWarps;
-    prologue_kernel<<<blocks, kProWarps * 32, 0, st>>>(p, ws.qhat, ws.khat, *rope, ws.plan.err);
+    // the layout of the rotary sections over the lanes' two groups (channel c and c + 64)
+    bool rot_b = false, crossed = false;
+    for (int g = 0; g < 32; ++g) {
+        rot_b |= g >= 16 && rope->axis[g] >= 0;
+        crossed |= (g < 16) != (rope->partner[g] < 16);
+    }
+    const int mode = crossed ? 2 : (rot_b ? 1 : 0);
+    if (mode == 0)
+        prologue_kernel<0><<<blocks, kProWarps * 32, 0, st>>>(p, ws.qhat, ws.khat, *rope, ws.plan.err);
+    else if (mode == 1)
+        prologue_kernel<1><<<blocks, kProWarps * 32, 0, st>>>(p, ws.qhat, ws.khat, *rope, ws.plan.err);
+    else
+        prologue_kernel<2><<<blocks, kProWarps * 32, 0, st>>>(p, ws.qhat, ws.khat, *rope, ws.plan.err);
     return cudaGetLastError();
 }
 
