@@ -148,3 +148,43 @@ def test_host_side_argument_errors():
     with pytest.raises(H3AttnError) as e:
         h2.forward(qm, d["k"], d["v"], d["q_norm_w"], d["k_norm_w"], d["pos"], d["seg_offsets"])
     assert e.value.status == ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("tensor", ["q", "k"])
+def test_fp16_range_of_the_rotated_rows(tensor):
+    """q^ and k^ are kept as fp16: a finite normed and rotated value beyond its range is a
+    device error (status INVALID_ARG, then cleared).  A normed row has |n_c| <= sqrt(128)
+    and a rotation keeps a pair's length, so |q^|, |k^| <= sqrt(128) max|w|: the per-value
+    check runs only when 16 max|w| reaches 60000, and below that nothing can be flagged.
+    A one-hot row in an unrotated channel reaches the bound exactly."""
+    need_gpu()
+    from invariant_dit_attention_gb300.h3attn import ERR_INVALID_ARG, OK, to_device
+    inp = W.make_inputs([40, 24], 2, seed=11)
+    h = make_handle(2, 64)
+    d = to_device(inp)
+    x = d[tensor].clone()
+    x[5, 1, :] = 0
+    x[5, 1, 100] = 1.0
+    wname = "q_norm_w" if tensor == "q" else "k_norm_w"
+
+    def run(w, rows):
+        args = dict(d)
+        args[tensor] = rows
+        args[wname] = w
+        return h.forward(args["q"], args["k"], args["v"], args["q_norm_w"], args["k_norm_w"], args["pos"],
+                         args["seg_offsets"])
+
+    w = torch.ones(128, device="cuda")
+    w[100] = 6000.0  # sqrt(128) * 6000 = 67882 > 65504
+    run(w, x)
+    assert h.device_status() == ERR_INVALID_ARG
+    assert h.device_status() == OK
+    # a non-finite row is not a range error, also where the check runs
+    nan_rows = x.clone()
+    nan_rows[5, 1, 100] = float("nan")
+    run(w, nan_rows)
+    assert h.device_status() == OK
+    w[100] = 3000.0  # 33941: inside the range, the per-value check is skipped
+    out, lse = run(w, x)
+    assert h.device_status() == OK
+    assert bool(torch.isfinite(out.float()).all()) and bool(torch.isfinite(lse).all())
