@@ -17,12 +17,12 @@
 // at the sample start in ascending order, so a sample's gradients are the same
 // bits alone or packed.
 //
-// dkdv and dq_tc are persistent (one CTA per SM, 640 threads): warps 0 and 2 TMA
-// producers (one per streamed ring), warp 1 the single-thread tcgen05 issuer,
-// in dkdv warp 3 the stager of each block's lse / Delta columns in shared memory,
-// warps 4-19 four warpgroups that split each 128 x 128 score block by columns
-// (thread = TMEM lane = one row of the CTA's 128-row tile) and compute on
-// register pairs.  Operands: S on fp16 q^/k^, dP on bf16 dO/v, P (bf16) and dS
+// dkdv and dq_tc are persistent (one CTA per SM): warps 0 and 2 TMA producers
+// (one per streamed ring), warp 1 the single-thread tcgen05 issuer, in dkdv warp 3
+// the stager of each block's lse / Delta columns in shared memory; then the
+// warpgroups that split each 128 x 128 score block by columns (thread = TMEM
+// lane = one row of the CTA's 128-row tile) and compute on register pairs: two
+// of 64 columns in dkdv (384 threads), four of 32 in dq_tc (640 threads).  Operands: S on fp16 q^/k^, dP on bf16 dO/v, P (bf16) and dS
 // (fp16) for the accumulating products.  An item's accumulators are drained to
 // HBM as soon as its last MMA completed, so the next item's loads and products
 // start right away.
@@ -216,13 +216,13 @@ __device__ __forceinline__ void ring_producer(const BwdTcParams& p, const RingSp
 // ring (a slot is held from S^T(b), one block ahead, to dK(b)), dO through a
 // 2-slot ring (dP^T(b) to dV(b)).
 namespace kvt {
-constexpr int kThreads = 640;                       // warps 0-3: producers, MMA issuer, column stager; 4-19: four warpgroups
+constexpr int kThreads = 384;                       // warps 0-3: producers, MMA issuer, column stager; 4-11: two warpgroups
 constexpr int kQSlots = 3, kOSlots = 2;
 constexpr int kOffFixed = 0;                        // k^ + v tiles
 constexpr int kOffQ = bwdt::kPair;                  // q^ ring
 constexpr int kOffO = kOffQ + kQSlots * bwdt::kTile;  // dO ring
 constexpr int kOffBar = kOffO + kOSlots * bwdt::kTile;
-// per warpgroup and block parity: the block's 32 query columns as -lse2 then -Delta (FP32)
+// per warpgroup and block parity: the block's 64 query columns as -lse2 then -Delta (FP32)
 // (written by warp 3, read by the warpgroup's four softmax warps)
 constexpr int kOffCol = kOffBar + 256;
 constexpr int kSmem = kOffCol + 4 * 2 * 64 * 4;     // the dynamic shared memory base is 1024-aligned (checked)
@@ -232,18 +232,13 @@ enum { bFixedFull = 0, bQFull, bQEmpty = bQFull + kQSlots, bOFull = bQEmpty + kQ
 static_assert(8 * bCount + 8 <= 256, "barrier area");
 static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
 constexpr uint32_t cB = 128;
-// Column pairs of a warpgroup's 32 query columns (bit e = columns 2e, 2e + 1)
-// whose 2^x would run on the FMA pipe (exp2_poly_pair) instead of the SFU,
-// fixed by the column's place in the block.  None: measured on the packed
-// 13539-token batch with the block loop free of spills, one pair in four made
-// this kernel 6% slower and two in sixteen 2.6%.
-constexpr uint32_t kPolyPairs = 0x0u;
 }  // namespace kvt
 
 // TMEM column of the A operand for K-step kk (queries 16kk .. 16kk + 15) of P^T
-// (half = 0) or dS^T (half = 1): warpgroup kk / 2 packed its 32 queries at
-// B + 32 (kk / 2) + 16 half.
-__device__ __forceinline__ uint32_t kv_acol(int kk, int half) { return kvt::cB + 32 * (kk >> 1) + 16 * half + 8 * (kk & 1); }
+// (half = 0) or dS^T (half = 1): warpgroup kk / 4 packed its 64 queries at
+// B + 64 (kk / 4) + 32 half.
+__device__ __forceinline__ uint32_t kv_acol(int kk, int half) { return kvt::cB + 64 * (kk >> 2) + 32 * half + 8 * (kk & 3); }
+
 
 __global__ void __launch_bounds__(kvt::kThreads, 1)
 dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
@@ -278,9 +273,9 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         }
         tc::mbar_init(bar(bSFull), 1);
         tc::mbar_init(bar(bPFull), 1);
-        tc::mbar_init(bar(bSUsed), 16);
-        tc::mbar_init(bar(bPtFull), 16);
-        tc::mbar_init(bar(bDsFull), 16);
+        tc::mbar_init(bar(bSUsed), 8);
+        tc::mbar_init(bar(bPtFull), 8);
+        tc::mbar_init(bar(bDsFull), 8);
         tc::mbar_init(bar(bAccDone), 1);
         tc::mbar_init(bar(bTailQ), 1);
         tc::mbar_init(bar(bTailO), 1);
@@ -288,7 +283,7 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         tc::mbar_init(bar(bNever), 1);  // nothing arrives: the target of a test's stall
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(bar(bColReady + i), 1);  // warp 3
-            tc::mbar_init(bar(bColFree + i), 16);  // the softmax warps
+            tc::mbar_init(bar(bColFree + i), 8);  // the softmax warps
         }
         *abort_flag = 0;
         tc::fence_mbar_init();
@@ -307,8 +302,8 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         *abort_flag = 1;
         atomicOr(p.plan.err, kErrTimeout);
     };
-    // 640 threads x 96 registers: the MMA issuer and the softmax warps both need about 96,
-    // so no setmaxnreg split
+    // 384 threads x 168 registers, no setmaxnreg split (a 152 / 176 split made the
+    // softmax warps spill)
 
     if (warp == 0 || warp == 2) {
         // ------------------------------------- TMA producers: warp 0 the fixed k^ / v
@@ -415,8 +410,8 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
     } else if (warp == 3) {
         // ------------------------------------- lse / Delta column stager
         // Block n's 128 query columns, -lse in log2 units and -Delta (+0 past the
-        // sample end), into buffer n & 1: warpgroup g's 32 columns at 128 g + 64 (n & 1)
-        // floats.  The values are loaded before waiting for the buffer (the softmax
+        // sample end), into buffer n & 1: warpgroup w's 64 columns at 256 w + 128 (n & 1)
+        // floats, their Delta 64 floats further.  The values are loaded before waiting for the buffer (the softmax
         // warps' release of block n - 2), so the stager runs up to two blocks ahead
         // and the softmax warps issue no global loads in their block loop.
         float* const colbase = reinterpret_cast<float*>(smem + kOffCol) + lane;
@@ -440,8 +435,8 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 if (!ok) { fail(); break; }
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
-                    colbase[128 * g + 64 * (n & 1)] = 0.f - rl[g] * kLog2e;
-                    colbase[128 * g + 64 * (n & 1) + 32] = 0.f - rd[g];
+                    colbase[256 * (g >> 1) + 128 * (n & 1) + 32 * (g & 1)] = 0.f - rl[g] * kLog2e;
+                    colbase[256 * (g >> 1) + 128 * (n & 1) + 32 * (g & 1) + 64] = 0.f - rd[g];
                 }
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(bar(bColReady + (n & 1)));
@@ -449,10 +444,10 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         }
     } else if (warp >= 4) {
         // ------------------------------------- softmax gradient + drain
-        const int wg = (warp - 4) >> 2;                 // query quarter of the score tile
+        const int wg = (warp - 4) >> 2;                 // query half of the score tile
         const int t = tid - 128 * (1 + wg);             // key row == TMEM lane
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-        const uint32_t tS = tmem + lane_base + 32 * wg, tB = tmem + lane_base + cB + 32 * wg;
+        const uint32_t tS = tmem + lane_base + 64 * wg, tB = tmem + lane_base + cB + 64 * wg;
         const float c = p.scale * kLog2e;
         const uint64_t pol = tc::policy_evict_first();  // the stored dS blocks are streamed once
         uint32_t cntS = 0, items = 0;
@@ -461,18 +456,16 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             if (!bwd_item(p, i, it)) break;
             const int nq = (it.L + 127) / 128;
             const bool key_ok = 128 * it.tile + t < it.L;
-            // the item's stored dS rows of this thread: block qj at dsrow + qj * 8192 words
-            // (layout [32-query chunk wg][key][32 queries] per 128 x 128 block)
+            // the item's stored dS rows of this thread: chunks 2 wg and 2 wg + 1 of block qj at
+            // dsrow + qj * 8192 words and 2048 words further (layout [32-query chunk][key][32 queries])
             const long long blk0 = p.ds ? ds_base(p, it) + (long long)it.tile * nq : 0;
-            // blocks of the item inside the workspace (all of them unless it was sized too small):
-            // one 32-bit count, as a live 64-bit bound cost the block loop a spill reload
             const int ds_in = (int)max(0LL, min((long long)nq, p.ds_blocks - blk0));
-            const size_t dsrow = (size_t)blk0 * (128 * 128 / 2) + ((size_t)wg * 128 + t) * 16;  // in 32-bit words
-            // lse / Delta of the warpgroup's 32 query columns come staged in shared memory
+            const size_t dsrow = (size_t)blk0 * (128 * 128 / 2) + ((size_t)(2 * wg) * 128 + t) * 16;  // in 32-bit words
+            // lse / Delta of the warpgroup's 64 query columns come staged in shared memory
             // (warp 3, above) and are read as broadcast 16-byte loads
             for (int qj = 0; qj < nq; ++qj) {
                 const uint32_t n = cntS;
-                const int validq = it.L - 128 * qj - 32 * wg;  // columns of this quarter inside the sample
+                const int validq = it.L - 128 * qj - 64 * wg;  // columns of this half inside the sample
                 bool ok = true;
                 if (lane == 0) {
                     if (p.stall == tc::kStallConsumer && warp == 4 && cntS == 0)
@@ -484,78 +477,88 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 if (!ok) { fail(); break; }
                 __syncwarp();  // lane 0's acquire of the staged columns covers the warp
                 tc::fence_after_sync();
-                const float4* const cl = reinterpret_cast<const float4*>(smem + kOffCol) + 32 * wg + 16 * (n & 1);
-                const float4* const cd = cl + 8;
-                uint64_t p2[16];  // S^T column pairs, then P in FP32
-                tc::tmem_ld32_pairs(tS, p2);
+                const float4* const cl = reinterpret_cast<const float4*>(smem + kOffCol) + 64 * wg + 32 * (n & 1);
+                const float4* const cd = cl + 16;
+                uint64_t p2[32];  // S^T column pairs, then P in FP32
+                tc::tmem_ld64_pairs(tS, p2);
                 tc::fence_before_sync();
                 __syncwarp();
                 tc::mbar_arrive_lane0(bar(bSUsed), lane);
                 // ---- P = 2^(s c - lse2_col)
                 const uint64_t c2 = f2pack(c, c);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
+                for (int j = 0; j < 16; ++j) {
                     const float4 v = cl[j];
-                    const uint64_t n0 = f2pack(v.x, v.y), n1 = f2pack(v.z, v.w);
-                    p2[2 * j] = ((kvt::kPolyPairs >> (2 * j)) & 1) ? exp2_poly_pair(p2[2 * j], c2, n0)
-                                                                     : exp2_pair(p2[2 * j], c2, n0);
-                    p2[2 * j + 1] = ((kvt::kPolyPairs >> (2 * j + 1)) & 1) ? exp2_poly_pair(p2[2 * j + 1], c2, n1)
-                                                                             : exp2_pair(p2[2 * j + 1], c2, n1);
+                    p2[2 * j] = exp2_pair(p2[2 * j], c2, f2pack(v.x, v.y));
+                    p2[2 * j + 1] = exp2_pair(p2[2 * j + 1], c2, f2pack(v.z, v.w));
                 }
-                if (validq < 32) {  // tail block: columns past the sample end are exact zeros
+                if (validq < 64) {  // tail block: columns past the sample end are exact zeros
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) p2[e] = mask_pair(p2[e], 2 * e, validq);
+                    for (int e = 0; e < 32; ++e) p2[e] = mask_pair(p2[e], 2 * e, validq);
                 }
-                // ---- dP^T(b) from B, then P^T (bf16) over B's first 16 columns of this quarter
+                // ---- dP^T(b) from B, then P^T (bf16) over B's first 32 columns of this half
                 if (lane == 0) ok = tc::mbar_wait(bar(bPFull), cntS & 1, abort_flag);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) { fail(); break; }
                 ++cntS;
                 tc::fence_after_sync();
+                // dP^T in two halves: the first (queries 0-31) before P^T is written over it,
+                // the second (queries 32-63) before dS^T is
                 uint64_t d2[16];
                 tc::tmem_ld32_pairs(tB, d2);
-                {
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
                     uint32_t pk[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) pk[e] = bf16_pair(p2[e]);
-                    tc::tmem_st16(tB, pk);
+                    for (int e = 0; e < 16; ++e) pk[e] = bf16_pair(p2[16 * h2 + e]);
+                    tc::tmem_st16(tB + 16 * h2, pk);
                 }
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
                 __syncwarp();
                 tc::mbar_arrive_lane0(bar(bPtFull), lane);
-                // ---- dS = P (dP - Delta_col), fp16, over B's other 16 columns (zero where P is)
-                uint32_t dk[16];
+                // ---- dS = P (dP - Delta_col), fp16, over B's other 32 columns (zero where P is)
+                uint32_t dk[32];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const float4 v = cd[j];
                     dk[2 * j] = ds_f16_pair(p2[2 * j], d2[2 * j], f2pack(v.x, v.y));
                     dk[2 * j + 1] = ds_f16_pair(p2[2 * j + 1], d2[2 * j + 1], f2pack(v.z, v.w));
                 }
-                tc::tmem_st16(tB + 16, dk);
+                tc::tmem_ld32_pairs(tB + 32, d2);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float4 v = cd[8 + j];
+                    dk[16 + 2 * j] = ds_f16_pair(p2[16 + 2 * j], d2[2 * j], f2pack(v.x, v.y));
+                    dk[16 + 2 * j + 1] = ds_f16_pair(p2[16 + 2 * j + 1], d2[2 * j + 1], f2pack(v.z, v.w));
+                }
+                tc::tmem_st32(tB + 32, dk);
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
                 __syncwarp();
                 tc::mbar_arrive_lane0(bar(bDsFull), lane);
                 tc::mbar_arrive_lane0(bar(bColFree + (n & 1)), lane);  // the warp's reads of the columns are done
-                if (p.ds) {  // the block for the dQ kernel (key row t, this quarter's 32 queries), off the
-                             // tensor cores' path; a warp's 32 key rows of its chunk are 2 KB contiguous,
-                             // and rows past the sample end hold zeros
+                if (p.ds) {  // the block for the dQ kernel (key row t, this half's two 32-query chunks)
                     if (qj < ds_in) {
                         uint32_t* const dst = reinterpret_cast<uint32_t*>(p.ds) + dsrow + (size_t)qj * (128 * 128 / 2);
-                        if (key_ok) {
 #pragma unroll
-                            for (int e = 0; e < 2; ++e)
-                                asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;"
-                                             ::"l"(dst + 8 * e), "r"(dk[8 * e]), "r"(dk[8 * e + 1]), "r"(dk[8 * e + 2]),
-                                             "r"(dk[8 * e + 3]), "r"(dk[8 * e + 4]), "r"(dk[8 * e + 5]),
-                                             "r"(dk[8 * e + 6]), "r"(dk[8 * e + 7]), "l"(pol)
-                                             : "memory");
-                        } else {
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            if (key_ok) {
 #pragma unroll
-                            for (int e = 0; e < 2; ++e)
-                                asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %1, %1, %1, %1, %1, %1, %1}, %2;"
-                                             ::"l"(dst + 8 * e), "r"(0u), "l"(pol) : "memory");
+                                for (int e = 0; e < 2; ++e)
+                                    asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;"
+                                                 ::"l"(dst + 2048 * h2 + 8 * e), "r"(dk[16 * h2 + 8 * e]),
+                                                 "r"(dk[16 * h2 + 8 * e + 1]), "r"(dk[16 * h2 + 8 * e + 2]),
+                                                 "r"(dk[16 * h2 + 8 * e + 3]), "r"(dk[16 * h2 + 8 * e + 4]),
+                                                 "r"(dk[16 * h2 + 8 * e + 5]), "r"(dk[16 * h2 + 8 * e + 6]),
+                                                 "r"(dk[16 * h2 + 8 * e + 7]), "l"(pol)
+                                                 : "memory");
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 2; ++e)
+                                    asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %1, %1, %1, %1, %1, %1, %1}, %2;"
+                                                 ::"l"(dst + 2048 * h2 + 8 * e), "r"(0u), "l"(pol) : "memory");
+                            }
                         }
                     } else if (lane == 0) {
                         atomicOr(p.plan.err, kErrRange);
@@ -563,7 +566,7 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 }
             }
             if (failed) break;
-            // ---- drain: each warpgroup its 32 channels of dV (bf16 output rows) and of
+            // ---- drain: each warpgroup its 64 channels of dV (bf16 output rows) and of
             // scale * dk^ (FP32 rows for the RoPE^-1 / RMSNorm backward)
             bool ok = true;
             if (lane == 0) ok = tc::mbar_wait(bar(bAccDone), items & 1, abort_flag);
@@ -571,74 +574,78 @@ dkdv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             if (!ok) { fail(); break; }
             ++items;
             tc::fence_after_sync();
-            // A thread holds its key row's 32 channels of this quarter: 64 bytes of dV,
-            // 128 of scale * dk^.  Storing them as is would touch 32 token rows (cache
-            // lines) per instruction; lanes first trade 32-byte pieces (pairs for dV,
-            // quads for dk^: one- and two-bit transposes of (lane, piece) by xor
-            // shuffles), so that each store instruction writes 16 rows' 64 contiguous
+            // A thread holds its key row's 64 channels of this half, drained 32 at a time: 64
+            // bytes of dV and 128 of scale * dk^ per 32.  Lanes trade 32-byte pieces first
+            // (pairs for dV, quads for dk^: one- and two-bit transposes of (lane, piece) by
+            // xor shuffles), so that each store instruction writes 16 rows' 64 contiguous
             // bytes of dV, or 8 rows' whole 128-byte lines of dk^.
             const int m = lane & 3;
             const int r0 = 32 * (warp & 3);  // the warp's first row of the tile
-            auto row_ptr = [&](int r) {      // row r of the warp's 32, if inside the sample
-                return 128 * it.tile + r0 + r < it.L ? ((size_t)(it.row0 + r0 + r) * p.H + it.h) * kD + 32 * wg
-                                                     : (size_t)-1;
-            };
-            {
-                uint32_t r[32];
-                tc::tmem_ld32(tmem + lane_base + 256 + 32 * wg, r);
-                tc::tmem_wait_ld_dep(r);
-                uint32_t w[16];  // pieces 0, 1: channels 0-15, 16-31 as bf16 pairs
+#pragma unroll 1
+            for (int hq = 0; hq < 2; ++hq) {
+                const int ch = 64 * wg + 32 * hq;  // first channel of this 32
+                auto row_ptr = [&](int r) {        // row r of the warp's 32, if inside the sample
+                    return 128 * it.tile + r0 + r < it.L ? ((size_t)(it.row0 + r0 + r) * p.H + it.h) * kD + ch
+                                                         : (size_t)-1;
+                };
+                {
+                    uint32_t r[32];
+                    tc::tmem_ld32(tmem + lane_base + 256 + ch, r);
+                    tc::tmem_wait_ld_dep(r);
+                    uint32_t w[16];  // pieces 0, 1: channels 0-15, 16-31 as bf16 pairs
 #pragma unroll
-                for (int e = 0; e < 16; ++e) w[e] = pack_bf16(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
+                    for (int e = 0; e < 16; ++e) w[e] = pack_bf16(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {  // lane 2k + b ends with piece b of rows 2k, 2k + 1
-                    const uint32_t send = (m & 1) ? w[j] : w[8 + j];
-                    const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 1);
-                    if (m & 1) w[j] = recv; else w[8 + j] = recv;
-                }
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const size_t off = row_ptr((lane & ~1) + e);
-                    __nv_bfloat16* const d = p.dv + off + 16 * (m & 1);
-                    if (off == (size_t)-1) continue;
-                    if (p.dv_align32) {
-                        asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
-                                     ::"l"(d), "r"(w[8 * e]), "r"(w[8 * e + 1]), "r"(w[8 * e + 2]), "r"(w[8 * e + 3]),
-                                     "r"(w[8 * e + 4]), "r"(w[8 * e + 5]), "r"(w[8 * e + 6]), "r"(w[8 * e + 7])
-                                     : "memory");
-                    } else {
-                        *reinterpret_cast<uint4*>(d) = make_uint4(w[8 * e], w[8 * e + 1], w[8 * e + 2], w[8 * e + 3]);
-                        *reinterpret_cast<uint4*>(d + 8) = make_uint4(w[8 * e + 4], w[8 * e + 5], w[8 * e + 6], w[8 * e + 7]);
+                    for (int j = 0; j < 8; ++j) {  // lane 2k + b ends with piece b of rows 2k, 2k + 1
+                        const uint32_t send = (m & 1) ? w[j] : w[8 + j];
+                        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 1);
+                        if (m & 1) w[j] = recv; else w[8 + j] = recv;
                     }
-                }
-            }
-            {
-                uint32_t r[32];  // pieces 0-3: channels 8q .. 8q + 7
-                tc::tmem_ld32(tmem + lane_base + 384 + 32 * wg, r);
-                tc::tmem_wait_ld_dep(r);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * p.scale);
-#pragma unroll
-                for (int bit = 1; bit <= 2; bit <<= 1) {  // lane 4k + q ends with piece q of rows 4k .. 4k + 3
-#pragma unroll
-                    for (int q0 = 0; q0 < 4; ++q0) {
-                        if (q0 & bit) continue;
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const uint32_t send = (m & bit) ? r[8 * q0 + j] : r[8 * (q0 | bit) + j];
-                            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, bit);
-                            if (m & bit) r[8 * q0 + j] = recv; else r[8 * (q0 | bit) + j] = recv;
+                    for (int e = 0; e < 2; ++e) {
+                        const size_t off = row_ptr((lane & ~1) + e);
+                        __nv_bfloat16* const d = p.dv + off + 16 * (m & 1);
+                        if (off == (size_t)-1) continue;
+                        if (p.dv_align32) {
+                            asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                                         ::"l"(d), "r"(w[8 * e]), "r"(w[8 * e + 1]), "r"(w[8 * e + 2]), "r"(w[8 * e + 3]),
+                                         "r"(w[8 * e + 4]), "r"(w[8 * e + 5]), "r"(w[8 * e + 6]), "r"(w[8 * e + 7])
+                                         : "memory");
+                        } else {
+                            *reinterpret_cast<uint4*>(d) = make_uint4(w[8 * e], w[8 * e + 1], w[8 * e + 2], w[8 * e + 3]);
+                            *reinterpret_cast<uint4*>(d + 8) =
+                                make_uint4(w[8 * e + 4], w[8 * e + 5], w[8 * e + 6], w[8 * e + 7]);
                         }
                     }
                 }
+                {
+                    uint32_t r[32];  // pieces 0-3: channels 8q .. 8q + 7
+                    tc::tmem_ld32(tmem + lane_base + 384 + ch, r);
+                    tc::tmem_wait_ld_dep(r);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const size_t off = row_ptr((lane & ~3) + e);
-                    if (off != (size_t)-1)
-                        asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
-                                     ::"l"(p.dyhat + off + 8 * m), "r"(r[8 * e]), "r"(r[8 * e + 1]), "r"(r[8 * e + 2]),
-                                     "r"(r[8 * e + 3]), "r"(r[8 * e + 4]), "r"(r[8 * e + 5]), "r"(r[8 * e + 6]),
-                                     "r"(r[8 * e + 7]) : "memory");
+                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * p.scale);
+#pragma unroll
+                    for (int bit = 1; bit <= 2; bit <<= 1) {  // lane 4k + q ends with piece q of rows 4k .. 4k + 3
+#pragma unroll
+                        for (int q0 = 0; q0 < 4; ++q0) {
+                            if (q0 & bit) continue;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const uint32_t send = (m & bit) ? r[8 * q0 + j] : r[8 * (q0 | bit) + j];
+                                const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, bit);
+                                if (m & bit) r[8 * q0 + j] = recv; else r[8 * (q0 | bit) + j] = recv;
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const size_t off = row_ptr((lane & ~3) + e);
+                        if (off != (size_t)-1)
+                            asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                                         ::"l"(p.dyhat + off + 8 * m), "r"(r[8 * e]), "r"(r[8 * e + 1]), "r"(r[8 * e + 2]),
+                                         "r"(r[8 * e + 3]), "r"(r[8 * e + 4]), "r"(r[8 * e + 5]), "r"(r[8 * e + 6]),
+                                         "r"(r[8 * e + 7]) : "memory");
+                    }
                 }
             }
             // the next item's first dV/dK products overwrite the accumulators only after

@@ -197,6 +197,48 @@ __device__ __forceinline__ void tmem_ld32_pairs(uint32_t taddr, uint64_t (&r)[16
         : "=l"(r[0]), "=l"(r[1]), "=l"(r[2]), "=l"(r[3]), "=l"(r[4]), "=l"(r[5]), "=l"(r[6]), "=l"(r[7]), "=l"(r[8]), "=l"(r[9]), "=l"(r[10]), "=l"(r[11]), "=l"(r[12]), "=l"(r[13]), "=l"(r[14]), "=l"(r[15])
         : "r"(taddr) : "memory");
 }
+// 32 lanes x 64 columns of 32-bit in one load, waited, as 32 column pairs.
+__device__ __forceinline__ void tmem_ld64_pairs(uint32_t taddr, uint64_t (&r)[32]) {
+    asm volatile(
+        "{\n.reg .b32 a<64>;\n"
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {a0,a1,a2,a3,a4,a5,a6,a7,a8,a9,a10,a11,a12,a13,a14,a15,a16,a17,a18,a19,a20,a21,a22,a23,a24,a25,a26,a27,a28,a29,a30,a31,a32,a33,a34,a35,a36,a37,a38,a39,a40,a41,a42,a43,a44,a45,a46,a47,a48,a49,a50,a51,a52,a53,a54,a55,a56,a57,a58,a59,a60,a61,a62,a63}, [%32];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        "mov.b64 %0, {a0, a1};\n"
+        "mov.b64 %1, {a2, a3};\n"
+        "mov.b64 %2, {a4, a5};\n"
+        "mov.b64 %3, {a6, a7};\n"
+        "mov.b64 %4, {a8, a9};\n"
+        "mov.b64 %5, {a10, a11};\n"
+        "mov.b64 %6, {a12, a13};\n"
+        "mov.b64 %7, {a14, a15};\n"
+        "mov.b64 %8, {a16, a17};\n"
+        "mov.b64 %9, {a18, a19};\n"
+        "mov.b64 %10, {a20, a21};\n"
+        "mov.b64 %11, {a22, a23};\n"
+        "mov.b64 %12, {a24, a25};\n"
+        "mov.b64 %13, {a26, a27};\n"
+        "mov.b64 %14, {a28, a29};\n"
+        "mov.b64 %15, {a30, a31};\n"
+        "mov.b64 %16, {a32, a33};\n"
+        "mov.b64 %17, {a34, a35};\n"
+        "mov.b64 %18, {a36, a37};\n"
+        "mov.b64 %19, {a38, a39};\n"
+        "mov.b64 %20, {a40, a41};\n"
+        "mov.b64 %21, {a42, a43};\n"
+        "mov.b64 %22, {a44, a45};\n"
+        "mov.b64 %23, {a46, a47};\n"
+        "mov.b64 %24, {a48, a49};\n"
+        "mov.b64 %25, {a50, a51};\n"
+        "mov.b64 %26, {a52, a53};\n"
+        "mov.b64 %27, {a54, a55};\n"
+        "mov.b64 %28, {a56, a57};\n"
+        "mov.b64 %29, {a58, a59};\n"
+        "mov.b64 %30, {a60, a61};\n"
+        "mov.b64 %31, {a62, a63};\n"
+        "}\n"
+        : "=l"(r[0]), "=l"(r[1]), "=l"(r[2]), "=l"(r[3]), "=l"(r[4]), "=l"(r[5]), "=l"(r[6]), "=l"(r[7]), "=l"(r[8]), "=l"(r[9]), "=l"(r[10]), "=l"(r[11]), "=l"(r[12]), "=l"(r[13]), "=l"(r[14]), "=l"(r[15]), "=l"(r[16]), "=l"(r[17]), "=l"(r[18]), "=l"(r[19]), "=l"(r[20]), "=l"(r[21]), "=l"(r[22]), "=l"(r[23]), "=l"(r[24]), "=l"(r[25]), "=l"(r[26]), "=l"(r[27]), "=l"(r[28]), "=l"(r[29]), "=l"(r[30]), "=l"(r[31])
+        : "r"(taddr) : "memory");
+}
 // 32 lanes x 128 columns of 32-bit in one load, waited, as 64 column pairs.
 __device__ __forceinline__ void tmem_ld128_pairs(uint32_t taddr, uint64_t (&r)[64]) {
     asm volatile(
